@@ -1,0 +1,483 @@
+/*
+ * spec_oracle.c -- plain, slow, fp64 CPU oracle for the speculative-decoding
+ * verify step.
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path may call, link or load
+ * this file: only tests/, __graft_entry__.smoke() and bench.py's cpu_baseline
+ * leg use it.  It shares no code, header, table or constant generator with the
+ * CUDA path in speculative_decoding_verification_36_gb300/csrc/.
+ *
+ * Every step follows the method as the source pages state it, in their order
+ * and notation, and is written for a reader to check by eye: no blocking, no
+ * fusion, no reordering.  Citations name the page and its section:
+ *
+ *   [P1] "Speculative Decoding & Draft Model Topologies: Slashing Enterprise LLM
+ *        Latency by 3.5x in 2026", sec. 2 "Mathematical Foundation: Speculative
+ *        Verification & Rejection Sampling" (acceptance probability
+ *        alpha = min(1, p(x)/q(x)), draw u ~ U(0,1), discard on rejection, the
+ *        residual max(0, p - q) / sum max(0, p - q)); sec. 4 (token tree, 2D
+ *        tree mask, longest accepted path).
+ *   [P2] "Speculative Decoding for LLM Inference: How Draft-and-Verify
+ *        Accelerates Token Generation", sections "The draft-and-verify loop"
+ *        (longest accepted prefix, resample on rejection, bonus token when all
+ *        are accepted) and "The correctness guarantee" (min(1, p/q),
+ *        norm(max(0, p - q))).
+ *   [P3] "Speculative Decoding at Scale: Latency Reduction in Distributed LLM
+ *        Serving", sequence diagram (accept matching tokens + 1 bonus token)
+ *        and sec. 1 (relu(P - Q) / sum relu(P - Q)).
+ *   [P4] "Speculative Decoding in Production: How Small Draft Models & Medusa
+ *        Heads Deliver 2x-3x LLM Speedups Without Accuracy Loss", sec. 2
+ *        (P_accept = min(1, p/q); p >= q always accepted) and sec. 4 (SpecInfer
+ *        tree of top-2 candidates verified with a 2D causal mask).
+ *
+ * Where the pages are silent the oracle takes these readings (all of them are
+ * also listed, with reasons, in the design notes):
+ *   - p = softmax(z_target / tau), q = softmax(z_draft / tau), the same tau for
+ *     both; tau == 0 selects greedy verification.
+ *   - accept iff p(x) >= q(x) or u * q(x) < p(x)   (strict "<"; [P1] writes
+ *     "u <= alpha", which differs only on a set of measure zero).
+ *   - uniforms come from Philox-4x64-10 with key (seed, 0x5350454356455249)
+ *     and counter (sequence b, position, stream, 0); stream 0 is the
+ *     acceptance draw, stream 1 the resampling draw.  The first output word r
+ *     maps to u = (2 * (r >> 41) + 1) * 2^-24, an odd multiple of 2^-24 in
+ *     (0, 1).
+ *   - the replacement / bonus token is drawn by inverse CDF in vocabulary
+ *     order: the smallest j with C_j > w * Z, C_j = sum_{v <= j} r(v).
+ *   - greedy ties go to the lowest token id.
+ *   - tree: row 0 is the root, row i + 1 is node i, parents precede children;
+ *     the deepest accepted node wins, ties to the lowest node index.
+ *   - bad data (NaN or +inf logit, all -inf row, token id outside [0, V),
+ *     parent index not in [-1, i)) marks the sequence: n = -1 and all outputs
+ *     of that sequence are -1.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+
+#define ORC_DTYPE_F32 0
+#define ORC_DTYPE_BF16 1
+
+/* ------------------------------------------------------------------------ */
+/* Philox-4x64-10 counter-based generator, written from its published        */
+/* definition: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As Easy */
+/* as 1, 2, 3", SC'11.  Ten rounds; each round multiplies words 0 and 2 by   */
+/* the two round multipliers, xors the high halves with the other two words  */
+/* and the key, and the key is bumped by the two Weyl constants between      */
+/* rounds.                                                                   */
+/* ------------------------------------------------------------------------ */
+static void philox_mulhilo(uint64_t a, uint64_t b, uint64_t *hi, uint64_t *lo)
+{
+    unsigned __int128 prod = (unsigned __int128)a * (unsigned __int128)b;
+    *hi = (uint64_t)(prod >> 64);
+    *lo = (uint64_t)prod;
+}
+
+void oracle_philox4x64_10(const uint64_t ctr_in[4], const uint64_t key_in[2], uint64_t out[4])
+{
+    const uint64_t mult0 = 0xD2E7470EE14C6C93ULL;
+    const uint64_t mult1 = 0xCA5A826395121157ULL;
+    const uint64_t weyl0 = 0x9E3779B97F4A7C15ULL;
+    const uint64_t weyl1 = 0xBB67AE8584CAA73BULL;
+    uint64_t x0 = ctr_in[0], x1 = ctr_in[1], x2 = ctr_in[2], x3 = ctr_in[3];
+    uint64_t k0 = key_in[0], k1 = key_in[1];
+    for (int round = 0; round < 10; ++round) {
+        uint64_t hi0, lo0, hi1, lo1;
+        if (round > 0) {
+            k0 += weyl0;
+            k1 += weyl1;
+        }
+        philox_mulhilo(mult0, x0, &hi0, &lo0);
+        philox_mulhilo(mult1, x2, &hi1, &lo1);
+        uint64_t y0 = hi1 ^ x1 ^ k0;
+        uint64_t y1 = lo1;
+        uint64_t y2 = hi0 ^ x3 ^ k1;
+        uint64_t y3 = lo0;
+        x0 = y0; x1 = y1; x2 = y2; x3 = y3;
+    }
+    out[0] = x0; out[1] = x1; out[2] = x2; out[3] = x3;
+}
+
+/* The uniform draw u ~ U(0,1) for (seed, sequence b, position, stream). */
+double oracle_uniform(uint64_t seed, uint64_t b, uint64_t position, uint64_t stream)
+{
+    const uint64_t key[2] = {seed, 0x5350454356455249ULL};
+    const uint64_t ctr[4] = {b, position, stream, 0};
+    uint64_t out[4];
+    oracle_philox4x64_10(ctr, key, out);
+    uint64_t top23 = out[0] >> 41;
+    return (double)(2 * top23 + 1) * ldexp(1.0, -24);
+}
+
+/* ------------------------------------------------------------------------ */
+/* logits                                                                    */
+/* ------------------------------------------------------------------------ */
+static double logit_at(const void *base, int dtype, size_t i)
+{
+    if (dtype == ORC_DTYPE_F32)
+        return (double)((const float *)base)[i];
+    uint32_t bits = ((uint32_t)((const uint16_t *)base)[i]) << 16;
+    float f;
+    memcpy(&f, &bits, sizeof f);
+    return (double)f;
+}
+
+/* A row is usable when it has no NaN, no +inf and at least one finite entry. */
+static int row_is_bad(const void *row, int dtype, int V)
+{
+    int any_finite_or_neg = 0;
+    for (int v = 0; v < V; ++v) {
+        double z = logit_at(row, dtype, (size_t)v);
+        if (isnan(z) || z == INFINITY)
+            return 1;
+        if (z != -INFINITY)
+            any_finite_or_neg = 1;
+    }
+    return !any_finite_or_neg;
+}
+
+/*
+ * Temperature softmax of one row: p[v] = exp(z_v / tau - m) / s with
+ * m = max_v z_v / tau and s = sum_v exp(z_v / tau - m).  ([P1] sec. 2 and
+ * [P2] "The correctness guarantee": p and q are the two models' probabilities.)
+ */
+static void softmax_row(const void *row, int dtype, int V, double tau, double *p,
+                        double *m_out, double *s_out)
+{
+    double m = -INFINITY;
+    for (int v = 0; v < V; ++v) {
+        double x = logit_at(row, dtype, (size_t)v) / tau;
+        if (x > m)
+            m = x;
+    }
+    double s = 0.0;
+    for (int v = 0; v < V; ++v) {
+        double e = exp(logit_at(row, dtype, (size_t)v) / tau - m);
+        p[v] = e;
+        s += e;
+    }
+    for (int v = 0; v < V; ++v)
+        p[v] = p[v] / s;
+    *m_out = m;
+    *s_out = s;
+}
+
+/* Inverse CDF in vocabulary order: the smallest j with C_j > theta, where C_j
+ * is the running sum of r.  When rounding leaves no such j, the largest j with
+ * r(j) > 0.  Also reports the distance from theta to the nearest C. */
+static int inverse_cdf(const double *r, int V, double theta, double *dist_out)
+{
+    double c_prev = 0.0, c = 0.0;
+    for (int j = 0; j < V; ++j) {
+        c_prev = c;
+        c = c + r[j];
+        if (c > theta) {
+            double d0 = theta - c_prev, d1 = c - theta;
+            *dist_out = d0 < d1 ? d0 : d1;
+            return j;
+        }
+    }
+    for (int j = V - 1; j >= 0; --j) {
+        if (r[j] > 0.0) {
+            *dist_out = 0.0;
+            return j;
+        }
+    }
+    *dist_out = 0.0;
+    return 0;
+}
+
+/*
+ * Speculative-sampling verification of B independent sequences.
+ *
+ * target: B x (K+1) x V logits, sequence b at target + b * t_stride_b elements;
+ * draft:  B x K x V logits, sequence b at draft + b * d_stride_b elements
+ *         (a stride of 0 broadcasts one sequence to every b);
+ * tokens: B x K drafted ids (row stride K);
+ * out_tokens: B x (K+1), out_n: B.
+ *
+ * Optional diagnostics (each may be NULL):
+ *   row_logmax, row_sum: B x (2K+1), target rows 0..K then draft rows 0..K-1;
+ *                        the max of z / tau and sum exp(z / tau - max);
+ *   px, qx, u, acc_margin: B x K, p_i(x_i), q_i(x_i), the acceptance draw and
+ *                        |u - min(1, p/q)| (NaN for positions not examined);
+ *   resid_mass, theta, w, sample_margin: B; Z = sum of the unnormalised
+ *                        replacement weights, w * Z, w, and the distance from
+ *                        w * Z to the nearest cumulative sum divided by Z;
+ *   degenerate: B, 1 when a rejection left Z == 0 and p_n was used instead.
+ *
+ * Returns 0; sequences with bad data get n = -1 and -1 everywhere.
+ */
+int oracle_spec_verify(const void *target, const void *draft, int dtype,
+                       long long t_stride_b, long long d_stride_b,
+                       const int32_t *tokens, long long tok_stride_b,
+                       int B, int K, int V, double tau, uint64_t seed,
+                       int32_t *out_tokens, int32_t *out_n,
+                       double *row_logmax, double *row_sum,
+                       double *px_out, double *qx_out, double *u_out, double *acc_margin,
+                       double *resid_mass, double *theta_out, double *w_out,
+                       double *sample_margin, int32_t *degenerate)
+{
+    const size_t esz = dtype == ORC_DTYPE_F32 ? 4 : 2;
+    const int R = 2 * K + 1;
+    double *probs = (double *)malloc(sizeof(double) * (size_t)R * (size_t)V);
+    double *r = (double *)malloc(sizeof(double) * (size_t)V);
+    if (!probs || !r) {
+        free(probs);
+        free(r);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        const char *tb = (const char *)target + (size_t)((long long)b * t_stride_b) * esz;
+        const char *db = (const char *)draft + (size_t)((long long)b * d_stride_b) * esz;
+        const int32_t *x = tokens + (long long)b * tok_stride_b;
+        int32_t *out = out_tokens + (size_t)b * (size_t)(K + 1);
+        for (int j = 0; j <= K; ++j)
+            out[j] = -1;
+        for (int i = 0; i < K && px_out; ++i) {
+            px_out[(size_t)b * K + i] = NAN;
+            qx_out[(size_t)b * K + i] = NAN;
+        }
+        for (int i = 0; i < K && acc_margin; ++i)
+            acc_margin[(size_t)b * K + i] = NAN;
+        for (int i = 0; i < K && u_out; ++i)
+            u_out[(size_t)b * K + i] = NAN;
+        if (resid_mass) resid_mass[b] = NAN;
+        if (theta_out) theta_out[b] = NAN;
+        if (w_out) w_out[b] = NAN;
+        if (sample_margin) sample_margin[b] = NAN;
+        if (degenerate) degenerate[b] = 0;
+
+        /* bad data: any unusable row or an out-of-range drafted token */
+        int bad = 0;
+        for (int rr = 0; rr < R && !bad; ++rr) {
+            const char *row = rr <= K ? tb + (size_t)rr * V * esz : db + (size_t)(rr - K - 1) * V * esz;
+            bad = row_is_bad(row, dtype, V);
+        }
+        for (int i = 0; i < K && !bad; ++i)
+            bad = x[i] < 0 || x[i] >= V;
+        if (bad) {
+            out_n[b] = -1;
+            continue;
+        }
+
+        /* step 1: temperature softmax of every target row and draft row */
+        for (int rr = 0; rr < R; ++rr) {
+            const char *row = rr <= K ? tb + (size_t)rr * V * esz : db + (size_t)(rr - K - 1) * V * esz;
+            double m, s;
+            softmax_row(row, dtype, V, tau, probs + (size_t)rr * V, &m, &s);
+            if (row_logmax) row_logmax[(size_t)b * R + rr] = m;
+            if (row_sum) row_sum[(size_t)b * R + rr] = s;
+        }
+        const double *p_rows = probs;                        /* p_0 .. p_K */
+        const double *q_rows = probs + (size_t)(K + 1) * V;  /* q_0 .. q_{K-1} */
+
+        /* steps 2-4: gather p(x_i), q(x_i); accept with probability
+         * min(1, p/q); stop at the first rejection */
+        int n = K;
+        for (int i = 0; i < K; ++i) {
+            double p = p_rows[(size_t)i * V + x[i]];
+            double q = q_rows[(size_t)i * V + x[i]];
+            double u = oracle_uniform(seed, (uint64_t)b, (uint64_t)i, 0);
+            double alpha = q > 0.0 ? fmin(1.0, p / q) : 1.0;
+            if (px_out) {
+                px_out[(size_t)b * K + i] = p;
+                qx_out[(size_t)b * K + i] = q;
+            }
+            if (u_out) u_out[(size_t)b * K + i] = u;
+            if (acc_margin) acc_margin[(size_t)b * K + i] = fabs(u - alpha);
+            int accept = (p >= q) || (u * q < p);
+            if (!accept) {
+                n = i;
+                break;
+            }
+            out[i] = x[i];
+        }
+
+        /* step 5: the replacement distribution max(0, p_n - q_n) after a
+         * rejection, or the bonus distribution p_K when all K were accepted */
+        double Z = 0.0;
+        if (n < K) {
+            for (int v = 0; v < V; ++v) {
+                double d = p_rows[(size_t)n * V + v] - q_rows[(size_t)n * V + v];
+                r[v] = d > 0.0 ? d : 0.0;
+                Z += r[v];
+            }
+            if (Z == 0.0) {
+                if (degenerate) degenerate[b] = 1;
+                for (int v = 0; v < V; ++v) {
+                    r[v] = p_rows[(size_t)n * V + v];
+                    Z += r[v];
+                }
+            }
+        } else {
+            for (int v = 0; v < V; ++v) {
+                r[v] = p_rows[(size_t)K * V + v];
+                Z += r[v];
+            }
+        }
+
+        /* step 6: inverse-CDF draw with the stream-1 uniform */
+        double w = oracle_uniform(seed, (uint64_t)b, (uint64_t)n, 1);
+        double theta = w * Z;
+        double dist;
+        int j = inverse_cdf(r, V, theta, &dist);
+        out[n] = j;
+        out_n[b] = n;
+        if (resid_mass) resid_mass[b] = Z;
+        if (theta_out) theta_out[b] = theta;
+        if (w_out) w_out[b] = w;
+        if (sample_margin) sample_margin[b] = dist / Z;
+    }
+    free(probs);
+    free(r);
+    return 0;
+}
+
+/* First index of the maximum of a row (lowest id wins ties). */
+static int row_argmax(const void *row, int dtype, int V)
+{
+    int best = 0;
+    double best_z = logit_at(row, dtype, 0);
+    for (int v = 1; v < V; ++v) {
+        double z = logit_at(row, dtype, (size_t)v);
+        if (z > best_z) {
+            best_z = z;
+            best = v;
+        }
+    }
+    return best;
+}
+
+/*
+ * Greedy verification (tau == 0): accept drafted tokens while they equal the
+ * target argmax ([P3] "accept matching tokens ... + 1 bonus token", "reject
+ * mismatched"); the token after the accepted prefix is the argmax of that
+ * target row, which is the bonus token when all K match.
+ * Layouts as in oracle_spec_verify; draft logits are not read.
+ */
+int oracle_spec_verify_greedy(const void *target, int dtype, long long t_stride_b,
+                              const int32_t *tokens, long long tok_stride_b,
+                              int B, int K, int V, int32_t *out_tokens, int32_t *out_n,
+                              int32_t *row_argmax_out)
+{
+    const size_t esz = dtype == ORC_DTYPE_F32 ? 4 : 2;
+    for (int b = 0; b < B; ++b) {
+        const char *tb = (const char *)target + (size_t)((long long)b * t_stride_b) * esz;
+        const int32_t *x = tokens + (long long)b * tok_stride_b;
+        int32_t *out = out_tokens + (size_t)b * (size_t)(K + 1);
+        for (int j = 0; j <= K; ++j)
+            out[j] = -1;
+        int bad = 0;
+        for (int rr = 0; rr <= K && !bad; ++rr)
+            bad = row_is_bad(tb + (size_t)rr * V * esz, dtype, V);
+        for (int i = 0; i < K && !bad; ++i)
+            bad = x[i] < 0 || x[i] >= V;
+        if (bad) {
+            out_n[b] = -1;
+            for (int rr = 0; rr <= K && row_argmax_out; ++rr)
+                row_argmax_out[(size_t)b * (K + 1) + rr] = -1;
+            continue;
+        }
+        int n = K;
+        for (int rr = 0; rr <= K; ++rr) {
+            int a = row_argmax(tb + (size_t)rr * V * esz, dtype, V);
+            if (row_argmax_out) row_argmax_out[(size_t)b * (K + 1) + rr] = a;
+        }
+        for (int i = 0; i < K; ++i) {
+            int a = row_argmax(tb + (size_t)i * V * esz, dtype, V);
+            if (x[i] != a) {
+                n = i;
+                break;
+            }
+            out[i] = x[i];
+        }
+        out[n] = row_argmax(tb + (size_t)n * V * esz, dtype, V);
+        out_n[b] = n;
+    }
+    return 0;
+}
+
+/*
+ * Greedy verification of a candidate tree ([P1] sec. 4: all nodes verified in
+ * one pass, the longest accepted path is selected; [P4] sec. 4: a SpecInfer
+ * tree of top-2 candidates under a 2D causal mask).
+ *
+ * target: B x (N+1) x V; row 0 is the root's next-token row, row i+1 belongs
+ * to node i.  tree_tokens, parent_idx: B x N; parent -1 is the root.
+ * Node i is accepted when every node on its root path carries the argmax of
+ * its parent's row.  Outputs: out_path B x (N+1) token ids (the accepted path
+ * from the root's child down, then the bonus argmax of the deepest accepted
+ * node's row, -1 padding), out_len B (path length + 1), out_mask
+ * B x N x ceil(N/32) words with bit j of row i set iff j == i or j is an
+ * ancestor of i.  Everything is computed by explicit ancestor walks.
+ */
+int oracle_tree_verify_greedy(const void *target, int dtype, const int32_t *tree_tokens,
+                              const int32_t *parent_idx, int B, int N, int V,
+                              int32_t *out_path, int32_t *out_len, uint32_t *out_mask)
+{
+    const size_t esz = dtype == ORC_DTYPE_F32 ? 4 : 2;
+    const int W = (N + 31) / 32;
+    int *g = (int *)malloc(sizeof(int) * (size_t)(N + 1));
+    int *acc = (int *)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
+    int *depth = (int *)malloc(sizeof(int) * (size_t)(N > 0 ? N : 1));
+    int *walk = (int *)malloc(sizeof(int) * (size_t)(N + 1));
+    if (!g || !acc || !depth || !walk) {
+        free(g); free(acc); free(depth); free(walk);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        const char *tb = (const char *)target + (size_t)b * (size_t)(N + 1) * V * esz;
+        const int32_t *tok = tree_tokens + (size_t)b * N;
+        const int32_t *par = parent_idx + (size_t)b * N;
+        int32_t *path = out_path + (size_t)b * (size_t)(N + 1);
+        uint32_t *mask = out_mask + (size_t)b * (size_t)N * W;
+        for (int j = 0; j <= N; ++j)
+            path[j] = -1;
+        for (size_t w = 0; w < (size_t)N * W; ++w)
+            mask[w] = 0;
+        int bad = 0;
+        for (int rr = 0; rr <= N && !bad; ++rr)
+            bad = row_is_bad(tb + (size_t)rr * V * esz, dtype, V);
+        for (int i = 0; i < N && !bad; ++i)
+            bad = par[i] < -1 || par[i] >= i || tok[i] < 0 || tok[i] >= V;
+        if (bad) {
+            out_len[b] = -1;
+            continue;
+        }
+        for (int rr = 0; rr <= N; ++rr)
+            g[rr] = row_argmax(tb + (size_t)rr * V * esz, dtype, V);
+        /* acceptance and depth of every node by walking its ancestors */
+        for (int i = 0; i < N; ++i) {
+            int ok = 1, d = 0;
+            for (int node = i; node != -1; node = par[node]) {
+                int prow = par[node] + 1; /* parent -1 (root) uses row 0 */
+                if (tok[node] != g[prow])
+                    ok = 0;
+                d += 1;
+            }
+            acc[i] = ok;
+            depth[i] = d;
+        }
+        int best = -1, best_depth = 0;
+        for (int i = 0; i < N; ++i)
+            if (acc[i] && depth[i] > best_depth) {
+                best = i;
+                best_depth = depth[i];
+            }
+        /* path tokens root -> best, then the bonus token */
+        int len = 0;
+        for (int node = best; node != -1; node = par[node])
+            walk[len++] = node;
+        for (int k = 0; k < len; ++k)
+            path[k] = tok[walk[len - 1 - k]];
+        path[len] = g[best + 1];
+        out_len[b] = len + 1;
+        /* ancestor mask */
+        for (int i = 0; i < N; ++i)
+            for (int node = i; node != -1; node = par[node])
+                mask[(size_t)i * W + (size_t)(node / 32)] |= 1u << (node % 32);
+    }
+    free(g); free(acc); free(depth); free(walk);
+    return 0;
+}

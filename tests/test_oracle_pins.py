@@ -1,0 +1,433 @@
+"""Pins of the fp64 CPU oracle against what the pages and mathematics fix.
+
+Every test here runs on the CPU (no GPU marker).  None of them re-types the
+oracle's own formula: each compares the oracle with an independent library
+routine (numpy's Philox, torch's log_softmax / argmax, numpy's searchsorted),
+with a closed form printed on the pages, with brute-force enumeration, or with
+a statistical property (acceptance rate, losslessness) that a dropped term, a
+swapped p/q, a wrong row index or a wrong sign would break.
+"""
+import itertools
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+U64 = 2**64 - 1
+
+
+# --------------------------------------------------------------------------
+# Philox-4x64-10 and the uniform draws
+# --------------------------------------------------------------------------
+def _numpy_block(counter, key):
+    """numpy's Philox increments its 256-bit counter before each block, so the
+    block for counter c comes from a generator started at c - 1."""
+    c = [int(x) for x in counter]
+    # subtract one with borrow across the four 64-bit words
+    for i in range(4):
+        if c[i] > 0:
+            c[i] -= 1
+            break
+        c[i] = U64
+    g = np.random.Philox(key=np.array(key, dtype=np.uint64),
+                         counter=np.array(c, dtype=np.uint64))
+    return g.random_raw(4)
+
+
+@pytest.mark.parametrize("case", range(12))
+def test_philox_matches_numpy(case):
+    rng = np.random.default_rng(case)
+    counter = rng.integers(0, 2**63, size=4, dtype=np.uint64)
+    key = rng.integers(0, 2**63, size=2, dtype=np.uint64)
+    if case == 0:
+        counter[:] = 0
+        key[:] = 0
+    if case == 1:
+        counter[:] = np.uint64(U64)
+        key[:] = np.uint64(U64)
+    ours = oracle.philox4x64_10(counter, key)
+    assert np.array_equal(ours, _numpy_block(counter, key))
+
+
+def test_uniform_uses_counter_layout_and_is_odd_multiple():
+    key_hi = 0x5350454356455249
+    for seed, b, pos, stream in [(0, 0, 0, 0), (7, 3, 2, 1), (2**40 + 5, 255, 7, 0)]:
+        u = oracle.uniform(seed, b, pos, stream)
+        r0 = int(_numpy_block([b, pos, stream, 0], [seed, key_hi])[0])
+        k = u * 2**24
+        assert k == int(k) and int(k) % 2 == 1
+        assert int(k) // 2 == r0 >> 41
+        assert 0.0 < u < 1.0
+
+
+def test_uniform_distribution_ks():
+    from scipy import stats
+    us = np.array([oracle.uniform(11, b, 0, 0) for b in range(20000)])
+    assert stats.kstest(us, "uniform").pvalue > 1e-3
+    # streams and positions are different draws
+    assert oracle.uniform(11, 0, 0, 0) != oracle.uniform(11, 0, 0, 1)
+    assert oracle.uniform(11, 0, 0, 0) != oracle.uniform(11, 0, 1, 0)
+
+
+# --------------------------------------------------------------------------
+# temperature softmax statistics and the gather
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype,tau", [(torch.float32, 1.0), (torch.bfloat16, 0.7),
+                                       (torch.float32, 2.5)])
+def test_row_stats_match_torch_logsumexp(dtype, tau):
+    g = torch.Generator().manual_seed(3)
+    B, K, V = 3, 3, 257
+    target = (4 * torch.randn(B, K + 1, V, generator=g)).to(dtype)
+    draft = (4 * torch.randn(B, K, V, generator=g)).to(dtype)
+    tokens = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    out = oracle.spec_verify(target, draft, tokens, tau, 5)
+    rows = torch.cat([target, draft], dim=1).double() / tau  # (B, 2K+1, V)
+    lse = torch.logsumexp(rows, dim=-1).numpy()
+    rmax = rows.max(dim=-1).values.numpy()
+    np.testing.assert_allclose(out["row_logmax"], rmax, rtol=0, atol=0)
+    np.testing.assert_allclose(out["row_logmax"] + np.log(out["row_sum"]), lse,
+                               rtol=1e-13, atol=1e-12)
+    logp = torch.log_softmax(target.double() / tau, dim=-1)
+    logq = torch.log_softmax(draft.double() / tau, dim=-1)
+    for b in range(B):
+        for i in range(out["n"][b] + 1 if out["n"][b] < K else K):
+            x = int(tokens[b, i])
+            assert out["px"][b, i] == pytest.approx(math.exp(logp[b, i, x]), rel=1e-12)
+            assert out["qx"][b, i] == pytest.approx(math.exp(logq[b, i, x]), rel=1e-12)
+
+
+def _simple_rows(p_rows, q_rows):
+    """fp32 logits whose softmax is (up to fp32 rounding of the logs) the given
+    probabilities; zero probabilities become -inf logits.  Returns the logits
+    and the exact probabilities those fp32 logits define (torch, fp64)."""
+    def logits(P):
+        P = np.asarray(P, dtype=np.float64)
+        with np.errstate(divide="ignore"):
+            return torch.from_numpy(np.log(P).astype(np.float32))
+    t = logits(p_rows)
+    d = logits(q_rows)
+    return t, d, torch.softmax(t.double(), -1).numpy(), torch.softmax(d.double(), -1).numpy()
+
+
+# --------------------------------------------------------------------------
+# acceptance: alpha = E(min(p, q)), q == p, p(x) = 0
+# --------------------------------------------------------------------------
+def test_acceptance_rate_is_sum_of_min():
+    """Page 2, 'How much speedup to expect': alpha = E(min(p, q)).  With x ~ q
+    the acceptance frequency at position 0 must equal sum_x min(p(x), q(x))."""
+    p0 = [0.5, 0.2, 0.2, 0.1]
+    q0 = [0.1, 0.6, 0.2, 0.1]
+    t, d, P, Q = _simple_rows([p0, p0], [q0])
+    alpha = np.minimum(P[0], Q[0]).sum()
+    n_rep = 200000
+    rng = np.random.default_rng(1)
+    x = rng.choice(4, size=(n_rep, 1), p=Q[0]).astype(np.int32)
+    out = oracle.spec_verify(t, d, x, 1.0, 99, broadcast=True, n_seq=n_rep)
+    acc = (out["n"] >= 1).mean()
+    sigma = math.sqrt(alpha * (1 - alpha) / n_rep)
+    assert abs(acc - alpha) < 5 * sigma
+    # the swapped ratio q/p would give a different rate here
+    swapped = (Q[0] * np.minimum(1, Q[0] / P[0])).sum()
+    assert abs(swapped - alpha) > 20 * sigma
+
+
+def test_identical_draft_accepts_everything():
+    """q == p: min(1, p/q) = 1, so every drafted token is kept and the bonus
+    token is drawn from p_K."""
+    g = torch.Generator().manual_seed(4)
+    K, V = 4, 50
+    target = 3 * torch.randn(1, K + 1, V, generator=g)
+    draft = target[:, :K].clone()
+    n_rep = 20000
+    x = torch.randint(0, V, (n_rep, K), generator=g, dtype=torch.int32)
+    out = oracle.spec_verify(target[0], draft[0], x, 1.0, 3, broadcast=True, n_seq=n_rep)
+    assert (out["n"] == K).all()
+    assert np.array_equal(out["tokens"][:, :K], x.numpy())
+
+
+def test_zero_target_probability_always_rejects():
+    t, d, P, Q = _simple_rows([[0.0, 0.5, 0.5], [1 / 3] * 3], [[0.5, 0.25, 0.25]])
+    x = np.zeros((5000, 1), dtype=np.int32)  # p(0) = 0 < q(0)
+    out = oracle.spec_verify(t, d, x, 1.0, 8, broadcast=True, n_seq=5000)
+    assert (out["n"] == 0).all()
+    # the replacement never lands on a token where p <= q (token 0 here)
+    assert (out["tokens"][:, 0] != 0).all()
+
+
+def test_zero_draft_probability_always_accepts():
+    t, d, P, Q = _simple_rows([[0.5, 0.5], [0.5, 0.5]], [[0.0, 1.0]])
+    x = np.zeros((1000, 1), dtype=np.int32)  # q(0) = 0 <= p(0)
+    out = oracle.spec_verify(t, d, x, 1.0, 8, broadcast=True, n_seq=1000)
+    assert (out["n"] == 1).all()
+
+
+# --------------------------------------------------------------------------
+# the residual, the inverse CDF and losslessness
+# --------------------------------------------------------------------------
+def test_replacement_token_follows_normalised_residual():
+    """After a rejection the replacement comes from max(0, p - q) / sum (page 1
+    sec. 2, page 2 'The correctness guarantee', page 3 sec. 1)."""
+    from scipy import stats
+    p0 = [0.05, 0.4, 0.3, 0.05, 0.2]
+    q0 = [0.5, 0.1, 0.2, 0.15, 0.05]
+    t, d, P, Q = _simple_rows([p0, [0.2] * 5], [q0])
+    n_rep = 300000
+    x = np.zeros((n_rep, 1), dtype=np.int32)  # p(0)/q(0) = 0.1
+    out = oracle.spec_verify(t, d, x, 1.0, 21, broadcast=True, n_seq=n_rep)
+    rej = out["n"] == 0
+    resid = np.maximum(P[0] - Q[0], 0.0)
+    resid /= resid.sum()
+    counts = np.bincount(out["tokens"][rej, 0], minlength=5)
+    expected = resid * rej.sum()
+    mask = expected > 0
+    assert counts[~mask].sum() == 0
+    assert stats.chisquare(counts[mask], expected[mask]).pvalue > 1e-4
+    # resid mass reported by the oracle is sum max(0, p - q)
+    np.testing.assert_allclose(out["resid_mass"][rej][:10],
+                               np.maximum(P[0] - Q[0], 0).sum(), rtol=1e-12)
+
+
+def test_inverse_cdf_matches_searchsorted():
+    g = torch.Generator().manual_seed(9)
+    B, K, V = 64, 3, 300
+    target = 2 * torch.randn(B, K + 1, V, generator=g, dtype=torch.float64).float()
+    draft = (target[:, :K] + torch.randn(B, K, V, generator=g)).float()
+    tokens = torch.multinomial(torch.softmax(draft.reshape(-1, V), -1), 1,
+                               generator=g).reshape(B, K).int()
+    out = oracle.spec_verify(target, draft, tokens, 1.0, 77)
+    P = torch.softmax(target.double(), -1).numpy()
+    Q = torch.softmax(draft.double(), -1).numpy()
+    checked = 0
+    for b in range(B):
+        n = out["n"][b]
+        r = np.maximum(P[b, n] - Q[b, n], 0) if n < K else P[b, K]
+        if out["sample_margin"][b] < 1e-9:
+            continue
+        j = np.searchsorted(np.cumsum(r), out["theta"][b], side="right")
+        assert out["tokens"][b, n] == j
+        assert out["theta"][b] == pytest.approx(out["w"][b] * r.sum(), rel=1e-12)
+        checked += 1
+    assert checked > 50
+
+
+def _exact_output_marginals(P, Q):
+    """Brute force over every drafted tuple x (weight prod q_i(x_i)) and both
+    branches of every acceptance test: returns M[j, v] = Pr(position j is
+    reached and emits v), from the page formulas alone (min(1, p/q),
+    normalised max(0, p - q), bonus p_K)."""
+    K = Q.shape[0]
+    V = P.shape[1]
+    M = np.zeros((K + 1, V))
+    for x in itertools.product(range(V), repeat=K):
+        w = np.prod([Q[i, x[i]] for i in range(K)])
+        if w == 0:
+            continue
+        reach = w
+        for i in range(K):
+            a = 1.0 if Q[i, x[i]] == 0 else min(1.0, P[i, x[i]] / Q[i, x[i]])
+            resid = np.maximum(P[i] - Q[i], 0)
+            if resid.sum() > 0:
+                M[i] += reach * (1 - a) * resid / resid.sum()
+            M[i, x[i]] += reach * a
+            reach *= a
+        M[K] += reach * P[K]
+    return M
+
+
+def test_brute_force_enumeration_is_lossless():
+    rng = np.random.default_rng(5)
+    for K, V in [(1, 3), (2, 3), (3, 4)]:
+        P = rng.dirichlet(np.ones(V), size=K + 1)
+        Q = rng.dirichlet(np.ones(V), size=K)
+        M = _exact_output_marginals(P, Q)
+        reach = M.sum(axis=1, keepdims=True)
+        np.testing.assert_allclose(M / reach, P, atol=1e-12)
+
+
+@pytest.mark.parametrize("K,V,seed", [(1, 4, 1), (2, 6, 2), (3, 8, 3)])
+def test_chi_square_losslessness(K, V, seed):
+    """For every position j, the emitted token given that j was reached follows
+    p_j (page 1 sec. 2, page 2 'The correctness guarantee', page 4 sec. 2).
+    10^6 replicates, drafts drawn from q with numpy."""
+    from scipy import stats
+    g = torch.Generator().manual_seed(seed)
+    target = (2 * torch.randn(K + 1, V, generator=g)).float()
+    draft = (target[:K] + 1.5 * torch.randn(K, V, generator=g)).float()
+    P = torch.softmax(target.double(), -1).numpy()
+    Q = torch.softmax(draft.double(), -1).numpy()
+    n_rep = 1000000
+    rng = np.random.default_rng(seed)
+    x = np.stack([rng.choice(V, size=n_rep, p=Q[i]) for i in range(K)], axis=1).astype(np.int32)
+    out = oracle.spec_verify(target, draft, x, 1.0, 1000 + seed, broadcast=True, n_seq=n_rep)
+    M = _exact_output_marginals(P, Q)
+    for j in range(K + 1):
+        reached = out["n"] >= j
+        counts = np.bincount(out["tokens"][reached, j], minlength=V)
+        assert stats.chisquare(counts, P[j] * reached.sum()).pvalue > 1e-4
+        # how often position j is reached matches the enumeration
+        pr = M[j].sum()
+        sig = math.sqrt(pr * (1 - pr) / n_rep) + 1e-12
+        assert abs(reached.mean() - pr) < 5 * sig
+
+
+def test_expected_tokens_closed_form_and_page_example():
+    """Page 2: E[tokens] = (1 - alpha^(gamma+1)) / (1 - alpha); worked example
+    0.7 -> about 2.8, 0.9 -> about 4.1 for gamma = 4 (tests/golden)."""
+    rows = [ln.split() for ln in open(os.path.join(GOLDEN, "expected_tokens.txt"))
+            if ln.strip() and not ln.startswith("#")]
+    for a_s, g_s, printed in rows:
+        alpha, gamma = float(a_s), int(g_s)
+        closed = (1 - alpha ** (gamma + 1)) / (1 - alpha)
+        assert abs(closed - float(printed)) <= 0.05
+        # rows with a fixed per-position acceptance alpha: q = (1, 0),
+        # p = (alpha, 1 - alpha), so x = 0 is accepted with probability alpha
+        t, d, P, Q = _simple_rows([[alpha, 1 - alpha]] * (gamma + 1), [[1.0, 0.0]] * gamma)
+        a = P[0, 0]
+        n_rep = 400000
+        x = np.zeros((n_rep, gamma), dtype=np.int32)
+        out = oracle.spec_verify(t, d, x, 1.0, 31, broadcast=True, n_seq=n_rep)
+        tokens_per_iter = out["n"] + 1
+        mean = tokens_per_iter.mean()
+        expect = (1 - a ** (gamma + 1)) / (1 - a)
+        assert abs(mean - expect) < 5 * tokens_per_iter.std() / math.sqrt(n_rep)
+
+
+# --------------------------------------------------------------------------
+# temperature, greedy, bad data
+# --------------------------------------------------------------------------
+def test_temperature_divides_both_models():
+    """Scaling logits and temperature together changes nothing."""
+    g = torch.Generator().manual_seed(12)
+    B, K, V = 8, 3, 64
+    target = torch.randn(B, K + 1, V, generator=g)
+    draft = torch.randn(B, K, V, generator=g)
+    tokens = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    a = oracle.spec_verify(target, draft, tokens, 0.5, 4)
+    b = oracle.spec_verify(target * 4, draft * 4, tokens, 2.0, 4)
+    assert np.array_equal(a["tokens"], b["tokens"]) and np.array_equal(a["n"], b["n"])
+    np.testing.assert_allclose(a["px"], b["px"], rtol=1e-6, equal_nan=True)
+
+
+def test_greedy_matches_torch_argmax():
+    g = torch.Generator().manual_seed(2)
+    B, K, V = 40, 4, 1000
+    target = (4 * torch.randn(B, K + 1, V, generator=g)).to(torch.bfloat16)
+    # plant exact ties: copy the max value to a later and an earlier index
+    target[0, 0, 10] = 30.0
+    target[0, 0, 900] = 30.0
+    amax = torch.argmax(target.float(), dim=-1).int()
+    tokens = amax[:, :K].clone()
+    tokens[::3, 2] = (tokens[::3, 2] + 1) % V
+    out = oracle.spec_verify_greedy(target, tokens)
+    assert np.array_equal(out["row_argmax"], amax.numpy())
+    assert out["row_argmax"][0, 0] == 10
+    for b in range(B):
+        n = 2 if b % 3 == 0 else K
+        assert out["n"][b] == n
+        assert list(out["tokens"][b, :n]) == list(tokens[b, :n].numpy())
+        assert out["tokens"][b, n] == amax[b, n]
+        assert (out["tokens"][b, n + 1:] == -1).all()
+
+
+def test_bad_data_marks_sequence():
+    g = torch.Generator().manual_seed(6)
+    B, K, V = 5, 2, 16
+    target = torch.randn(B, K + 1, V, generator=g)
+    draft = torch.randn(B, K, V, generator=g)
+    tokens = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    target[1, 2, 3] = float("nan")
+    draft[2, 0, :] = float("-inf")
+    tokens[3, 1] = V
+    target[4, 0, 5] = float("inf")
+    out = oracle.spec_verify(target, draft, tokens, 1.0, 1)
+    assert list(out["n"]) [1:] == [-1, -1, -1, -1]
+    assert out["n"][0] >= 0
+    assert (out["tokens"][1:] == -1).all()
+    # -inf entries alone are legal (masked vocabulary)
+    target2 = target[:1].clone()
+    target2[0, :, 7] = float("-inf")
+    assert oracle.spec_verify(target2, draft[:1], tokens[:1], 1.0, 1)["n"][0] >= 0
+
+
+# --------------------------------------------------------------------------
+# tree verification
+# --------------------------------------------------------------------------
+def _ancestors_closed_form(i, j):
+    """Complete binary tree in BFS order with the root outside the node list:
+    node j is an ancestor-or-self of node i iff (j + 2) == (i + 2) >> k, k >= 0."""
+    a, b = i + 2, j + 2
+    while a >= b:
+        if a == b:
+            return True
+        a >>= 1
+    return False
+
+
+def test_tree_mask_closed_form_and_brute_force():
+    from speculative_decoding_verification_36_gb300.workloads import complete_binary_parents
+    depth = 4
+    par = complete_binary_parents(depth).numpy()
+    N = len(par)
+    assert N == 30
+    V = 8
+    target = torch.zeros(1, N + 1, V)
+    out = oracle.tree_verify_greedy(target, np.zeros((1, N), np.int32), par[None])
+    mask = out["mask"][0, :, 0]
+    for i in range(N):
+        for j in range(N):
+            bit = (int(mask[i]) >> j) & 1
+            assert bit == int(_ancestors_closed_form(i, j))
+
+
+def _paths_brute_force(par):
+    """All root-to-node paths, as node lists."""
+    paths = []
+    for i in range(len(par)):
+        p, node = [], i
+        while node != -1:
+            p.append(node)
+            node = par[node]
+        paths.append(p[::-1])
+    return paths
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_tree_path_brute_force(seed):
+    rng = np.random.default_rng(seed)
+    N, V = 25, 6
+    par = np.array([-1] + [int(rng.integers(-1, i)) for i in range(1, N)], dtype=np.int32)
+    target = torch.from_numpy(rng.normal(size=(2, N + 1, V)).astype(np.float32))
+    g = torch.argmax(target, -1).numpy()
+    tok = rng.integers(0, V, size=(2, N)).astype(np.int32)
+    # make roughly half the nodes match their parent's argmax
+    for b in range(2):
+        for i in range(N):
+            if rng.random() < 0.6:
+                tok[b, i] = g[b, par[i] + 1]
+    out = oracle.tree_verify_greedy(target, tok, np.stack([par, par]))
+    for b in range(2):
+        best = []
+        for p in _paths_brute_force(par):
+            if all(tok[b, node] == g[b, par[node] + 1] for node in p) and len(p) > len(best):
+                best = p
+        exp = [int(tok[b, node]) for node in best] + [int(g[b, (best[-1] + 1) if best else 0])]
+        assert out["length"][b] == len(exp)
+        assert list(out["path"][b, :len(exp)]) == exp
+        assert (out["path"][b, len(exp):] == -1).all()
+        # mask rows: ancestor-or-self from the explicit path lists
+        for i, p in enumerate(_paths_brute_force(par)):
+            words = out["mask"][b, i]
+            got = {j for j in range(N) if (int(words[j // 32]) >> (j % 32)) & 1}
+            assert got == set(p)
+
+
+def test_tree_bad_parent_is_flagged():
+    target = torch.zeros(1, 4, 5)
+    out = oracle.tree_verify_greedy(target, np.zeros((1, 3), np.int32),
+                                    np.array([[-1, 0, 2]], np.int32))
+    assert out["length"][0] == -1 and (out["path"] == -1).all() and (out["mask"] == 0).all()

@@ -1,0 +1,393 @@
+"""Benchmark of the speculative-decoding verify step on GB300.
+
+One step = one spec_verify call over a batch of the c3 workload (B=256
+sequences, K=8 drafts, V=152064, bf16 logits, temperature 0.7): temperature
+softmax of 17 rows per sequence, gather, acceptance, first-rejection scan and
+the residual / bonus draw.  Prints one JSON line (see the keys below).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
+
+With N > 1 (torchrun), every rank verifies its own batch of B sequences
+(independent sequences: weak scaling, no collective on the data path); the
+timing uses a barrier on both sides and the maximum over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+WORKLOAD = "c3"
+METRIC = "verified sequences/sec (spec_verify, HBM-roofline reported)"
+UNIT = "seq/s"
+L2_BYTES = 129 * 2**20
+FALLBACK_HBM_GBS = 6800.0
+TRAFFIC_FILE = os.path.join(ROOT, "profiles", "spec_verify_c3_traffic.txt")
+
+
+# --------------------------------------------------------------------------
+# helpers shared with the multi-rank CPU tests
+# --------------------------------------------------------------------------
+def dist_env():
+    """(rank, world_size, local_rank) from the torchrun environment."""
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def rank_seed(rank: int, step: int) -> int:
+    """Philox seed of one rank's batch at one step (independent batches)."""
+    return (rank << 32) | step
+
+
+def max_over_ranks(value: float, world: int) -> float:
+    """Maximum of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return value
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([value], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world: int):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def source_hash() -> str:
+    """sha256 over the CUDA sources (ties a stored ncu traffic figure to the
+    kernel it was measured on)."""
+    csrc = os.path.join(ROOT, "speculative_decoding_verification_36_gb300", "csrc")
+    h = hashlib.sha256()
+    for name in sorted(os.listdir(csrc)):
+        if name.endswith((".cu", ".cuh", ".h")):
+            h.update(name.encode())
+            h.update(open(os.path.join(csrc, name), "rb").read())
+    return h.hexdigest()
+
+
+def stored_traffic():
+    """DRAM bytes per launch from the committed ncu summary, if it was taken
+    on the current kernel sources; else None."""
+    if not os.path.exists(TRAFFIC_FILE):
+        return None
+    kv = {}
+    for line in open(TRAFFIC_FILE):
+        if ":" in line and not line.startswith("#"):
+            k, v = line.split(":", 1)
+            kv[k.strip()] = v.strip()
+    if kv.get("source_sha256") != source_hash():
+        return None
+    try:
+        return float(kv["dram_bytes_per_launch"])
+    except (KeyError, ValueError):
+        return None
+
+
+def peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return float(d["hbm_gbs"]), "measured"
+        except Exception:
+            pass
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("uuid,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, uuid: str | None):
+        self.uuid = uuid
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+
+    def __enter__(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            time.sleep(0.15)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+            self.fh.close()
+
+    def summary(self):
+        if self.proc is None or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            if self.uuid and self.uuid not in parts[0]:
+                continue
+            rows.append(parts)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        sm = [float(r[1]) for r in rows if r[1].replace(".", "").isdigit()]
+        mx = [float(r[2]) for r in rows if r[2].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in rows for i in range(4) if r[5 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": reasons,
+                "samples": len(rows)}
+
+
+# --------------------------------------------------------------------------
+# workload
+# --------------------------------------------------------------------------
+def workload_config(p, two_sets: bool):
+    return {
+        "workload": f"{p.name}: chain verify B={p.B} K={p.K} V={p.V} logits bf16 tau={p.temperature}; "
+                    "target N(0,4^2) - 1.1 ln(v+1), draft = target + N(0,2^2), drafts sampled from "
+                    "the draft softmax",
+        "B": p.B, "K": p.K, "V": p.V, "logits": "bf16", "temperature": p.temperature,
+        "bytes_per_step": algorithmic_bytes(p),
+        "l2": ("inputs larger than L2 (%.2f GB per step vs 129 MB)" % (algorithmic_bytes(p) / 1e9))
+              + ("; two input sets alternate" if two_sets else ""),
+    }
+
+
+def algorithmic_bytes(p) -> int:
+    """Logits read once (2K+1 rows of V bf16 per sequence) plus the drafted
+    tokens read and the outputs written."""
+    return p.B * (2 * p.K + 1) * p.V * 2 + p.B * p.K * 4 + p.B * (p.K + 2) * 4
+
+
+def oracle_seq_per_s(x_cpu, p, budget_s: float, max_seq: int):
+    """The fp64 oracle timed on this host's cores on a bounded sample of the
+    same inputs (sequence by sequence until the time budget is used)."""
+    import oracle
+    oracle.build()
+    done = 0
+    t0 = time.perf_counter()
+    while done < max_seq:
+        b = done % p.B
+        oracle.spec_verify(x_cpu["target"][b:b + 1], x_cpu["draft"][b:b + 1], x_cpu["tokens"][b:b + 1],
+                           p.temperature, 0, seq_ids=[b])
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    dt = time.perf_counter() - t0
+    return done / dt, done, dt
+
+
+# --------------------------------------------------------------------------
+# the two arms
+# --------------------------------------------------------------------------
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import torch
+    from speculative_decoding_verification_36_gb300 import workloads as wl
+    p = wl.preset(WORKLOAD)
+    x = wl.make_chain(wl.preset(WORKLOAD, B=8), device="cpu", seed=0)
+    import oracle
+    oracle.build()
+
+    def step(i):
+        b = i % 8
+        oracle.spec_verify(x["target"][b:b + 1], x["draft"][b:b + 1], x["tokens"][b:b + 1],
+                           p.temperature, 0, seq_ids=[b])
+
+    for i in range(args.warmup):
+        step(i)
+    t0 = time.perf_counter()
+    for i in range(args.steps):
+        step(i)
+    dt = time.perf_counter() - t0
+    value = args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * dt / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(p, False),
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": 1, "kind": "oracle",
+                         "sample": "one c3 sequence (17 rows x 152064) per step, fp64 C oracle, "
+                                   "single thread"},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_gpu(args):
+    import torch
+    rank, world, local = dist_env()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+
+    import speculative_decoding_verification_36_gb300 as sv
+    from speculative_decoding_verification_36_gb300 import build as _build
+    from speculative_decoding_verification_36_gb300 import workloads as wl
+    _build.build()
+
+    p = wl.preset(WORKLOAD)
+    sets = [wl.make_chain(p, device=dev, seed=rank * 2 + i) for i in range(2)]
+    stream = torch.cuda.current_stream(dev)
+    outs = [(torch.empty((p.B, p.K + 1), dtype=torch.int32, device=dev),
+             torch.empty((p.B,), dtype=torch.int32, device=dev)) for _ in range(2)]
+
+    def step(i):
+        x = sets[i % 2]
+        o = outs[i % 2]
+        sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, rank_seed(rank, i),
+                       out_tokens=o[0], out_n_accepted=o[1], stream=stream)
+
+    for i in range(max(args.warmup, 3)):
+        step(i)
+    torch.cuda.synchronize(dev)
+    assert sv.spec_get_status() == 0
+
+    # device-resident timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+          for _ in range(args.steps)]
+    uuid = None
+    try:
+        uuid = str(torch.cuda.get_device_properties(dev).uuid)
+    except Exception:
+        pass
+    with ClockSampler(uuid) as clk:
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            ev[i][0].record(stream)
+            step(i)
+            ev[i][1].record(stream)
+        t_end.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+    total_ms = t_start.elapsed_time(t_end)
+    per_launch = [a.elapsed_time(b) for a, b in ev]
+    total_ms = max_over_ranks(total_ms, world)
+    avg_launch_ms = max_over_ranks(sum(per_launch) / len(per_launch), world)
+    value = world * p.B * args.steps / (total_ms / 1e3)
+    flags = sv.spec_get_status()
+
+    # end to end through the public API from pinned host buffers
+    e2e_steps = max(3, min(args.steps, args.e2e_steps))
+    host = [{k: sets[i][k].cpu().pin_memory() for k in ("target", "draft", "tokens")}
+            for i in range(2)]
+    host_out = (torch.empty((p.B, p.K + 1), dtype=torch.int32).pin_memory(),
+                torch.empty((p.B,), dtype=torch.int32).pin_memory())
+    dbuf = {k: torch.empty_like(sets[0][k]) for k in ("target", "draft", "tokens")}
+    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in host[0])
+    d2h = host_out[0].numel() * 4 + host_out[1].numel() * 4
+
+    def e2e_step(i):
+        src = host[i % 2]
+        for k in dbuf:
+            dbuf[k].copy_(src[k], non_blocking=True)
+        t, n = sv.spec_verify(dbuf["target"], dbuf["draft"], dbuf["tokens"], p.temperature,
+                              rank_seed(rank, i), stream=stream)
+        host_out[0].copy_(t, non_blocking=True)
+        host_out[1].copy_(n, non_blocking=True)
+
+    e2e_step(0)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = world * p.B * e2e_steps / (e2e_ms / 1e3)
+
+    if rank != 0:
+        if world > 1:
+            import torch.distributed as dist
+            dist.destroy_process_group()
+        return 0
+
+    peak, peak_kind = peaks()
+    abytes = algorithmic_bytes(p)
+    achieved = abytes / (avg_launch_ms / 1e3) / 1e9
+    traffic = stored_traffic()
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
+        "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
+        "data": "synthetic", "config": workload_config(p, True),
+        "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
+                     "frac": achieved / peak, "traffic": traffic,
+                     "kernel": "sv::sample_kernel<BF16,8>",
+                     "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"
+                     if peak_kind == "measured" else "fallback 6.8 TB/s",
+                     "avg_launch_ms": avg_launch_ms, "bytes_per_launch": abytes},
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "gpu_launches": args.steps,
+        "clocks": clk.summary(),
+        "status_flags": flags,
+    }
+    if world == 1 and not args.no_cpu_baseline:
+        x_cpu = {k: sets[0][k][:64].cpu() for k in ("target", "draft", "tokens")}
+        pp = wl.preset(WORKLOAD, B=64)
+        v, done, dt = oracle_seq_per_s(x_cpu, pp, args.cpu_budget, 64)
+        line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
+                                "sample": f"{done} c3 sequences in {dt:.1f} s, fp64 C oracle, "
+                                          "single thread"}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args(argv)
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_gpu(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

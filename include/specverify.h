@@ -1,0 +1,182 @@
+/*
+ * specverify.h -- C ABI of the GB300 speculative-decoding verify library
+ * (libspecverify.so, CUDA kernels for sm_103a).
+ *
+ * The verify step compares K drafted tokens with the target model's
+ * distributions and emits between 1 and K+1 tokens per sequence:
+ *
+ *   "Speculative Decoding & Draft Model Topologies: Slashing Enterprise LLM
+ *   Latency by 3.5x in 2026", sec. 2 (Mathematical Foundation: Speculative
+ *   Verification & Rejection Sampling): accept x with probability
+ *   min(1, p(x)/q(x)) using u ~ U(0,1); on rejection discard x and every later
+ *   draft and resample from max(0, p - q) / sum max(0, p - q).
+ *   "Speculative Decoding for LLM Inference: How Draft-and-Verify Accelerates
+ *   Token Generation", sections "The draft-and-verify loop" (longest accepted
+ *   prefix, one resampled token, one bonus token when every draft is accepted)
+ *   and "The correctness guarantee".
+ *   "Speculative Decoding at Scale: Latency Reduction in Distributed LLM
+ *   Serving", sequence diagram (greedy form: accept matching tokens, reject the
+ *   first mismatch, plus one bonus token) and sec. 1 (relu(P - Q) residual).
+ *   "Speculative Decoding in Production: How Small Draft Models & Medusa Heads
+ *   Deliver 2x-3x LLM Speedups Without Accuracy Loss", sec. 2 (P_accept) and
+ *   sec. 4 (SpecInfer candidate trees verified under a 2D causal mask).
+ *
+ * Conventions shared by every entry point
+ *   - All array arguments are DEVICE pointers to contiguous row-major memory
+ *     owned by the caller.  The library keeps no reference after the call.
+ *   - Calls are asynchronous and ordered on `stream` (0 = legacy default
+ *     stream).  Per-call scratch memory comes from a library-owned,
+ *     stream-ordered CUDA memory pool on the current device and is returned on
+ *     the same stream.
+ *   - bf16 logits are passed as their raw 16-bit patterns (uint16_t).
+ *   - Logits may be -inf (masked vocabulary).  A row containing NaN or +inf,
+ *     a row with no finite entry, a drafted token outside [0, V), or a tree
+ *     parent index outside [-1, i) is bad data: that sequence's count is -1,
+ *     every one of its output tokens is -1 (tree: mask words 0), and bit
+ *     SPEC_FLAG_BAD_DATA is set in the device status word (spec_get_status).
+ *     The call itself still returns SPEC_OK and never traps.
+ *   - Return codes: SPEC_OK, or a negative SPEC_ERR_* from host-side checks
+ *     (nothing is launched) or from the CUDA runtime.
+ *   - Results are deterministic: the same inputs and seed give bit-identical
+ *     outputs on every run.
+ */
+#ifndef SPECVERIFY_H
+#define SPECVERIFY_H
+
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define SPEC_OK 0
+#define SPEC_ERR_NULL (-1)        /* a required pointer is NULL */
+#define SPEC_ERR_SHAPE (-2)       /* B < 0, K outside [0, 255], V < 1, N outside [0, 1024], or size overflow */
+#define SPEC_ERR_TEMPERATURE (-3) /* temperature NaN, negative, or in (0, 1e-30) */
+#define SPEC_ERR_CUDA (-4)        /* CUDA runtime error; spec_status_string(-4) gives the message */
+
+#define SPEC_FLAG_BAD_DATA 1u     /* some sequence had bad data (see above) */
+#define SPEC_FLAG_TIMEOUT 2u      /* an internal bounded wait ran out; outputs of that call are invalid */
+
+/*
+ * Speculative-sampling verification of B independent sequences.
+ *
+ *   target_logits  [B, K+1, V]  target row i scores draft position i; row K is
+ *                               the bonus row.
+ *   draft_logits   [B, K, V]    draft row i is the distribution x_i was drawn
+ *                               from.  May be NULL when temperature == 0 or K == 0.
+ *   draft_tokens   [B, K]       int32 drafted ids x_i.  May be NULL when K == 0.
+ *   temperature    tau > 0: p = softmax(target / tau), q = softmax(draft / tau)
+ *                  (the same tau divides both).  tau == 0 selects greedy
+ *                  verification: x_i is accepted while it equals the lowest-id
+ *                  argmax g_i of target row i; the token after the accepted
+ *                  prefix is g_n; draft_logits is not read.
+ *   seed           64-bit Philox-4x64-10 key word.  Position i's acceptance
+ *                  uniform uses counter (b, i, 0, 0), the resampling uniform
+ *                  counter (b, n, 1, 0); key (seed, 0x5350454356455249).  The
+ *                  first output word r gives u = (2 (r >> 41) + 1) 2^-24.
+ *   out_tokens     [B, K+1] int32: x_0 .. x_{n-1}, then the resampled (n < K)
+ *                  or bonus (n == K) token, then -1 padding.
+ *   out_n_accepted [B] int32: n in [0, K], or -1 for bad data.
+ *
+ * Acceptance: x_i is kept iff q_i(x_i) == 0 or u_i < p_i(x_i) / q_i(x_i).
+ * n is the first rejected position (K if none).  The emitted token at n is the
+ * smallest id j whose running sum (vocabulary order) of the weights exceeds
+ * w * (total weight), w the resampling uniform; the weights are
+ * max(0, p_n - q_n) when n < K and p_K when n == K (p_n when a rejection left
+ * no positive residual through rounding).
+ * B == 0 is a no-op.  Sizes: K <= 255, (K+1) * V and B * (K+1) * V must fit in
+ * 62 bits.
+ */
+int spec_verify_f32(const float *target_logits, const float *draft_logits,
+                    const int32_t *draft_tokens, int B, int K, int V, float temperature,
+                    uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
+                    cudaStream_t stream);
+int spec_verify_bf16(const uint16_t *target_logits, const uint16_t *draft_logits,
+                     const int32_t *draft_tokens, int B, int K, int V, float temperature,
+                     uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
+                     cudaStream_t stream);
+
+/*
+ * spec_verify_* plus the verify step's intermediate probabilities, for
+ * checking against a reference.  Same arguments, then (each may be NULL):
+ *   out_row_stats  [B, 2K+1, 2] float: for target rows 0..K then draft rows
+ *                  0..K-1, max_v z_v / tau and sum_v exp(z_v / tau - max).
+ *                  (tau == 0: not written.)
+ *   out_pq         [B, K, 2] float: p_i(x_i), q_i(x_i) for every position.
+ *   out_resid_mass [B] float: total mass of the distribution the token at n
+ *                  was drawn from (sum max(0, p_n - q_n), or about 1 for the
+ *                  bonus row).
+ * With temperature == 0 the extra outputs are not written (the greedy argmax
+ * of every target row comes from spec_verify_greedy_argmax_*).
+ */
+int spec_verify_stats_f32(const float *target_logits, const float *draft_logits,
+                          const int32_t *draft_tokens, int B, int K, int V, float temperature,
+                          uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
+                          float *out_row_stats, float *out_pq, float *out_resid_mass,
+                          cudaStream_t stream);
+int spec_verify_stats_bf16(const uint16_t *target_logits, const uint16_t *draft_logits,
+                           const int32_t *draft_tokens, int B, int K, int V, float temperature,
+                           uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
+                           float *out_row_stats, float *out_pq, float *out_resid_mass,
+                           cudaStream_t stream);
+
+/*
+ * Greedy verification (temperature 0) that also writes the lowest-id argmax of
+ * every target row: out_row_argmax [B, K+1] int32 (-1 for an unusable row).
+ */
+int spec_verify_greedy_argmax_f32(const float *target_logits, const int32_t *draft_tokens,
+                                  int B, int K, int V, int32_t *out_tokens,
+                                  int32_t *out_n_accepted, int32_t *out_row_argmax,
+                                  cudaStream_t stream);
+int spec_verify_greedy_argmax_bf16(const uint16_t *target_logits, const int32_t *draft_tokens,
+                                   int B, int K, int V, int32_t *out_tokens,
+                                   int32_t *out_n_accepted, int32_t *out_row_argmax,
+                                   cudaStream_t stream);
+
+/*
+ * Greedy verification of a candidate tree per sequence (SpecInfer-style).
+ *
+ *   target_logits [B, N+1, V]  row 0: the root's next-token row; row i+1: node i.
+ *   tree_tokens   [B, N] int32 the candidate token of node i.
+ *   parent_idx    [B, N] int32 parent of node i, -1 for a child of the root;
+ *                              parents precede children (parent_idx[i] < i).
+ *   out_path      [B, N+1] int32: tokens of the accepted path from the root's
+ *                 child down to the deepest accepted node, then the bonus
+ *                 token (argmax of that node's row; of row 0 when no node is
+ *                 accepted), then -1 padding.
+ *   out_len       [B] int32: path length + 1, or -1 for bad data.
+ *   out_mask      [B, N, ceil(N/32)] uint32: bit j of word j/32 in row i is set
+ *                 iff j == i or node j is an ancestor of node i (the 2D tree
+ *                 attention mask; it depends only on parent_idx).
+ * Node i is accepted iff its parent is accepted (the root always is) and its
+ * token equals the lowest-id argmax of its parent's row; the deepest accepted
+ * node wins, the lowest node index on ties.  N <= 1024.  N == 0 emits the
+ * bonus token of row 0 only.
+ */
+int spec_tree_verify_greedy_f32(const float *target_logits, const int32_t *tree_tokens,
+                                const int32_t *parent_idx, int B, int N, int V,
+                                int32_t *out_path, int32_t *out_len, uint32_t *out_mask,
+                                cudaStream_t stream);
+int spec_tree_verify_greedy_bf16(const uint16_t *target_logits, const int32_t *tree_tokens,
+                                 const int32_t *parent_idx, int B, int N, int V,
+                                 int32_t *out_path, int32_t *out_len, uint32_t *out_mask,
+                                 cudaStream_t stream);
+
+/*
+ * Synchronises `stream`, then returns in *flags_out (may be NULL) the device
+ * status word of the current device (an OR of SPEC_FLAG_* set by every call
+ * since the last read) and clears it.  Returns SPEC_OK or SPEC_ERR_CUDA.
+ */
+int spec_get_status(cudaStream_t stream, uint32_t *flags_out);
+
+/* Static description of a return code; for SPEC_ERR_CUDA the message of the
+ * calling thread's most recent CUDA error. */
+const char *spec_status_string(int code);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SPECVERIFY_H */

@@ -56,7 +56,7 @@ def _load():
     lib.oracle_philox4x64_10.restype = None
     lib.oracle_uniform.argtypes = [u64, u64, u64, u64]
     lib.oracle_uniform.restype = f64
-    lib.oracle_spec_verify.argtypes = [P, P, i32, i64, i64, P, i64, i32, i32, i32, f64, u64,
+    lib.oracle_spec_verify.argtypes = [P, P, i32, i64, i64, P, i64, i32, i32, i32, f64, u64, P,
                                        P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.oracle_spec_verify.restype = i32
     lib.oracle_spec_verify_greedy.argtypes = [P, i32, i64, P, i64, i32, i32, i32, P, P, P]
@@ -121,13 +121,15 @@ def uniform(seed: int, b: int, position: int, stream: int) -> float:
 
 
 def spec_verify(target, draft, draft_tokens, temperature: float, seed: int,
-                broadcast: bool = False, n_seq: int | None = None):
+                broadcast: bool = False, n_seq: int | None = None, seq_ids=None):
     """Speculative-sampling verification of a batch (temperature > 0).
 
     target: [B, K+1, V]; draft: [B, K, V]; draft_tokens: [B, K].  With
     ``broadcast=True`` target/draft hold ONE sequence ([K+1, V], [K, V]) that
     is shared by all ``n_seq`` batch entries (each entry still draws its own
-    uniforms through its batch index).  Returns a dict of numpy arrays:
+    uniforms through its batch index).  ``seq_ids`` (optional, [B]) gives the
+    sequence number each batch entry draws its uniforms with, so that a subset
+    of a larger batch reproduces that batch's draws.  Returns a dict of numpy arrays:
     tokens [B, K+1], n [B] and the per-sequence diagnostics documented in
     spec_oracle.c.
     """
@@ -162,9 +164,15 @@ def spec_verify(target, draft, draft_tokens, temperature: float, seed: int,
     # keep a valid pointer even when K == 0 (empty draft array)
     d_buf = d if d.size else np.zeros(1, dtype=d.dtype)
     x_buf = x if x.size else np.zeros(1, dtype=np.int32)
+    ids = None
+    if seq_ids is not None:
+        ids = np.ascontiguousarray(np.asarray(seq_ids, dtype=np.int64).reshape(-1))
+        if ids.shape[0] != B:
+            raise ValueError("seq_ids must have one entry per sequence")
     rc = lib.oracle_spec_verify(
         _ptr(t), _ptr(d_buf), dt, t_stride, d_stride, _ptr(x_buf), tok_stride,
         B, K, V, float(temperature), int(seed) & (2**64 - 1),
+        _ptr(ids) if ids is not None else None,
         _ptr(out["tokens"]), _ptr(out["n"]), _ptr(out["row_logmax"]), _ptr(out["row_sum"]),
         _ptr(out["px"]), _ptr(out["qx"]), _ptr(out["u"]), _ptr(out["acc_margin"]),
         _ptr(out["resid_mass"]), _ptr(out["theta"]), _ptr(out["w"]),

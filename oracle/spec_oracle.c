@@ -194,6 +194,9 @@ static int inverse_cdf(const double *r, int V, double theta, double *dist_out)
  * draft:  B x K x V logits, sequence b at draft + b * d_stride_b elements
  *         (a stride of 0 broadcasts one sequence to every b);
  * tokens: B x K drafted ids (row stride K);
+ * seq_ids: optional B sequence numbers used as the Philox sequence counter
+ *         (NULL: the batch index b), so that a subset of a batch can be
+ *         verified with the uniforms the whole batch would draw;
  * out_tokens: B x (K+1), out_n: B.
  *
  * Optional diagnostics (each may be NULL):
@@ -212,6 +215,7 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype,
                        long long t_stride_b, long long d_stride_b,
                        const int32_t *tokens, long long tok_stride_b,
                        int B, int K, int V, double tau, uint64_t seed,
+                       const long long *seq_ids,
                        int32_t *out_tokens, int32_t *out_n,
                        double *row_logmax, double *row_sum,
                        double *px_out, double *qx_out, double *u_out, double *acc_margin,
@@ -231,6 +235,7 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype,
         const char *tb = (const char *)target + (size_t)((long long)b * t_stride_b) * esz;
         const char *db = (const char *)draft + (size_t)((long long)b * d_stride_b) * esz;
         const int32_t *x = tokens + (long long)b * tok_stride_b;
+        const uint64_t seq = seq_ids ? (uint64_t)seq_ids[b] : (uint64_t)b;
         int32_t *out = out_tokens + (size_t)b * (size_t)(K + 1);
         for (int j = 0; j <= K; ++j)
             out[j] = -1;
@@ -278,7 +283,7 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype,
         for (int i = 0; i < K; ++i) {
             double p = p_rows[(size_t)i * V + x[i]];
             double q = q_rows[(size_t)i * V + x[i]];
-            double u = oracle_uniform(seed, (uint64_t)b, (uint64_t)i, 0);
+            double u = oracle_uniform(seed, seq, (uint64_t)i, 0);
             double alpha = q > 0.0 ? fmin(1.0, p / q) : 1.0;
             if (px_out) {
                 px_out[(size_t)b * K + i] = p;
@@ -318,7 +323,7 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype,
         }
 
         /* step 6: inverse-CDF draw with the stream-1 uniform */
-        double w = oracle_uniform(seed, (uint64_t)b, (uint64_t)n, 1);
+        double w = oracle_uniform(seed, seq, (uint64_t)n, 1);
         double theta = w * Z;
         double dist;
         int j = inverse_cdf(r, V, theta, &dist);

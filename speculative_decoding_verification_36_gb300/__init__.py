@@ -1,0 +1,184 @@
+"""GB300-native speculative-decoding verify step.
+
+A thin binding over libspecverify.so (C ABI in include/specverify.h).  Each
+function checks and marshals torch CUDA tensors (device, dtype, contiguity,
+shapes), allocates outputs that were not given, and calls the C entry point of
+the same name on the current stream; every step of the verify path runs in the
+library's CUDA kernels.  There is no CPU fallback.
+
+    spec_verify(target_logits, draft_logits, draft_tokens, temperature, seed)
+    spec_verify_stats(...)            # plus row statistics, p(x), q(x), mass
+    spec_verify_greedy_argmax(...)    # greedy chain plus every row's argmax
+    spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx)
+    spec_get_status()                 # device status word (bad data, timeouts)
+"""
+from __future__ import annotations
+
+import torch
+
+from . import _lib
+from ._lib import SPEC_FLAG_BAD_DATA, SPEC_FLAG_TIMEOUT, SpecError
+
+__all__ = [
+    "spec_verify", "spec_verify_stats", "spec_verify_greedy_argmax",
+    "spec_tree_verify_greedy", "spec_get_status", "SpecError",
+    "SPEC_FLAG_BAD_DATA", "SPEC_FLAG_TIMEOUT",
+]
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    if isinstance(stream, torch.cuda.Stream):
+        return stream.cuda_stream
+    return int(stream)
+
+
+def _is_bf16(t: torch.Tensor, name: str) -> bool:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if t.dtype == torch.bfloat16:
+        return True
+    if t.dtype == torch.float32:
+        return False
+    raise TypeError(f"{name} must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t):
+    if t is None or t.numel() == 0:
+        return None
+    return t.data_ptr()
+
+
+def _i32(t: torch.Tensor, shape, name: str):
+    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
+    if tuple(t.shape) != tuple(shape):
+        raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    return t
+
+
+def _out(t, shape, dtype, device, name):
+    if t is None:
+        return torch.empty(shape, dtype=dtype, device=device)
+    if t.dtype != dtype or not t.is_contiguous() or tuple(t.shape) != tuple(shape) or t.device != device:
+        raise ValueError(f"{name} must be a contiguous {dtype} tensor of shape {tuple(shape)} on {device}")
+    return t
+
+
+def _chain_args(target_logits, draft_logits, draft_tokens, temperature):
+    bf16 = _is_bf16(target_logits, "target_logits")
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, K+1, V]")
+    B, K1, V = target_logits.shape
+    K = K1 - 1
+    if temperature > 0 and K > 0:
+        if draft_logits is None:
+            raise ValueError("draft_logits is required when temperature > 0")
+        if _is_bf16(draft_logits, "draft_logits") != bf16:
+            raise TypeError("target_logits and draft_logits must share a dtype")
+        if tuple(draft_logits.shape) != (B, K, V):
+            raise ValueError(f"draft_logits has shape {tuple(draft_logits.shape)}, expected {(B, K, V)}")
+    if K > 0:
+        _i32(draft_tokens, (B, K), "draft_tokens")
+    return bf16, B, K, V
+
+
+def spec_verify(target_logits, draft_logits, draft_tokens, temperature: float, seed: int,
+                out_tokens=None, out_n_accepted=None, stream=None):
+    """Verify K drafted tokens per sequence; returns (out_tokens [B,K+1], n [B])."""
+    bf16, B, K, V = _chain_args(target_logits, draft_logits, draft_tokens, temperature)
+    dev = target_logits.device
+    out_tokens = _out(out_tokens, (B, K + 1), torch.int32, dev, "out_tokens")
+    out_n_accepted = _out(out_n_accepted, (B,), torch.int32, dev, "out_n_accepted")
+    lib = _lib.load()
+    fn = lib.spec_verify_bf16 if bf16 else lib.spec_verify_f32
+    with torch.cuda.device(dev):
+        _lib.check(fn(_ptr(target_logits), _ptr(draft_logits) if temperature > 0 else None,
+                      _ptr(draft_tokens) if K > 0 else None, B, K, V, float(temperature),
+                      int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
+                      _stream(stream)))
+    return out_tokens, out_n_accepted
+
+
+def spec_verify_stats(target_logits, draft_logits, draft_tokens, temperature: float, seed: int,
+                      stream=None):
+    """spec_verify plus the intermediate probabilities (temperature > 0).
+
+    Returns dict(tokens [B,K+1], n [B], row_stats [B,2K+1,2] (max z/tau, sum
+    exp(z/tau - max)), pq [B,K,2] (p_i(x_i), q_i(x_i)), resid_mass [B])."""
+    if not temperature > 0:
+        raise ValueError("spec_verify_stats needs temperature > 0")
+    bf16, B, K, V = _chain_args(target_logits, draft_logits, draft_tokens, temperature)
+    dev = target_logits.device
+    tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    n = torch.empty((B,), dtype=torch.int32, device=dev)
+    row_stats = torch.empty((B, 2 * K + 1, 2), dtype=torch.float32, device=dev)
+    pq = torch.empty((B, K, 2), dtype=torch.float32, device=dev)
+    resid = torch.empty((B,), dtype=torch.float32, device=dev)
+    lib = _lib.load()
+    fn = lib.spec_verify_stats_bf16 if bf16 else lib.spec_verify_stats_f32
+    with torch.cuda.device(dev):
+        _lib.check(fn(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens) if K > 0 else None,
+                      B, K, V, float(temperature), int(seed) & (2**64 - 1), _ptr(tokens), _ptr(n),
+                      _ptr(row_stats), _ptr(pq), _ptr(resid), _stream(stream)))
+    return dict(tokens=tokens, n=n, row_stats=row_stats, pq=pq, resid_mass=resid)
+
+
+def spec_verify_greedy_argmax(target_logits, draft_tokens, stream=None):
+    """Greedy chain verification that also returns every target row's argmax.
+
+    Returns (out_tokens [B,K+1], n [B], row_argmax [B,K+1])."""
+    bf16, B, K, V = _chain_args(target_logits, None, draft_tokens, 0.0)
+    dev = target_logits.device
+    tokens = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    n = torch.empty((B,), dtype=torch.int32, device=dev)
+    amax = torch.empty((B, K + 1), dtype=torch.int32, device=dev)
+    lib = _lib.load()
+    fn = lib.spec_verify_greedy_argmax_bf16 if bf16 else lib.spec_verify_greedy_argmax_f32
+    with torch.cuda.device(dev):
+        _lib.check(fn(_ptr(target_logits), _ptr(draft_tokens) if K > 0 else None, B, K, V,
+                      _ptr(tokens), _ptr(n), _ptr(amax), _stream(stream)))
+    return tokens, n, amax
+
+
+def spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx, out_path=None, out_len=None,
+                            out_mask=None, stream=None):
+    """Greedy verification of a candidate tree per sequence.
+
+    target_logits [B, N+1, V]; tree_tokens, parent_idx [B, N] int32.
+    Returns (out_path [B, N+1], out_len [B], out_mask [B, N, ceil(N/32)] as int32 bits)."""
+    bf16 = _is_bf16(target_logits, "target_logits")
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, N+1, V]")
+    B, N1, V = target_logits.shape
+    N = N1 - 1
+    W = (N + 31) // 32
+    if N > 0:
+        _i32(tree_tokens, (B, N), "tree_tokens")
+        _i32(parent_idx, (B, N), "parent_idx")
+    dev = target_logits.device
+    out_path = _out(out_path, (B, N + 1), torch.int32, dev, "out_path")
+    out_len = _out(out_len, (B,), torch.int32, dev, "out_len")
+    # torch has no uint32 arithmetic on every version: the mask words travel as int32 bits
+    out_mask = _out(out_mask, (B, N, W), torch.int32, dev, "out_mask")
+    lib = _lib.load()
+    fn = lib.spec_tree_verify_greedy_bf16 if bf16 else lib.spec_tree_verify_greedy_f32
+    with torch.cuda.device(dev):
+        _lib.check(fn(_ptr(target_logits), _ptr(tree_tokens) if N > 0 else None,
+                      _ptr(parent_idx) if N > 0 else None, B, N, V, _ptr(out_path), _ptr(out_len),
+                      _ptr(out_mask), _stream(stream)))
+    return out_path, out_len, out_mask
+
+
+def spec_get_status(stream=None, device=None) -> int:
+    """Synchronise and return (then clear) the device status word: an OR of
+    SPEC_FLAG_BAD_DATA / SPEC_FLAG_TIMEOUT set since the last read."""
+    import ctypes
+    flags = ctypes.c_uint32(0)
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _lib.check(_lib.load().spec_get_status(_stream(stream), ctypes.addressof(flags)))
+    return int(flags.value)

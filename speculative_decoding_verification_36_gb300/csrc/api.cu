@@ -1,0 +1,365 @@
+// api.cu -- the C ABI of libspecverify.so (declared in include/specverify.h).
+//
+// Host-side argument checks, per-device state (SM count, occupancy, the
+// stream-ordered scratch pool, the device status word), the choice of chunk
+// length and grid, and the launches.  No verify arithmetic happens here.
+#include "specverify.h"
+#include "sv_kernels.h"
+
+#include <math.h>
+#include <stdint.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <mutex>
+
+// Sticky per-device status word (SPEC_FLAG_* bits), read and cleared by
+// spec_get_status.
+__device__ unsigned g_spec_status;
+
+namespace {
+
+struct DeviceState {
+  bool init = false;
+  int sms = 0;
+  cudaMemPool_t pool = nullptr;
+  unsigned* status = nullptr;
+  int occ_sample[2][2] = {{0, 0}, {0, 0}};  // [bf16][vec]
+  int occ_greedy[2][2] = {{0, 0}, {0, 0}};
+  int occ_tree[2][2] = {{0, 0}, {0, 0}};
+};
+
+constexpr int kMaxDevices = 64;
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+thread_local char g_cuda_msg[256] = "no CUDA error recorded";
+
+int cuda_fail(cudaError_t e, const char* where) {
+  snprintf(g_cuda_msg, sizeof g_cuda_msg, "%s: %s (%s)", where, cudaGetErrorString(e),
+           cudaGetErrorName(e));
+  return SPEC_ERR_CUDA;
+}
+
+int get_device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return cuda_fail(cudaErrorInvalidDevice, "device index");
+  std::lock_guard<std::mutex> lock(g_mu);
+  DeviceState& d = g_dev[dev];
+  if (!d.init) {
+    e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    cudaMemPoolProps props;
+    memset(&props, 0, sizeof props);
+    props.allocType = cudaMemAllocationTypePinned;
+    props.location.type = cudaMemLocationTypeDevice;
+    props.location.id = dev;
+    e = cudaMemPoolCreate(&d.pool, &props);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+    uint64_t keep = UINT64_MAX;  // keep freed scratch in the pool between calls
+    e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolSetAttribute");
+    e = cudaGetSymbolAddress((void**)&d.status, g_spec_status);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
+    for (int bf = 0; bf < 2; ++bf)
+      for (int v = 0; v < 2; ++v) {
+        d.occ_sample[bf][v] = sv::sample_blocks_per_sm(bf, v);
+        d.occ_greedy[bf][v] = sv::greedy_blocks_per_sm(bf, v);
+        d.occ_tree[bf][v] = sv::tree_blocks_per_sm(bf, v);
+      }
+    d.init = true;
+  }
+  *out = &d;
+  return SPEC_OK;
+}
+
+bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
+
+// Chunk length: about four units per resident CTA, between 2048 elements and
+// the largest chunk whose pieces fit the kernels' shared buffer, equalised so
+// that the chunks of a row differ by at most one vector.
+void choose_chunks(long long rows_total, int V, int vec_elems, int capacity, int* CH, int* C) {
+  const long long cap_max = (long long)sv::kMaxSteps * sv::kThreads * vec_elems;
+  const long long hi = cap_max < 32768 ? cap_max : 32768;
+  const long long lo = 2048 < hi ? 2048 : hi;
+  const long long target_units = 4LL * (capacity > 0 ? capacity : 1);
+  long long ideal = (rows_total * (long long)V + target_units - 1) / target_units;
+  if (ideal < lo) ideal = lo;
+  if (ideal > hi) ideal = hi;
+  long long c = (V + ideal - 1) / ideal;
+  if (c < 1) c = 1;
+  long long ch = (V + c - 1) / c;
+  ch = (ch + 7) / 8 * 8;
+  c = (V + ch - 1) / ch;
+  *CH = (int)ch;
+  *C = (int)c;
+}
+
+bool sizes_ok(int B, int rows, int V) {
+  const double total = (double)B * (double)rows * (double)V;
+  return V <= 0x7fff0000 && total < 4.0e18;
+}
+
+int run_scratch(DeviceState* d, size_t bytes, size_t counter_bytes, cudaStream_t stream, void** ws) {
+  cudaError_t e = cudaMallocFromPoolAsync(ws, bytes, d->pool, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
+  e = cudaMemsetAsync(*ws, 0, counter_bytes, stream);
+  if (e != cudaSuccess) {
+    cudaFreeAsync(*ws, stream);
+    return cuda_fail(e, "cudaMemsetAsync");
+  }
+  return SPEC_OK;
+}
+
+int greedy_impl(bool bf16, const void* target, const int32_t* tokens, int B, int K, int V,
+                int32_t* out_tokens, int32_t* out_n, int32_t* out_row_argmax, cudaStream_t stream) {
+  if (!target || !out_tokens || !out_n || (K > 0 && !tokens)) return SPEC_ERR_NULL;
+  if (B < 0 || K < 0 || K > sv::kMaxK || V < 1 || !sizes_ok(B, K + 1, V)) return SPEC_ERR_SHAPE;
+  if (B == 0) return SPEC_OK;
+  DeviceState* d = nullptr;
+  int rc = get_device_state(&d);
+  if (rc) return rc;
+  const size_t esz = bf16 ? 2 : 4;
+  const bool vec = aligned16(target) && ((size_t)V * esz) % 16 == 0;
+  const int capacity = d->sms * d->occ_greedy[bf16][vec];
+  sv::GreedyArgs a;
+  memset(&a, 0, sizeof a);
+  a.target = target;
+  a.tokens = tokens;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.R = K + 1;
+  choose_chunks((long long)B * a.R, V, vec ? (bf16 ? 8 : 4) : 1, capacity, &a.CH, &a.C);
+  a.map.B = B;
+  a.map.A = a.R * a.C;
+  a.map.T = 0;
+  a.map.delta = 0;
+  a.map.total = (long long)B * a.map.A;
+  a.out_tokens = out_tokens;
+  a.out_n = out_n;
+  a.out_row_argmax = out_row_argmax;
+  a.status = d->status;
+  size_t counter_bytes = 0;
+  const size_t bytes = sv::greedy_workspace_bytes(B, a.R, a.C, &counter_bytes);
+  void* ws = nullptr;
+  rc = run_scratch(d, bytes, counter_bytes, stream, &ws);
+  if (rc) return rc;
+  sv::greedy_bind_workspace(a, ws);
+  const long long grid = a.map.total < capacity ? a.map.total : capacity;
+  cudaError_t e = sv::launch_greedy(a, bf16, vec, (int)grid, stream);
+  cudaError_t e2 = cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "greedy verify launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
+  return SPEC_OK;
+}
+
+int verify_impl(bool bf16, const void* target, const void* draft, const int32_t* tokens, int B,
+                int K, int V, float temperature, uint64_t seed, int32_t* out_tokens, int32_t* out_n,
+                float* out_row_stats, float* out_pq, float* out_resid, cudaStream_t stream) {
+  if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-30f))
+    return SPEC_ERR_TEMPERATURE;
+  if (temperature == 0.f)
+    return greedy_impl(bf16, target, tokens, B, K, V, out_tokens, out_n, nullptr, stream);
+  if (!target || !out_tokens || !out_n || (K > 0 && (!tokens || !draft))) return SPEC_ERR_NULL;
+  if (B < 0 || K < 0 || K > sv::kMaxK || V < 1 || !sizes_ok(B, 2 * K + 1, V)) return SPEC_ERR_SHAPE;
+  if (B == 0) return SPEC_OK;
+  DeviceState* d = nullptr;
+  int rc = get_device_state(&d);
+  if (rc) return rc;
+  const size_t esz = bf16 ? 2 : 4;
+  const bool vec = aligned16(target) && (K == 0 || aligned16(draft)) && ((size_t)V * esz) % 16 == 0;
+  const int capacity = d->sms * d->occ_sample[bf16][vec];
+  sv::SampleArgs a;
+  memset(&a, 0, sizeof a);
+  a.target = target;
+  a.draft = draft;
+  a.tokens = tokens;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.R = 2 * K + 1;
+  choose_chunks((long long)B * a.R, V, vec ? (bf16 ? 8 : 4) : 1, capacity, &a.CH, &a.C);
+  a.P = sv::sample_pieces_per_unit(a.CH, bf16, vec);
+  a.map.B = B;
+  a.map.A = a.R * a.C;
+  a.map.T = a.C;
+  const long long grid = (long long)B * (a.map.A + a.map.T) < capacity
+                             ? (long long)B * (a.map.A + a.map.T)
+                             : capacity;
+  a.map.delta = (int)((grid + a.map.A + a.map.T - 1) / (a.map.A + a.map.T)) + 1;
+  a.map.total = (long long)B * (a.map.A + a.map.T);
+  const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
+  a.c64 = c;
+  a.c_hi = (float)c;
+  a.c_lo = (float)(c - (double)a.c_hi);
+  a.inv_tau = 1.0 / (double)temperature;
+  a.seed = seed;
+  a.out_tokens = out_tokens;
+  a.out_n = out_n;
+  a.out_row_stats = out_row_stats;
+  a.out_pq = out_pq;
+  a.out_resid = out_resid;
+  a.status = d->status;
+  size_t counter_bytes = 0;
+  const size_t bytes = sv::sample_workspace_bytes(B, K, a.C, a.P, &counter_bytes);
+  void* ws = nullptr;
+  rc = run_scratch(d, bytes, counter_bytes, stream, &ws);
+  if (rc) return rc;
+  sv::sample_bind_workspace(a, ws);
+  cudaError_t e = sv::launch_sample(a, bf16, vec, (int)grid, stream);
+  cudaError_t e2 = cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "sampling verify launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
+  return SPEC_OK;
+}
+
+int tree_impl(bool bf16, const void* target, const int32_t* tree_tokens, const int32_t* parents,
+              int B, int N, int V, int32_t* out_path, int32_t* out_len, uint32_t* out_mask,
+              cudaStream_t stream) {
+  if (!target || !out_path || !out_len || (N > 0 && (!tree_tokens || !parents || !out_mask)))
+    return SPEC_ERR_NULL;
+  if (B < 0 || N < 0 || N > sv::kMaxTreeNodes || V < 1 || !sizes_ok(B, N + 1, V))
+    return SPEC_ERR_SHAPE;
+  if (B == 0) return SPEC_OK;
+  DeviceState* d = nullptr;
+  int rc = get_device_state(&d);
+  if (rc) return rc;
+  const size_t esz = bf16 ? 2 : 4;
+  const bool vec = aligned16(target) && ((size_t)V * esz) % 16 == 0;
+  const int capacity = d->sms * d->occ_tree[bf16][vec];
+  sv::GreedyArgs a;
+  memset(&a, 0, sizeof a);
+  a.target = target;
+  a.tokens = tree_tokens;
+  a.parents = parents;
+  a.B = B;
+  a.K = N;
+  a.V = V;
+  a.R = N + 1;
+  choose_chunks((long long)B * a.R, V, vec ? (bf16 ? 8 : 4) : 1, capacity, &a.CH, &a.C);
+  a.map.B = B;
+  a.map.A = a.R * a.C;
+  a.map.T = 0;
+  a.map.delta = 0;
+  a.map.total = (long long)B * a.map.A;
+  a.out_tokens = out_path;
+  a.out_n = out_len;
+  a.out_mask = out_mask;
+  a.status = d->status;
+  size_t counter_bytes = 0;
+  const size_t bytes = sv::greedy_workspace_bytes(B, a.R, a.C, &counter_bytes);
+  void* ws = nullptr;
+  rc = run_scratch(d, bytes, counter_bytes, stream, &ws);
+  if (rc) return rc;
+  sv::greedy_bind_workspace(a, ws);
+  const long long grid = a.map.total < capacity ? a.map.total : capacity;
+  cudaError_t e = sv::launch_tree(a, bf16, vec, (int)grid, stream);
+  cudaError_t e2 = cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tree verify launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
+  return SPEC_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+int spec_verify_f32(const float* target_logits, const float* draft_logits,
+                    const int32_t* draft_tokens, int B, int K, int V, float temperature,
+                    uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
+                    cudaStream_t stream) {
+  return verify_impl(false, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
+                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream);
+}
+
+int spec_verify_bf16(const uint16_t* target_logits, const uint16_t* draft_logits,
+                     const int32_t* draft_tokens, int B, int K, int V, float temperature,
+                     uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
+                     cudaStream_t stream) {
+  return verify_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
+                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream);
+}
+
+int spec_verify_stats_f32(const float* target_logits, const float* draft_logits,
+                          const int32_t* draft_tokens, int B, int K, int V, float temperature,
+                          uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
+                          float* out_row_stats, float* out_pq, float* out_resid_mass,
+                          cudaStream_t stream) {
+  return verify_impl(false, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
+                     out_tokens, out_n_accepted, out_row_stats, out_pq, out_resid_mass, stream);
+}
+
+int spec_verify_stats_bf16(const uint16_t* target_logits, const uint16_t* draft_logits,
+                           const int32_t* draft_tokens, int B, int K, int V, float temperature,
+                           uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
+                           float* out_row_stats, float* out_pq, float* out_resid_mass,
+                           cudaStream_t stream) {
+  return verify_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
+                     out_tokens, out_n_accepted, out_row_stats, out_pq, out_resid_mass, stream);
+}
+
+int spec_verify_greedy_argmax_f32(const float* target_logits, const int32_t* draft_tokens, int B,
+                                  int K, int V, int32_t* out_tokens, int32_t* out_n_accepted,
+                                  int32_t* out_row_argmax, cudaStream_t stream) {
+  return greedy_impl(false, target_logits, draft_tokens, B, K, V, out_tokens, out_n_accepted,
+                     out_row_argmax, stream);
+}
+
+int spec_verify_greedy_argmax_bf16(const uint16_t* target_logits, const int32_t* draft_tokens,
+                                   int B, int K, int V, int32_t* out_tokens,
+                                   int32_t* out_n_accepted, int32_t* out_row_argmax,
+                                   cudaStream_t stream) {
+  return greedy_impl(true, target_logits, draft_tokens, B, K, V, out_tokens, out_n_accepted,
+                     out_row_argmax, stream);
+}
+
+int spec_tree_verify_greedy_f32(const float* target_logits, const int32_t* tree_tokens,
+                                const int32_t* parent_idx, int B, int N, int V, int32_t* out_path,
+                                int32_t* out_len, uint32_t* out_mask, cudaStream_t stream) {
+  return tree_impl(false, target_logits, tree_tokens, parent_idx, B, N, V, out_path, out_len,
+                   out_mask, stream);
+}
+
+int spec_tree_verify_greedy_bf16(const uint16_t* target_logits, const int32_t* tree_tokens,
+                                 const int32_t* parent_idx, int B, int N, int V,
+                                 int32_t* out_path, int32_t* out_len, uint32_t* out_mask,
+                                 cudaStream_t stream) {
+  return tree_impl(true, target_logits, tree_tokens, parent_idx, B, N, V, out_path, out_len,
+                   out_mask, stream);
+}
+
+int spec_get_status(cudaStream_t stream, uint32_t* flags_out) {
+  DeviceState* d = nullptr;
+  int rc = get_device_state(&d);
+  if (rc) return rc;
+  unsigned v = 0;
+  cudaError_t e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamSynchronize");
+  e = cudaMemcpyAsync(&v, d->status, sizeof v, cudaMemcpyDeviceToHost, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync(d->status, 0, sizeof v, stream);
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  if (e != cudaSuccess) return cuda_fail(e, "status word");
+  if (flags_out) *flags_out = v;
+  return SPEC_OK;
+}
+
+const char* spec_status_string(int code) {
+  switch (code) {
+    case SPEC_OK:
+      return "ok";
+    case SPEC_ERR_NULL:
+      return "a required pointer is NULL";
+    case SPEC_ERR_SHAPE:
+      return "bad shape: B < 0, K outside [0, 255], N outside [0, 1024], V < 1, or size overflow";
+    case SPEC_ERR_TEMPERATURE:
+      return "bad temperature: NaN, negative, or in (0, 1e-30)";
+    case SPEC_ERR_CUDA:
+      return g_cuda_msg;
+    default:
+      return "unknown status code";
+  }
+}
+
+}  // extern "C"

@@ -1,0 +1,45 @@
+"""Comparison helpers for the GPU parity tests (no test functions here).
+
+The CUDA path accumulates softmax sums in fp32; the oracle works in fp64.  A
+decision (accept / reject, or which token an inverse CDF lands on) may only
+differ where the oracle's own draw lies within 1e-6 of the decision boundary:
+|u - min(1, p/q)| < 1e-6 for an acceptance draw, or a distance below 1e-6 * Z
+from w * Z to the nearest cumulative sum for a resampling draw.  Such
+sequences are counted and reported; every other sequence must match exactly.
+"""
+from __future__ import annotations
+
+import numpy as np
+
+BOUNDARY = 1e-6
+
+
+def chain_report(tokens, n, ref):
+    """Compare GPU chain outputs with the oracle's.
+
+    Returns dict(mismatch=[...] sequences differing outside the boundary
+    window, boundary=[...] sequences differing inside it, boundary_draws=count
+    of oracle draws inside the window)."""
+    tokens = np.asarray(tokens)
+    n = np.asarray(n)
+    mism, bnd = [], []
+    for b in range(len(n)):
+        if n[b] == ref["n"][b] and np.array_equal(tokens[b], ref["tokens"][b]):
+            continue
+        if n[b] != ref["n"][b] and ref["n"][b] >= 0 and n[b] >= 0:
+            i = min(int(n[b]), int(ref["n"][b]))
+            (bnd if ref["acc_margin"][b, i] < BOUNDARY else mism).append(b)
+        elif n[b] == ref["n"][b] and n[b] >= 0 and ref["sample_margin"][b] < BOUNDARY:
+            bnd.append(b)
+        else:
+            mism.append(b)
+    am = ref["acc_margin"]
+    draws = int(np.sum(am[np.isfinite(am)] < BOUNDARY) +
+                np.sum(ref["sample_margin"][np.isfinite(ref["sample_margin"])] < BOUNDARY))
+    return dict(mismatch=mism, boundary=bnd, boundary_draws=draws)
+
+
+def rel_err(a, b):
+    a = np.asarray(a, dtype=np.float64)
+    b = np.asarray(b, dtype=np.float64)
+    return np.abs(a - b) / np.maximum(np.abs(b), 1e-300)

@@ -1,0 +1,94 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports every
+symbol include/specverify.h declares, and rejects bad arguments on the host
+with the documented codes before any CUDA call."""
+import ctypes
+import math
+
+import pytest
+
+from speculative_decoding_verification_36_gb300 import _lib, build
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def test_header_declares_expected_entry_points():
+    names = set(_lib.header_symbols())
+    assert {"spec_verify_f32", "spec_verify_bf16", "spec_tree_verify_greedy_f32",
+            "spec_tree_verify_greedy_bf16", "spec_get_status", "spec_status_string"} <= names
+    assert names == set(_lib.SIGNATURES), "binding signatures and header disagree"
+
+
+def test_library_exports_every_header_symbol(lib):
+    for name in _lib.header_symbols():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code in (0, -1, -2, -3, -4, 99):
+        assert isinstance(lib.spec_status_string(code), bytes)
+
+
+# fake, never-dereferenced device addresses: the host checks return before any use
+FAKE = 0x10000
+
+
+def _chain(lib, fn="spec_verify_f32", target=FAKE, draft=FAKE, tokens=FAKE, B=2, K=3, V=16,
+           temperature=1.0, out_tokens=FAKE, out_n=FAKE):
+    return getattr(lib, fn)(target, draft, tokens, B, K, V, temperature, 0, out_tokens, out_n, None)
+
+
+@pytest.mark.parametrize("fn", ["spec_verify_f32", "spec_verify_bf16"])
+def test_null_pointers(lib, fn):
+    assert _chain(lib, fn, target=None) == _lib.SPEC_ERR_NULL
+    assert _chain(lib, fn, out_tokens=None) == _lib.SPEC_ERR_NULL
+    assert _chain(lib, fn, out_n=None) == _lib.SPEC_ERR_NULL
+    assert _chain(lib, fn, tokens=None) == _lib.SPEC_ERR_NULL
+    assert _chain(lib, fn, draft=None) == _lib.SPEC_ERR_NULL
+
+
+@pytest.mark.parametrize("fn", ["spec_verify_f32", "spec_verify_bf16"])
+def test_bad_shapes(lib, fn):
+    assert _chain(lib, fn, B=-1) == _lib.SPEC_ERR_SHAPE
+    assert _chain(lib, fn, K=-1) == _lib.SPEC_ERR_SHAPE
+    assert _chain(lib, fn, K=256) == _lib.SPEC_ERR_SHAPE
+    assert _chain(lib, fn, V=0) == _lib.SPEC_ERR_SHAPE
+    assert _chain(lib, fn, B=2**30, K=255, V=2**30) == _lib.SPEC_ERR_SHAPE
+
+
+@pytest.mark.parametrize("tau", [math.nan, -1.0, 1e-35])
+def test_bad_temperature(lib, tau):
+    assert _chain(lib, temperature=tau) == _lib.SPEC_ERR_TEMPERATURE
+
+
+def test_empty_batch_is_a_noop(lib):
+    # B == 0 returns before touching the device
+    assert _chain(lib, B=0) == _lib.SPEC_OK
+    assert _chain(lib, B=0, temperature=0.0) == _lib.SPEC_OK
+
+
+def test_greedy_needs_no_draft(lib):
+    # temperature 0 does not require draft logits; a bad shape still fails first
+    assert _chain(lib, draft=None, temperature=0.0, V=0) == _lib.SPEC_ERR_SHAPE
+    assert _chain(lib, draft=None, temperature=0.0, B=0) == _lib.SPEC_OK
+
+
+def test_tree_checks(lib):
+    f = lib.spec_tree_verify_greedy_bf16
+    assert f(None, FAKE, FAKE, 1, 3, 8, FAKE, FAKE, FAKE, None) == _lib.SPEC_ERR_NULL
+    assert f(FAKE, None, FAKE, 1, 3, 8, FAKE, FAKE, FAKE, None) == _lib.SPEC_ERR_NULL
+    assert f(FAKE, FAKE, FAKE, 1, 3, 8, FAKE, FAKE, None, None) == _lib.SPEC_ERR_NULL
+    assert f(FAKE, FAKE, FAKE, 1, 1025, 8, FAKE, FAKE, FAKE, None) == _lib.SPEC_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, 1, -1, 8, FAKE, FAKE, FAKE, None) == _lib.SPEC_ERR_SHAPE
+    assert f(FAKE, FAKE, FAKE, 0, 3, 8, FAKE, FAKE, FAKE, None) == _lib.SPEC_OK
+
+
+def test_python_binding_rejects_cpu_tensors():
+    import torch
+    import speculative_decoding_verification_36_gb300 as sv
+    t = torch.zeros(1, 2, 8)
+    with pytest.raises(ValueError):
+        sv.spec_verify(t, t[:, :1], torch.zeros(1, 1, dtype=torch.int32), 1.0, 0)

@@ -11,6 +11,8 @@
 #include <stdio.h>
 #include <string.h>
 
+#include <stdlib.h>
+
 #include <mutex>
 
 // Sticky per-device status word (SPEC_FLAG_* bits), read and cleared by
@@ -76,39 +78,99 @@ int get_device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Chunk length: about four units per resident CTA, between 2048 elements and
-// the largest chunk whose pieces fit the kernels' shared buffer, equalised so
-// that the chunks of a row differ by at most one vector.
-void choose_chunks(long long rows_total, int V, int vec_elems, int capacity, int* CH, int* C) {
-  const long long cap_max = (long long)sv::kMaxSteps * sv::kThreads * vec_elems;
-  const long long hi = cap_max < 32768 ? cap_max : 32768;
-  const long long lo = 2048 < hi ? 2048 : hi;
-  const long long target_units = 4LL * (capacity > 0 ? capacity : 1);
-  long long ideal = (rows_total * (long long)V + target_units - 1) / target_units;
-  if (ideal < lo) ideal = lo;
-  if (ideal > hi) ideal = hi;
-  long long c = (V + ideal - 1) / ideal;
-  if (c < 1) c = 1;
-  long long ch = (V + c - 1) / c;
-  ch = (ch + 7) / 8 * 8;
-  c = (V + ch - 1) / ch;
-  *CH = (int)ch;
-  *C = (int)c;
+// Tuning knobs (environment, read once): SPECVERIFY_SLICE_BYTES (bytes of
+// logits per slice, default 8192) and SPECVERIFY_DELTA (sequences between a
+// sequence's statistics and tail units; 0 = automatic).
+int env_int(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  const long x = strtol(v, nullptr, 10);
+  return (x > 0 && x < (1L << 30)) ? (int)x : dflt;
 }
 
+// Slice length: a whole number of warp load batches (32 lanes x kUnroll
+// vectors) covering about SPECVERIFY_SLICE_BYTES; a row shorter than one slice
+// is one slice.
+void choose_slices(int V, int vec_elems, size_t esz, int* SL, int* CS, int* CU) {
+  static const int bytes = env_int("SPECVERIFY_SLICE_BYTES", 8192);
+  const long long batch = 32LL * vec_elems * sv::kUnroll;
+  long long k = ((long long)bytes / (long long)esz + batch - 1) / batch;
+  if (k < 1) k = 1;
+  long long sl = k * batch;
+  if (sl >= V) sl = ((long long)V + 7) / 8 * 8;
+  *SL = (int)sl;
+  *CS = (int)((V + sl - 1) / sl);
+  *CU = (*CS + sv::kSlices - 1) / sv::kSlices;
+}
+
+// Each counter's units are shared by one warp of every CTA, so a grid of
+// `total_units` CTAs already gives every unit its own warp.
+int grid_for(int total_units, int capacity) {
+  if (total_units < 1) total_units = 1;
+  return total_units < capacity ? total_units : capacity;
+}
+
+// Element offsets are 64-bit; unit indices and per-row positions are 32-bit.
 bool sizes_ok(int B, int rows, int V) {
   const double total = (double)B * (double)rows * (double)V;
-  return V <= 0x7fff0000 && total < 4.0e18;
+  const double units = (double)B * (double)(rows + 1) * ((double)V / 1024.0 + 1.0);
+  return V <= 0x7fff0000 && total < 4.0e18 && units < 2.0e9;
 }
 
-int run_scratch(DeviceState* d, size_t bytes, size_t counter_bytes, cudaStream_t stream, void** ws) {
-  cudaError_t e = cudaMallocFromPoolAsync(ws, bytes, d->pool, stream);
+// Stream-ordered scratch from the library's pool, with the zero region and
+// the "not yet written" marker region initialised on the stream.
+int run_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, void** ws) {
+  cudaError_t e = cudaMallocFromPoolAsync(ws, l.total, d->pool, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
-  e = cudaMemsetAsync(*ws, 0, counter_bytes, stream);
+  e = cudaMemsetAsync(*ws, 0, l.zero_bytes, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, stream);
   if (e != cudaSuccess) {
     cudaFreeAsync(*ws, stream);
     return cuda_fail(e, "cudaMemsetAsync");
   }
+  return SPEC_OK;
+}
+
+// Greedy chain (tree == false) or tree (tree == true) verification.
+int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
+                const int32_t* parents, int B, int K, int V, int32_t* out_tokens, int32_t* out_n,
+                uint32_t* out_mask, int32_t* out_row_argmax, cudaStream_t stream) {
+  DeviceState* d = nullptr;
+  int rc = get_device_state(&d);
+  if (rc) return rc;
+  const size_t esz = bf16 ? 2 : 4;
+  const bool vec = aligned16(target) && ((size_t)V * esz) % 16 == 0;
+  const int capacity = d->sms * (tree ? d->occ_tree[bf16][vec] : d->occ_greedy[bf16][vec]);
+  sv::GreedyArgs a;
+  memset(&a, 0, sizeof a);
+  a.target = target;
+  a.tokens = tokens;
+  a.parents = parents;
+  a.B = B;
+  a.K = K;
+  a.V = V;
+  a.R = K + 1;
+  choose_slices(V, vec ? (bf16 ? 8 : 4) : 1, esz, &a.SL, &a.CS, &a.CU);
+  a.map.B = B;
+  a.map.A = a.R * a.CU;
+  a.map.T = 0;
+  a.map.delta = 0;
+  a.map.total = B * a.map.A;
+  a.out_tokens = out_tokens;
+  a.out_n = out_n;
+  a.out_mask = out_mask;
+  a.out_row_argmax = out_row_argmax;
+  a.status = d->status;
+  void* ws = nullptr;
+  rc = run_scratch(d, sv::greedy_workspace(B, a.R, a.CU), stream, &ws);
+  if (rc) return rc;
+  sv::greedy_bind_workspace(a, ws);
+  const int grid = grid_for(a.map.total, capacity);
+  cudaError_t e = tree ? sv::launch_tree(a, bf16, vec, grid, stream)
+                       : sv::launch_greedy(a, bf16, vec, grid, stream);
+  cudaError_t e2 = cudaFreeAsync(ws, stream);
+  if (e != cudaSuccess) return cuda_fail(e, tree ? "tree verify launch" : "greedy verify launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
   return SPEC_OK;
 }
 
@@ -117,42 +179,8 @@ int greedy_impl(bool bf16, const void* target, const int32_t* tokens, int B, int
   if (!target || !out_tokens || !out_n || (K > 0 && !tokens)) return SPEC_ERR_NULL;
   if (B < 0 || K < 0 || K > sv::kMaxK || V < 1 || !sizes_ok(B, K + 1, V)) return SPEC_ERR_SHAPE;
   if (B == 0) return SPEC_OK;
-  DeviceState* d = nullptr;
-  int rc = get_device_state(&d);
-  if (rc) return rc;
-  const size_t esz = bf16 ? 2 : 4;
-  const bool vec = aligned16(target) && ((size_t)V * esz) % 16 == 0;
-  const int capacity = d->sms * d->occ_greedy[bf16][vec];
-  sv::GreedyArgs a;
-  memset(&a, 0, sizeof a);
-  a.target = target;
-  a.tokens = tokens;
-  a.B = B;
-  a.K = K;
-  a.V = V;
-  a.R = K + 1;
-  choose_chunks((long long)B * a.R, V, vec ? (bf16 ? 8 : 4) : 1, capacity, &a.CH, &a.C);
-  a.map.B = B;
-  a.map.A = a.R * a.C;
-  a.map.T = 0;
-  a.map.delta = 0;
-  a.map.total = (long long)B * a.map.A;
-  a.out_tokens = out_tokens;
-  a.out_n = out_n;
-  a.out_row_argmax = out_row_argmax;
-  a.status = d->status;
-  size_t counter_bytes = 0;
-  const size_t bytes = sv::greedy_workspace_bytes(B, a.R, a.C, &counter_bytes);
-  void* ws = nullptr;
-  rc = run_scratch(d, bytes, counter_bytes, stream, &ws);
-  if (rc) return rc;
-  sv::greedy_bind_workspace(a, ws);
-  const long long grid = a.map.total < capacity ? a.map.total : capacity;
-  cudaError_t e = sv::launch_greedy(a, bf16, vec, (int)grid, stream);
-  cudaError_t e2 = cudaFreeAsync(ws, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "greedy verify launch");
-  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
-  return SPEC_OK;
+  return argmax_impl(false, bf16, target, tokens, nullptr, B, K, V, out_tokens, out_n, nullptr,
+                     out_row_argmax, stream);
 }
 
 int verify_impl(bool bf16, const void* target, const void* draft, const int32_t* tokens, int B,
@@ -180,16 +208,19 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.K = K;
   a.V = V;
   a.R = 2 * K + 1;
-  choose_chunks((long long)B * a.R, V, vec ? (bf16 ? 8 : 4) : 1, capacity, &a.CH, &a.C);
-  a.P = sv::sample_pieces_per_unit(a.CH, bf16, vec);
+  const int vec_elems = vec ? (bf16 ? 8 : 4) : 1;
+  choose_slices(V, vec_elems, esz, &a.SL, &a.CS, &a.CU);
+  a.P = (a.SL + 32 * vec_elems - 1) / (32 * vec_elems);
   a.map.B = B;
-  a.map.A = a.R * a.C;
-  a.map.T = a.C;
-  const long long grid = (long long)B * (a.map.A + a.map.T) < capacity
-                             ? (long long)B * (a.map.A + a.map.T)
-                             : capacity;
-  a.map.delta = (int)((grid + a.map.A + a.map.T - 1) / (a.map.A + a.map.T)) + 1;
-  a.map.total = (long long)B * (a.map.A + a.map.T);
+  a.map.A = a.R * a.CU;
+  a.map.T = a.CU;
+  a.map.total = B * (a.map.A + a.map.T);
+  const int grid = grid_for(a.map.total, capacity);
+  // Tail units trail their sequence by the units claimed while a sequence's
+  // statistics complete and its decision is made (about two grids' worth).
+  static const int delta_env = env_int("SPECVERIFY_DELTA", 0);
+  a.map.delta = delta_env > 0 ? delta_env
+                              : (2 * grid + a.map.A + a.map.T - 1) / (a.map.A + a.map.T) + 1;
   const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
   a.c64 = c;
   a.c_hi = (float)c;
@@ -202,13 +233,11 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.out_pq = out_pq;
   a.out_resid = out_resid;
   a.status = d->status;
-  size_t counter_bytes = 0;
-  const size_t bytes = sv::sample_workspace_bytes(B, K, a.C, a.P, &counter_bytes);
   void* ws = nullptr;
-  rc = run_scratch(d, bytes, counter_bytes, stream, &ws);
+  rc = run_scratch(d, sv::sample_workspace(B, K, a.CU, a.P), stream, &ws);
   if (rc) return rc;
   sv::sample_bind_workspace(a, ws);
-  cudaError_t e = sv::launch_sample(a, bf16, vec, (int)grid, stream);
+  cudaError_t e = sv::launch_sample(a, bf16, vec, grid, stream);
   cudaError_t e2 = cudaFreeAsync(ws, stream);
   if (e != cudaSuccess) return cuda_fail(e, "sampling verify launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
@@ -223,43 +252,8 @@ int tree_impl(bool bf16, const void* target, const int32_t* tree_tokens, const i
   if (B < 0 || N < 0 || N > sv::kMaxTreeNodes || V < 1 || !sizes_ok(B, N + 1, V))
     return SPEC_ERR_SHAPE;
   if (B == 0) return SPEC_OK;
-  DeviceState* d = nullptr;
-  int rc = get_device_state(&d);
-  if (rc) return rc;
-  const size_t esz = bf16 ? 2 : 4;
-  const bool vec = aligned16(target) && ((size_t)V * esz) % 16 == 0;
-  const int capacity = d->sms * d->occ_tree[bf16][vec];
-  sv::GreedyArgs a;
-  memset(&a, 0, sizeof a);
-  a.target = target;
-  a.tokens = tree_tokens;
-  a.parents = parents;
-  a.B = B;
-  a.K = N;
-  a.V = V;
-  a.R = N + 1;
-  choose_chunks((long long)B * a.R, V, vec ? (bf16 ? 8 : 4) : 1, capacity, &a.CH, &a.C);
-  a.map.B = B;
-  a.map.A = a.R * a.C;
-  a.map.T = 0;
-  a.map.delta = 0;
-  a.map.total = (long long)B * a.map.A;
-  a.out_tokens = out_path;
-  a.out_n = out_len;
-  a.out_mask = out_mask;
-  a.status = d->status;
-  size_t counter_bytes = 0;
-  const size_t bytes = sv::greedy_workspace_bytes(B, a.R, a.C, &counter_bytes);
-  void* ws = nullptr;
-  rc = run_scratch(d, bytes, counter_bytes, stream, &ws);
-  if (rc) return rc;
-  sv::greedy_bind_workspace(a, ws);
-  const long long grid = a.map.total < capacity ? a.map.total : capacity;
-  cudaError_t e = sv::launch_tree(a, bf16, vec, (int)grid, stream);
-  cudaError_t e2 = cudaFreeAsync(ws, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "tree verify launch");
-  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
-  return SPEC_OK;
+  return argmax_impl(true, bf16, target, tree_tokens, parents, B, N, V, out_path, out_len, out_mask,
+                     nullptr, stream);
 }
 
 }  // namespace

@@ -15,10 +15,10 @@
 // (lowest node index on ties), the bonus argmax of that node's row, and the
 // N x N ancestor-or-self bitmask of the tree.
 //
-// Both use the persistent unit loop of the sampling kernel without tail
-// units: a unit is one chunk of one row reduced to (max, lowest argmax, NaN
-// seen); the CTA finishing a sequence's last unit (atomic ticket) merges the
-// chunks in order and writes that sequence's outputs.
+// Both use the sliced-unit loop of the sampling kernel without tail units: a
+// slice of one row is reduced to (max, lowest argmax, NaN seen); the warp
+// taking a sequence's last ticket merges the slices in order and writes that
+// sequence's outputs.
 #include "sv_common.cuh"
 #include "sv_kernels.h"
 
@@ -26,46 +26,31 @@
 
 namespace sv {
 
-struct ArgmaxSmem {
-  long long next;
-  int flag;
-  float wv[kWarps];
-  int wi[kWarps];
-};
-
-struct TreeSmem {
-  ArgmaxSmem base;
-  int g[kMaxTreeNodes + 1];
-  int depth[kMaxTreeNodes];
-  unsigned char acc[kMaxTreeNodes];
-  int best;
-};
-
 template <class E>
 __device__ __forceinline__ const typename E::storage* grow(const GreedyArgs& a, int b, int r) {
   return (const typename E::storage*)a.target + ((size_t)b * a.R + r) * (size_t)a.V;
 }
 
-// One chunk of one row: returns true in every thread of the CTA that finished
-// the sequence's last unit.
+__device__ __forceinline__ uint32_t bf16x2_max_nan(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.NaN.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
+}
+
+// Batch maximum that propagates NaN (a NaN anywhere makes the result NaN).
 template <class E, int VEC>
-__device__ bool argmax_unit(const GreedyArgs& a, int b, int idx, ArgmaxSmem& sm) {
-  using S = typename E::storage;
-  constexpr int STEP = kThreads * VEC;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int r = idx / a.C, c = idx - (idx / a.C) * a.C;
-  const S* row = grow<E>(a, b, r);
-  const int v0 = c * a.CH, v1 = min(a.V, v0 + a.CH);
-  float best = neg_inf();
-  int bi = INT_MAX;
-  bool nan = false;
-  const int nbatch = (v1 - v0 + STEP * kUnroll - 1) / (STEP * kUnroll);
-  int e = v0 + threadIdx.x * VEC;
-  for (int bt = 0; bt < nbatch; ++bt, e += STEP * kUnroll) {
-    Raw<E, VEC> z[kUnroll];
+__device__ __forceinline__ float batch_max_nan(const Raw<E, VEC> (&z)[kUnroll]) {
+  if constexpr (VEC == 8) {
+    uint32_t mw = bf16x2_max_nan(bf16x2_max_nan(z[0].w.x, z[0].w.y), bf16x2_max_nan(z[0].w.z, z[0].w.w));
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) z[u] = load_raw<E, VEC>(row, e + u * STEP, v1);
+    for (int u = 1; u < kUnroll; ++u)
+      mw = bf16x2_max_nan(mw, bf16x2_max_nan(bf16x2_max_nan(z[u].w.x, z[u].w.y),
+                                             bf16x2_max_nan(z[u].w.z, z[u].w.w)));
+    const float lo = bf16_lo(mw), hi = bf16_hi(mw);
+    return (lo != lo || hi != hi) ? lo + hi : fmaxf(lo, hi);
+  } else {
     float bm = neg_inf();
+    bool nan = false;
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
@@ -74,176 +59,231 @@ __device__ bool argmax_unit(const GreedyArgs& a, int b, int idx, ArgmaxSmem& sm)
         bm = fmaxf(bm, x);
         nan |= x != x;
       }
-    if (bm > best) {
-      int found = INT_MAX;
+    return nan ? __int_as_float(0x7fc00000) : bm;
+  }
+}
+
+template <class E, int VEC>
+__device__ __forceinline__ void argmax_batch(const Raw<E, VEC> (&z)[kUnroll], int e, float& best, int& bi,
+                                             bool& nan) {
+  constexpr int STEPW = 32 * VEC;
+  const float bm = batch_max_nan<E, VEC>(z);
+  if (bm != bm) {
+    nan = true;
+  } else if (bm > best) {
+    int found = INT_MAX;
 #pragma unroll
-      for (int u = kUnroll - 1; u >= 0; --u)
+    for (int u = kUnroll - 1; u >= 0; --u)
 #pragma unroll
-        for (int q = VEC - 1; q >= 0; --q)
-          if (elem(z[u], q) == bm) found = e + u * STEP + q;
-      best = bm;
-      bi = found;
+      for (int q = VEC - 1; q >= 0; --q)
+        if (elem(z[u], q) == bm) found = e + u * STEPW + q;
+    best = bm;
+    bi = found;
+  }
+}
+
+template <class E, int VEC>
+__device__ __forceinline__ void gload_batch(Raw<E, VEC> (&z)[kUnroll], const typename E::storage* row, int e,
+                                            int v1) {
+  constexpr int STEPW = 32 * VEC;
+#pragma unroll
+  for (int u = 0; u < kUnroll; ++u) z[u] = load_raw<E, VEC>(row, e + u * STEPW, v1);
+}
+
+// Slice w of unit idx of sequence b (one warp): (max, lowest argmax, NaN
+// seen) into the workspace as one 64-bit word, then the row's ticket; returns
+// the atomic's old value (lane 0).
+template <class E, int VEC>
+__device__ int argmax_slice(const GreedyArgs& a, int b, int idx, int w) {
+  using S = typename E::storage;
+  constexpr int BATCH = 32 * VEC * kUnroll;
+  const int lane = threadIdx.x & 31;
+  const int r = idx / a.CU, uc = idx - (idx / a.CU) * a.CU;
+  const int s = uc * kSlices + w;
+  const S* row = grow<E>(a, b, r);
+  const int v0 = s * a.SL, v1 = min(a.V, v0 + a.SL);
+  float best = neg_inf();
+  int bi = INT_MAX;
+  bool nan = false;
+  const int nb = v1 > v0 ? (v1 - v0 + BATCH - 1) / BATCH : 0;
+  int e = v0 + lane * VEC;
+  Raw<E, VEC> z0[kUnroll], z1[kUnroll];
+  if constexpr (VEC > 1) {
+    if (lane == 0 && v1 > v0) prefetch_l2(row + v0, (unsigned)((v1 - v0) * sizeof(S)));
+  }
+  if (nb > 0) gload_batch<E, VEC>(z0, row, e, v1);
+  for (int bt = 0; bt < nb; bt += 2, e += 2 * BATCH) {
+    if (bt + 1 < nb) gload_batch<E, VEC>(z1, row, e + BATCH, v1);
+    argmax_batch<E, VEC>(z0, e, best, bi, nan);
+    if (bt + 1 < nb) {
+      if (bt + 2 < nb) gload_batch<E, VEC>(z0, row, e + 2 * BATCH, v1);
+      argmax_batch<E, VEC>(z1, e + BATCH, best, bi, nan);
     }
   }
   warp_am(best, bi);
+  const bool anynan = __any_sync(0xffffffffu, nan);
+  int old = 0;
   if (lane == 0) {
-    sm.wv[warp] = best;
-    sm.wi[warp] = bi;
+    const size_t o = ((size_t)b * a.R + r) * (a.CU * kSlices) + s;
+    st_relaxed_u2(a.part + o, __float_as_uint(best), (uint32_t)bi | (anynan ? 0x80000000u : 0u));
+    old = atom_add_relaxed(&a.rowticket[((size_t)b * a.R + r) * kTicketStride], 1);
   }
-  const int any_nan = __syncthreads_or(nan);
-  if (warp == 0) {
-    best = lane < kWarps ? sm.wv[lane] : neg_inf();
-    bi = lane < kWarps ? sm.wi[lane] : INT_MAX;
-    warp_am(best, bi);
-    if (lane == 0) {
-      const size_t o = ((size_t)b * a.R + r) * a.C + c;
-      a.part_v[o] = best;
-      a.part_i[o] = bi;
-      a.part_nan[o] = any_nan;
-      __threadfence();
-      const int done = atomicAdd(&a.ticket1[b], 1);
-      sm.flag = done == a.map.A - 1;
-    }
-  }
-  __syncthreads();
-  if (sm.flag) __threadfence();
-  return sm.flag != 0;
+  return old;
 }
 
-// Merge the chunk results of row r (chunk order, lowest index on ties).
-// Returns the argmax, or -1 when the row is unusable (NaN, +inf, all -inf).
-__device__ __forceinline__ int merged_argmax(const GreedyArgs& a, int b, int r) {
-  const size_t o = ((size_t)b * a.R + r) * a.C;
+// Row finisher (one warp): merges the slice results of row r (lowest index
+// wins ties, so the merge order does not matter) into g[b][r] (-2 for an
+// unusable row: NaN, +inf, all -inf); returns true in the lane-uniform sense
+// when this was the sequence's last row.
+__device__ __noinline__ bool row_argmax_finisher(const GreedyArgs& a, int b, int r) {
+  const int lane = threadIdx.x & 31;
+  const int C = a.CU * kSlices;
+  const uint2* pp = a.part + ((size_t)b * a.R + r) * C;
   float v = neg_inf();
   int i = INT_MAX;
-  int nan = 0;
-  for (int c = 0; c < a.C; ++c) {
-    am_merge(v, i, __ldcg(a.part_v + o + c), __ldcg(a.part_i + o + c));
-    nan |= __ldcg(a.part_nan + o + c);
+  bool nan = false;
+  for (int c = lane; c < C; c += 32) {
+    const uint2 w = wait_u2(pp + c, a.status);
+    am_merge(v, i, __uint_as_float(w.x), (int)(w.y & 0x7fffffffu));
+    nan |= (w.y >> 31) != 0;
   }
-  if (nan || !(v > neg_inf()) || !(v < INFINITY) || i == INT_MAX) return -1;
-  return i;
+  warp_am(v, i);
+  nan = __any_sync(0xffffffffu, nan);
+  const int gv = (nan || !(v > neg_inf()) || !(v < INFINITY) || i == INT_MAX) ? -2 : i;
+  int old = 0;
+  if (lane == 0) {
+    st_relaxed_s32(a.g + (size_t)b * a.R + r, gv);
+    old = atom_add_relaxed(&a.seqticket[b], 1);
+  }
+  old = __shfl_sync(0xffffffffu, old, 0);
+  return old == a.R - 1;
 }
 
-template <class E, int VEC>
-__global__ void __launch_bounds__(kThreads) greedy_kernel(const GreedyArgs a) {
-  __shared__ ArgmaxSmem sm;
-  __shared__ int g[kMaxK + 1];
-  if (threadIdx.x == 0) sm.next = (long long)atomicAdd((unsigned long long*)a.counter, 1ull);
-  __syncthreads();
-  long long unit = sm.next;
-  __syncthreads();
-  while (unit < a.map.total) {
-    if (threadIdx.x == 0) sm.next = (long long)atomicAdd((unsigned long long*)a.counter, 1ull);
-    const int b = (int)(unit / a.map.A), idx = (int)(unit % a.map.A);
-    if (argmax_unit<E, VEC>(a, b, idx, sm)) {
-      const int K = a.K;
-      for (int r = threadIdx.x; r <= K; r += kThreads) {
-        g[r] = merged_argmax(a, b, r);
-        if (a.out_row_argmax) a.out_row_argmax[(size_t)b * (K + 1) + r] = g[r];
-      }
-      __syncthreads();
-      if (threadIdx.x < 32) {
-        const int lane = threadIdx.x;
-        const int32_t* x = a.tokens + (size_t)b * K;
-        bool bad = false;
-        for (int r = lane; r <= K; r += 32) bad |= g[r] < 0;
-        for (int i = lane; i < K; i += 32) bad |= x[i] < 0 || x[i] >= a.V;
-        bad = __any_sync(0xffffffffu, bad);
-        int n = K;
-        for (int i0 = 0; i0 < K && !bad; i0 += 32) {
-          const int i = i0 + lane;
-          const unsigned mis = __ballot_sync(0xffffffffu, i < K && x[i] != g[i]);
-          if (mis) {
-            n = i0 + __ffs(mis) - 1;
-            break;
-          }
-        }
-        int32_t* out = a.out_tokens + (size_t)b * (K + 1);
-        for (int j = lane; j <= K; j += 32)
-          out[j] = bad ? -1 : (j < n ? x[j] : (j == n ? g[n] : -1));
-        if (lane == 0) {
-          a.out_n[b] = bad ? -1 : n;
-          if (bad) atomicOr(a.status, kStatusBadData);
-        }
-      }
+// The finished argmax of row r (waits for the row finisher's store).
+__device__ __forceinline__ int row_g(const GreedyArgs& a, int b, int r) {
+  return wait_s32(a.g + (size_t)b * a.R + r, a.status);
+}
+
+// Chain finisher (one warp): acceptance while x_i equals the argmax.
+__device__ __noinline__ void chain_finisher(const GreedyArgs& a, int b) {
+  const int K = a.K;
+  const int lane = threadIdx.x & 31;
+  const int* g = a.g + (size_t)b * (K + 1);
+  for (int r = lane; r <= K; r += 32) {
+    const int v = row_g(a, b, r);
+    if (a.out_row_argmax) a.out_row_argmax[(size_t)b * (K + 1) + r] = v < 0 ? -1 : v;
+  }
+  __syncwarp();
+  const int32_t* x = a.tokens + (size_t)b * K;
+  bool bad = false;
+  for (int r = lane; r <= K; r += 32) bad |= __ldcg(g + r) < 0;
+  for (int i = lane; i < K; i += 32) bad |= x[i] < 0 || x[i] >= a.V;
+  bad = __any_sync(0xffffffffu, bad);
+  int n = K;
+  for (int i0 = 0; i0 < K && !bad; i0 += 32) {
+    const int i = i0 + lane;
+    const unsigned mis = __ballot_sync(0xffffffffu, i < K && x[i] != __ldcg(g + min(i, K)));
+    if (mis) {
+      n = i0 + __ffs(mis) - 1;
+      break;
     }
-    __syncthreads();
-    unit = sm.next;
-    __syncthreads();
   }
+  const int gn = bad ? -1 : __ldcg(g + n);
+  int32_t* out = a.out_tokens + (size_t)b * (K + 1);
+  for (int j = lane; j <= K; j += 32) out[j] = bad ? -1 : (j < n ? x[j] : (j == n ? gn : -1));
+  if (lane == 0) {
+    a.out_n[b] = bad ? -1 : n;
+    if (bad) atomicOr(a.status, kStatusBadData);
+  }
+  __syncwarp();
 }
 
-template <class E, int VEC>
-__global__ void __launch_bounds__(kThreads) tree_kernel(const GreedyArgs a) {
-  __shared__ TreeSmem ts;
-  ArgmaxSmem& sm = ts.base;
-  if (threadIdx.x == 0) sm.next = (long long)atomicAdd((unsigned long long*)a.counter, 1ull);
-  __syncthreads();
-  long long unit = sm.next;
-  __syncthreads();
+// Tree finisher (one warp): argmax of every row, acceptance in node order
+// (parents precede children), the deepest accepted path, the bonus token and
+// the ancestor-or-self bitmask (one word column per lane).
+__device__ __noinline__ void tree_finisher(const GreedyArgs& a, int b) {
   const int N = a.K;
   const int W = (N + 31) >> 5;
-  while (unit < a.map.total) {
-    if (threadIdx.x == 0) sm.next = (long long)atomicAdd((unsigned long long*)a.counter, 1ull);
-    const int b = (int)(unit / a.map.A), idx = (int)(unit % a.map.A);
-    if (argmax_unit<E, VEC>(a, b, idx, sm)) {
-      const int32_t* tok = a.tokens + (size_t)b * N;
-      const int32_t* par = a.parents + (size_t)b * N;
-      int bad = 0;
-      for (int r = threadIdx.x; r <= N; r += kThreads) {
-        ts.g[r] = merged_argmax(a, b, r);
-        bad |= ts.g[r] < 0;
-        if (a.out_row_argmax) a.out_row_argmax[(size_t)b * (N + 1) + r] = ts.g[r];
-      }
-      for (int i = threadIdx.x; i < N; i += kThreads)
-        bad |= par[i] < -1 || par[i] >= i || tok[i] < 0 || tok[i] >= a.V;
-      bad = __syncthreads_or(bad);
-      int32_t* path = a.out_tokens + (size_t)b * (N + 1);
-      uint32_t* mask = a.out_mask + (size_t)b * N * W;
-      if (bad) {
-        for (int j = threadIdx.x; j <= N; j += kThreads) path[j] = -1;
-        for (int j = threadIdx.x; j < N * W; j += kThreads) mask[j] = 0u;
-        if (threadIdx.x == 0) {
-          a.out_n[b] = -1;
-          atomicOr(a.status, kStatusBadData);
-        }
-      } else {
-        if (threadIdx.x == 0) {
-          // parents precede children, so one pass in node order settles acceptance
-          int best = -1, bd = 0;
-          for (int i = 0; i < N; ++i) {
-            const int p = par[i];
-            const bool ok = (p < 0 || ts.acc[p]) && tok[i] == ts.g[p + 1];
-            ts.acc[i] = ok;
-            ts.depth[i] = p < 0 ? 1 : ts.depth[p] + 1;
-            if (ok && ts.depth[i] > bd) {
-              bd = ts.depth[i];
-              best = i;
-            }
-          }
-          int pos = bd - 1;
-          for (int node = best; node >= 0; node = par[node]) path[pos--] = tok[node];
-          path[bd] = ts.g[best + 1];
-          a.out_n[b] = bd + 1;
-          ts.best = bd;
-        }
-        __syncthreads();
-        for (int j = ts.best + 1 + threadIdx.x; j <= N; j += kThreads) path[j] = -1;
-        // ancestor-or-self bitmask, one word column per thread, node order
-        for (int w = threadIdx.x; w < W; w += kThreads) {
-          for (int i = 0; i < N; ++i) {
-            const int p = par[i];
-            uint32_t word = p >= 0 ? mask[(size_t)p * W + w] : 0u;
-            if ((i >> 5) == w) word |= 1u << (i & 31);
-            mask[(size_t)i * W + w] = word;
-          }
-        }
+  const int lane = threadIdx.x & 31;
+  const int32_t* tok = a.tokens + (size_t)b * N;
+  const int32_t* par = a.parents + (size_t)b * N;
+  const int* g = a.g + (size_t)b * (N + 1);
+  int* depth = a.depth + (size_t)b * (N + 1);
+  int* acc = a.acc + (size_t)b * (N + 1);
+  bool bad = false;
+  for (int r = lane; r <= N; r += 32) {
+    const int v = row_g(a, b, r);
+    bad |= v < 0;
+    if (a.out_row_argmax) a.out_row_argmax[(size_t)b * (N + 1) + r] = v < 0 ? -1 : v;
+  }
+  for (int i = lane; i < N; i += 32) bad |= par[i] < -1 || par[i] >= i || tok[i] < 0 || tok[i] >= a.V;
+  bad = __any_sync(0xffffffffu, bad);
+  __threadfence();
+  __syncwarp();
+  int32_t* path = a.out_tokens + (size_t)b * (N + 1);
+  uint32_t* mask = a.out_mask + (size_t)b * N * W;
+  if (bad) {
+    for (int j = lane; j <= N; j += 32) path[j] = -1;
+    for (int j = lane; j < N * W; j += 32) mask[j] = 0u;
+    if (lane == 0) {
+      a.out_n[b] = -1;
+      atomicOr(a.status, kStatusBadData);
+    }
+    __syncwarp();
+    return;
+  }
+  int bd = 0;
+  if (lane == 0) {
+    int best = -1;
+    for (int i = 0; i < N; ++i) {
+      const int p = par[i];
+      const bool ok = (p < 0 || acc[p]) && tok[i] == __ldcg(g + p + 1);
+      acc[i] = ok;
+      depth[i] = p < 0 ? 1 : depth[p] + 1;
+      if (ok && depth[i] > bd) {
+        bd = depth[i];
+        best = i;
       }
     }
-    __syncthreads();
-    unit = sm.next;
-    __syncthreads();
+    int pos = bd - 1;
+    for (int node = best; node >= 0; node = par[node]) path[pos--] = tok[node];
+    path[bd] = __ldcg(g + best + 1);
+    a.out_n[b] = bd + 1;
+  }
+  bd = __shfl_sync(0xffffffffu, bd, 0);
+  for (int j = bd + 1 + lane; j <= N; j += 32) path[j] = -1;
+  for (int w = lane; w < W; w += 32) {
+    for (int i = 0; i < N; ++i) {
+      const int p = par[i];
+      uint32_t word = p >= 0 ? mask[(size_t)p * W + w] : 0u;
+      if ((i >> 5) == w) word |= 1u << (i & 31);
+      mask[(size_t)i * W + w] = word;
+    }
+  }
+  __syncwarp();
+}
+
+// Independent warps claim units in increasing order from their counters.
+// The warp taking a row's last ticket merges the row; the one merging a
+// sequence's last row runs its finisher.  The only waits are for stores that
+// are already issued (slots leaving the marker state).
+template <class E, int VEC, bool TREE>
+__global__ void __launch_bounds__(kThreads, kMinBlocks) argmax_kernel(const __grid_constant__ GreedyArgs a) {
+  const int lane = threadIdx.x & 31;
+  const int w = slice_of_warp();
+  const int last = a.CU * kSlices - 1;  // the last slice of a row
+  int unit = bcast(claim_unit(a.counter, lane));
+  while (unit < a.map.total) {
+    const int next = claim_unit(a.counter, lane);
+    const int b = unit / a.map.A, idx = unit - (unit / a.map.A) * a.map.A;
+    const int old = __shfl_sync(0xffffffffu, argmax_slice<E, VEC>(a, b, idx, w), 0);
+    if (old == last && row_argmax_finisher(a, b, idx / a.CU)) {
+      if (TREE)
+        tree_finisher(a, b);
+      else
+        chain_finisher(a, b);
+    }
+    unit = bcast(next);
   }
 }
 
@@ -252,48 +292,60 @@ __global__ void __launch_bounds__(kThreads) tree_kernel(const GreedyArgs a) {
 // ---------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-size_t greedy_workspace_bytes(int B, int R, int C, size_t* counter_bytes) {
-  size_t off = 16 + align_up((size_t)B * 4, 16);
-  if (counter_bytes) *counter_bytes = off;
-  off = align_up(off, 256);
-  const size_t n = (size_t)B * R * C;
-  off += align_up(n * 4, 256) * 3;
-  return off;
+// Workspace: [zero-filled: counters, tickets][marker-filled: part, g][depth, acc].
+static void greedy_layout(int B, int R, int CU, size_t* off) {
+  const size_t C = (size_t)CU * kSlices;
+  size_t o = 0;
+  off[0] = o; o += kCounterBytes;                                     // counter
+  off[1] = o; o += align_up((size_t)B * R * kTicketStride * 4, 16);  // rowticket
+  off[2] = o; o += align_up((size_t)B * 4, 16);                      // seqticket
+  o = align_up(o, 256);
+  off[3] = o;                                                         // end of zero region
+  off[4] = o; o += align_up((size_t)B * R * C * sizeof(uint2), 256);  // part
+  off[5] = o; o += align_up((size_t)B * R * 4, 256);                  // g
+  off[6] = o;                                                         // end of marker region
+  off[7] = o; o += align_up((size_t)B * R * 4, 256);                  // depth
+  off[8] = o; o += align_up((size_t)B * R * 4, 256);                  // acc
+  off[9] = o;
+}
+
+WsLayout greedy_workspace(int B, int R, int CU) {
+  size_t off[10];
+  greedy_layout(B, R, CU, off);
+  WsLayout l;
+  l.total = off[9];
+  l.zero_bytes = off[3];
+  l.marker_off = off[4];
+  l.marker_bytes = off[6] - off[4];
+  return l;
 }
 
 void greedy_bind_workspace(GreedyArgs& a, void* ws) {
+  size_t off[10];
+  greedy_layout(a.B, a.R, a.CU, off);
   char* p = (char*)ws;
-  a.counter = (int*)p;
-  p += 16;
-  a.ticket1 = (int*)p;
-  p += align_up((size_t)a.B * 4, 16);
-  p = (char*)ws + align_up((size_t)(p - (char*)ws), 256);
-  const size_t n = (size_t)a.B * a.R * a.C;
-  a.part_v = (float*)p;
-  p += align_up(n * 4, 256);
-  a.part_i = (int*)p;
-  p += align_up(n * 4, 256);
-  a.part_nan = (int*)p;
+  a.counter = (unsigned long long*)(p + off[0]);
+  a.rowticket = (int*)(p + off[1]);
+  a.seqticket = (int*)(p + off[2]);
+  a.part = (uint2*)(p + off[4]);
+  a.g = (int*)(p + off[5]);
+  a.depth = (int*)(p + off[7]);
+  a.acc = (int*)(p + off[8]);
 }
 
-template <class E, int VEC>
-static cudaError_t launch_greedy_t(const GreedyArgs& a, int grid, cudaStream_t s) {
-  greedy_kernel<E, VEC><<<grid, kThreads, 0, s>>>(a);
-  return cudaGetLastError();
-}
-template <class E, int VEC>
-static cudaError_t launch_tree_t(const GreedyArgs& a, int grid, cudaStream_t s) {
-  tree_kernel<E, VEC><<<grid, kThreads, 0, s>>>(a);
+template <class E, int VEC, bool TREE>
+static cudaError_t launch_t(const GreedyArgs& a, int grid, cudaStream_t s) {
+  argmax_kernel<E, VEC, TREE><<<grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
 cudaError_t launch_greedy(const GreedyArgs& a, bool bf16, bool vec, int grid, cudaStream_t s) {
-  if (bf16) return vec ? launch_greedy_t<BF16, 8>(a, grid, s) : launch_greedy_t<BF16, 1>(a, grid, s);
-  return vec ? launch_greedy_t<F32, 4>(a, grid, s) : launch_greedy_t<F32, 1>(a, grid, s);
+  if (bf16) return vec ? launch_t<BF16, 8, false>(a, grid, s) : launch_t<BF16, 1, false>(a, grid, s);
+  return vec ? launch_t<F32, 4, false>(a, grid, s) : launch_t<F32, 1, false>(a, grid, s);
 }
 cudaError_t launch_tree(const GreedyArgs& a, bool bf16, bool vec, int grid, cudaStream_t s) {
-  if (bf16) return vec ? launch_tree_t<BF16, 8>(a, grid, s) : launch_tree_t<BF16, 1>(a, grid, s);
-  return vec ? launch_tree_t<F32, 4>(a, grid, s) : launch_tree_t<F32, 1>(a, grid, s);
+  if (bf16) return vec ? launch_t<BF16, 8, true>(a, grid, s) : launch_t<BF16, 1, true>(a, grid, s);
+  return vec ? launch_t<F32, 4, true>(a, grid, s) : launch_t<F32, 1, true>(a, grid, s);
 }
 
 template <class K>
@@ -304,12 +356,12 @@ static int occ(K kernel) {
 }
 
 int greedy_blocks_per_sm(bool bf16, bool vec) {
-  if (bf16) return vec ? occ(greedy_kernel<BF16, 8>) : occ(greedy_kernel<BF16, 1>);
-  return vec ? occ(greedy_kernel<F32, 4>) : occ(greedy_kernel<F32, 1>);
+  if (bf16) return vec ? occ(argmax_kernel<BF16, 8, false>) : occ(argmax_kernel<BF16, 1, false>);
+  return vec ? occ(argmax_kernel<F32, 4, false>) : occ(argmax_kernel<F32, 1, false>);
 }
 int tree_blocks_per_sm(bool bf16, bool vec) {
-  if (bf16) return vec ? occ(tree_kernel<BF16, 8>) : occ(tree_kernel<BF16, 1>);
-  return vec ? occ(tree_kernel<F32, 4>) : occ(tree_kernel<F32, 1>);
+  if (bf16) return vec ? occ(argmax_kernel<BF16, 8, true>) : occ(argmax_kernel<BF16, 1, true>);
+  return vec ? occ(argmax_kernel<F32, 4, true>) : occ(argmax_kernel<F32, 1, true>);
 }
 
 }  // namespace sv

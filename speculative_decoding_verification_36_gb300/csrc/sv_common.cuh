@@ -14,11 +14,11 @@
 
 namespace sv {
 
-constexpr unsigned kSpinLimit = 1u << 22; // bounded waits: about 0.5 s with 128 ns naps
+constexpr unsigned kSpinLimit = 1u << 22;  // bounded waits: about 0.5 s with 128 ns naps
 
 // status bits OR-ed into the library's device status word
-constexpr unsigned kStatusBadData = 1u;   // NaN / +inf logit, empty row, bad token or parent
-constexpr unsigned kStatusTimeout = 2u;   // a bounded wait ran out (should never happen)
+constexpr unsigned kStatusBadData = 1u;  // NaN / +inf logit, empty row, bad token or parent
+constexpr unsigned kStatusTimeout = 2u;  // a bounded wait ran out (should never happen)
 
 __device__ __forceinline__ float neg_inf() { return __int_as_float(0xff800000); }
 
@@ -27,6 +27,87 @@ __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
+}
+
+// ---------------------------------------------------------------------------
+// packed fp32 pairs (f32x2 arithmetic: two IEEE operations per instruction)
+// ---------------------------------------------------------------------------
+typedef unsigned long long f2_t;
+__device__ __forceinline__ f2_t f2(float lo, float hi) {
+  f2_t r;
+  asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
+  return r;
+}
+__device__ __forceinline__ float f2lo(f2_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  (void)hi;
+  return lo;
+}
+__device__ __forceinline__ float f2hi(f2_t v) {
+  float lo, hi;
+  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
+  (void)lo;
+  return hi;
+}
+__device__ __forceinline__ f2_t f2sub(f2_t a, f2_t b) {
+  f2_t r;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t f2mul(f2_t a, f2_t b) {
+  f2_t r;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+__device__ __forceinline__ f2_t f2fma(f2_t a, f2_t b, f2_t c) {
+  f2_t r;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(r) : "l"(a), "l"(b), "l"(c));
+  return r;
+}
+__device__ __forceinline__ f2_t f2add(f2_t a, f2_t b) {
+  f2_t r;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
+  return r;
+}
+// 2^{(z - base) * c} for both halves, accumulated into acc (per-element IEEE
+// rounding identical to the scalar sequence sub, mul, ex2, add).
+__device__ __forceinline__ void f2_exp_acc(f2_t& acc, f2_t z, f2_t base, f2_t c) {
+  const f2_t t = f2mul(f2sub(z, base), c);
+  acc = f2add(acc, f2(ex2(f2lo(t)), ex2(f2hi(t))));
+}
+
+// 2^t for both halves of t (t <= 0) on the FMA pipe instead of the MUFU unit.
+// Cody and Waite's reduction t = j + f with j = rint(t) (the 1.5 * 2^23
+// rounding constant) and |f| <= 1/2; 2^f from the degree-6 polynomial fitted to
+// the relative error on [-1/2, 1/2] by the Remez exchange (gen_exp2_poly.py:
+// at most 1.01e-7 relative after fp32 evaluation, comparable to ex2.approx);
+// 2^j is added to the exponent field.  Inputs below -125 are clamped, so the
+// result is never below 2^-125.5 (an exact 0 is never produced).
+__device__ __forceinline__ f2_t exp2_poly2(f2_t t) {
+  const f2_t tc = f2(fmaxf(f2lo(t), -125.f), fmaxf(f2hi(t), -125.f));
+  const f2_t magic = f2(12582912.f, 12582912.f);
+  const f2_t r = f2add(tc, magic);               // bits(r) = 0x4b400000 + j
+  const f2_t f = f2sub(tc, f2sub(r, magic));     // exact, |f| <= 1/2
+  f2_t p = f2fma(f, f2(0x1.41d334p-13f, 0x1.41d334p-13f), f2(0x1.5f456ap-10f, 0x1.5f456ap-10f));
+  p = f2fma(f, p, f2(0x1.3b2dbcp-7f, 0x1.3b2dbcp-7f));
+  p = f2fma(f, p, f2(0x1.c6aed4p-5f, 0x1.c6aed4p-5f));
+  p = f2fma(f, p, f2(0x1.ebfbdap-3f, 0x1.ebfbdap-3f));
+  p = f2fma(f, p, f2(0x1.62e430p-1f, 0x1.62e430p-1f));
+  p = f2fma(f, p, f2(1.f, 1.f));
+  // (0x4b400000 << 23) vanishes modulo 2^32, so bits(r) << 23 is j << 23
+  const uint32_t lo = __float_as_uint(f2lo(p)) + (__float_as_uint(f2lo(r)) << 23);
+  const uint32_t hi = __float_as_uint(f2hi(p)) + (__float_as_uint(f2hi(r)) << 23);
+  return f2(__uint_as_float(lo), __uint_as_float(hi));
+}
+__device__ __forceinline__ void f2_exp_acc_poly(f2_t& acc, f2_t z, f2_t base, f2_t c) {
+  acc = f2add(acc, exp2_poly2(f2mul(f2sub(z, base), c)));
+}
+
+__device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
+  uint32_t r;
+  asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
+  return r;
 }
 
 // 16-byte streaming load that does not allocate in L1 (the data is read once
@@ -60,7 +141,7 @@ struct BF16 {
 };
 
 // VEC elements kept in their storage form (16 bytes on the vector path) and
-// widened to fp32 when used; this halves the registers a bf16 batch needs.
+// widened to fp32 when used.
 template <class E, int VEC>
 struct Raw {
   uint4 w;
@@ -103,8 +184,46 @@ __device__ __forceinline__ float elem(const Raw<E, VEC>& r, int q) {
   }
 }
 
-// Coherent (L1-bypassing) loads of workspace values written by other CTAs.
-__device__ __forceinline__ float2 ldcg_f2(const float2* p) { return __ldcg(p); }
+// Elements 2p and 2p+1 of a loaded vector as a packed pair.
+template <class E, int VEC>
+__device__ __forceinline__ f2_t elem_pair(const Raw<E, VEC>& r, int p) {
+  if constexpr (VEC == 8) {
+    const uint32_t w = word_of(r.w, p);
+    return f2(bf16_lo(w), bf16_hi(w));
+  } else {
+    return f2(__uint_as_float(word_of(r.w, 2 * p)), __uint_as_float(word_of(r.w, 2 * p + 1)));
+  }
+}
+
+// Maximum over a batch of kUnroll loaded vectors (NaN never wins: max ignores
+// a NaN operand).
+template <class E, int VEC>
+__device__ __forceinline__ float batch_max(const Raw<E, VEC> (&z)[kUnroll]) {
+  if constexpr (VEC == 8) {
+    uint32_t mw = bf16x2_max(bf16x2_max(z[0].w.x, z[0].w.y), bf16x2_max(z[0].w.z, z[0].w.w));
+#pragma unroll
+    for (int u = 1; u < kUnroll; ++u)
+      mw = bf16x2_max(mw, bf16x2_max(bf16x2_max(z[u].w.x, z[u].w.y), bf16x2_max(z[u].w.z, z[u].w.w)));
+    return fmaxf(bf16_lo(mw), bf16_hi(mw));
+  } else {
+    float bm = neg_inf();
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u)
+#pragma unroll
+      for (int q = 0; q < VEC; ++q) bm = fmaxf(bm, elem(z[u], q));
+    return bm;
+  }
+}
+
+// Bulk L2 prefetch (TMA engine) of a contiguous byte range: one instruction
+// starts streaming a whole slice into L2 while the warp works, so the warp's
+// own loads mostly wait on L2 rather than DRAM.  Start and size must be
+// multiples of 16 bytes (the vector path guarantees both).
+__device__ __forceinline__ void prefetch_l2(const void* p, unsigned bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p), "r"(bytes) : "memory");
+}
+
+// Coherent loads / stores / atomics on workspace values shared between warps.
 __device__ __forceinline__ int ld_acquire(const int* p) {
   int v;
   asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
@@ -113,6 +232,87 @@ __device__ __forceinline__ int ld_acquire(const int* p) {
 __device__ __forceinline__ void st_release(int* p, int v) {
   asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
+__device__ __forceinline__ int atom_add_acq_rel(int* p, int v) {
+  int old;
+  asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Relaxed (unordered, cheap) 64-bit stores / loads and atomics for per-slice
+// results.  A reader learns that a slot is complete from its content: slots are
+// pre-filled with the kMarker pattern (a NaN no result ever takes).
+__device__ __forceinline__ void st_relaxed_u2(void* p, uint32_t x, uint32_t y) {
+  asm volatile("st.relaxed.gpu.global.v2.u32 [%0], {%1,%2};" ::"l"(p), "r"(x), "r"(y) : "memory");
+}
+__device__ __forceinline__ uint2 ld_relaxed_u2(const void* p) {
+  uint2 v;
+  asm volatile("ld.relaxed.gpu.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_relaxed_s32(int* p, int v) {
+  asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+__device__ __forceinline__ int ld_relaxed_s32(const int* p) {
+  int v;
+  asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ void st_release_f64(double* p, double v) {
+  asm volatile("st.release.gpu.global.f64 [%0], %1;" ::"l"(p), "d"(v) : "memory");
+}
+__device__ __forceinline__ double ld_acquire_f64(const double* p) {
+  double v;
+  asm volatile("ld.acquire.gpu.global.f64 %0, [%1];" : "=d"(v) : "l"(p) : "memory");
+  return v;
+}
+__device__ __forceinline__ int atom_add_relaxed(int* p, int v) {
+  int old;
+  asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+  return old;
+}
+
+// Bounded waits for a slot to leave the marker state.  A ticket count says
+// every writer has issued its store; the store itself may land a moment later.
+__device__ __forceinline__ uint2 wait_u2(const void* p, unsigned* status) {
+  uint2 v = ld_relaxed_u2(p);
+  unsigned it = 0;
+  while (v.x == kMarker && ++it < kSpinLimit) {
+    __nanosleep(64);
+    v = ld_relaxed_u2(p);
+  }
+  if (v.x == kMarker) atomicOr(status, kStatusTimeout);
+  return v;
+}
+__device__ __forceinline__ int wait_s32(const int* p, unsigned* status) {
+  int v = ld_relaxed_s32(p);
+  unsigned it = 0;
+  while (v == (int)kMarker && ++it < kSpinLimit) {
+    __nanosleep(64);
+    v = ld_relaxed_s32(p);
+  }
+  if (v == (int)kMarker) atomicOr(status, kStatusTimeout);
+  return v;
+}
+__device__ __forceinline__ double wait_f64_acquire(const double* p, unsigned* status) {
+  double v = ld_acquire_f64(p);
+  unsigned it = 0;
+  while (__double_as_longlong(v) == -1LL && ++it < kSpinLimit) {
+    __nanosleep(64);
+    v = ld_acquire_f64(p);
+  }
+  if (__double_as_longlong(v) == -1LL) atomicOr(status, kStatusTimeout);
+  return v;
+}
+
+// Lane 0 of warp w claims the next unit from counter w; the value is
+// broadcast when it is used.
+__device__ __forceinline__ int slice_of_warp() { return (threadIdx.x >> 5) % kSlices; }
+__device__ __forceinline__ int claim_unit(unsigned long long* counter, int lane) {
+  int v = 0;
+  if (lane == 0) v = (int)atomicAdd(counter + slice_of_warp() * kCounterStride, 1ull);
+  return v;
+}
+__device__ __forceinline__ int bcast(int v) { return __shfl_sync(0xffffffffu, v, 0); }
 
 // ---------------------------------------------------------------------------
 // Online softmax statistics: (m, s) with m the running max of the raw logits
@@ -126,14 +326,18 @@ __device__ __forceinline__ void ms_merge(float& m, float& s, float m2, float s2,
   m = mn;
 }
 
-// Butterfly merge of (m, s) across the 32 lanes; every lane ends with the total.
+// (m, s) over the 32 lanes, every lane ends with the total: the warp max
+// first, then each lane's sum rescaled to it once, then a butterfly sum.
 __device__ __forceinline__ void warp_ms(float& m, float& s, float c) {
+  float mx = m;
 #pragma unroll
-  for (int off = 16; off > 0; off >>= 1) {
-    float m2 = __shfl_xor_sync(0xffffffffu, m, off);
-    float s2 = __shfl_xor_sync(0xffffffffu, s, off);
-    ms_merge(m, s, m2, s2, c);
-  }
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  const float base = (mx == neg_inf()) ? 0.f : mx;
+  float t = s * ex2((m - base) * c);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
+  m = mx;
+  s = t;
 }
 
 // Argmax with the lowest index winning ties.

@@ -1,5 +1,15 @@
 // sv_kernels.h -- parameter blocks and launchers shared by the C-ABI layer
 // (api.cu) and the kernel translation units.  Internal to the library.
+//
+// Work decomposition (all three kernels): a persistent grid of independent
+// warps.  A row is cut into slices of SL elements; eight consecutive slices of
+// a row form a unit.  Warp w of every CTA claims units from counter w (one of
+// eight) and processes slice w of each unit it claims, so the eight slices of
+// a unit are streamed at about the same time by eight different warps while
+// each claim counter sees only one eighth of the traffic.  A slice is reduced
+// to one partial result in the workspace; the warp that takes a sequence's
+// last ticket runs that sequence's finisher.  There are no CTA-wide barriers:
+// a warp that waits or finishes a sequence stalls only itself.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -7,12 +17,14 @@
 
 namespace sv {
 
-constexpr int kThreads = 512;             // threads per CTA for every kernel
+constexpr int kThreads = 256;  // 8 independent warps per CTA
 constexpr int kWarps = kThreads / 32;
-constexpr int kUnroll = 4;                // 16-byte vectors in flight per thread (statistics, argmax)
-constexpr int kTailUnroll = 2;            // vectors in flight per row in the tail units
-constexpr int kMaxSteps = 32;             // steps (kThreads vectors) per chunk: pieces <= 512
-constexpr int kMaxK = 255;                // rows per sequence stay <= 2*255+1 < kThreads
+constexpr int kSlices = kWarps;  // slices per unit (warp w takes slice w)
+constexpr int kCounterStride = 16;  // claim counters 128 bytes apart
+constexpr int kTicketStride = 8;    // per-row tickets 32 bytes apart (no same-address pile-up)
+constexpr int kMinBlocks = 4;  // resident CTAs per SM the register budget allows (64 regs)
+constexpr int kUnroll = 2;     // 16-byte vectors per lane per load batch; two batches in flight
+constexpr int kMaxK = 255;
 constexpr int kMaxTreeNodes = 1024;
 
 // Per-sequence decision left by the statistics finisher for the tail units.
@@ -30,16 +42,15 @@ constexpr int kModeResidual = 0;
 constexpr int kModeBonus = 1;
 constexpr int kModeBad = 2;
 
-// Work units are chunks of rows.  A persistent grid claims them in a global
-// order in which each sequence's statistics units come first and its tail
-// units (the residual / bonus row, split the same way) follow `delta`
-// sequences later, so that the re-read of the tail row hits L2.
+// The global order of units: each sequence's statistics units come first and
+// its tail units (the residual / bonus row, chunked the same way) follow
+// `delta` sequences later, so that the re-read of the tail row hits L2.
 struct UnitMap {
   int B;
-  int A;      // statistics units per sequence (rows * chunks)
-  int T;      // tail units per sequence (0 for the greedy kernels)
+  int A;      // statistics units per sequence (rows * CU)
+  int T;      // tail units per sequence (CU; 0 for the argmax kernels)
   int delta;  // slack, in sequences, between statistics and tail units
-  long long total;
+  int total;  // units per counter: B * (A + T)
 };
 
 struct SampleArgs {
@@ -48,9 +59,10 @@ struct SampleArgs {
   const int32_t* tokens;
   int B, K, V;
   int R;   // rows per sequence = 2K+1
-  int CH;  // chunk length in elements (multiple of 8)
-  int C;   // chunks per row
-  int P;   // piece slots per tail unit
+  int SL;  // slice length in elements (a whole number of load batches)
+  int CS;  // slices per row = ceil(V / SL)
+  int CU;  // units per row = ceil(CS / kSlices)
+  int P;   // pieces (warp steps) per slice
   UnitMap map;
   float c_hi, c_lo;  // log2(e)/temperature as a float pair
   double c64;        // the same in double
@@ -61,42 +73,54 @@ struct SampleArgs {
   float* out_row_stats;  // optional [B, R, 2]: max(z)/tau, sum exp(z/tau - max)
   float* out_pq;         // optional [B, K, 2]: p_i(x_i), q_i(x_i)
   float* out_resid;      // optional [B]: mass of the replacement distribution
-  // workspace
-  int* counter;   // [1] 64-bit count of claimed units
-  int* ticket1;   // [B] finished statistics units
-  int* ticket2;   // [B] finished tail units
-  int* ready;     // [B] 0 until the statistics finisher published SeqInfo
-  float2* part;   // [B, R, C] per-chunk (m, s)
-  SeqInfo* info;  // [B]
-  double* tailsum;  // [B, C] per tail-unit mass
-  float* pieces;    // [B, C, P] per-piece mass
+  // workspace.  Zero-filled before the launch: counter, rowticket, seqticket,
+  // tailticket, ready.  Filled with all-ones bytes (a NaN "not yet written"
+  // marker) before the launch: part, rowstat, tailsum.
+  unsigned long long* counter;  // kSlices claim counters, kCounterStride apart
+  int* rowticket;   // [B, R] (kTicketStride apart) finished slices of a row
+  int* seqticket;   // [B] finished rows of a sequence
+  int* tailticket;  // [B] finished tail slices
+  int* ready;       // [B] 0 until the statistics finisher published SeqInfo
+  float2* part;     // [B, R, CU * kSlices] per-slice (m, s)
+  float2* rowstat;  // [B, R] merged (m, s) of each row
+  double* tailsum;  // [B, CU * kSlices] per tail-slice mass
+  SeqInfo* info;    // [B]
+  float* pieces;    // [B, CU * kSlices, P] per-piece mass
   unsigned* status;
 };
 
 struct GreedyArgs {
   const void* target;
-  const int32_t* tokens;     // chain: [B, K]; tree: [B, N]
-  const int32_t* parents;    // tree only: [B, N]
-  int B, K, V;               // chain: K drafts; tree: K = N nodes
-  int R;                     // rows per sequence: K+1 (chain) or N+1 (tree)
-  int CH, C;
+  const int32_t* tokens;   // chain: [B, K]; tree: [B, N]
+  const int32_t* parents;  // tree only: [B, N]
+  int B, K, V;             // chain: K drafts; tree: K = N nodes
+  int R;                   // rows per sequence: K+1 (chain) or N+1 (tree)
+  int SL, CS, CU;          // slice length, slices per row, units per row
   UnitMap map;
-  int32_t* out_tokens;       // chain [B, K+1]; tree out_path [B, N+1]
-  int32_t* out_n;            // chain [B];     tree out_len  [B]
-  uint32_t* out_mask;        // tree [B, N, ceil(N/32)]
-  int32_t* out_row_argmax;   // optional [B, R]
-  int* counter;
-  int* ticket1;
-  float* part_v;             // [B, R, C] chunk max
-  int* part_i;               // [B, R, C] chunk argmax (lowest index)
-  int* part_nan;             // [B, R, C] chunk saw a NaN
+  int32_t* out_tokens;      // chain [B, K+1]; tree out_path [B, N+1]
+  int32_t* out_n;           // chain [B];     tree out_len  [B]
+  uint32_t* out_mask;       // tree [B, N, ceil(N/32)]
+  int32_t* out_row_argmax;  // optional [B, R]
+  // workspace.  Zero-filled: counter, rowticket, seqticket.  All-ones
+  // ("not yet written" marker): part, g.
+  unsigned long long* counter;  // kSlices claim counters, kCounterStride apart
+  int* rowticket;  // [B, R] (kTicketStride apart) finished slices of a row
+  int* seqticket;  // [B] finished rows of a sequence
+  uint2* part;     // [B, R, CU * kSlices] slice (max bits, argmax | NaN-seen << 31)
+  int* g;          // [B, R] row argmax, -2 for an unusable row
+  int* depth;     // [B, R] tree finisher scratch
+  int* acc;       // [B, R] tree finisher scratch
   unsigned* status;
 };
 
-// Workspace bytes for each kernel (the counters come first and are zeroed by
-// the caller before every launch; `counter_bytes` reports how many).
-size_t sample_workspace_bytes(int B, int K, int C, int P, size_t* counter_bytes);
-size_t greedy_workspace_bytes(int B, int R, int C, size_t* counter_bytes);
+// Workspace layout of each kernel: `total` bytes; [0, zero_bytes) must be
+// zero-filled and [marker_off, marker_off + marker_bytes) filled with 0xff
+// bytes before every launch.
+struct WsLayout {
+  size_t total, zero_bytes, marker_off, marker_bytes;
+};
+WsLayout sample_workspace(int B, int K, int CU, int P);
+WsLayout greedy_workspace(int B, int R, int CU);
 
 // Bind workspace pointers into the argument blocks.
 void sample_bind_workspace(SampleArgs& a, void* ws);
@@ -113,7 +137,14 @@ int sample_blocks_per_sm(bool bf16, bool vec);
 int greedy_blocks_per_sm(bool bf16, bool vec);
 int tree_blocks_per_sm(bool bf16, bool vec);
 
-// Piece slots per tail unit for a chunk of CH elements.
-int sample_pieces_per_unit(int CH, bool bf16, bool vec);
+// Elements per warp step (32 lanes x one vector) and per load batch.
+inline int step_elems(bool bf16, bool vec) { return 32 * (vec ? (bf16 ? 8 : 4) : 1); }
+inline int batch_elems(bool bf16, bool vec) { return step_elems(bf16, vec) * kUnroll; }
+
+// Bytes of the claim-counter block at the start of each workspace.
+constexpr size_t kCounterBytes = (size_t)kSlices * kCounterStride * 8;
+
+// The bit pattern of a slot that has not been written yet.
+constexpr unsigned kMarker = 0xffffffffu;
 
 }  // namespace sv

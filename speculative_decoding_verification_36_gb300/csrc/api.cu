@@ -78,9 +78,8 @@ int get_device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Tuning knobs (environment, read once): SPECVERIFY_SLICE_BYTES (bytes of
-// logits per slice, default 8192) and SPECVERIFY_DELTA (sequences between a
-// sequence's statistics and tail units; 0 = automatic).
+// Tuning knob (environment, read once): SPECVERIFY_SLICE_BYTES, the bytes of
+// logits per slice (default 8192).
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
@@ -151,10 +150,7 @@ int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
   a.V = V;
   a.R = K + 1;
   choose_slices(V, vec ? (bf16 ? 8 : 4) : 1, esz, &a.SL, &a.CS, &a.CU);
-  a.map.B = B;
   a.map.A = a.R * a.CU;
-  a.map.T = 0;
-  a.map.delta = 0;
   a.map.total = B * a.map.A;
   a.out_tokens = out_tokens;
   a.out_n = out_n;
@@ -211,16 +207,9 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   const int vec_elems = vec ? (bf16 ? 8 : 4) : 1;
   choose_slices(V, vec_elems, esz, &a.SL, &a.CS, &a.CU);
   a.P = (a.SL + 32 * vec_elems - 1) / (32 * vec_elems);
-  a.map.B = B;
   a.map.A = a.R * a.CU;
-  a.map.T = a.CU;
-  a.map.total = B * (a.map.A + a.map.T);
+  a.map.total = B * a.map.A;
   const int grid = grid_for(a.map.total, capacity);
-  // Tail units trail their sequence by the units claimed while a sequence's
-  // statistics complete and its decision is made (about two grids' worth).
-  static const int delta_env = env_int("SPECVERIFY_DELTA", 0);
-  a.map.delta = delta_env > 0 ? delta_env
-                              : (2 * grid + a.map.A + a.map.T - 1) / (a.map.A + a.map.T) + 1;
   const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
   a.c64 = c;
   a.c_hi = (float)c;

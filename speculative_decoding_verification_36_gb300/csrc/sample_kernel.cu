@@ -17,13 +17,16 @@
 //     exp2) pass with 16-byte streaming loads and packed f32x2 arithmetic,
 //     reduced to one (m, s) pair in the workspace.  The warp that takes a
 //     sequence's last statistics ticket merges the slice pairs, runs steps
-//     2-4 in fp64 and publishes the sequence's decision.
-//   * tail slice = SL elements of the tail row (pair): after the decision is
-//     published (a bounded wait) it writes the mass of every warp step
-//     ("piece") of the replacement / bonus distribution.  Tail units are
-//     queued `delta` sequences after the statistics units, so the re-read rows
-//     are still in L2.  The warp that takes the last tail ticket finds the CDF
-//     crossing from the slice and piece masses and rescans one piece.
+//     2-4 in fp64 and appends the sequence's decision to the decision queue.
+//   * tail slice = SL elements of the tail row (pair) of a decided sequence:
+//     the mass of every warp step ("piece") of the replacement / bonus
+//     distribution.  Tail item t (queue position t / CU, unit t % CU) belongs
+//     to warp slot w of CTA t % grid.  A warp polls its next item's queue
+//     entry while it streams statistics slices and takes the item as soon as
+//     the entry is there, so no warp ever waits for a decision while
+//     statistics work is left, and the re-read rows are still in L2.  The warp
+//     that takes the last tail ticket finds the CDF crossing from the slice
+//     and piece masses and rescans one piece.
 // Every reduction runs in a fixed order, so results are run-to-run identical.
 #include "sv_common.cuh"
 #include "sv_kernels.h"
@@ -31,46 +34,6 @@
 #include <math.h>
 
 namespace sv {
-
-struct UnitRef {
-  int kind;  // 0 statistics, 1 tail
-  int b;
-  int idx;
-};
-
-// Unit index -> (kind, sequence, index within the sequence); 32-bit arithmetic
-// (the host keeps the unit count below 2^31).
-__device__ __forceinline__ UnitRef decode_unit(const UnitMap& m, int p) {
-  const int A = m.A, T = m.T, AT = m.A + m.T;
-  const int n1 = m.delta < m.B ? m.delta : m.B;         // statistics-only blocks
-  const int n2 = m.B - m.delta > 0 ? m.B - m.delta : 0;  // statistics + tail blocks
-  UnitRef u;
-  if (p < n1 * A) {
-    u.kind = 0;
-    u.b = p / A;
-    u.idx = p - u.b * A;
-    return u;
-  }
-  p -= n1 * A;
-  if (p < n2 * AT) {
-    const int blk = p / AT, o = p - blk * AT;
-    if (o < A) {
-      u.kind = 0;
-      u.b = m.delta + blk;
-      u.idx = o;
-    } else {
-      u.kind = 1;
-      u.b = blk;
-      u.idx = o - A;
-    }
-    return u;
-  }
-  p -= n2 * AT;
-  u.kind = 1;
-  u.b = n2 + p / T;
-  u.idx = p - (p / T) * T;
-  return u;
-}
 
 // ---------------------------------------------------------------------------
 // Replacement / bonus weights.  Both are scaled by the target row's sum sT so
@@ -168,17 +131,53 @@ __device__ __forceinline__ TailConsts tail_consts(const SampleArgs& a, const Seq
   return k;
 }
 
-__device__ __forceinline__ SeqInfo load_info(const SampleArgs& a, int b) {
-  const SeqInfo* g = a.info + b;
+// ---------------------------------------------------------------------------
+// decision queue.  The statistics finisher of a sequence takes the next queue
+// position and writes its SeqInfo there with two relaxed 16-byte stores; a
+// reader validates each field against kMarker (a NaN no field ever holds).
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void publish_decision(const SampleArgs& a, const SeqInfo& si) {
+  const int pos = atom_add_relaxed(a.qcount, 1);
+  uint32_t* e = (uint32_t*)(a.queue + pos);
+  st_relaxed_v4(e, (uint32_t)si.b, (uint32_t)si.n, (uint32_t)si.mode, __float_as_uint(si.mT));
+  st_relaxed_v4(e + 4, __float_as_uint(si.mD), __float_as_uint(si.lam_hi), __float_as_uint(si.lam_lo),
+                __float_as_uint(si.sT));
+}
+
+__device__ __forceinline__ bool word_set(uint32_t v) { return v != kMarker; }
+
+// First word (the sequence id) of queue entry pos, without waiting.
+__device__ __forceinline__ uint32_t poll_decision(const SampleArgs& a, int pos) {
+  return ld_relaxed_s32((const int*)(a.queue + pos));
+}
+
+// The whole entry, once its first word has been seen; the other fields were
+// stored at the same moment, so the bounded wait is at most a few round trips.
+__device__ __noinline__ SeqInfo read_decision(const SampleArgs& a, int pos) {
+  const uint32_t* e = (const uint32_t*)(a.queue + pos);
+  uint4 x = ld_relaxed_v4(e), y = ld_relaxed_v4(e + 4);
+  unsigned it = 0;
+  while (!(word_set(x.x) && word_set(x.y) && word_set(x.z) && word_set(x.w) && word_set(y.x) &&
+           word_set(y.y) && word_set(y.z) && word_set(y.w)) &&
+         ++it < kSpinLimit) {
+    __nanosleep(64);
+    x = ld_relaxed_v4(e);
+    y = ld_relaxed_v4(e + 4);
+  }
   SeqInfo si;
-  si.n = __ldcg(&g->n);
-  si.mode = __ldcg(&g->mode);
-  si.mT = __ldcg(&g->mT);
-  si.mD = __ldcg(&g->mD);
-  si.lam_hi = __ldcg(&g->lam_hi);
-  si.lam_lo = __ldcg(&g->lam_lo);
-  si.sT = __ldcg(&g->sT);
-  si.pad = 0;
+  if (it >= kSpinLimit) {
+    atomicOr(a.status, kStatusTimeout);
+    si.mode = kModeBad;  // treated as undecided: the tail slices do nothing
+  } else {
+    si.mode = (int)x.z;
+  }
+  si.b = (int)x.x;
+  si.n = (int)x.y;
+  si.mT = __uint_as_float(x.w);
+  si.mD = __uint_as_float(y.x);
+  si.lam_hi = __uint_as_float(y.y);
+  si.lam_lo = __uint_as_float(y.z);
+  si.sT = __uint_as_float(y.w);
   return si;
 }
 
@@ -270,10 +269,10 @@ __device__ __noinline__ void stats_finisher(const SampleArgs& a, int b) {
 
   int32_t* out = a.out_tokens + (size_t)b * (K + 1);
   SeqInfo si;
-  si.pad = 0;
+  si.b = b;
   if (bad) {
     for (int j = lane; j <= K; j += 32) out[j] = -1;
-    si.n = -1;
+    si.n = 0;
     si.mode = kModeBad;
     si.mT = si.mD = si.lam_hi = si.lam_lo = si.sT = 0.f;
     if (lane == 0) {
@@ -304,11 +303,7 @@ __device__ __noinline__ void stats_finisher(const SampleArgs& a, int b) {
     }
     if (lane == 0) a.out_n[b] = n;
   }
-  if (lane == 0) {
-    a.info[b] = si;
-    __threadfence();
-    st_release(&a.ready[b], 1);
-  }
+  if (lane == 0) publish_decision(a, si);
   __syncwarp();
 }
 
@@ -369,60 +364,85 @@ __device__ double tail_slice_mass(const SampleArgs& a, int b, int s, const SeqIn
 }
 
 // ---------------------------------------------------------------------------
-// select finisher (one warp): inverse CDF over the tail units' masses
+// select finisher (one warp): inverse CDF over the tail slices' masses
 // ---------------------------------------------------------------------------
+
+// First position i < count with positive mass whose running sum (from `run`
+// on, in index order) exceeds theta; when rounding leaves theta past every
+// running sum, the last position with mass.  Values are read 32 at a time, the
+// running sum is a warp prefix in fp64.  Returns -1 when no value is positive;
+// *before gets the running sum just before the chosen position.
+template <class LOAD>
+__device__ __forceinline__ int warp_cdf_search(int count, double theta, double run, LOAD load,
+                                               double* before) {
+  const int lane = threadIdx.x & 31;
+  int last = -1;
+  double last_before = 0.0;
+  for (int c0 = 0; c0 < count; c0 += 32) {
+    const int i = c0 + lane;
+    const double v = i < count ? load(i) : 0.0;
+    const bool pos = v > 0.0;
+    double incl = v;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const double o = __shfl_up_sync(0xffffffffu, incl, off);
+      if (lane >= off) incl += o;
+    }
+    double excl = __shfl_up_sync(0xffffffffu, incl, 1);
+    if (lane == 0) excl = 0.0;
+    const unsigned hit = __ballot_sync(0xffffffffu, pos && run + incl > theta);
+    const unsigned has = __ballot_sync(0xffffffffu, pos);
+    if (hit) {
+      const int L = __ffs(hit) - 1;
+      *before = __shfl_sync(0xffffffffu, run + excl, L);
+      return c0 + L;
+    }
+    if (has) {
+      const int L = 31 - __clz(has);
+      last = c0 + L;
+      last_before = __shfl_sync(0xffffffffu, run + excl, L);
+    }
+    run += __shfl_sync(0xffffffffu, incl, 31);
+  }
+  *before = last_before;
+  return last;
+}
+
 template <class E, int VEC>
-__device__ __noinline__ void select_finisher(const SampleArgs& a, int b) {
+__device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   using S = typename E::storage;
   constexpr int STEPW = 32 * VEC;
   const int lane = threadIdx.x & 31;
-  if (!ld_acquire(&a.ready[b])) return;
-  SeqInfo si = load_info(a, b);
-  if (si.mode == kModeBad) return;
+  const int b = si.b, n = si.n;
   const int C = a.CU * kSlices;  // tail slices of the row, in vocabulary order
   double* ts = a.tailsum + (size_t)b * C;
-  double Z = 0.0;
-  for (int t = 0; t < C; ++t) Z += wait_f64_acquire(ts + t, a.status);
+  // Z: lane-strided acquire loads (they order the piece reads below), then a
+  // fixed-order butterfly
+  double z = 0.0;
+  for (int t = lane; t < C; t += 32) z += wait_f64_acquire(ts + t, a.status);
+  double Z = warp_sum_f64(z);
   // Z == 0 after a rejection can only come from rounding (p(x_n) < q(x_n)
   // forces a positive residual); then the draw falls back to p_n itself, and
   // this warp recomputes every piece in bonus mode with the same arithmetic.
   if (si.mode == kModeResidual && !(Z > 0.0)) {
     si.mode = kModeBonus;
+    z = 0.0;
     for (int t = 0; t < C; ++t) {
       const double tot = tail_slice_mass<E, VEC>(a, b, t, si);
       if (lane == 0) ts[t] = tot;
+      if (lane == (t & 31)) z += tot;
     }
     __threadfence();
     __syncwarp();
-    Z = 0.0;
-    for (int t = 0; t < C; ++t) Z += __ldcg(ts + t);
+    Z = warp_sum_f64(z);
   }
-  const int n = si.n;
   const double theta = uniform_draw(a.seed, (uint64_t)b, (uint64_t)n, 1) * Z;
 
-  // Slice, then piece, then lane, then element holding the crossing, each by
-  // a sequential fp64 prefix.  Only positions with positive mass are ever
-  // chosen, so the emitted token always carries weight (and lies below V);
-  // when rounding leaves theta past every partial sum, the last position with
-  // mass is taken.
+  // Slice, then piece, then lane, then element holding the crossing.  Only
+  // positions with positive mass are ever chosen, so the emitted token always
+  // carries weight (and lies below V).
   double acc = 0.0;
-  int tsel = -1, tlast = -1;
-  double acc_last = 0.0;
-  for (int t = 0; t < C; ++t) {
-    const double v = __ldcg(ts + t);
-    if (!(v > 0.0)) continue;
-    if (acc + v > theta) {
-      tsel = t;
-      break;
-    }
-    tlast = t;
-    acc_last = acc;
-    acc += v;
-  }
-  if (tsel < 0) {
-    tsel = tlast;
-    acc = acc_last;
-  }
+  const int tsel = warp_cdf_search(C, theta, 0.0, [&](int t) { return __ldcg(ts + t); }, &acc);
   if (tsel < 0) {  // no slice with mass: only an expired wait can cause this
     if (lane == 0) {
       a.out_tokens[(size_t)b * (a.K + 1) + n] = -1;
@@ -434,23 +454,9 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, int b) {
   const int v0 = tsel * a.SL, v1 = min(a.V, v0 + a.SL);
   const int np = (v1 - v0 + STEPW - 1) / STEPW;
   const float* gp = a.pieces + ((size_t)b * C + tsel) * a.P;
-  int psel = -1, plast = -1;
-  double acc2 = acc, acc2_last = acc;
-  for (int q = 0; q < np; ++q) {
-    const double v = (double)__ldcg(gp + q);
-    if (!(v > 0.0)) continue;
-    if (acc2 + v > theta) {
-      psel = q;
-      break;
-    }
-    plast = q;
-    acc2_last = acc2;
-    acc2 += v;
-  }
-  if (psel < 0) {
-    psel = plast;
-    acc2 = acc2_last;
-  }
+  double acc2 = acc;
+  const int psel =
+      warp_cdf_search(np, theta, acc, [&](int q) { return (double)__ldcg(gp + q); }, &acc2);
   if (psel < 0) {  // pieces inconsistent with their slice mass (expired wait)
     if (lane == 0) {
       a.out_tokens[(size_t)b * (a.K + 1) + n] = -1;
@@ -535,20 +541,11 @@ __device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], flo
     for (int u = 0; u < kUnroll; ++u) lo += ex2((z[u].f - base) * cc);
     acc = f2(lo, f2hi(acc));
   } else {
-    // The MUFU unit takes the first kMufuPairs element pairs of the batch and
-    // the FMA pipe (exp2_poly2) the rest, so that neither unit limits the pass.
-    constexpr int kPairs = kUnroll * VEC / 2;
-    constexpr int kMufuPairs = kPairs - kPairs / 2;
     const f2_t b2 = f2(base, base), c2 = f2(cc, cc);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
-      for (int p = 0; p < VEC / 2; ++p) {
-        if (u * (VEC / 2) + p < kMufuPairs)
-          f2_exp_acc(acc, elem_pair<E, VEC>(z[u], p), b2, c2);
-        else
-          f2_exp_acc_poly(acc, elem_pair<E, VEC>(z[u], p), b2, c2);
-      }
+      for (int p = 0; p < VEC / 2; ++p) f2_exp_acc(acc, elem_pair<E, VEC>(z[u], p), b2, c2);
   }
 }
 
@@ -593,65 +590,79 @@ __device__ int stats_slice(const SampleArgs& a, int b, int idx, int w) {
   return old;
 }
 
-// Slice w of tail unit uc of sequence b: wait for the decision (bounded),
-// claim the next unit, then the slice's pieces and the sequence's ticket.
+// Slice w of tail unit uc of a decided sequence: the slice's pieces and mass,
+// then the sequence's tail ticket; the last ticket runs the select finisher.
 template <class E, int VEC>
-__device__ int tail_slice(const SampleArgs& a, int b, int uc, int w, int& next) {
+__device__ __noinline__ void tail_slice(const SampleArgs& a, const SeqInfo& si, int uc, int w) {
   const int lane = threadIdx.x & 31;
-  int st = 0;
-  next = 0;
-  if (lane == 0) {
-    st = ld_acquire(&a.ready[b]);
-    unsigned it = 0;
-    while (st == 0 && ++it < kSpinLimit) {
-      __nanosleep(128);
-      st = ld_acquire(&a.ready[b]);
-    }
-    if (st == 0) atomicOr(a.status, kStatusTimeout);
-    // nothing below waits, so this claim cannot hold up another warp
-    next = (int)atomicAdd(a.counter + w * kCounterStride, 1ull);
-  }
-  st = __shfl_sync(0xffffffffu, st, 0);
+  if (si.mode == kModeBad) return;  // outputs already written by the statistics finisher
+  const int b = si.b;
   const int s = uc * kSlices + w;
-  double tot = 0.0;
-  if (st) {
-    const SeqInfo si = load_info(a, b);
-    if (si.mode != kModeBad) tot = tail_slice_mass<E, VEC>(a, b, s, si);
-  }
+  const double tot = tail_slice_mass<E, VEC>(a, b, s, si);
   int old = 0;
   if (lane == 0) {
     // release: the pieces stored by this lane are visible to whoever sees the mass
     st_release_f64(a.tailsum + (size_t)b * a.CU * kSlices + s, tot);
     old = atom_add_relaxed(&a.tailticket[b], 1);
   }
-  return old;
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old == a.CU * kSlices - 1) select_finisher<E, VEC>(a, si);
 }
 
-// Units are only ever claimed by a warp that is already running, and each
-// counter hands them out in increasing order.  A tail slice waits only on the
-// statistics slices of its sequence, which belong to units with smaller
-// indices on every counter; a warp never holds another claim while it waits,
-// and it settles its own tickets before taking new work.  So every slice a
-// wait depends on is being processed by a running warp, and every wait ends,
-// even when other work keeps part of the grid from being resident.
+// Scheduling.  Statistics units come from the warp slot's claim counter; the
+// next one is claimed before the current unit is processed, so the atomic's
+// latency hides behind the stream.  Tail items are owned, not claimed: warp
+// slot w of CTA c takes items c, c + grid, c + 2 grid, ... of slot w, in order,
+// and polls the queue entry of its next item with a relaxed load issued before
+// each statistics slice.  A published item is taken before the next
+// statistics unit.  Only when a warp has no statistics unit left does it wait
+// (bounded) for its next entry.
+//
+// Progress: statistics slices and the finishers they trigger wait only for
+// stores that other warps have already issued (their tickets were counted), a
+// warp holding a claimed statistics unit never waits, and every sequence is
+// decided once its statistics units are done.  So every queue entry is
+// eventually written and every wait ends, whatever part of the grid is
+// resident.
 template <class E, int VEC>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __grid_constant__ SampleArgs a) {
   const int lane = threadIdx.x & 31;
   const int w = slice_of_warp();
-  const int row_last = a.CU * kSlices - 1, tail_last = a.map.T * kSlices - 1;
+  const int row_last = a.CU * kSlices - 1;
+  const int TT = a.B * a.CU;  // tail items of this slot
+  int t = blockIdx.x;         // this warp's next tail item
   int unit = bcast(claim_unit(a.counter, lane));
-  while (unit < a.map.total) {
-    const UnitRef u = decode_unit(a.map, unit);
-    int next = 0;
-    if (u.kind == 0) {
-      next = claim_unit(a.counter, lane);
-      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC>(a, u.b, u.idx, w), 0);
-      if (old == row_last) row_finisher<E>(a, u.b, u.idx / a.CU);
-    } else {
-      const int old = __shfl_sync(0xffffffffu, tail_slice<E, VEC>(a, u.b, u.idx, w, next), 0);
-      if (old == tail_last) select_finisher<E, VEC>(a, u.b);
+  uint32_t seen = (lane == 0 && t < TT) ? (uint32_t)poll_decision(a, t / a.CU) : kMarker;
+  for (;;) {
+    if (t < TT && word_set(bcast((int)seen))) {
+      const SeqInfo si = read_decision(a, t / a.CU);
+      tail_slice<E, VEC>(a, si, t % a.CU, w);
+      t += gridDim.x;
+      seen = (lane == 0 && t < TT) ? (uint32_t)poll_decision(a, t / a.CU) : kMarker;
+      continue;
     }
-    unit = bcast(next);
+    if (unit < a.map.total) {
+      const int next = claim_unit(a.counter, lane);
+      if (lane == 0 && t < TT) seen = (uint32_t)poll_decision(a, t / a.CU);
+      const int b = unit / a.map.A, idx = unit - b * a.map.A;
+      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC>(a, b, idx, w), 0);
+      if (old == row_last) row_finisher<E>(a, b, idx / a.CU);
+      unit = bcast(next);
+      continue;
+    }
+    if (t >= TT) break;
+    // no statistics work left: wait for this warp's next decision
+    if (lane == 0) {
+      unsigned it = 0, nap = 64;
+      seen = (uint32_t)poll_decision(a, t / a.CU);
+      while (!word_set(seen) && ++it < kSpinLimit) {
+        __nanosleep(nap);
+        if (nap < 1024) nap <<= 1;
+        seen = (uint32_t)poll_decision(a, t / a.CU);
+      }
+      if (!word_set(seen)) atomicOr(a.status, kStatusTimeout);
+    }
+    if (!word_set(bcast((int)seen))) break;
   }
 }
 
@@ -660,8 +671,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
 // ---------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [zero-filled: counters, tickets, ready][marker-filled: part,
-// rowstat, tailsum][info, pieces].
+// Workspace: [zero-filled: counters, tickets, queue count][marker-filled:
+// part, rowstat, tailsum, queue][pieces].
 static void sample_layout(int B, int R, int CU, int P, size_t* off) {
   const size_t C = (size_t)CU * kSlices;
   size_t o = 0;
@@ -669,14 +680,14 @@ static void sample_layout(int B, int R, int CU, int P, size_t* off) {
   off[1] = o; o += align_up((size_t)B * R * kTicketStride * 4, 16);       // rowticket
   off[2] = o; o += align_up((size_t)B * 4, 16);                           // seqticket
   off[3] = o; o += align_up((size_t)B * 4, 16);                           // tailticket
-  off[4] = o; o += align_up((size_t)B * 4, 16);                           // ready
+  off[4] = o; o += 16;                                                     // qcount
   o = align_up(o, 256);
   off[5] = o;                                                              // end of zero region
   off[6] = o; o += align_up((size_t)B * R * C * sizeof(float2), 256);     // part
   off[7] = o; o += align_up((size_t)B * R * sizeof(float2), 256);         // rowstat
   off[8] = o; o += align_up((size_t)B * C * sizeof(double), 256);         // tailsum
+  off[10] = o; o += align_up((size_t)B * sizeof(SeqInfo), 256);           // queue
   off[9] = o;                                                              // end of marker region
-  off[10] = o; o += align_up((size_t)B * sizeof(SeqInfo), 256);           // info
   off[11] = o; o += align_up((size_t)B * C * P * sizeof(float), 256);     // pieces
   off[12] = o;
 }
@@ -700,11 +711,11 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.rowticket = (int*)(p + off[1]);
   a.seqticket = (int*)(p + off[2]);
   a.tailticket = (int*)(p + off[3]);
-  a.ready = (int*)(p + off[4]);
+  a.qcount = (int*)(p + off[4]);
   a.part = (float2*)(p + off[6]);
   a.rowstat = (float2*)(p + off[7]);
   a.tailsum = (double*)(p + off[8]);
-  a.info = (SeqInfo*)(p + off[10]);
+  a.queue = (SeqInfo*)(p + off[10]);
   a.pieces = (float*)(p + off[11]);
 }
 

@@ -77,33 +77,6 @@ __device__ __forceinline__ void f2_exp_acc(f2_t& acc, f2_t z, f2_t base, f2_t c)
   acc = f2add(acc, f2(ex2(f2lo(t)), ex2(f2hi(t))));
 }
 
-// 2^t for both halves of t (t <= 0) on the FMA pipe instead of the MUFU unit.
-// Cody and Waite's reduction t = j + f with j = rint(t) (the 1.5 * 2^23
-// rounding constant) and |f| <= 1/2; 2^f from the degree-6 polynomial fitted to
-// the relative error on [-1/2, 1/2] by the Remez exchange (gen_exp2_poly.py:
-// at most 1.01e-7 relative after fp32 evaluation, comparable to ex2.approx);
-// 2^j is added to the exponent field.  Inputs below -125 are clamped, so the
-// result is never below 2^-125.5 (an exact 0 is never produced).
-__device__ __forceinline__ f2_t exp2_poly2(f2_t t) {
-  const f2_t tc = f2(fmaxf(f2lo(t), -125.f), fmaxf(f2hi(t), -125.f));
-  const f2_t magic = f2(12582912.f, 12582912.f);
-  const f2_t r = f2add(tc, magic);               // bits(r) = 0x4b400000 + j
-  const f2_t f = f2sub(tc, f2sub(r, magic));     // exact, |f| <= 1/2
-  f2_t p = f2fma(f, f2(0x1.41d334p-13f, 0x1.41d334p-13f), f2(0x1.5f456ap-10f, 0x1.5f456ap-10f));
-  p = f2fma(f, p, f2(0x1.3b2dbcp-7f, 0x1.3b2dbcp-7f));
-  p = f2fma(f, p, f2(0x1.c6aed4p-5f, 0x1.c6aed4p-5f));
-  p = f2fma(f, p, f2(0x1.ebfbdap-3f, 0x1.ebfbdap-3f));
-  p = f2fma(f, p, f2(0x1.62e430p-1f, 0x1.62e430p-1f));
-  p = f2fma(f, p, f2(1.f, 1.f));
-  // (0x4b400000 << 23) vanishes modulo 2^32, so bits(r) << 23 is j << 23
-  const uint32_t lo = __float_as_uint(f2lo(p)) + (__float_as_uint(f2lo(r)) << 23);
-  const uint32_t hi = __float_as_uint(f2hi(p)) + (__float_as_uint(f2hi(r)) << 23);
-  return f2(__uint_as_float(lo), __uint_as_float(hi));
-}
-__device__ __forceinline__ void f2_exp_acc_poly(f2_t& acc, f2_t z, f2_t base, f2_t c) {
-  acc = f2add(acc, exp2_poly2(f2mul(f2sub(z, base), c)));
-}
-
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -249,6 +222,18 @@ __device__ __forceinline__ uint2 ld_relaxed_u2(const void* p) {
   asm volatile("ld.relaxed.gpu.global.v2.u32 {%0,%1}, [%2];" : "=r"(v.x), "=r"(v.y) : "l"(p) : "memory");
   return v;
 }
+__device__ __forceinline__ void st_relaxed_v4(void* p, uint32_t x, uint32_t y, uint32_t z, uint32_t w) {
+  asm volatile("st.relaxed.gpu.global.v4.u32 [%0], {%1,%2,%3,%4};" ::"l"(p), "r"(x), "r"(y), "r"(z), "r"(w)
+               : "memory");
+}
+__device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
+  uint4 v;
+  asm volatile("ld.relaxed.gpu.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p)
+               : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_relaxed_s32(int* p, int v) {
   asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -354,6 +339,14 @@ __device__ __forceinline__ void warp_am(float& v, int& i) {
     int i2 = __shfl_xor_sync(0xffffffffu, i, off);
     am_merge(v, i, v2, i2);
   }
+}
+
+// Butterfly sums: every lane adds the same two operands at every stage, so all
+// lanes end with the same, run-to-run identical value.
+__device__ __forceinline__ double warp_sum_f64(double x) {
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
+  return x;
 }
 
 __device__ __forceinline__ float warp_sum(float x) {

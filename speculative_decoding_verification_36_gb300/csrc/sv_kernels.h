@@ -27,30 +27,30 @@ constexpr int kUnroll = 2;     // 16-byte vectors per lane per load batch; two b
 constexpr int kMaxK = 255;
 constexpr int kMaxTreeNodes = 1024;
 
-// Per-sequence decision left by the statistics finisher for the tail units.
+// Per-sequence decision, published by the statistics finisher as one 32-byte
+// entry of the decision queue.  Entries start filled with kMarker words and
+// every field is written once with a value that is never kMarker (n >= 0, and
+// the floats are finite), so a reader knows a field has arrived from its value
+// alone: no fence or acquire is needed on the hot path.
 struct SeqInfo {
-  int n;         // accepted count; the tail row is target row n (and draft row n)
+  int b;         // sequence
+  int n;         // accepted count (0 for a bad sequence); the tail row is row n
   int mode;      // kModeResidual, kModeBonus, kModeBad
   float mT;      // max raw logit of target row n
   float mD;      // max raw logit of draft row n (residual mode)
   float lam_hi;  // log2(sT / sD) as a float pair
   float lam_lo;
   float sT;      // sum_v exp2((z - mT) * c) of target row n
-  int pad;
 };
 constexpr int kModeResidual = 0;
 constexpr int kModeBonus = 1;
 constexpr int kModeBad = 2;
 
-// The global order of units: each sequence's statistics units come first and
-// its tail units (the residual / bonus row, chunked the same way) follow
-// `delta` sequences later, so that the re-read of the tail row hits L2.
+// Statistics units are numbered sequence-major: unit u is index u % A of
+// sequence u / A on every counter.
 struct UnitMap {
-  int B;
   int A;      // statistics units per sequence (rows * CU)
-  int T;      // tail units per sequence (CU; 0 for the argmax kernels)
-  int delta;  // slack, in sequences, between statistics and tail units
-  int total;  // units per counter: B * (A + T)
+  int total;  // statistics units per counter: B * A
 };
 
 struct SampleArgs {
@@ -74,17 +74,17 @@ struct SampleArgs {
   float* out_pq;         // optional [B, K, 2]: p_i(x_i), q_i(x_i)
   float* out_resid;      // optional [B]: mass of the replacement distribution
   // workspace.  Zero-filled before the launch: counter, rowticket, seqticket,
-  // tailticket, ready.  Filled with all-ones bytes (a NaN "not yet written"
-  // marker) before the launch: part, rowstat, tailsum.
+  // tailticket, qcount.  Filled with all-ones bytes (the kMarker "not yet
+  // written" pattern) before the launch: part, rowstat, tailsum, queue.
   unsigned long long* counter;  // kSlices claim counters, kCounterStride apart
   int* rowticket;   // [B, R] (kTicketStride apart) finished slices of a row
   int* seqticket;   // [B] finished rows of a sequence
   int* tailticket;  // [B] finished tail slices
-  int* ready;       // [B] 0 until the statistics finisher published SeqInfo
+  int* qcount;      // decision-queue positions taken so far
   float2* part;     // [B, R, CU * kSlices] per-slice (m, s)
   float2* rowstat;  // [B, R] merged (m, s) of each row
   double* tailsum;  // [B, CU * kSlices] per tail-slice mass
-  SeqInfo* info;    // [B]
+  SeqInfo* queue;   // [B] decisions in the order they were made
   float* pieces;    // [B, CU * kSlices, P] per-piece mass
   unsigned* status;
 };

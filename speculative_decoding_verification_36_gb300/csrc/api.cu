@@ -205,11 +205,20 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.V = V;
   a.R = 2 * K + 1;
   const int vec_elems = vec ? (bf16 ? 8 : 4) : 1;
-  choose_slices(V, vec_elems, esz, &a.SL, &a.CS, &a.CU);
-  a.P = (a.SL + 32 * vec_elems - 1) / (32 * vec_elems);
-  a.map.A = a.R * a.CU;
-  a.map.total = B * a.map.A;
-  const int grid = grid_for(a.map.total, capacity);
+  int CU = 0;
+  choose_slices(V, vec_elems, esz, &a.SL, &a.CS, &CU);
+  // tail slices: whole warp steps, half a statistics slice per row, so that a
+  // tail item (target and draft slice) carries as many bytes as a statistics
+  // slice
+  const int step = 32 * vec_elems;
+  a.P = ((a.SL + 1) / 2 + step - 1) / step;
+  a.TL = a.P * step;
+  a.TC = (int)(((long long)V + a.TL - 1) / a.TL);
+  a.F = B * a.R * a.CS;
+  a.div_seq = sv::make_fastdiv((uint32_t)(a.R * a.CS));
+  a.div_cs = sv::make_fastdiv((uint32_t)a.CS);
+  a.div_tc = sv::make_fastdiv((uint32_t)a.TC);
+  const int grid = grid_for((a.F + sv::kSlices - 1) / sv::kSlices, capacity);
   const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
   a.c64 = c;
   a.c_hi = (float)c;
@@ -223,7 +232,7 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.out_resid = out_resid;
   a.status = d->status;
   void* ws = nullptr;
-  rc = run_scratch(d, sv::sample_workspace(B, K, a.CU, a.P), stream, &ws);
+  rc = run_scratch(d, sv::sample_workspace(B, K, a.CS, a.TC, a.P), stream, &ws);
   if (rc) return rc;
   sv::sample_bind_workspace(a, ws);
   cudaError_t e = sv::launch_sample(a, bf16, vec, grid, stream);

@@ -20,10 +20,9 @@
 //     2-4 in fp64 and appends the sequence's decision to the decision queue.
 //   * tail slice = SL elements of the tail row (pair) of a decided sequence:
 //     the mass of every warp step ("piece") of the replacement / bonus
-//     distribution.  Tail item t (queue position t / CU, unit t % CU) belongs
-//     to warp slot w of CTA t % grid.  A warp polls its next item's queue
-//     entry while it streams statistics slices and takes the item as soon as
-//     the entry is there, so no warp ever waits for a decision while
+//     distribution.  Tail items are owned by fixed warps; a warp polls its
+//     next item's queue entry while it streams statistics slices and takes
+//     the item as soon as the entry is there, so no warp ever waits for a decision while
 //     statistics work is left, and the re-read rows are still in L2.  The warp
 //     that takes the last tail ticket finds the CDF crossing from the slice
 //     and piece masses and rescans one piece.
@@ -41,7 +40,7 @@ namespace sv {
 //   bonus:     w(v) = 2^{(zT - mT) c}                        = sT * p(v)
 //   residual:  w(v) = 2^{(zT - mT) c} * (1 - 2^{-delta})     = sT * max(0, p(v) - q(v))
 //              delta = (dT - dD) c - log2(sT / sD)          (> 0 iff p(v) > q(v))
-// The form 2^{aT}(1 - 2^{-delta}) has no cancellation (see one_minus_exp2_neg).
+// The form 2^{aT}(1 - 2^{-delta}) has no cancellation (see resid_factor).
 // Explicit round-to-nearest operations (no contraction) keep the arithmetic
 // identical in the tail units and in the final rescan.
 // ---------------------------------------------------------------------------
@@ -50,19 +49,41 @@ struct TailConsts {
   int residual;
 };
 
-// 1 - 2^{-d} for d > 0 without cancellation.  For d < 1.4, with y = d ln 2:
-// 1 - e^{-y} = 2 sinh(y/2) e^{-y/2}; sinh(x) = x (1 + x^2/6 + x^4/120 + x^6/5040)
-// (x <= 0.49, the first omitted term is below 1e-8 relative) and e^{-y/2} from
-// ex2.  For d >= 1.4 the direct 1 - 2^{-d} (>= 0.62) loses nothing.
-__device__ __forceinline__ float one_minus_exp2_neg(float d) {
-  const float eh = ex2(__fmul_rn(d, -0.5f));  // 2^{-d/2}
-  if (d >= 1.4f) return __fsub_rn(1.f, __fmul_rn(eh, eh));
-  const float x = __fmul_rn(d, 0.346573590279972655f);  // (d ln 2) / 2
+// max(0, 1 - 2^{-d}) without cancellation and without branches.  With
+// eh = 2^{-d/2} (ex2) and x = d ln2 / 2:
+//   d >= 1.4:  1 - eh^2                                   (>= 0.62, nothing cancels)
+//   d <  1.4:  1 - e^{-2x} = 2 sinh(x) e^{-x} = x (2 + x^2/3 + x^4/60 + x^6/2520) eh
+// (|x| < 0.49 there, so the first omitted term is below 1e-8 relative).  For
+// d <= 0 the second form is <= 0 and the clamp returns 0.  Both forms are
+// evaluated and one is selected, so the packed version below can share every
+// instruction between the two elements of a pair.
+__device__ __forceinline__ float resid_factor(float d) {
+  const float eh = ex2(__fmul_rn(d, -0.5f));
+  const float A = __fsub_rn(1.f, __fmul_rn(eh, eh));
+  const float x = __fmul_rn(d, 0.346573590279972655f);
   const float xx = __fmul_rn(x, x);
-  float p = __fmaf_rn(xx, 1.f / 5040.f, 1.f / 120.f);
-  p = __fmaf_rn(xx, p, 1.f / 6.f);
-  p = __fmaf_rn(xx, p, 1.f);
-  return __fmul_rn(__fmul_rn(__fmul_rn(x, p), eh), 2.f);
+  float p = __fmaf_rn(xx, 1.f / 2520.f, 1.f / 60.f);
+  p = __fmaf_rn(xx, p, 1.f / 3.f);
+  p = __fmaf_rn(xx, p, 2.f);
+  const float Bv = __fmul_rn(__fmul_rn(x, p), eh);
+  return fmaxf(d >= 1.4f ? A : Bv, 0.f);
+}
+
+// resid_factor on both elements of a pair, with every operation rounding as
+// in the scalar version (bit-identical results).
+__device__ __forceinline__ f2_t resid_factor2(f2_t d) {
+  const f2_t hd = f2mul(d, f2(-0.5f, -0.5f));
+  const f2_t eh = f2(ex2(f2lo(hd)), ex2(f2hi(hd)));
+  const f2_t A = f2sub(f2(1.f, 1.f), f2mul(eh, eh));
+  const f2_t x = f2mul(d, f2(0.346573590279972655f, 0.346573590279972655f));
+  const f2_t xx = f2mul(x, x);
+  f2_t p = f2fma(xx, f2(1.f / 2520.f, 1.f / 2520.f), f2(1.f / 60.f, 1.f / 60.f));
+  p = f2fma(xx, p, f2(1.f / 3.f, 1.f / 3.f));
+  p = f2fma(xx, p, f2(2.f, 2.f));
+  const f2_t Bv = f2mul(f2mul(x, p), eh);
+  const float r0 = fmaxf(f2lo(d) >= 1.4f ? f2lo(A) : f2lo(Bv), 0.f);
+  const float r1 = fmaxf(f2hi(d) >= 1.4f ? f2hi(A) : f2hi(Bv), 0.f);
+  return f2(r0, r1);
 }
 
 __device__ __forceinline__ float tail_weight(float zT, float zD, const TailConsts& k) {
@@ -72,26 +93,21 @@ __device__ __forceinline__ float tail_weight(float zT, float zD, const TailConst
   const float dD = __fsub_rn(zD, k.mD);
   const float D = __fsub_rn(dT, dD);
   const float delta = __fadd_rn(__fmaf_rn(D, k.c_hi, -k.lam_hi), __fmaf_rn(D, k.c_lo, -k.lam_lo));
-  if (!(delta > 0.f)) return 0.f;
-  return __fmul_rn(eT, one_minus_exp2_neg(delta));
+  return __fmul_rn(eT, resid_factor(delta));
 }
 
 // The same weights for an element pair with packed f32x2 arithmetic: every
-// operation rounds exactly as the scalar version above, so pieces and the
-// final rescan agree bit for bit.
+// operation rounds exactly as the scalar version above.
 __device__ __forceinline__ f2_t tail_weight2(f2_t zT, f2_t zD, const TailConsts& k) {
   const f2_t dT = f2sub(zT, f2(k.mT, k.mT));
   const f2_t aT = f2mul(dT, f2(k.c_hi, k.c_hi));
-  const float eT0 = ex2(f2lo(aT)), eT1 = ex2(f2hi(aT));
-  if (!k.residual) return f2(eT0, eT1);
+  const f2_t eT = f2(ex2(f2lo(aT)), ex2(f2hi(aT)));
+  if (!k.residual) return eT;
   const f2_t dD = f2sub(zD, f2(k.mD, k.mD));
   const f2_t D = f2sub(dT, dD);
   const f2_t delta = f2add(f2fma(D, f2(k.c_hi, k.c_hi), f2(-k.lam_hi, -k.lam_hi)),
                            f2fma(D, f2(k.c_lo, k.c_lo), f2(-k.lam_lo, -k.lam_lo)));
-  const float d0 = f2lo(delta), d1 = f2hi(delta);
-  const float w0 = d0 > 0.f ? __fmul_rn(eT0, one_minus_exp2_neg(d0)) : 0.f;
-  const float w1 = d1 > 0.f ? __fmul_rn(eT1, one_minus_exp2_neg(d1)) : 0.f;
-  return f2(w0, w1);
+  return f2mul(eT, resid_factor2(delta));
 }
 
 // The VEC weights of one lane's vector, in element order.
@@ -146,9 +162,10 @@ __device__ __forceinline__ void publish_decision(const SampleArgs& a, const SeqI
 
 __device__ __forceinline__ bool word_set(uint32_t v) { return v != kMarker; }
 
-// First word (the sequence id) of queue entry pos, without waiting.
-__device__ __forceinline__ uint32_t poll_decision(const SampleArgs& a, int pos) {
-  return ld_relaxed_s32((const int*)(a.queue + pos));
+// First word (the sequence id) of queue entry pos, loaded by lane 0 when
+// `pred` holds (kMarker elsewhere); nothing waits for it until it is read.
+__device__ __forceinline__ uint32_t poll_decision(const SampleArgs& a, bool pred, int pos) {
+  return ld_relaxed_if(pred, a.queue + pos, kMarker);
 }
 
 // The whole entry, once its first word has been seen; the other fields were
@@ -192,7 +209,7 @@ __device__ __noinline__ void stats_finisher(const SampleArgs& a, int b);
 template <class E>
 __device__ __noinline__ void row_finisher(const SampleArgs& a, int b, int r) {
   const int lane = threadIdx.x & 31;
-  const int C = a.CU * kSlices;
+  const int C = a.CS;
   const float2* pp = a.part + ((size_t)b * a.R + r) * C;
   float m = neg_inf(), s = 0.f;
   for (int c = lane; c < C; c += 32) {
@@ -323,41 +340,51 @@ __device__ __forceinline__ float lane_mass(const Raw<E, VEC>& zt, const Raw<E, V
   return ls;
 }
 
-// One warp: the pieces of slice s of the tail row(s) into the workspace and
-// the slice's fp64 mass (sequential over pieces; returned in every lane).
+// One warp: the pieces of tail slice s of the tail row(s) into the workspace
+// and the slice's mass, the fp32 sum of its pieces in order (every lane).
+// The loads of the next warp step are issued before the current step's
+// arithmetic (two register buffers).
 template <class E, int VEC>
-__device__ double tail_slice_mass(const SampleArgs& a, int b, int s, const SeqInfo& si) {
+__device__ float tail_slice_mass(const SampleArgs& a, int b, int s, const SeqInfo& si) {
   using S = typename E::storage;
   constexpr int STEPW = 32 * VEC;
   const int lane = threadIdx.x & 31;
   const S* rowT = target_row<E>(a, b, si.n);
   const S* rowD = si.mode == kModeResidual ? draft_row<E>(a, b, si.n) : rowT;
   const TailConsts k = tail_consts(a, si);
-  const int v0 = s * a.SL, v1 = min(a.V, v0 + a.SL);
+  const int v0 = s * a.TL, v1 = min(a.V, v0 + a.TL);
   const int nsteps = v1 > v0 ? (v1 - v0 + STEPW - 1) / STEPW : 0;
-  float* gp = a.pieces + ((size_t)b * a.CU * kSlices + s) * a.P;
+  float* gp = a.pieces + ((size_t)b * a.TC + s) * a.P;
   if constexpr (VEC > 1) {
     if (lane == 0 && v1 > v0) {
       prefetch_l2(rowT + v0, (unsigned)((v1 - v0) * sizeof(S)));
       if (k.residual) prefetch_l2(rowD + v0, (unsigned)((v1 - v0) * sizeof(S)));
     }
   }
-  double total = 0.0;
+  float total = 0.f;
   int e = v0 + lane * VEC;
-  for (int st = 0; st < nsteps; st += kUnroll, e += STEPW * kUnroll) {
-    Raw<E, VEC> zt[kUnroll], zd[kUnroll];
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      zt[u] = load_raw<E, VEC>(rowT, e + u * STEPW, v1);
-      zd[u] = k.residual ? load_raw<E, VEC>(rowD, e + u * STEPW, v1) : zt[u];
+  Raw<E, VEC> t0{}, d0{}, t1{}, d1{};
+  if (nsteps > 0) {
+    t0 = load_raw<E, VEC>(rowT, e, v1);
+    d0 = k.residual ? load_raw<E, VEC>(rowD, e, v1) : t0;
+  }
+  for (int q = 0; q < nsteps; q += 2, e += 2 * STEPW) {
+    const bool has1 = q + 1 < nsteps;
+    if (has1) {
+      t1 = load_raw<E, VEC>(rowT, e + STEPW, v1);
+      d1 = k.residual ? load_raw<E, VEC>(rowD, e + STEPW, v1) : t1;
     }
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      if (st + u < nsteps) {
-        const float ps = warp_sum(lane_mass<E, VEC>(zt[u], zd[u], k));
-        if (lane == 0) gp[st + u] = ps;
-        total += (double)ps;
+    float ps = warp_sum(lane_mass<E, VEC>(t0, d0, k));
+    if (lane == 0) gp[q] = ps;
+    total += ps;
+    if (has1) {
+      if (q + 2 < nsteps) {
+        t0 = load_raw<E, VEC>(rowT, e + 2 * STEPW, v1);
+        d0 = k.residual ? load_raw<E, VEC>(rowD, e + 2 * STEPW, v1) : t0;
       }
+      ps = warp_sum(lane_mass<E, VEC>(t1, d1, k));
+      if (lane == 0) gp[q + 1] = ps;
+      total += ps;
     }
   }
   return total;
@@ -414,12 +441,12 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   constexpr int STEPW = 32 * VEC;
   const int lane = threadIdx.x & 31;
   const int b = si.b, n = si.n;
-  const int C = a.CU * kSlices;  // tail slices of the row, in vocabulary order
-  double* ts = a.tailsum + (size_t)b * C;
+  const int C = a.TC;  // tail slices of the row, in vocabulary order
+  float* ts = a.tailsum + (size_t)b * C;
   // Z: lane-strided acquire loads (they order the piece reads below), then a
   // fixed-order butterfly
   double z = 0.0;
-  for (int t = lane; t < C; t += 32) z += wait_f64_acquire(ts + t, a.status);
+  for (int t = lane; t < C; t += 32) z += (double)wait_f32_acquire(ts + t, a.status);
   double Z = warp_sum_f64(z);
   // Z == 0 after a rejection can only come from rounding (p(x_n) < q(x_n)
   // forces a positive residual); then the draw falls back to p_n itself, and
@@ -428,9 +455,9 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
     si.mode = kModeBonus;
     z = 0.0;
     for (int t = 0; t < C; ++t) {
-      const double tot = tail_slice_mass<E, VEC>(a, b, t, si);
+      const float tot = tail_slice_mass<E, VEC>(a, b, t, si);
       if (lane == 0) ts[t] = tot;
-      if (lane == (t & 31)) z += tot;
+      if (lane == (t & 31)) z += (double)tot;
     }
     __threadfence();
     __syncwarp();
@@ -442,7 +469,8 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   // positions with positive mass are ever chosen, so the emitted token always
   // carries weight (and lies below V).
   double acc = 0.0;
-  const int tsel = warp_cdf_search(C, theta, 0.0, [&](int t) { return __ldcg(ts + t); }, &acc);
+  const int tsel =
+      warp_cdf_search(C, theta, 0.0, [&](int t) { return (double)__ldcg(ts + t); }, &acc);
   if (tsel < 0) {  // no slice with mass: only an expired wait can cause this
     if (lane == 0) {
       a.out_tokens[(size_t)b * (a.K + 1) + n] = -1;
@@ -451,7 +479,7 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
     __syncwarp();
     return;
   }
-  const int v0 = tsel * a.SL, v1 = min(a.V, v0 + a.SL);
+  const int v0 = tsel * a.TL, v1 = min(a.V, v0 + a.TL);
   const int np = (v1 - v0 + STEPW - 1) / STEPW;
   const float* gp = a.pieces + ((size_t)b * C + tsel) * a.P;
   double acc2 = acc;
@@ -549,15 +577,13 @@ __device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], flo
   }
 }
 
-// Slice w of statistics unit idx of sequence b: one row's (m, s) over the
-// slice, then the row's ticket.  Returns the ticket's old value (lane 0).
+// Statistics slice s of row r of sequence b: the row's (m, s) over the slice,
+// then the row's ticket.  Returns the ticket's old value (lane 0).
 template <class E, int VEC>
-__device__ int stats_slice(const SampleArgs& a, int b, int idx, int w) {
+__device__ int stats_slice(const SampleArgs& a, int b, int r, int s) {
   using S = typename E::storage;
   constexpr int BATCH = 32 * VEC * kUnroll;
   const int lane = threadIdx.x & 31;
-  const int r = idx / a.CU, uc = idx - (idx / a.CU) * a.CU;
-  const int s = uc * kSlices + w;
   const S* row = r <= a.K ? target_row<E>(a, b, r) : draft_row<E>(a, b, r - a.K - 1);
   const int v0 = s * a.SL, v1 = min(a.V, v0 + a.SL);
   const float cc = a.c_hi;
@@ -583,82 +609,84 @@ __device__ int stats_slice(const SampleArgs& a, int b, int idx, int w) {
   warp_ms(m, sum, cc);
   int old = 0;
   if (lane == 0) {
-    st_relaxed_u2(a.part + ((size_t)b * a.R + r) * (a.CU * kSlices) + s, __float_as_uint(m),
-                  __float_as_uint(sum));
+    st_relaxed_u2(a.part + ((size_t)b * a.R + r) * a.CS + s, __float_as_uint(m), __float_as_uint(sum));
     old = atom_add_relaxed(&a.rowticket[((size_t)b * a.R + r) * kTicketStride], 1);
   }
   return old;
 }
 
-// Slice w of tail unit uc of a decided sequence: the slice's pieces and mass,
-// then the sequence's tail ticket; the last ticket runs the select finisher.
+// Tail slice s of a decided sequence: the slice's pieces and mass, then the
+// sequence's tail ticket; the last ticket runs the select finisher.
 template <class E, int VEC>
-__device__ __noinline__ void tail_slice(const SampleArgs& a, const SeqInfo& si, int uc, int w) {
+__device__ __noinline__ void tail_slice(const SampleArgs& a, const SeqInfo& si, int s) {
   const int lane = threadIdx.x & 31;
   if (si.mode == kModeBad) return;  // outputs already written by the statistics finisher
   const int b = si.b;
-  const int s = uc * kSlices + w;
-  const double tot = tail_slice_mass<E, VEC>(a, b, s, si);
+  const float tot = tail_slice_mass<E, VEC>(a, b, s, si);
   int old = 0;
   if (lane == 0) {
     // release: the pieces stored by this lane are visible to whoever sees the mass
-    st_release_f64(a.tailsum + (size_t)b * a.CU * kSlices + s, tot);
+    st_release_f32(a.tailsum + (size_t)b * a.TC + s, tot);
     old = atom_add_relaxed(&a.tailticket[b], 1);
   }
   old = __shfl_sync(0xffffffffu, old, 0);
-  if (old == a.CU * kSlices - 1) select_finisher<E, VEC>(a, si);
+  if (old == a.TC - 1) select_finisher<E, VEC>(a, si);
 }
 
-// Scheduling.  Statistics units come from the warp slot's claim counter; the
-// next one is claimed before the current unit is processed, so the atomic's
-// latency hides behind the stream.  Tail items are owned, not claimed: warp
-// slot w of CTA c takes items c, c + grid, c + 2 grid, ... of slot w, in order,
-// and polls the queue entry of its next item with a relaxed load issued before
-// each statistics slice.  A published item is taken before the next
-// statistics unit.  Only when a warp has no statistics unit left does it wait
-// (bounded) for its next entry.
+// Scheduling.  Statistics slices come from the warp slot's claim counter: the
+// k-th claim on counter w is flat slice f = k * kSlices + w.  The next claim
+// is issued before the current slice is processed, so the atomic's latency
+// hides behind the stream.  Tail slices are owned, not claimed: tail item j
+// (queue position j / TC, tail slice j % TC) belongs to global warp j % W,
+// where warp slot w of CTA c is global warp w * grid + c and W = 8 * grid.  A
+// warp takes its items in order and polls the queue entry of its next item
+// with a relaxed load issued before each statistics slice; a published item
+// is taken before the next statistics slice.  Only when a warp has no
+// statistics slice left does it wait (bounded) for its next entry.
 //
 // Progress: statistics slices and the finishers they trigger wait only for
 // stores that other warps have already issued (their tickets were counted), a
-// warp holding a claimed statistics unit never waits, and every sequence is
-// decided once its statistics units are done.  So every queue entry is
+// warp holding a claimed statistics slice never waits, and every sequence is
+// decided once its statistics slices are done.  So every queue entry is
 // eventually written and every wait ends, whatever part of the grid is
 // resident.
 template <class E, int VEC>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __grid_constant__ SampleArgs a) {
   const int lane = threadIdx.x & 31;
   const int w = slice_of_warp();
-  const int row_last = a.CU * kSlices - 1;
-  const int TT = a.B * a.CU;  // tail items of this slot
-  int t = blockIdx.x;         // this warp's next tail item
-  int unit = bcast(claim_unit(a.counter, lane));
-  uint32_t seen = (lane == 0 && t < TT) ? (uint32_t)poll_decision(a, t / a.CU) : kMarker;
+  const int per_seq = a.R * a.CS;
+  const int TT = a.B * a.TC;                       // tail items in all
+  const int W = kSlices * (int)gridDim.x;          // warps in the grid
+  int t = w * (int)gridDim.x + (int)blockIdx.x;    // this warp's next tail item
+  int f = bcast(claim_unit(a.counter, lane)) * kSlices + w;
+  uint32_t seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
   for (;;) {
     if (t < TT && word_set(bcast((int)seen))) {
-      const SeqInfo si = read_decision(a, t / a.CU);
-      tail_slice<E, VEC>(a, si, t % a.CU, w);
-      t += gridDim.x;
-      seen = (lane == 0 && t < TT) ? (uint32_t)poll_decision(a, t / a.CU) : kMarker;
+      const int pos = fdiv(t, a.div_tc);
+      const SeqInfo si = read_decision(a, pos);
+      tail_slice<E, VEC>(a, si, t - pos * a.TC);
+      t += W;
+      seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
       continue;
     }
-    if (unit < a.map.total) {
+    if (f < a.F) {
       const int next = claim_unit(a.counter, lane);
-      if (lane == 0 && t < TT) seen = (uint32_t)poll_decision(a, t / a.CU);
-      const int b = unit / a.map.A, idx = unit - b * a.map.A;
-      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC>(a, b, idx, w), 0);
-      if (old == row_last) row_finisher<E>(a, b, idx / a.CU);
-      unit = bcast(next);
+      seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
+      const int b = fdiv(f, a.div_seq), rs = f - b * per_seq, r = fdiv(rs, a.div_cs), s = rs - r * a.CS;
+      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC>(a, b, r, s), 0);
+      if (old == a.CS - 1) row_finisher<E>(a, b, r);
+      f = bcast(next) * kSlices + w;
       continue;
     }
     if (t >= TT) break;
     // no statistics work left: wait for this warp's next decision
     if (lane == 0) {
       unsigned it = 0, nap = 64;
-      seen = (uint32_t)poll_decision(a, t / a.CU);
+      seen = poll_decision(a, true, fdiv(t, a.div_tc));
       while (!word_set(seen) && ++it < kSpinLimit) {
         __nanosleep(nap);
         if (nap < 1024) nap <<= 1;
-        seen = (uint32_t)poll_decision(a, t / a.CU);
+        seen = poll_decision(a, true, fdiv(t, a.div_tc));
       }
       if (!word_set(seen)) atomicOr(a.status, kStatusTimeout);
     }
@@ -673,8 +701,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: [zero-filled: counters, tickets, queue count][marker-filled:
 // part, rowstat, tailsum, queue][pieces].
-static void sample_layout(int B, int R, int CU, int P, size_t* off) {
-  const size_t C = (size_t)CU * kSlices;
+static void sample_layout(int B, int R, int CS, int TC, int P, size_t* off) {
   size_t o = 0;
   off[0] = o; o += kCounterBytes;                                          // counter
   off[1] = o; o += align_up((size_t)B * R * kTicketStride * 4, 16);       // rowticket
@@ -683,18 +710,18 @@ static void sample_layout(int B, int R, int CU, int P, size_t* off) {
   off[4] = o; o += 16;                                                     // qcount
   o = align_up(o, 256);
   off[5] = o;                                                              // end of zero region
-  off[6] = o; o += align_up((size_t)B * R * C * sizeof(float2), 256);     // part
+  off[6] = o; o += align_up((size_t)B * R * CS * sizeof(float2), 256);    // part
   off[7] = o; o += align_up((size_t)B * R * sizeof(float2), 256);         // rowstat
-  off[8] = o; o += align_up((size_t)B * C * sizeof(double), 256);         // tailsum
+  off[8] = o; o += align_up((size_t)B * TC * sizeof(float), 256);         // tailsum
   off[10] = o; o += align_up((size_t)B * sizeof(SeqInfo), 256);           // queue
   off[9] = o;                                                              // end of marker region
-  off[11] = o; o += align_up((size_t)B * C * P * sizeof(float), 256);     // pieces
+  off[11] = o; o += align_up((size_t)B * TC * P * sizeof(float), 256);    // pieces
   off[12] = o;
 }
 
-WsLayout sample_workspace(int B, int K, int CU, int P) {
+WsLayout sample_workspace(int B, int K, int CS, int TC, int P) {
   size_t off[13];
-  sample_layout(B, 2 * K + 1, CU, P, off);
+  sample_layout(B, 2 * K + 1, CS, TC, P, off);
   WsLayout l;
   l.total = off[12];
   l.zero_bytes = off[5];
@@ -705,7 +732,7 @@ WsLayout sample_workspace(int B, int K, int CU, int P) {
 
 void sample_bind_workspace(SampleArgs& a, void* ws) {
   size_t off[13];
-  sample_layout(a.B, a.R, a.CU, a.P, off);
+  sample_layout(a.B, a.R, a.CS, a.TC, a.P, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
   a.rowticket = (int*)(p + off[1]);
@@ -714,7 +741,7 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.qcount = (int*)(p + off[4]);
   a.part = (float2*)(p + off[6]);
   a.rowstat = (float2*)(p + off[7]);
-  a.tailsum = (double*)(p + off[8]);
+  a.tailsum = (float*)(p + off[8]);
   a.queue = (SeqInfo*)(p + off[10]);
   a.pieces = (float*)(p + off[11]);
 }

@@ -38,18 +38,8 @@ __device__ __forceinline__ f2_t f2(float lo, float hi) {
   asm("mov.b64 %0, {%1,%2};" : "=l"(r) : "f"(lo), "f"(hi));
   return r;
 }
-__device__ __forceinline__ float f2lo(f2_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  (void)hi;
-  return lo;
-}
-__device__ __forceinline__ float f2hi(f2_t v) {
-  float lo, hi;
-  asm("mov.b64 {%0,%1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v));
-  (void)lo;
-  return hi;
-}
+__device__ __forceinline__ float f2lo(f2_t v) { return __uint_as_float((uint32_t)v); }
+__device__ __forceinline__ float f2hi(f2_t v) { return __uint_as_float((uint32_t)(v >> 32)); }
 __device__ __forceinline__ f2_t f2sub(f2_t a, f2_t b) {
   f2_t r;
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(r) : "l"(a), "l"(b));
@@ -242,12 +232,12 @@ __device__ __forceinline__ int ld_relaxed_s32(const int* p) {
   asm volatile("ld.relaxed.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
   return v;
 }
-__device__ __forceinline__ void st_release_f64(double* p, double v) {
-  asm volatile("st.release.gpu.global.f64 [%0], %1;" ::"l"(p), "d"(v) : "memory");
+__device__ __forceinline__ void st_release_f32(float* p, float v) {
+  asm volatile("st.release.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
-__device__ __forceinline__ double ld_acquire_f64(const double* p) {
-  double v;
-  asm volatile("ld.acquire.gpu.global.f64 %0, [%1];" : "=d"(v) : "l"(p) : "memory");
+__device__ __forceinline__ float ld_acquire_f32(const float* p) {
+  float v;
+  asm volatile("ld.acquire.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
   return v;
 }
 __device__ __forceinline__ int atom_add_relaxed(int* p, int v) {
@@ -278,23 +268,46 @@ __device__ __forceinline__ int wait_s32(const int* p, unsigned* status) {
   if (v == (int)kMarker) atomicOr(status, kStatusTimeout);
   return v;
 }
-__device__ __forceinline__ double wait_f64_acquire(const double* p, unsigned* status) {
-  double v = ld_acquire_f64(p);
+__device__ __forceinline__ float wait_f32_acquire(const float* p, unsigned* status) {
+  float v = ld_acquire_f32(p);
   unsigned it = 0;
-  while (__double_as_longlong(v) == -1LL && ++it < kSpinLimit) {
+  while (__float_as_uint(v) == kMarker && ++it < kSpinLimit) {
     __nanosleep(64);
-    v = ld_acquire_f64(p);
+    v = ld_acquire_f32(p);
   }
-  if (__double_as_longlong(v) == -1LL) atomicOr(status, kStatusTimeout);
+  if (__float_as_uint(v) == kMarker) atomicOr(status, kStatusTimeout);
   return v;
 }
 
-// Lane 0 of warp w claims the next unit from counter w; the value is
-// broadcast when it is used.
+// n / d for 0 <= n < 2^31 with d's FastDiv constants.
+__device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
+  return (int)(((unsigned long long)(unsigned)n * f.m) >> f.shift);
+}
+
+// Lane 0 of warp w claims the next unit from counter w.  The atomic is a
+// predicated instruction rather than a branch, so nothing reads its result
+// register until the value is broadcast: the claim's round trip overlaps
+// whatever the warp does in between.
 __device__ __forceinline__ int slice_of_warp() { return (threadIdx.x >> 5) % kSlices; }
 __device__ __forceinline__ int claim_unit(unsigned long long* counter, int lane) {
-  int v = 0;
-  if (lane == 0) v = (int)atomicAdd(counter + slice_of_warp() * kCounterStride, 1ull);
+  unsigned long long v = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %1, 0;\n\t"
+      "@p atom.relaxed.gpu.global.add.u64 %0, [%2], 1;\n\t}"
+      : "+l"(v)
+      : "r"(lane), "l"(counter + slice_of_warp() * kCounterStride)
+      : "memory");
+  return (int)v;
+}
+// The same for a relaxed 32-bit load issued only where `pred` holds; `v` is
+// returned unchanged elsewhere.
+__device__ __forceinline__ uint32_t ld_relaxed_if(bool pred, const void* p, uint32_t v) {
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "@q ld.relaxed.gpu.global.u32 %0, [%2];\n\t}"
+      : "+r"(v)
+      : "r"((unsigned)pred), "l"(p)
+      : "memory");
   return v;
 }
 __device__ __forceinline__ int bcast(int v) { return __shfl_sync(0xffffffffu, v, 0); }

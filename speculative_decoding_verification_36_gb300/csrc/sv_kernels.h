@@ -2,14 +2,14 @@
 // (api.cu) and the kernel translation units.  Internal to the library.
 //
 // Work decomposition (all three kernels): a persistent grid of independent
-// warps.  A row is cut into slices of SL elements; eight consecutive slices of
-// a row form a unit.  Warp w of every CTA claims units from counter w (one of
-// eight) and processes slice w of each unit it claims, so the eight slices of
-// a unit are streamed at about the same time by eight different warps while
-// each claim counter sees only one eighth of the traffic.  A slice is reduced
-// to one partial result in the workspace; the warp that takes a sequence's
-// last ticket runs that sequence's finisher.  There are no CTA-wide barriers:
-// a warp that waits or finishes a sequence stalls only itself.
+// warps.  A row is cut into slices of SL elements.  Slices are numbered flat,
+// sequence-major (sequence, row, slice), and slice f is handed out by claim
+// counter f % kSlices; warp w of every CTA claims from counter w, so each
+// counter sees one eighth of the claims and every counter has the same amount
+// of work.  A slice is reduced to one partial result in the workspace; the
+// warp that takes a row's (and then a sequence's) last ticket runs the
+// finisher.  There are no CTA-wide barriers: a warp that finishes a row or a
+// sequence stalls only itself.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -26,6 +26,23 @@ constexpr int kMinBlocks = 4;  // resident CTAs per SM the register budget allow
 constexpr int kUnroll = 2;     // 16-byte vectors per lane per load batch; two batches in flight
 constexpr int kMaxK = 255;
 constexpr int kMaxTreeNodes = 1024;
+
+// Division by a per-launch constant d >= 1 for dividends below 2^31, as one
+// widening multiply and a shift (Granlund and Montgomery, "Division by
+// invariant integers using multiplication", PLDI 1994, theorem 4.2 with N = 31:
+// l = ceil(log2 d), m = floor(2^(31+l) / d) + 1 < 2^32, q = (n m) >> (31 + l)).
+struct FastDiv {
+  uint32_t m;
+  int shift;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+  int l = 0;
+  while ((1ull << l) < d) ++l;
+  FastDiv f;
+  f.m = (uint32_t)((1ull << (31 + l)) / d + 1);
+  f.shift = 31 + l;
+  return f;
+}
 
 // Per-sequence decision, published by the statistics finisher as one 32-byte
 // entry of the decision queue.  Entries start filled with kMarker words and
@@ -59,11 +76,13 @@ struct SampleArgs {
   const int32_t* tokens;
   int B, K, V;
   int R;   // rows per sequence = 2K+1
-  int SL;  // slice length in elements (a whole number of load batches)
-  int CS;  // slices per row = ceil(V / SL)
-  int CU;  // units per row = ceil(CS / kSlices)
-  int P;   // pieces (warp steps) per slice
-  UnitMap map;
+  int SL;  // statistics slice length in elements (a whole number of load batches)
+  int CS;  // statistics slices per row = ceil(V / SL)
+  int TL;  // tail slice length in elements (a whole number of warp steps)
+  int TC;  // tail slices per row = ceil(V / TL)
+  int P;   // pieces (warp steps) per tail slice
+  int F;   // statistics slices in all: B * R * CS
+  FastDiv div_seq, div_cs, div_tc;  // division by R * CS, CS and TC
   float c_hi, c_lo;  // log2(e)/temperature as a float pair
   double c64;        // the same in double
   double inv_tau;    // 1 / temperature
@@ -81,11 +100,11 @@ struct SampleArgs {
   int* seqticket;   // [B] finished rows of a sequence
   int* tailticket;  // [B] finished tail slices
   int* qcount;      // decision-queue positions taken so far
-  float2* part;     // [B, R, CU * kSlices] per-slice (m, s)
+  float2* part;     // [B, R, CS] per-slice (m, s)
   float2* rowstat;  // [B, R] merged (m, s) of each row
-  double* tailsum;  // [B, CU * kSlices] per tail-slice mass
+  float* tailsum;   // [B, TC] per tail-slice mass
   SeqInfo* queue;   // [B] decisions in the order they were made
-  float* pieces;    // [B, CU * kSlices, P] per-piece mass
+  float* pieces;    // [B, TC, P] per-piece mass
   unsigned* status;
 };
 
@@ -119,7 +138,7 @@ struct GreedyArgs {
 struct WsLayout {
   size_t total, zero_bytes, marker_off, marker_bytes;
 };
-WsLayout sample_workspace(int B, int K, int CU, int P);
+WsLayout sample_workspace(int B, int K, int CS, int TC, int P);
 WsLayout greedy_workspace(int B, int R, int CU);
 
 // Bind workspace pointers into the argument blocks.

@@ -241,6 +241,43 @@ def run_reference(args):
     return 0
 
 
+def run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps):
+    """The same metric through the public API with the inputs copied from
+    pinned host memory and the outputs read back, every step."""
+    import torch
+    host = [{k: sets[i][k].cpu().pin_memory() for k in ("target", "draft", "tokens")}
+            for i in range(len(sets))]
+    host_out = (torch.empty((p.B, p.K + 1), dtype=torch.int32).pin_memory(),
+                torch.empty((p.B,), dtype=torch.int32).pin_memory())
+    dbuf = {k: torch.empty_like(sets[0][k]) for k in ("target", "draft", "tokens")}
+    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in host[0])
+    d2h = host_out[0].numel() * 4 + host_out[1].numel() * 4
+
+    def e2e_step(i):
+        src = host[i % len(host)]
+        for k in dbuf:
+            dbuf[k].copy_(src[k], non_blocking=True)
+        t, n = sv.spec_verify(dbuf["target"], dbuf["draft"], dbuf["tokens"], p.temperature,
+                              rank_seed(rank, i), stream=stream)
+        host_out[0].copy_(t, non_blocking=True)
+        host_out[1].copy_(n, non_blocking=True)
+
+    e2e_step(0)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(e2e_steps):
+        e2e_step(i)
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    barrier(world)
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
+    e2e_value = world * p.B * e2e_steps / (e2e_ms / 1e3)
+    return e2e_value, h2d, d2h
+
+
 def run_gpu(args):
     import torch
     rank, world, local = dist_env()
@@ -255,14 +292,14 @@ def run_gpu(args):
     from speculative_decoding_verification_36_gb300 import workloads as wl
     _build.build()
 
-    p = wl.preset(WORKLOAD)
-    sets = [wl.make_chain(p, device=dev, seed=rank * 2 + i) for i in range(2)]
+    p = wl.preset(WORKLOAD, B=args.batch) if args.batch else wl.preset(WORKLOAD)
+    sets = [wl.make_chain(p, device=dev, seed=rank * 2 + i) for i in range(args.sets)]
     stream = torch.cuda.current_stream(dev)
     outs = [(torch.empty((p.B, p.K + 1), dtype=torch.int32, device=dev),
              torch.empty((p.B,), dtype=torch.int32, device=dev)) for _ in range(2)]
 
     def step(i):
-        x = sets[i % 2]
+        x = sets[i % len(sets)]
         o = outs[i % 2]
         sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, rank_seed(rank, i),
                        out_tokens=o[0], out_n_accepted=o[1], stream=stream)
@@ -301,37 +338,10 @@ def run_gpu(args):
     flags = sv.spec_get_status()
 
     # end to end through the public API from pinned host buffers
-    e2e_steps = max(3, min(args.steps, args.e2e_steps))
-    host = [{k: sets[i][k].cpu().pin_memory() for k in ("target", "draft", "tokens")}
-            for i in range(2)]
-    host_out = (torch.empty((p.B, p.K + 1), dtype=torch.int32).pin_memory(),
-                torch.empty((p.B,), dtype=torch.int32).pin_memory())
-    dbuf = {k: torch.empty_like(sets[0][k]) for k in ("target", "draft", "tokens")}
-    h2d = sum(host[0][k].numel() * host[0][k].element_size() for k in host[0])
-    d2h = host_out[0].numel() * 4 + host_out[1].numel() * 4
-
-    def e2e_step(i):
-        src = host[i % 2]
-        for k in dbuf:
-            dbuf[k].copy_(src[k], non_blocking=True)
-        t, n = sv.spec_verify(dbuf["target"], dbuf["draft"], dbuf["tokens"], p.temperature,
-                              rank_seed(rank, i), stream=stream)
-        host_out[0].copy_(t, non_blocking=True)
-        host_out[1].copy_(n, non_blocking=True)
-
-    e2e_step(0)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e0 = torch.cuda.Event(enable_timing=True)
-    e1 = torch.cuda.Event(enable_timing=True)
-    e0.record(stream)
-    for i in range(e2e_steps):
-        e2e_step(i)
-    e1.record(stream)
-    torch.cuda.synchronize(dev)
-    barrier(world)
-    e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
-    e2e_value = world * p.B * e2e_steps / (e2e_ms / 1e3)
+    e2e_steps = min(args.steps, args.e2e_steps)
+    e2e_value, h2d, d2h = None, 0, 0
+    if e2e_steps > 0:
+        e2e_value, h2d, d2h = run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps)
 
     if rank != 0:
         if world > 1:
@@ -347,15 +357,15 @@ def run_gpu(args):
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": world, "steps": args.steps,
         "warmup": max(args.warmup, 3), "ms_per_step": total_ms / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32",
-        "data": "synthetic", "config": workload_config(p, True),
+        "data": "synthetic", "config": workload_config(p, len(sets) > 1),
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
                      "frac": achieved / peak, "traffic": traffic,
                      "kernel": "sv::sample_kernel<BF16,8>",
                      "peak_source": f"{peak_kind} hbm_gbs (MEASURED_PEAKS.json)"
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "avg_launch_ms": avg_launch_ms, "bytes_per_launch": abytes},
-        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "steps": e2e_steps},
+        "e2e": ({"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                 "d2h_bytes_per_step": d2h, "steps": e2e_steps} if e2e_steps > 0 else None),
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "status_flags": flags,
@@ -363,10 +373,10 @@ def run_gpu(args):
     if world == 1 and not args.no_cpu_baseline:
         x_cpu = {k: sets[0][k][:64].cpu() for k in ("target", "draft", "tokens")}
         pp = wl.preset(WORKLOAD, B=64)
-        v, done, dt = oracle_seq_per_s(x_cpu, pp, args.cpu_budget, 64)
+        v, done, dt = oracle_seq_per_s(x_cpu, pp, args.cpu_budget, 1 << 30)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
-                                "sample": f"{done} c3 sequences in {dt:.1f} s, fp64 C oracle, "
-                                          "single thread"}
+                                "sample": f"{done} c3 sequences (cycling over the first 64 of "
+                                          f"the batch) in {dt:.1f} s, fp64 C oracle, single thread"}
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist
@@ -380,7 +390,12 @@ def main(argv=None):
     ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
-    ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--e2e-steps", type=int, default=20,
+                    help="steps of the end-to-end (host buffers) measurement; 0 skips it")
+    ap.add_argument("--batch", type=int, default=0,
+                    help="sequences per rank (default: the workload's B); for profiling runs")
+    ap.add_argument("--sets", type=int, default=2, choices=[1, 2],
+                    help="input sets alternated between steps")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)

@@ -27,7 +27,8 @@
  *   - Calls are asynchronous and ordered on `stream` (0 = legacy default
  *     stream).  Per-call scratch memory comes from a library-owned,
  *     stream-ordered CUDA memory pool on the current device and is returned on
- *     the same stream.
+ *     the same stream (spec_verify_bf16_static_scratch alone uses a fixed
+ *     buffer instead).
  *   - bf16 logits are passed as their raw 16-bit patterns (uint16_t).
  *   - Logits may be -inf (masked vocabulary).  A row containing NaN or +inf,
  *     a row with no finite entry, a drafted token outside [0, V), or a tree
@@ -55,6 +56,11 @@ extern "C" {
 #define SPEC_ERR_SHAPE (-2)       /* B < 0, K outside [0, 255], V < 1, N outside [0, 1024], or size overflow */
 #define SPEC_ERR_TEMPERATURE (-3) /* temperature NaN, negative, or in (0, 1e-30) */
 #define SPEC_ERR_CUDA (-4)        /* CUDA runtime error; spec_status_string(-4) gives the message */
+#define SPEC_ERR_SCRATCH (-5)     /* spec_verify_bf16_static_scratch: the problem needs more than
+                                     SPEC_STATIC_SCRATCH_BYTES of scratch */
+
+/* Size of the fixed per-device scratch buffer of spec_verify_bf16_static_scratch. */
+#define SPEC_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
 
 #define SPEC_FLAG_BAD_DATA 1u     /* some sequence had bad data (see above) */
 #define SPEC_FLAG_TIMEOUT 2u      /* an internal bounded wait ran out; outputs of that call are invalid */
@@ -97,6 +103,38 @@ int spec_verify_bf16(const uint16_t *target_logits, const uint16_t *draft_logits
                      const int32_t *draft_tokens, int B, int K, int V, float temperature,
                      uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
                      cudaStream_t stream);
+
+/*
+ * spec_verify_bf16 without any device allocation.  The pages describe the
+ * verify step only; they have no counterpart of this entry point, which exists
+ * for callers that cannot let the library allocate: a serving process that
+ * reserved nearly all device memory up front, a latency-critical loop that
+ * must not enter the allocator, or a device without stream-ordered memory
+ * pools.
+ *
+ * Arguments, layouts, outputs, temperature == 0 (greedy) and results are
+ * exactly those of spec_verify_bf16: the same kernels run and give
+ * bit-identical outputs.  The difference is the scratch memory: instead of
+ * the stream-ordered pool, every call uses one fixed buffer of
+ * SPEC_STATIC_SCRATCH_BYTES per device that is part of the library image
+ * (a static __device__ array, created when the module is loaded); the call
+ * only clears parts of it with cudaMemsetAsync on `stream` and makes no
+ * cudaMalloc/cudaFree or other allocating call.
+ *   - A problem whose scratch exceeds SPEC_STATIC_SCRATCH_BYTES returns
+ *     SPEC_ERR_SCRATCH and launches nothing (for K = 8, V = 152064, B = 256
+ *     needs about 2.2 MB).
+ *   - The buffer's address is looked up on the first call on each device
+ *     (cudaGetSymbolAddress, which may load the module): make that first call
+ *     before any stream capture on that device.
+ *   - One buffer serves every call on a device, so calls that overlap in time
+ *     (different streams or host threads on the same device) race on it and
+ *     produce garbage; calls issued in order on one stream are safe.
+ */
+int spec_verify_bf16_static_scratch(const uint16_t *target_logits,
+                                    const uint16_t *draft_logits,
+                                    const int32_t *draft_tokens, int B, int K, int V,
+                                    float temperature, uint64_t seed, int32_t *out_tokens,
+                                    int32_t *out_n_accepted, cudaStream_t stream);
 
 /*
  * spec_verify_* plus the verify step's intermediate probabilities, for

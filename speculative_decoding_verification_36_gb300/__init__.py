@@ -20,7 +20,7 @@ from . import _lib
 from ._lib import SPEC_FLAG_BAD_DATA, SPEC_FLAG_TIMEOUT, SpecError
 
 __all__ = [
-    "spec_verify", "spec_verify_stats", "spec_verify_greedy_argmax",
+    "spec_verify", "spec_verify_static_scratch", "spec_verify_stats", "spec_verify_greedy_argmax",
     "spec_tree_verify_greedy", "spec_get_status", "SpecError",
     "SPEC_FLAG_BAD_DATA", "SPEC_FLAG_TIMEOUT",
 ]
@@ -100,6 +100,27 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature: float, s
                       _ptr(draft_tokens) if K > 0 else None, B, K, V, float(temperature),
                       int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
                       _stream(stream)))
+    return out_tokens, out_n_accepted
+
+
+def spec_verify_static_scratch(target_logits, draft_logits, draft_tokens, temperature: float,
+                               seed: int, out_tokens=None, out_n_accepted=None, stream=None):
+    """spec_verify for bf16 logits with the library's fixed per-device scratch
+    buffer instead of its memory pool (no device allocation by the library).
+    Calls that overlap in time on one device race on that buffer.  Pass
+    out_tokens / out_n_accepted to keep this wrapper allocation-free too."""
+    bf16, B, K, V = _chain_args(target_logits, draft_logits, draft_tokens, temperature)
+    if not bf16:
+        raise TypeError("spec_verify_static_scratch takes bf16 logits")
+    dev = target_logits.device
+    out_tokens = _out(out_tokens, (B, K + 1), torch.int32, dev, "out_tokens")
+    out_n_accepted = _out(out_n_accepted, (B,), torch.int32, dev, "out_n_accepted")
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        _lib.check(lib.spec_verify_bf16_static_scratch(
+            _ptr(target_logits), _ptr(draft_logits) if temperature > 0 else None,
+            _ptr(draft_tokens) if K > 0 else None, B, K, V, float(temperature),
+            int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted), _stream(stream)))
     return out_tokens, out_n_accepted
 
 

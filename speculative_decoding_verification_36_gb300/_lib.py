@@ -20,6 +20,8 @@ SPEC_ERR_NULL = -1
 SPEC_ERR_SHAPE = -2
 SPEC_ERR_TEMPERATURE = -3
 SPEC_ERR_CUDA = -4
+SPEC_ERR_SCRATCH = -5
+SPEC_STATIC_SCRATCH_BYTES = 8 << 20
 SPEC_FLAG_BAD_DATA = 1
 SPEC_FLAG_TIMEOUT = 2
 
@@ -35,6 +37,7 @@ _U64 = ctypes.c_uint64
 SIGNATURES = {
     "spec_verify_f32": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_verify_bf16": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
+    "spec_verify_bf16_static_scratch": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_verify_stats_f32": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P, _P, _P, _P],
     "spec_verify_stats_bf16": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P, _P, _P, _P],
     "spec_verify_greedy_argmax_f32": [_P, _P, _I, _I, _I, _P, _P, _P, _P],

@@ -19,12 +19,29 @@
 // spec_get_status.
 __device__ unsigned g_spec_status;
 
+// Scratch of spec_verify_bf16_static_scratch.  Some callers cannot let the
+// library allocate device memory on their behalf:
+//   * a serving process that reserved nearly all of HBM up front (for its KV
+//     cache) leaves the library's pool no room to grow, and a failed pool
+//     allocation in the middle of a decode step is not recoverable there;
+//   * latency-critical loops must not enter the allocator, whose locks and
+//     pool growth add jitter to an otherwise fixed-cost step;
+//   * devices or virtualised set-ups without stream-ordered memory pools
+//     (cudaDevAttrMemoryPoolsSupported == 0) cannot serve
+//     cudaMallocFromPoolAsync at all.
+// For them the library carries one fixed scratch buffer per device in its
+// own image: this file-scope array, created when the module is loaded.  Its
+// address is looked up once per device with cudaGetSymbolAddress.
+constexpr size_t kStaticScratchBytes = SPEC_STATIC_SCRATCH_BYTES;
+__device__ __align__(256) unsigned char g_static_scratch[kStaticScratchBytes];
+
 namespace {
 
 struct DeviceState {
   bool init = false;
   int sms = 0;
-  cudaMemPool_t pool = nullptr;
+  cudaMemPool_t pool = nullptr;  // created by the first call that allocates
+  void* static_scratch = nullptr;  // looked up by the first static-scratch call
   unsigned* status = nullptr;
   int occ_sample[2][2] = {{0, 0}, {0, 0}};  // [bf16][vec]
   int occ_greedy[2][2] = {{0, 0}, {0, 0}};
@@ -52,16 +69,6 @@ int get_device_state(DeviceState** out) {
   if (!d.init) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    cudaMemPoolProps props;
-    memset(&props, 0, sizeof props);
-    props.allocType = cudaMemAllocationTypePinned;
-    props.location.type = cudaMemLocationTypeDevice;
-    props.location.id = dev;
-    e = cudaMemPoolCreate(&d.pool, &props);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
-    uint64_t keep = UINT64_MAX;  // keep freed scratch in the pool between calls
-    e = cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &keep);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolSetAttribute");
     e = cudaGetSymbolAddress((void**)&d.status, g_spec_status);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
     for (int bf = 0; bf < 2; ++bf)
@@ -73,6 +80,32 @@ int get_device_state(DeviceState** out) {
     d.init = true;
   }
   *out = &d;
+  return SPEC_OK;
+}
+
+// The library's stream-ordered pool on the current device, created on first
+// use.
+int ensure_pool(DeviceState* d) {
+  std::lock_guard<std::mutex> lock(g_mu);
+  if (d->pool) return SPEC_OK;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  cudaMemPoolProps props;
+  memset(&props, 0, sizeof props);
+  props.allocType = cudaMemAllocationTypePinned;
+  props.location.type = cudaMemLocationTypeDevice;
+  props.location.id = dev;
+  cudaMemPool_t pool = nullptr;
+  e = cudaMemPoolCreate(&pool, &props);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
+  uint64_t keep = UINT64_MAX;  // keep freed scratch in the pool between calls
+  e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  if (e != cudaSuccess) {
+    cudaMemPoolDestroy(pool);
+    return cuda_fail(e, "cudaMemPoolSetAttribute");
+  }
+  d->pool = pool;
   return SPEC_OK;
 }
 
@@ -119,6 +152,8 @@ bool sizes_ok(int B, int rows, int V) {
 // Stream-ordered scratch from the library's pool, with the zero region and
 // the "not yet written" marker region initialised on the stream.
 int run_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, void** ws) {
+  const int rc = ensure_pool(d);
+  if (rc) return rc;
   cudaError_t e = cudaMallocFromPoolAsync(ws, l.total, d->pool, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
   e = cudaMemsetAsync(*ws, 0, l.zero_bytes, stream);
@@ -130,10 +165,43 @@ int run_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, void
   return SPEC_OK;
 }
 
+// The static scratch buffer, with the same two regions initialised on the
+// stream (cudaMemsetAsync only; nothing is allocated).  A layout larger than
+// the buffer is refused before anything is launched.
+int static_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, void** ws) {
+  if (l.total > kStaticScratchBytes) return SPEC_ERR_SCRATCH;
+  {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d->static_scratch) {
+      const cudaError_t e = cudaGetSymbolAddress(&d->static_scratch, g_static_scratch);
+      if (e != cudaSuccess) {
+        d->static_scratch = nullptr;
+        return cuda_fail(e, "cudaGetSymbolAddress");
+      }
+    }
+  }
+  *ws = d->static_scratch;
+  cudaError_t e = cudaMemsetAsync(*ws, 0, l.zero_bytes, stream);
+  if (e == cudaSuccess) e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
+  return SPEC_OK;
+}
+
+// Scratch for one call: stream-ordered from the pool (returned after the
+// launch), or the static buffer.
+int get_scratch(DeviceState* d, bool use_static, const sv::WsLayout& l, cudaStream_t stream,
+                void** ws) {
+  return use_static ? static_scratch(d, l, stream, ws) : run_scratch(d, l, stream, ws);
+}
+cudaError_t put_scratch(bool use_static, void* ws, cudaStream_t stream) {
+  return use_static ? cudaSuccess : cudaFreeAsync(ws, stream);
+}
+
 // Greedy chain (tree == false) or tree (tree == true) verification.
 int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
                 const int32_t* parents, int B, int K, int V, int32_t* out_tokens, int32_t* out_n,
-                uint32_t* out_mask, int32_t* out_row_argmax, cudaStream_t stream) {
+                uint32_t* out_mask, int32_t* out_row_argmax, cudaStream_t stream,
+                bool use_static = false) {
   DeviceState* d = nullptr;
   int rc = get_device_state(&d);
   if (rc) return rc;
@@ -158,34 +226,37 @@ int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
   a.out_row_argmax = out_row_argmax;
   a.status = d->status;
   void* ws = nullptr;
-  rc = run_scratch(d, sv::greedy_workspace(B, a.R, a.CU), stream, &ws);
+  rc = get_scratch(d, use_static, sv::greedy_workspace(B, a.R, a.CU), stream, &ws);
   if (rc) return rc;
   sv::greedy_bind_workspace(a, ws);
   const int grid = grid_for(a.map.total, capacity);
   cudaError_t e = tree ? sv::launch_tree(a, bf16, vec, grid, stream)
                        : sv::launch_greedy(a, bf16, vec, grid, stream);
-  cudaError_t e2 = cudaFreeAsync(ws, stream);
+  cudaError_t e2 = put_scratch(use_static, ws, stream);
   if (e != cudaSuccess) return cuda_fail(e, tree ? "tree verify launch" : "greedy verify launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
   return SPEC_OK;
 }
 
 int greedy_impl(bool bf16, const void* target, const int32_t* tokens, int B, int K, int V,
-                int32_t* out_tokens, int32_t* out_n, int32_t* out_row_argmax, cudaStream_t stream) {
+                int32_t* out_tokens, int32_t* out_n, int32_t* out_row_argmax, cudaStream_t stream,
+                bool use_static = false) {
   if (!target || !out_tokens || !out_n || (K > 0 && !tokens)) return SPEC_ERR_NULL;
   if (B < 0 || K < 0 || K > sv::kMaxK || V < 1 || !sizes_ok(B, K + 1, V)) return SPEC_ERR_SHAPE;
   if (B == 0) return SPEC_OK;
   return argmax_impl(false, bf16, target, tokens, nullptr, B, K, V, out_tokens, out_n, nullptr,
-                     out_row_argmax, stream);
+                     out_row_argmax, stream, use_static);
 }
 
 int verify_impl(bool bf16, const void* target, const void* draft, const int32_t* tokens, int B,
                 int K, int V, float temperature, uint64_t seed, int32_t* out_tokens, int32_t* out_n,
-                float* out_row_stats, float* out_pq, float* out_resid, cudaStream_t stream) {
+                float* out_row_stats, float* out_pq, float* out_resid, cudaStream_t stream,
+                bool use_static = false) {
   if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-30f))
     return SPEC_ERR_TEMPERATURE;
   if (temperature == 0.f)
-    return greedy_impl(bf16, target, tokens, B, K, V, out_tokens, out_n, nullptr, stream);
+    return greedy_impl(bf16, target, tokens, B, K, V, out_tokens, out_n, nullptr, stream,
+                       use_static);
   if (!target || !out_tokens || !out_n || (K > 0 && (!tokens || !draft))) return SPEC_ERR_NULL;
   if (B < 0 || K < 0 || K > sv::kMaxK || V < 1 || !sizes_ok(B, 2 * K + 1, V)) return SPEC_ERR_SHAPE;
   if (B == 0) return SPEC_OK;
@@ -232,11 +303,11 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.out_resid = out_resid;
   a.status = d->status;
   void* ws = nullptr;
-  rc = run_scratch(d, sv::sample_workspace(B, K, a.CS, a.TC, a.P), stream, &ws);
+  rc = get_scratch(d, use_static, sv::sample_workspace(B, K, a.CS, a.TC, a.P), stream, &ws);
   if (rc) return rc;
   sv::sample_bind_workspace(a, ws);
   cudaError_t e = sv::launch_sample(a, bf16, vec, grid, stream);
-  cudaError_t e2 = cudaFreeAsync(ws, stream);
+  cudaError_t e2 = put_scratch(use_static, ws, stream);
   if (e != cudaSuccess) return cuda_fail(e, "sampling verify launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
   return SPEC_OK;
@@ -272,6 +343,14 @@ int spec_verify_bf16(const uint16_t* target_logits, const uint16_t* draft_logits
                      cudaStream_t stream) {
   return verify_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
                      out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream);
+}
+
+int spec_verify_bf16_static_scratch(const uint16_t* target_logits, const uint16_t* draft_logits,
+                                    const int32_t* draft_tokens, int B, int K, int V,
+                                    float temperature, uint64_t seed, int32_t* out_tokens,
+                                    int32_t* out_n_accepted, cudaStream_t stream) {
+  return verify_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
+                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream, true);
 }
 
 int spec_verify_stats_f32(const float* target_logits, const float* draft_logits,
@@ -349,6 +428,9 @@ const char* spec_status_string(int code) {
       return "bad temperature: NaN, negative, or in (0, 1e-30)";
     case SPEC_ERR_CUDA:
       return g_cuda_msg;
+    case SPEC_ERR_SCRATCH:
+      return "the problem needs more scratch than the static buffer holds "
+             "(SPEC_STATIC_SCRATCH_BYTES)";
     default:
       return "unknown status code";
   }

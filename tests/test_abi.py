@@ -28,7 +28,7 @@ def test_library_exports_every_header_symbol(lib):
 
 
 def test_status_strings(lib):
-    for code in (0, -1, -2, -3, -4, 99):
+    for code in (0, -1, -2, -3, -4, -5, 99):
         assert isinstance(lib.spec_status_string(code), bytes)
 
 
@@ -41,7 +41,10 @@ def _chain(lib, fn="spec_verify_f32", target=FAKE, draft=FAKE, tokens=FAKE, B=2,
     return getattr(lib, fn)(target, draft, tokens, B, K, V, temperature, 0, out_tokens, out_n, None)
 
 
-@pytest.mark.parametrize("fn", ["spec_verify_f32", "spec_verify_bf16"])
+CHAIN_FNS = ["spec_verify_f32", "spec_verify_bf16", "spec_verify_bf16_static_scratch"]
+
+
+@pytest.mark.parametrize("fn", CHAIN_FNS)
 def test_null_pointers(lib, fn):
     assert _chain(lib, fn, target=None) == _lib.SPEC_ERR_NULL
     assert _chain(lib, fn, out_tokens=None) == _lib.SPEC_ERR_NULL
@@ -50,7 +53,7 @@ def test_null_pointers(lib, fn):
     assert _chain(lib, fn, draft=None) == _lib.SPEC_ERR_NULL
 
 
-@pytest.mark.parametrize("fn", ["spec_verify_f32", "spec_verify_bf16"])
+@pytest.mark.parametrize("fn", CHAIN_FNS)
 def test_bad_shapes(lib, fn):
     assert _chain(lib, fn, B=-1) == _lib.SPEC_ERR_SHAPE
     assert _chain(lib, fn, K=-1) == _lib.SPEC_ERR_SHAPE
@@ -59,15 +62,17 @@ def test_bad_shapes(lib, fn):
     assert _chain(lib, fn, B=2**30, K=255, V=2**30) == _lib.SPEC_ERR_SHAPE
 
 
+@pytest.mark.parametrize("fn", CHAIN_FNS)
 @pytest.mark.parametrize("tau", [math.nan, -1.0, 1e-35])
-def test_bad_temperature(lib, tau):
-    assert _chain(lib, temperature=tau) == _lib.SPEC_ERR_TEMPERATURE
+def test_bad_temperature(lib, fn, tau):
+    assert _chain(lib, fn, temperature=tau) == _lib.SPEC_ERR_TEMPERATURE
 
 
-def test_empty_batch_is_a_noop(lib):
+@pytest.mark.parametrize("fn", CHAIN_FNS)
+def test_empty_batch_is_a_noop(lib, fn):
     # B == 0 returns before touching the device
-    assert _chain(lib, B=0) == _lib.SPEC_OK
-    assert _chain(lib, B=0, temperature=0.0) == _lib.SPEC_OK
+    assert _chain(lib, fn, B=0) == _lib.SPEC_OK
+    assert _chain(lib, fn, B=0, temperature=0.0) == _lib.SPEC_OK
 
 
 def test_greedy_needs_no_draft(lib):

@@ -112,7 +112,7 @@ int ensure_pool(DeviceState* d) {
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Tuning knob (environment, read once): SPECVERIFY_SLICE_BYTES, the bytes of
-// logits per slice (default 8192).
+// logits per slice (default 12288).
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
@@ -124,7 +124,7 @@ int env_int(const char* name, int dflt) {
 // vectors) covering about SPECVERIFY_SLICE_BYTES; a row shorter than one slice
 // is one slice.
 void choose_slices(int V, int vec_elems, size_t esz, int* SL, int* CS, int* CU) {
-  static const int bytes = env_int("SPECVERIFY_SLICE_BYTES", 8192);
+  static const int bytes = env_int("SPECVERIFY_SLICE_BYTES", 12288);
   const long long batch = 32LL * vec_elems * sv::kUnroll;
   long long k = ((long long)bytes / (long long)esz + batch - 1) / batch;
   if (k < 1) k = 1;

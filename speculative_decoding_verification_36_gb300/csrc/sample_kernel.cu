@@ -152,8 +152,20 @@ __device__ __forceinline__ TailConsts tail_consts(const SampleArgs& a, const Seq
 // position and writes its SeqInfo there with two relaxed 16-byte stores; a
 // reader validates each field against kMarker (a NaN no field ever holds).
 // ---------------------------------------------------------------------------
-__device__ __forceinline__ void publish_decision(const SampleArgs& a, const SeqInfo& si) {
-  const int pos = atom_add_relaxed(a.qcount, 1);
+// Lane 0 takes the next queue position (a predicated atomic: nothing waits
+// for it until the entry is written).
+__device__ __forceinline__ int reserve_decision(const SampleArgs& a, int lane) {
+  int v = 0;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %1, 0;\n\t"
+      "@p atom.relaxed.gpu.global.add.s32 %0, [%2], 1;\n\t}"
+      : "+r"(v)
+      : "r"(lane), "l"(a.qcount)
+      : "memory");
+  return v;
+}
+
+__device__ __forceinline__ void publish_decision(const SampleArgs& a, int pos, const SeqInfo& si) {
   uint32_t* e = (uint32_t*)(a.queue + pos);
   st_relaxed_v4(e, (uint32_t)si.b, (uint32_t)si.n, (uint32_t)si.mode, __float_as_uint(si.mT));
   st_relaxed_v4(e + 4, __float_as_uint(si.mD), __float_as_uint(si.lam_hi), __float_as_uint(si.lam_lo),
@@ -199,13 +211,43 @@ __device__ __noinline__ SeqInfo read_decision(const SampleArgs& a, int pos) {
 }
 
 // ---------------------------------------------------------------------------
+// Inputs of the statistics finisher for one chunk of 32 positions (lane i:
+// position i0 + i): target row i's and draft row i's (m, s), the drafted token
+// and the logits at it.  One round of independent relaxed loads; slots still
+// holding the marker are waited for by the finisher.
+// ---------------------------------------------------------------------------
+struct FinIn {
+  uint2 st, sd;
+  int xi;
+  float zT, zD;
+};
+
+__device__ __forceinline__ FinIn load_fin_inputs(const SampleArgs& a, int b, int i0) {
+  const int K = a.K, R = a.R;
+  const int i = i0 + (threadIdx.x & 31);
+  const bool hasT = i <= K, hasD = i < K;
+  const float2* rs = a.rowstat + (size_t)b * R;
+  const float* zx = a.zx + (size_t)b * R;
+  FinIn in;
+  in.st = hasT ? ld_relaxed_u2(rs + i) : make_uint2(0u, 0u);
+  in.sd = hasD ? ld_relaxed_u2(rs + K + 1 + i) : make_uint2(0u, 0u);
+  in.xi = hasD ? __ldg(a.tokens + (size_t)b * K + i) : 0;
+  in.zT = hasD ? ld_relaxed_f32(zx + i) : 0.f;
+  in.zD = hasD ? ld_relaxed_f32(zx + K + 1 + i) : 0.f;
+  return in;
+}
+
+// ---------------------------------------------------------------------------
 // row finisher (one warp): merges the slice partials of row r in slice order
 // (lane-strided, then the fixed warp merge) into rowstat; the last row of a
 // sequence then runs the statistics finisher.
 // ---------------------------------------------------------------------------
 template <class E>
-__device__ __noinline__ void stats_finisher(const SampleArgs& a, int b);
+__device__ __noinline__ void stats_finisher(const SampleArgs& a, int b, FinIn pre);
 
+// The sequence ticket is taken with a predicated atomic, and the finisher's
+// inputs for positions 0..31 are loaded while it is in flight, so the last
+// row goes on to the finisher without another round trip.
 template <class E>
 __device__ __noinline__ void row_finisher(const SampleArgs& a, int b, int r) {
   const int lane = threadIdx.x & 31;
@@ -217,100 +259,114 @@ __device__ __noinline__ void row_finisher(const SampleArgs& a, int b, int r) {
     ms_merge(m, s, __uint_as_float(w.x), __uint_as_float(w.y), a.c_hi);
   }
   warp_ms(m, s, a.c_hi);
-  int old = 0;
-  if (lane == 0) {
-    st_relaxed_u2(a.rowstat + (size_t)b * a.R + r, __float_as_uint(m), __float_as_uint(s));
-    old = atom_add_relaxed(&a.seqticket[b], 1);
-  }
+  if (lane == 0) st_relaxed_u2(a.rowstat + (size_t)b * a.R + r, __float_as_uint(m), __float_as_uint(s));
+  int old = atom_add_if(lane == 0, &a.seqticket[b], 1);
+  const FinIn pre = load_fin_inputs(a, b, 0);
   old = __shfl_sync(0xffffffffu, old, 0);
-  if (old == a.R - 1) stats_finisher<E>(a, b);
+  if (old == a.R - 1) stats_finisher<E>(a, b, pre);
 }
 
 // ---------------------------------------------------------------------------
 // statistics finisher (one warp): steps 2-4 for sequence b
 // ---------------------------------------------------------------------------
+__device__ __forceinline__ bool row_ok(uint2 w) {
+  const float m = __uint_as_float(w.x), sum = __uint_as_float(w.y);
+  return sum > 0.f && sum < INFINITY && m < INFINITY && m > neg_inf();
+}
+__device__ __forceinline__ uint2 shfl_u2(uint2 v, int src) {
+  return make_uint2(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src));
+}
+
+// Position i of a chunk is lane i: target row i, draft row i, the drafted
+// token x_i and the two logits at x_i (recorded by the statistics slices that
+// hold them).  Target row K rides along as position K.  Every chunk issues one
+// round of independent loads; the decision is published before the output
+// tokens are written, and its queue position is taken first so that the
+// atomic's round trip overlaps the loads.
 template <class E>
-__device__ __noinline__ void stats_finisher(const SampleArgs& a, int b) {
+__device__ __noinline__ void stats_finisher(const SampleArgs& a, int b, FinIn pre) {
   const int R = a.R, K = a.K;
   const int lane = threadIdx.x & 31;
   const float2* rs = a.rowstat + (size_t)b * R;
-  for (int r = lane; r < R; r += 32) {
-    const uint2 w = wait_u2(rs + r, a.status);  // the row finisher's (m, s)
+  const float* zx = a.zx + (size_t)b * R;
+  const int32_t* x = a.tokens + (size_t)b * K;
+  const int qpos = reserve_decision(a, lane);
+  bool bad = false;
+  int n = K;
+  uint2 stn = make_uint2(0u, 0u), sdn = make_uint2(0u, 0u);
+  for (int i0 = 0; i0 <= K; i0 += 32) {
+    const int i = i0 + lane;
+    const bool hasT = i <= K, hasD = i < K;
+    const FinIn in = i0 == 0 ? pre : load_fin_inputs(a, b, i0);
+    uint2 st = in.st, sd = in.sd;
+    const int xi = in.xi;
+    float zT = in.zT, zD = in.zD;
+    if (hasT && st.x == kMarker) st = wait_u2(rs + i, a.status);
+    if (hasD && sd.x == kMarker) sd = wait_u2(rs + K + 1 + i, a.status);
     if (a.out_row_stats) {
-      a.out_row_stats[((size_t)b * R + r) * 2 + 0] = (float)((double)__uint_as_float(w.x) * a.inv_tau);
-      a.out_row_stats[((size_t)b * R + r) * 2 + 1] = __uint_as_float(w.y);
+      if (hasT) {
+        a.out_row_stats[((size_t)b * R + i) * 2 + 0] = (float)((double)__uint_as_float(st.x) * a.inv_tau);
+        a.out_row_stats[((size_t)b * R + i) * 2 + 1] = __uint_as_float(st.y);
+      }
+      if (hasD) {
+        a.out_row_stats[((size_t)b * R + K + 1 + i) * 2 + 0] =
+            (float)((double)__uint_as_float(sd.x) * a.inv_tau);
+        a.out_row_stats[((size_t)b * R + K + 1 + i) * 2 + 1] = __uint_as_float(sd.y);
+      }
+    }
+    bool ok = !hasT || row_ok(st);
+    if (hasD) ok = ok && row_ok(sd) && xi >= 0 && xi < a.V;
+    bad |= !ok;
+    bool reject = false;
+    if (hasD && ok) {
+      // the slice holding x_i writes these; a valid token always has one
+      if (__float_as_uint(zT) == kMarker) zT = wait_f32(zx + i, a.status);
+      if (__float_as_uint(zD) == kMarker) zD = wait_f32(zx + K + 1 + i, a.status);
+      const double mT = __uint_as_float(st.x), sT = __uint_as_float(st.y);
+      const double mD = __uint_as_float(sd.x), sD = __uint_as_float(sd.y);
+      // log2 of the unnormalised probabilities, from exact differences
+      const double lp = ((double)zT - mT) * a.c64;
+      const double lq = ((double)zD - mD) * a.c64;
+      const double u = uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0);
+      bool accept;
+      if (zD == neg_inf()) {
+        accept = true;  // q(x) = 0 <= p(x)
+      } else {
+        const double ratio = exp2(lp - lq) * (sD / sT);  // p(x) / q(x)
+        accept = u < ratio;
+      }
+      reject = !accept;
+      if (a.out_pq) {
+        a.out_pq[((size_t)b * K + i) * 2 + 0] = (float)(exp2(lp) / sT);
+        a.out_pq[((size_t)b * K + i) * 2 + 1] = (float)(exp2(lq) / sD);
+      }
+    }
+    const unsigned bal = __ballot_sync(0xffffffffu, reject);
+    if (n == K && bal) {
+      const int L = __ffs(bal) - 1;
+      n = i0 + L;
+      stn = shfl_u2(st, L);
+      sdn = shfl_u2(sd, L);
+    } else if (n == K && K - i0 < 32) {  // the chunk holding position K, nothing rejected
+      stn = shfl_u2(st, K - i0);
     }
   }
-  __syncwarp();
-  const int32_t* x = a.tokens + (size_t)b * K;
-  bool bad = false;
-  for (int r = lane; r < R; r += 32) {
-    const float2 v = __ldcg(rs + r);
-    bad |= !(v.y > 0.f) || !(v.y < INFINITY) || !(v.x < INFINITY) || !(v.x > neg_inf());
-  }
-  for (int i = lane; i < K; i += 32) bad |= x[i] < 0 || x[i] >= a.V;
   bad = __any_sync(0xffffffffu, bad);
 
-  int n = K;
-  if (!bad) {
-    for (int i0 = 0; i0 < K; i0 += 32) {
-      const int i = i0 + lane;
-      bool reject = false;
-      if (i < K) {
-        const int xi = x[i];
-        const float zT = E::load1(target_row<E>(a, b, i) + xi);
-        const float zD = E::load1(draft_row<E>(a, b, i) + xi);
-        const float2 st = __ldcg(rs + i), sd = __ldcg(rs + K + 1 + i);
-        const double mT = st.x, sT = st.y, mD = sd.x, sD = sd.y;
-        // log2 of the unnormalised probabilities, from exact differences
-        const double lp = ((double)zT - mT) * a.c64;
-        const double lq = ((double)zD - mD) * a.c64;
-        const double u = uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0);
-        bool accept;
-        if (zD == neg_inf()) {
-          accept = true;  // q(x) = 0 <= p(x)
-        } else {
-          const double ratio = exp2(lp - lq) * (sD / sT);  // p(x) / q(x)
-          accept = u < ratio;
-        }
-        reject = !accept;
-        if (a.out_pq) {
-          a.out_pq[((size_t)b * K + i) * 2 + 0] = (float)(exp2(lp) / sT);
-          a.out_pq[((size_t)b * K + i) * 2 + 1] = (float)(exp2(lq) / sD);
-        }
-      }
-      const unsigned bal = __ballot_sync(0xffffffffu, reject);
-      if (bal && n == K) n = i0 + __ffs(bal) - 1;
-    }
-  }
-
-  int32_t* out = a.out_tokens + (size_t)b * (K + 1);
   SeqInfo si;
   si.b = b;
   if (bad) {
-    for (int j = lane; j <= K; j += 32) out[j] = -1;
     si.n = 0;
     si.mode = kModeBad;
     si.mT = si.mD = si.lam_hi = si.lam_lo = si.sT = 0.f;
-    if (lane == 0) {
-      a.out_n[b] = -1;
-      atomicOr(a.status, kStatusBadData);
-      if (a.out_resid) a.out_resid[b] = NAN;
-    }
   } else {
-    for (int j = lane; j <= K; j += 32) {
-      if (j < n) out[j] = x[j];
-      else if (j > n) out[j] = -1;
-    }
-    const float2 st = __ldcg(rs + n);
     si.n = n;
-    si.mT = st.x;
-    si.sT = st.y;
+    si.mT = __uint_as_float(stn.x);
+    si.sT = __uint_as_float(stn.y);
     if (n < K) {
-      const float2 sd = __ldcg(rs + K + 1 + n);
       si.mode = kModeResidual;
-      si.mD = sd.x;
-      const double lam = log2((double)st.y) - log2((double)sd.y);
+      si.mD = __uint_as_float(sdn.x);
+      const double lam = log2((double)si.sT) - log2((double)__uint_as_float(sdn.y));
       si.lam_hi = (float)lam;
       si.lam_lo = (float)(lam - (double)si.lam_hi);
     } else {
@@ -318,9 +374,24 @@ __device__ __noinline__ void stats_finisher(const SampleArgs& a, int b) {
       si.mD = 0.f;
       si.lam_hi = si.lam_lo = 0.f;
     }
+  }
+  if (lane == 0) publish_decision(a, qpos, si);
+
+  int32_t* out = a.out_tokens + (size_t)b * (K + 1);
+  if (bad) {
+    for (int j = lane; j <= K; j += 32) out[j] = -1;
+    if (lane == 0) {
+      a.out_n[b] = -1;
+      atomicOr(a.status, kStatusBadData);
+      if (a.out_resid) a.out_resid[b] = NAN;
+    }
+  } else {
+    for (int j = lane; j <= K; j += 32) {
+      if (j < n) out[j] = __ldg(x + j);
+      else if (j > n) out[j] = -1;
+    }
     if (lane == 0) a.out_n[b] = n;
   }
-  if (lane == 0) publish_decision(a, si);
   __syncwarp();
 }
 
@@ -375,7 +446,7 @@ __device__ float tail_slice_mass(const SampleArgs& a, int b, int s, const SeqInf
       d1 = k.residual ? load_raw<E, VEC>(rowD, e + STEPW, v1) : t1;
     }
     float ps = warp_sum(lane_mass<E, VEC>(t0, d0, k));
-    if (lane == 0) gp[q] = ps;
+    if (lane == 0) st_relaxed_f32(gp + q, ps);
     total += ps;
     if (has1) {
       if (q + 2 < nsteps) {
@@ -383,7 +454,7 @@ __device__ float tail_slice_mass(const SampleArgs& a, int b, int s, const SeqInf
         d0 = k.residual ? load_raw<E, VEC>(rowD, e + 2 * STEPW, v1) : t0;
       }
       ps = warp_sum(lane_mass<E, VEC>(t1, d1, k));
-      if (lane == 0) gp[q + 1] = ps;
+      if (lane == 0) st_relaxed_f32(gp + q + 1, ps);
       total += ps;
     }
   }
@@ -396,40 +467,51 @@ __device__ float tail_slice_mass(const SampleArgs& a, int b, int s, const SeqInf
 
 // First position i < count with positive mass whose running sum (from `run`
 // on, in index order) exceeds theta; when rounding leaves theta past every
-// running sum, the last position with mass.  Values are read 32 at a time, the
-// running sum is a warp prefix in fp64.  Returns -1 when no value is positive;
-// *before gets the running sum just before the chosen position.
+// running sum, the last position with mass.  Values are read 128 at a time
+// (four per lane, one round of loads), the running sum is a warp prefix in
+// fp64 over each group of 32.  Returns -1 when no value is positive; *before
+// gets the running sum just before the chosen position.
 template <class LOAD>
 __device__ __forceinline__ int warp_cdf_search(int count, double theta, double run, LOAD load,
                                                double* before) {
   const int lane = threadIdx.x & 31;
   int last = -1;
   double last_before = 0.0;
-  for (int c0 = 0; c0 < count; c0 += 32) {
-    const int i = c0 + lane;
-    const double v = i < count ? load(i) : 0.0;
-    const bool pos = v > 0.0;
-    double incl = v;
+  for (int b0 = 0; b0 < count; b0 += 128) {
+    double vals[4];
 #pragma unroll
-    for (int off = 1; off < 32; off <<= 1) {
-      const double o = __shfl_up_sync(0xffffffffu, incl, off);
-      if (lane >= off) incl += o;
+    for (int q = 0; q < 4; ++q) {
+      const int i = b0 + 32 * q + lane;
+      vals[q] = i < count ? load(i) : 0.0;
     }
-    double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-    if (lane == 0) excl = 0.0;
-    const unsigned hit = __ballot_sync(0xffffffffu, pos && run + incl > theta);
-    const unsigned has = __ballot_sync(0xffffffffu, pos);
-    if (hit) {
-      const int L = __ffs(hit) - 1;
-      *before = __shfl_sync(0xffffffffu, run + excl, L);
-      return c0 + L;
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c0 = b0 + 32 * q;
+      if (c0 >= count) break;
+      const double v = vals[q];
+      const bool pos = v > 0.0;
+      double incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const double o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      double excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) excl = 0.0;
+      const unsigned hit = __ballot_sync(0xffffffffu, pos && run + incl > theta);
+      const unsigned has = __ballot_sync(0xffffffffu, pos);
+      if (hit) {
+        const int L = __ffs(hit) - 1;
+        *before = __shfl_sync(0xffffffffu, run + excl, L);
+        return c0 + L;
+      }
+      if (has) {
+        const int L = 31 - __clz(has);
+        last = c0 + L;
+        last_before = __shfl_sync(0xffffffffu, run + excl, L);
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
     }
-    if (has) {
-      const int L = 31 - __clz(has);
-      last = c0 + L;
-      last_before = __shfl_sync(0xffffffffu, run + excl, L);
-    }
-    run += __shfl_sync(0xffffffffu, incl, 31);
   }
   *before = last_before;
   return last;
@@ -443,10 +525,24 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   const int b = si.b, n = si.n;
   const int C = a.TC;  // tail slices of the row, in vocabulary order
   float* ts = a.tailsum + (size_t)b * C;
-  // Z: lane-strided acquire loads (they order the piece reads below), then a
+  const double w = uniform_draw(a.seed, (uint64_t)b, (uint64_t)n, 1);
+  // Z: the slice masses, lane-strided, four per lane per round of loads, then a
   // fixed-order butterfly
   double z = 0.0;
-  for (int t = lane; t < C; t += 32) z += (double)wait_f32_acquire(ts + t, a.status);
+  for (int c0 = 0; c0 < C; c0 += 128) {
+    float v[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int t = c0 + 32 * q + lane;
+      v[q] = t < C ? ld_relaxed_f32(ts + t) : 0.f;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int t = c0 + 32 * q + lane;
+      if (t < C && __float_as_uint(v[q]) == kMarker) v[q] = wait_f32(ts + t, a.status);
+      z += (double)v[q];
+    }
+  }
   double Z = warp_sum_f64(z);
   // Z == 0 after a rejection can only come from rounding (p(x_n) < q(x_n)
   // forces a positive residual); then the draw falls back to p_n itself, and
@@ -456,21 +552,21 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
     z = 0.0;
     for (int t = 0; t < C; ++t) {
       const float tot = tail_slice_mass<E, VEC>(a, b, t, si);
-      if (lane == 0) ts[t] = tot;
+      if (lane == 0) st_relaxed_f32(ts + t, tot);
       if (lane == (t & 31)) z += (double)tot;
     }
-    __threadfence();
     __syncwarp();
     Z = warp_sum_f64(z);
   }
-  const double theta = uniform_draw(a.seed, (uint64_t)b, (uint64_t)n, 1) * Z;
+  const double theta = w * Z;
 
   // Slice, then piece, then lane, then element holding the crossing.  Only
   // positions with positive mass are ever chosen, so the emitted token always
   // carries weight (and lies below V).
+  // (every slice mass has been seen above, so plain relaxed reloads return it)
   double acc = 0.0;
   const int tsel =
-      warp_cdf_search(C, theta, 0.0, [&](int t) { return (double)__ldcg(ts + t); }, &acc);
+      warp_cdf_search(C, theta, 0.0, [&](int t) { return (double)ld_relaxed_f32(ts + t); }, &acc);
   if (tsel < 0) {  // no slice with mass: only an expired wait can cause this
     if (lane == 0) {
       a.out_tokens[(size_t)b * (a.K + 1) + n] = -1;
@@ -483,8 +579,8 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   const int np = (v1 - v0 + STEPW - 1) / STEPW;
   const float* gp = a.pieces + ((size_t)b * C + tsel) * a.P;
   double acc2 = acc;
-  const int psel =
-      warp_cdf_search(np, theta, acc, [&](int q) { return (double)__ldcg(gp + q); }, &acc2);
+  const int psel = warp_cdf_search(
+      np, theta, acc, [&](int q) { return (double)wait_f32(gp + q, a.status); }, &acc2);
   if (psel < 0) {  // pieces inconsistent with their slice mass (expired wait)
     if (lane == 0) {
       a.out_tokens[(size_t)b * (a.K + 1) + n] = -1;
@@ -578,14 +674,20 @@ __device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], flo
 }
 
 // Statistics slice s of row r of sequence b: the row's (m, s) over the slice,
-// then the row's ticket.  Returns the ticket's old value (lane 0).
+// then the row's ticket.  Returns the ticket's old value (lane 0).  Kept out
+// of line so that the stream loop has the register file to itself.
 template <class E, int VEC>
-__device__ int stats_slice(const SampleArgs& a, int b, int r, int s) {
+__device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int r, int s) {
   using S = typename E::storage;
   constexpr int BATCH = 32 * VEC * kUnroll;
   const int lane = threadIdx.x & 31;
   const S* row = r <= a.K ? target_row<E>(a, b, r) : draft_row<E>(a, b, r - a.K - 1);
   const int v0 = s * a.SL, v1 = min(a.V, v0 + a.SL);
+  // the drafted token scored by this row (target rows 0..K-1 and every draft
+  // row); its load overlaps the stream, and the slice holding it records the
+  // logit there for the statistics finisher
+  const int ti = r < a.K ? r : (r > a.K ? r - a.K - 1 : -1);
+  const uint32_t xt = ld_relaxed_if(lane == 0 && ti >= 0, a.tokens + (size_t)b * a.K + ti, kMarker);
   const float cc = a.c_hi;
   float m = neg_inf();
   f2_t acc = f2(0.f, 0.f);
@@ -611,6 +713,8 @@ __device__ int stats_slice(const SampleArgs& a, int b, int r, int s) {
   if (lane == 0) {
     st_relaxed_u2(a.part + ((size_t)b * a.R + r) * a.CS + s, __float_as_uint(m), __float_as_uint(sum));
     old = atom_add_relaxed(&a.rowticket[((size_t)b * a.R + r) * kTicketStride], 1);
+    const int xi = (int)xt;
+    if (ti >= 0 && xi >= v0 && xi < v1) st_relaxed_f32(a.zx + (size_t)b * a.R + r, E::load1(row + xi));
   }
   return old;
 }
@@ -625,16 +729,25 @@ __device__ __noinline__ void tail_slice(const SampleArgs& a, const SeqInfo& si, 
   const float tot = tail_slice_mass<E, VEC>(a, b, s, si);
   int old = 0;
   if (lane == 0) {
-    // release: the pieces stored by this lane are visible to whoever sees the mass
-    st_release_f32(a.tailsum + (size_t)b * a.TC + s, tot);
+    // pieces and mass are marker-validated by the reader: no ordering needed
+    st_relaxed_f32(a.tailsum + (size_t)b * a.TC + s, tot);
     old = atom_add_relaxed(&a.tailticket[b], 1);
   }
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old == a.TC - 1) select_finisher<E, VEC>(a, si);
 }
 
-// Scheduling.  Statistics slices come from the warp slot's claim counter: the
-// k-th claim on counter w is flat slice f = k * kSlices + w.  The next claim
+// The next counter after ctr (cyclically) that this warp has not seen run dry.
+__device__ __forceinline__ int next_live_counter(int ctr, unsigned dead) {
+  for (int k = 1; k <= kSlices; ++k) {
+    const int c = (ctr + k) & (kSlices - 1);
+    if (!((dead >> c) & 1u)) return c;
+  }
+  return ctr;
+}
+
+// Scheduling.  Statistics slices come from eight claim counters: the k-th
+// claim on counter c is flat slice f = k * kSlices + c.  The next claim
 // is issued before the current slice is processed, so the atomic's latency
 // hides behind the stream.  Tail slices are owned, not claimed: tail item j
 // (queue position j / TC, tail slice j % TC) belongs to global warp j % W,
@@ -658,10 +771,45 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
   const int TT = a.B * a.TC;                       // tail items in all
   const int W = kSlices * (int)gridDim.x;          // warps in the grid
   int t = w * (int)gridDim.x + (int)blockIdx.x;    // this warp's next tail item
-  int f = bcast(claim_unit(a.counter, lane)) * kSlices + w;
+  // Statistics claims rotate over the eight counters (warp slot w starts at
+  // counter w), so every warp draws equally from every counter and the
+  // counters advance together: a sequence's slices, spread over all eight,
+  // are then processed close together in time.  A claim past a counter's end
+  // marks that counter dead for this warp; the warp leaves the statistics
+  // work only when it has seen all eight dead, so no slice is ever left
+  // unclaimed.  A claimed slice is processed before a tail item that became
+  // ready (other warps' decisions may wait on it); the claim after it is then
+  // deferred until the tail item is done.
+  unsigned dead = 0;
+  int ctr = w;
+  int f = bcast(claim_from(a.counter, ctr, lane)) * kSlices + ctr;
+  bool held = true;  // f is the result of a claim on counter ctr
   uint32_t seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
   for (;;) {
-    if (t < TT && word_set(bcast((int)seen))) {
+    const bool tail_ready = t < TT && word_set(bcast((int)seen));
+    if (held && f >= a.F) {  // the claim came back past the counter's end
+      dead |= 1u << ctr;
+      held = false;
+    }
+    if (held) {
+      int nctr = ctr, next = 0;
+      if (!tail_ready) {
+        nctr = next_live_counter(ctr, dead);
+        next = claim_from(a.counter, nctr, lane);
+        seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
+      }
+      const int b = fdiv(f, a.div_seq), rs = f - b * per_seq, r = fdiv(rs, a.div_cs), s = rs - r * a.CS;
+      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC>(a, b, r, s), 0);
+      if (old == a.CS - 1) row_finisher<E>(a, b, r);
+      if (!tail_ready) {
+        f = bcast(next) * kSlices + nctr;
+        ctr = nctr;
+      } else {
+        held = false;
+      }
+      continue;
+    }
+    if (tail_ready) {
       const int pos = fdiv(t, a.div_tc);
       const SeqInfo si = read_decision(a, pos);
       tail_slice<E, VEC>(a, si, t - pos * a.TC);
@@ -669,13 +817,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
       seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
       continue;
     }
-    if (f < a.F) {
-      const int next = claim_unit(a.counter, lane);
-      seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
-      const int b = fdiv(f, a.div_seq), rs = f - b * per_seq, r = fdiv(rs, a.div_cs), s = rs - r * a.CS;
-      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC>(a, b, r, s), 0);
-      if (old == a.CS - 1) row_finisher<E>(a, b, r);
-      f = bcast(next) * kSlices + w;
+    if (dead != 0xffu) {  // nothing held: claim from the next live counter
+      ctr = next_live_counter(ctr, dead);
+      f = bcast(claim_from(a.counter, ctr, lane)) * kSlices + ctr;
+      held = true;
       continue;
     }
     if (t >= TT) break;
@@ -700,7 +845,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: [zero-filled: counters, tickets, queue count][marker-filled:
-// part, rowstat, tailsum, queue][pieces].
+// part, rowstat, tailsum, queue, pieces, zx].
 static void sample_layout(int B, int R, int CS, int TC, int P, size_t* off) {
   size_t o = 0;
   off[0] = o; o += kCounterBytes;                                          // counter
@@ -714,13 +859,14 @@ static void sample_layout(int B, int R, int CS, int TC, int P, size_t* off) {
   off[7] = o; o += align_up((size_t)B * R * sizeof(float2), 256);         // rowstat
   off[8] = o; o += align_up((size_t)B * TC * sizeof(float), 256);         // tailsum
   off[10] = o; o += align_up((size_t)B * sizeof(SeqInfo), 256);           // queue
-  off[9] = o;                                                              // end of marker region
   off[11] = o; o += align_up((size_t)B * TC * P * sizeof(float), 256);    // pieces
+  off[13] = o; o += align_up((size_t)B * R * sizeof(float), 256);         // zx
+  off[9] = o;                                                              // end of marker region
   off[12] = o;
 }
 
 WsLayout sample_workspace(int B, int K, int CS, int TC, int P) {
-  size_t off[13];
+  size_t off[14];
   sample_layout(B, 2 * K + 1, CS, TC, P, off);
   WsLayout l;
   l.total = off[12];
@@ -731,7 +877,7 @@ WsLayout sample_workspace(int B, int K, int CS, int TC, int P) {
 }
 
 void sample_bind_workspace(SampleArgs& a, void* ws) {
-  size_t off[13];
+  size_t off[14];
   sample_layout(a.B, a.R, a.CS, a.TC, a.P, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
@@ -744,6 +890,7 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.tailsum = (float*)(p + off[8]);
   a.queue = (SeqInfo*)(p + off[10]);
   a.pieces = (float*)(p + off[11]);
+  a.zx = (float*)(p + off[13]);
 }
 
 template <class E, int VEC>

@@ -224,6 +224,14 @@ __device__ __forceinline__ uint4 ld_relaxed_v4(const void* p) {
                : "memory");
   return v;
 }
+__device__ __forceinline__ void st_relaxed_f32(float* p, float v) {
+  asm volatile("st.relaxed.gpu.global.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+__device__ __forceinline__ float ld_relaxed_f32(const float* p) {
+  float v;
+  asm volatile("ld.relaxed.gpu.global.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_relaxed_s32(int* p, int v) {
   asm volatile("st.relaxed.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
 }
@@ -268,6 +276,16 @@ __device__ __forceinline__ int wait_s32(const int* p, unsigned* status) {
   if (v == (int)kMarker) atomicOr(status, kStatusTimeout);
   return v;
 }
+__device__ __forceinline__ float wait_f32(const float* p, unsigned* status) {
+  float v = ld_relaxed_f32(p);
+  unsigned it = 0;
+  while (__float_as_uint(v) == kMarker && ++it < kSpinLimit) {
+    __nanosleep(64);
+    v = ld_relaxed_f32(p);
+  }
+  if (__float_as_uint(v) == kMarker) atomicOr(status, kStatusTimeout);
+  return v;
+}
 __device__ __forceinline__ float wait_f32_acquire(const float* p, unsigned* status) {
   float v = ld_acquire_f32(p);
   unsigned it = 0;
@@ -289,15 +307,30 @@ __device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
 // register until the value is broadcast: the claim's round trip overlaps
 // whatever the warp does in between.
 __device__ __forceinline__ int slice_of_warp() { return (threadIdx.x >> 5) % kSlices; }
-__device__ __forceinline__ int claim_unit(unsigned long long* counter, int lane) {
+__device__ __forceinline__ int claim_from(unsigned long long* counter, int ctr, int lane) {
   unsigned long long v = 0;
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %1, 0;\n\t"
       "@p atom.relaxed.gpu.global.add.u64 %0, [%2], 1;\n\t}"
       : "+l"(v)
-      : "r"(lane), "l"(counter + slice_of_warp() * kCounterStride)
+      : "r"(lane), "l"(counter + ctr * kCounterStride)
       : "memory");
   return (int)v;
+}
+__device__ __forceinline__ int claim_unit(unsigned long long* counter, int lane) {
+  return claim_from(counter, slice_of_warp(), lane);
+}
+// A relaxed atomic add issued only where `pred` holds (0 elsewhere), with no
+// wait at the issue point.
+__device__ __forceinline__ int atom_add_if(bool pred, int* p, int v) {
+  int r = 0;
+  asm volatile(
+      "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
+      "@q atom.relaxed.gpu.global.add.s32 %0, [%2], %3;\n\t}"
+      : "+r"(r)
+      : "r"((unsigned)pred), "l"(p), "r"(v)
+      : "memory");
+  return r;
 }
 // The same for a relaxed 32-bit load issued only where `pred` holds; `v` is
 // returned unchanged elsewhere.

@@ -19,7 +19,8 @@ namespace sv {
 
 constexpr int kThreads = 256;  // 8 independent warps per CTA
 constexpr int kWarps = kThreads / 32;
-constexpr int kSlices = kWarps;  // slices per unit (warp w takes slice w)
+constexpr int kSlices = kWarps;  // claim counters (and warp slots) per CTA
+static_assert((kSlices & (kSlices - 1)) == 0, "counter rotation masks with kSlices - 1");
 constexpr int kCounterStride = 16;  // claim counters 128 bytes apart
 constexpr int kTicketStride = 8;    // per-row tickets 32 bytes apart (no same-address pile-up)
 constexpr int kMinBlocks = 4;  // resident CTAs per SM the register budget allows (64 regs)
@@ -94,7 +95,8 @@ struct SampleArgs {
   float* out_resid;      // optional [B]: mass of the replacement distribution
   // workspace.  Zero-filled before the launch: counter, rowticket, seqticket,
   // tailticket, qcount.  Filled with all-ones bytes (the kMarker "not yet
-  // written" pattern) before the launch: part, rowstat, tailsum, queue.
+  // written" pattern) before the launch: part, rowstat, zx, tailsum, queue,
+  // pieces.
   unsigned long long* counter;  // kSlices claim counters, kCounterStride apart
   int* rowticket;   // [B, R] (kTicketStride apart) finished slices of a row
   int* seqticket;   // [B] finished rows of a sequence
@@ -102,6 +104,7 @@ struct SampleArgs {
   int* qcount;      // decision-queue positions taken so far
   float2* part;     // [B, R, CS] per-slice (m, s)
   float2* rowstat;  // [B, R] merged (m, s) of each row
+  float* zx;        // [B, R] logit at the drafted token, written by the slice holding it
   float* tailsum;   // [B, TC] per tail-slice mass
   SeqInfo* queue;   // [B] decisions in the order they were made
   float* pieces;    // [B, TC, P] per-piece mass

@@ -61,11 +61,12 @@ def test_caller_buffers_are_written_in_place():
 
 
 def test_oversized_problem_is_refused_without_launch():
-    # K = 8, V = 152064 needs about 8.6 KB of scratch per sequence: B = 1024
-    # exceeds the 8 MiB buffer.  Only shapes are used before the refusal, but
-    # the inputs are real device buffers all the same.
-    p = wl.preset("c3", B=1024, V=152064)
-    B, K, V = p.B, p.K, p.V
+    # Scratch grows with the number of rows and input with their length: 512
+    # sequences of K = 255 drafts over V = 16 need about 13 MB of scratch
+    # (per-row tickets, partials, row statistics) from 8 MB of logits, more
+    # than the 8 MiB buffer.  Only shapes are used before the refusal, but the
+    # inputs are real device buffers of the declared shapes all the same.
+    B, K, V = 512, 255, 16
     target = torch.zeros((B, K + 1, V), dtype=torch.bfloat16, device=DEV)
     draft = torch.zeros((B, K, V), dtype=torch.bfloat16, device=DEV)
     tokens = torch.zeros((B, K), dtype=torch.int32, device=DEV)

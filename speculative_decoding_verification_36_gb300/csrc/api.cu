@@ -111,8 +111,11 @@ int ensure_pool(DeviceState* d) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Tuning knob (environment, read once): SPECVERIFY_SLICE_BYTES, the bytes of
-// logits per slice (default 12288).
+// Tuning knobs (environment, read once per process): SPECVERIFY_SLICE_BYTES,
+// the bytes of logits per statistics slice (default 12288);
+// SPECVERIFY_TAIL_BYTES, the bytes of one row per tail slice (default half a
+// statistics slice); SPECVERIFY_CLAIM_TAIL, the number of final statistics
+// slices that are not claimed ahead (default one per warp of the grid).
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
@@ -282,7 +285,10 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   // tail item (target and draft slice) carries as many bytes as a statistics
   // slice
   const int step = 32 * vec_elems;
-  a.P = ((a.SL + 1) / 2 + step - 1) / step;
+  static const int tail_bytes = env_int("SPECVERIFY_TAIL_BYTES", 0);
+  const long long tl_elems = tail_bytes > 0 ? tail_bytes / (long long)esz : (a.SL + 1) / 2;
+  a.P = (int)((tl_elems + step - 1) / step);
+  if (a.P < 1) a.P = 1;
   a.TL = a.P * step;
   a.TC = (int)(((long long)V + a.TL - 1) / a.TL);
   a.F = B * a.R * a.CS;
@@ -290,6 +296,8 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.div_cs = sv::make_fastdiv((uint32_t)a.CS);
   a.div_tc = sv::make_fastdiv((uint32_t)a.TC);
   const int grid = grid_for((a.F + sv::kSlices - 1) / sv::kSlices, capacity);
+  static const int claim_tail_env = env_int("SPECVERIFY_CLAIM_TAIL", 0);
+  a.claim_tail = claim_tail_env > 0 ? claim_tail_env : grid * sv::kSlices;  // one slice per warp
   const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
   a.c64 = c;
   a.c_hi = (float)c;

@@ -793,19 +793,22 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
     }
     if (held) {
       int nctr = ctr, next = 0;
-      if (!tail_ready) {
+      // Near the end of the statistics stream a claim made ahead would sit
+      // behind this slice while idle warps could start it at once, so the
+      // last slices are claimed only when a warp is free.
+      const bool ahead = !tail_ready && f < a.F - a.claim_tail;
+      if (!ahead) held = false;
+      if (ahead) {
         nctr = next_live_counter(ctr, dead);
         next = claim_from(a.counter, nctr, lane);
-        seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
       }
+      if (!tail_ready) seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
       const int b = fdiv(f, a.div_seq), rs = f - b * per_seq, r = fdiv(rs, a.div_cs), s = rs - r * a.CS;
       const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC>(a, b, r, s), 0);
       if (old == a.CS - 1) row_finisher<E>(a, b, r);
-      if (!tail_ready) {
+      if (ahead) {
         f = bcast(next) * kSlices + nctr;
         ctr = nctr;
-      } else {
-        held = false;
       }
       continue;
     }

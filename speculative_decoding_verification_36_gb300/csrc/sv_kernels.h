@@ -83,6 +83,7 @@ struct SampleArgs {
   int TC;  // tail slices per row = ceil(V / TL)
   int P;   // pieces (warp steps) per tail slice
   int F;   // statistics slices in all: B * R * CS
+  int claim_tail;  // within this many slices of the end, claims are not made ahead
   FastDiv div_seq, div_cs, div_tc;  // division by R * CS, CS and TC
   float c_hi, c_lo;  // log2(e)/temperature as a float pair
   double c64;        // the same in double

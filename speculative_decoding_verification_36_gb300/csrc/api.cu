@@ -112,7 +112,9 @@ int ensure_pool(DeviceState* d) {
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Tuning knobs (environment, read once per process): SPECVERIFY_SLICE_BYTES,
-// the bytes of logits per statistics slice (default 12288);
+// the bytes of logits per statistics slice of the sampling kernel (default
+// 12288); SPECVERIFY_ARGMAX_SLICE_BYTES, the same for the greedy and tree
+// kernels (default 8192);
 // SPECVERIFY_TAIL_BYTES, the bytes of one row per tail slice (default half a
 // statistics slice); SPECVERIFY_CLAIM_TAIL, the number of final statistics
 // slices that are not claimed ahead (default one per warp of the grid).
@@ -124,10 +126,8 @@ int env_int(const char* name, int dflt) {
 }
 
 // Slice length: a whole number of warp load batches (32 lanes x kUnroll
-// vectors) covering about SPECVERIFY_SLICE_BYTES; a row shorter than one slice
-// is one slice.
-void choose_slices(int V, int vec_elems, size_t esz, int* SL, int* CS, int* CU) {
-  static const int bytes = env_int("SPECVERIFY_SLICE_BYTES", 12288);
+// vectors) covering about `bytes`; a row shorter than one slice is one slice.
+void choose_slices(int V, int vec_elems, size_t esz, int bytes, int* SL, int* CS, int* CU) {
   const long long batch = 32LL * vec_elems * sv::kUnroll;
   long long k = ((long long)bytes / (long long)esz + batch - 1) / batch;
   if (k < 1) k = 1;
@@ -159,7 +159,7 @@ int run_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, void
   if (rc) return rc;
   cudaError_t e = cudaMallocFromPoolAsync(ws, l.total, d->pool, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
-  e = cudaMemsetAsync(*ws, 0, l.zero_bytes, stream);
+  if (l.zero_bytes) e = cudaMemsetAsync(*ws, 0, l.zero_bytes, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, stream);
   if (e != cudaSuccess) {
     cudaFreeAsync(*ws, stream);
@@ -184,7 +184,8 @@ int static_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, v
     }
   }
   *ws = d->static_scratch;
-  cudaError_t e = cudaMemsetAsync(*ws, 0, l.zero_bytes, stream);
+  cudaError_t e = cudaSuccess;
+  if (l.zero_bytes) e = cudaMemsetAsync(*ws, 0, l.zero_bytes, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemsetAsync");
   return SPEC_OK;
@@ -220,7 +221,8 @@ int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
   a.K = K;
   a.V = V;
   a.R = K + 1;
-  choose_slices(V, vec ? (bf16 ? 8 : 4) : 1, esz, &a.SL, &a.CS, &a.CU);
+  static const int slice_bytes = env_int("SPECVERIFY_ARGMAX_SLICE_BYTES", 8192);
+  choose_slices(V, vec ? (bf16 ? 8 : 4) : 1, esz, slice_bytes, &a.SL, &a.CS, &a.CU);
   a.map.A = a.R * a.CU;
   a.map.total = B * a.map.A;
   a.out_tokens = out_tokens;
@@ -280,7 +282,8 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.R = 2 * K + 1;
   const int vec_elems = vec ? (bf16 ? 8 : 4) : 1;
   int CU = 0;
-  choose_slices(V, vec_elems, esz, &a.SL, &a.CS, &CU);
+  static const int slice_bytes = env_int("SPECVERIFY_SLICE_BYTES", 12288);
+  choose_slices(V, vec_elems, esz, slice_bytes, &a.SL, &a.CS, &CU);
   // tail slices: whole warp steps, half a statistics slice per row, so that a
   // tail item (target and draft slice) carries as many bytes as a statistics
   // slice

@@ -126,7 +126,7 @@ __device__ int argmax_slice(const GreedyArgs& a, int b, int idx, int w) {
   if (lane == 0) {
     const size_t o = ((size_t)b * a.R + r) * (a.CU * kSlices) + s;
     st_relaxed_u2(a.part + o, __float_as_uint(best), (uint32_t)bi | (anynan ? 0x80000000u : 0u));
-    old = atom_add_relaxed(&a.rowticket[((size_t)b * a.R + r) * kTicketStride], 1);
+    old = ticket_take(&a.rowticket[((size_t)b * a.R + r) * kTicketStride]);
   }
   return old;
 }
@@ -153,7 +153,7 @@ __device__ __noinline__ bool row_argmax_finisher(const GreedyArgs& a, int b, int
   int old = 0;
   if (lane == 0) {
     st_relaxed_s32(a.g + (size_t)b * a.R + r, gv);
-    old = atom_add_relaxed(&a.seqticket[b], 1);
+    old = ticket_take(&a.seqticket[b]);
   }
   old = __shfl_sync(0xffffffffu, old, 0);
   return old == a.R - 1;
@@ -198,9 +198,18 @@ __device__ __noinline__ void chain_finisher(const GreedyArgs& a, int b) {
   __syncwarp();
 }
 
-// Tree finisher (one warp): argmax of every row, acceptance in node order
-// (parents precede children), the deepest accepted path, the bonus token and
-// the ancestor-or-self bitmask (one word column per lane).
+// Tree finisher (one warp): argmax of every row, acceptance of every node,
+// the deepest accepted path, the bonus token and the ancestor-or-self bitmask.
+//
+// Nodes are resolved 32 at a time (lane = node), in index order.  Parents
+// precede children, so a node's parent is either the root, a node of an
+// earlier chunk (its results are already in the workspace) or a node of the
+// same chunk.  Within a chunk, pointer jumping over the in-chunk parent links
+// (five shuffle rounds) combines acceptance (AND), depth (sum) and the
+// ancestor bits of the chunk's own mask column; everything above the chunk
+// comes from the topmost in-chunk ancestor's outside parent.  Ancestors have
+// smaller indices than their descendants, so mask columns to the right of a
+// node's chunk are zero.
 __device__ __noinline__ void tree_finisher(const GreedyArgs& a, int b) {
   const int N = a.K;
   const int W = (N + 31) >> 5;
@@ -218,7 +227,6 @@ __device__ __noinline__ void tree_finisher(const GreedyArgs& a, int b) {
   }
   for (int i = lane; i < N; i += 32) bad |= par[i] < -1 || par[i] >= i || tok[i] < 0 || tok[i] >= a.V;
   bad = __any_sync(0xffffffffu, bad);
-  __threadfence();
   __syncwarp();
   int32_t* path = a.out_tokens + (size_t)b * (N + 1);
   uint32_t* mask = a.out_mask + (size_t)b * N * W;
@@ -232,34 +240,80 @@ __device__ __noinline__ void tree_finisher(const GreedyArgs& a, int b) {
     __syncwarp();
     return;
   }
-  int bd = 0;
-  if (lane == 0) {
-    int best = -1;
-    for (int i = 0; i < N; ++i) {
-      const int p = par[i];
-      const bool ok = (p < 0 || acc[p]) && tok[i] == __ldcg(g + p + 1);
-      acc[i] = ok;
-      depth[i] = p < 0 ? 1 : depth[p] + 1;
-      if (ok && depth[i] > bd) {
-        bd = depth[i];
-        best = i;
+  int best_d = 0, best_i = -1;  // the root: depth 0
+  for (int c = 0; c < W; ++c) {
+    const int i0 = 32 * c, i = i0 + lane;
+    const bool valid = i < N;
+    const int p = valid ? __ldg(par + i) : -1;
+    const int t = valid ? __ldg(tok + i) : -1;
+    const bool inside = valid && p >= i0;  // parent in this chunk
+    // outside parent (or the root): its acceptance and depth are final
+    const int gp = valid ? __ldcg(g + p + 1) : -1;
+    int ok = valid && t == gp;
+    int d = 1;
+    if (valid && !inside && p >= 0) {
+      ok = ok && __ldcg(acc + p);
+      d += __ldcg(depth + p);
+    }
+    int link = inside ? p - i0 : -1;
+    int top = lane;
+    uint32_t colbits = valid ? 1u << lane : 0u;  // ancestor-or-self bits in column c
+#pragma unroll
+    for (int step = 0; step < 5; ++step) {
+      const int src = link >= 0 ? link : lane;
+      const int ok_s = __shfl_sync(0xffffffffu, ok, src);
+      const int d_s = __shfl_sync(0xffffffffu, d, src);
+      const int link_s = __shfl_sync(0xffffffffu, link, src);
+      const int top_s = __shfl_sync(0xffffffffu, top, src);
+      const uint32_t bits_s = __shfl_sync(0xffffffffu, colbits, src);
+      if (link >= 0) {
+        ok = ok && ok_s;
+        d += d_s;
+        colbits |= bits_s;
+        top = top_s;
+        link = link_s;
       }
     }
-    int pos = bd - 1;
-    for (int node = best; node >= 0; node = par[node]) path[pos--] = tok[node];
-    path[bd] = __ldcg(g + best + 1);
-    a.out_n[b] = bd + 1;
+    // the outside parent of the topmost in-chunk ancestor
+    const int ext = __shfl_sync(0xffffffffu, p, top);
+    if (valid) {
+      st_relaxed_s32(acc + i, ok);
+      st_relaxed_s32(depth + i, d);
+      uint32_t* row = mask + (size_t)i * W;
+      for (int w = 0; w < c; ++w) row[w] = ext >= 0 ? __ldcg(mask + (size_t)ext * W + w) : 0u;
+      row[c] = colbits;
+      for (int w = c + 1; w < W; ++w) row[w] = 0u;
+    }
+    // deepest accepted node, lowest index on ties
+    int kd = valid && ok ? d : 0, ki = valid && ok ? i : INT_MAX;
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+      const int od = __shfl_xor_sync(0xffffffffu, kd, off);
+      const int oi = __shfl_xor_sync(0xffffffffu, ki, off);
+      if (od > kd || (od == kd && oi < ki)) {
+        kd = od;
+        ki = oi;
+      }
+    }
+    if (kd > best_d) {
+      best_d = kd;
+      best_i = ki;
+    }
+    __threadfence();  // this chunk's acc, depth and mask rows before the next chunk reads them
+    __syncwarp();
   }
-  bd = __shfl_sync(0xffffffffu, bd, 0);
-  for (int j = bd + 1 + lane; j <= N; j += 32) path[j] = -1;
-  for (int w = lane; w < W; w += 32) {
-    for (int i = 0; i < N; ++i) {
-      const int p = par[i];
-      uint32_t word = p >= 0 ? mask[(size_t)p * W + w] : 0u;
-      if ((i >> 5) == w) word |= 1u << (i & 31);
-      mask[(size_t)i * W + w] = word;
+  // path tokens: every ancestor-or-self j of the best node sits at depth[j] - 1
+  if (best_i >= 0) {
+    const uint32_t* brow = mask + (size_t)best_i * W;
+    for (int j = lane; j <= best_i; j += 32) {
+      if ((__ldcg(brow + (j >> 5)) >> (j & 31)) & 1u) path[__ldcg(depth + j) - 1] = __ldg(tok + j);
     }
   }
+  if (lane == 0) {
+    path[best_d] = __ldcg(g + best_i + 1);
+    a.out_n[b] = best_d + 1;
+  }
+  for (int j = best_d + 1 + lane; j <= N; j += 32) path[j] = -1;
   __syncwarp();
 }
 
@@ -292,7 +346,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) argmax_kernel(const __gr
 // ---------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [zero-filled: counters, tickets][marker-filled: part, g][depth, acc].
+// Workspace: [counters, tickets (start at -1)][marker-filled: part, g][depth,
+// acc]; one 0xff fill initialises the first two parts.
 static void greedy_layout(int B, int R, int CU, size_t* off) {
   const size_t C = (size_t)CU * kSlices;
   size_t o = 0;
@@ -314,9 +369,9 @@ WsLayout greedy_workspace(int B, int R, int CU) {
   greedy_layout(B, R, CU, off);
   WsLayout l;
   l.total = off[9];
-  l.zero_bytes = off[3];
-  l.marker_off = off[4];
-  l.marker_bytes = off[6] - off[4];
+  l.zero_bytes = 0;  // counters and tickets start at -1: one 0xff fill covers everything
+  l.marker_off = 0;
+  l.marker_bytes = off[6];
   return l;
 }
 

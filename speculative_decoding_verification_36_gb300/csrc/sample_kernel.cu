@@ -155,14 +155,14 @@ __device__ __forceinline__ TailConsts tail_consts(const SampleArgs& a, const Seq
 // Lane 0 takes the next queue position (a predicated atomic: nothing waits
 // for it until the entry is written).
 __device__ __forceinline__ int reserve_decision(const SampleArgs& a, int lane) {
-  int v = 0;
+  int v = -1;
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %1, 0;\n\t"
       "@p atom.relaxed.gpu.global.add.s32 %0, [%2], 1;\n\t}"
       : "+r"(v)
       : "r"(lane), "l"(a.qcount)
       : "memory");
-  return v;
+  return v + 1;
 }
 
 __device__ __forceinline__ void publish_decision(const SampleArgs& a, int pos, const SeqInfo& si) {
@@ -260,7 +260,7 @@ __device__ __noinline__ void row_finisher(const SampleArgs& a, int b, int r) {
   }
   warp_ms(m, s, a.c_hi);
   if (lane == 0) st_relaxed_u2(a.rowstat + (size_t)b * a.R + r, __float_as_uint(m), __float_as_uint(s));
-  int old = atom_add_if(lane == 0, &a.seqticket[b], 1);
+  int old = ticket_take_if(lane == 0, &a.seqticket[b]);
   const FinIn pre = load_fin_inputs(a, b, 0);
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old == a.R - 1) stats_finisher<E>(a, b, pre);
@@ -712,7 +712,7 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int r, int s
   int old = 0;
   if (lane == 0) {
     st_relaxed_u2(a.part + ((size_t)b * a.R + r) * a.CS + s, __float_as_uint(m), __float_as_uint(sum));
-    old = atom_add_relaxed(&a.rowticket[((size_t)b * a.R + r) * kTicketStride], 1);
+    old = ticket_take(&a.rowticket[((size_t)b * a.R + r) * kTicketStride]);
     const int xi = (int)xt;
     if (ti >= 0 && xi >= v0 && xi < v1) st_relaxed_f32(a.zx + (size_t)b * a.R + r, E::load1(row + xi));
   }
@@ -731,7 +731,7 @@ __device__ __noinline__ void tail_slice(const SampleArgs& a, const SeqInfo& si, 
   if (lane == 0) {
     // pieces and mass are marker-validated by the reader: no ordering needed
     st_relaxed_f32(a.tailsum + (size_t)b * a.TC + s, tot);
-    old = atom_add_relaxed(&a.tailticket[b], 1);
+    old = ticket_take(&a.tailticket[b]);
   }
   old = __shfl_sync(0xffffffffu, old, 0);
   if (old == a.TC - 1) select_finisher<E, VEC>(a, si);
@@ -847,8 +847,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
 // ---------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [zero-filled: counters, tickets, queue count][marker-filled:
-// part, rowstat, tailsum, queue, pieces, zx].
+// Workspace: [counters, tickets, queue count (all start at -1)][marker-filled
+// result slots: part, rowstat, tailsum, queue, pieces, zx]; one 0xff fill
+// initialises both parts.
 static void sample_layout(int B, int R, int CS, int TC, int P, size_t* off) {
   size_t o = 0;
   off[0] = o; o += kCounterBytes;                                          // counter
@@ -873,9 +874,9 @@ WsLayout sample_workspace(int B, int K, int CS, int TC, int P) {
   sample_layout(B, 2 * K + 1, CS, TC, P, off);
   WsLayout l;
   l.total = off[12];
-  l.zero_bytes = off[5];
-  l.marker_off = off[6];
-  l.marker_bytes = off[9] - off[6];
+  l.zero_bytes = 0;  // counters and tickets start at -1: one 0xff fill covers everything
+  l.marker_off = 0;
+  l.marker_bytes = off[9];
   return l;
 }
 

@@ -253,6 +253,8 @@ __device__ __forceinline__ int atom_add_relaxed(int* p, int v) {
   asm volatile("atom.relaxed.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
   return old;
 }
+// A ticket on a counter that starts at -1: the number of earlier takers.
+__device__ __forceinline__ int ticket_take(int* p) { return atom_add_relaxed(p, 1) + 1; }
 
 // Bounded waits for a slot to leave the marker state.  A ticket count says
 // every writer has issued its store; the store itself may land a moment later.
@@ -307,30 +309,33 @@ __device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
 // register until the value is broadcast: the claim's round trip overlaps
 // whatever the warp does in between.
 __device__ __forceinline__ int slice_of_warp() { return (threadIdx.x >> 5) % kSlices; }
+// Claim counters and tickets start at all-ones (-1), so that one 0xff fill
+// initialises the whole workspace; the helpers below return the number of
+// earlier increments (the first taker gets 0).
 __device__ __forceinline__ int claim_from(unsigned long long* counter, int ctr, int lane) {
-  unsigned long long v = 0;
+  unsigned long long v = ~0ull;
   asm volatile(
       "{\n\t.reg .pred p;\n\tsetp.eq.s32 p, %1, 0;\n\t"
       "@p atom.relaxed.gpu.global.add.u64 %0, [%2], 1;\n\t}"
       : "+l"(v)
       : "r"(lane), "l"(counter + ctr * kCounterStride)
       : "memory");
-  return (int)v;
+  return (int)(v + 1);
 }
 __device__ __forceinline__ int claim_unit(unsigned long long* counter, int lane) {
   return claim_from(counter, slice_of_warp(), lane);
 }
-// A relaxed atomic add issued only where `pred` holds (0 elsewhere), with no
-// wait at the issue point.
-__device__ __forceinline__ int atom_add_if(bool pred, int* p, int v) {
-  int r = 0;
+// A ticket taken only where `pred` holds (0 elsewhere), with no wait at the
+// issue point.
+__device__ __forceinline__ int ticket_take_if(bool pred, int* p) {
+  int r = -1;
   asm volatile(
       "{\n\t.reg .pred q;\n\tsetp.ne.u32 q, %1, 0;\n\t"
-      "@q atom.relaxed.gpu.global.add.s32 %0, [%2], %3;\n\t}"
+      "@q atom.relaxed.gpu.global.add.s32 %0, [%2], 1;\n\t}"
       : "+r"(r)
-      : "r"((unsigned)pred), "l"(p), "r"(v)
+      : "r"((unsigned)pred), "l"(p)
       : "memory");
-  return r;
+  return r + 1;
 }
 // The same for a relaxed 32-bit load issued only where `pred` holds; `v` is
 // returned unchanged elsewhere.

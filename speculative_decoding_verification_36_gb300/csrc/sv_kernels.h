@@ -94,10 +94,10 @@ struct SampleArgs {
   float* out_row_stats;  // optional [B, R, 2]: max(z)/tau, sum exp(z/tau - max)
   float* out_pq;         // optional [B, K, 2]: p_i(x_i), q_i(x_i)
   float* out_resid;      // optional [B]: mass of the replacement distribution
-  // workspace.  Zero-filled before the launch: counter, rowticket, seqticket,
-  // tailticket, qcount.  Filled with all-ones bytes (the kMarker "not yet
-  // written" pattern) before the launch: part, rowstat, zx, tailsum, queue,
-  // pieces.
+  // workspace, filled with all-ones bytes before the launch: the counters and
+  // tickets (counter, rowticket, seqticket, tailticket, qcount) then start at
+  // -1, and the result slots (part, rowstat, zx, tailsum, queue, pieces) hold
+  // the kMarker "not yet written" pattern.
   unsigned long long* counter;  // kSlices claim counters, kCounterStride apart
   int* rowticket;   // [B, R] (kTicketStride apart) finished slices of a row
   int* seqticket;   // [B] finished rows of a sequence
@@ -124,8 +124,9 @@ struct GreedyArgs {
   int32_t* out_n;           // chain [B];     tree out_len  [B]
   uint32_t* out_mask;       // tree [B, N, ceil(N/32)]
   int32_t* out_row_argmax;  // optional [B, R]
-  // workspace.  Zero-filled: counter, rowticket, seqticket.  All-ones
-  // ("not yet written" marker): part, g.
+  // workspace, filled with all-ones bytes before the launch: counter,
+  // rowticket and seqticket start at -1; part and g hold the "not yet
+  // written" marker.
   unsigned long long* counter;  // kSlices claim counters, kCounterStride apart
   int* rowticket;  // [B, R] (kTicketStride apart) finished slices of a row
   int* seqticket;  // [B] finished rows of a sequence
@@ -137,7 +138,8 @@ struct GreedyArgs {
 };
 
 // Workspace layout of each kernel: `total` bytes; [0, zero_bytes) must be
-// zero-filled and [marker_off, marker_off + marker_bytes) filled with 0xff
+// zero-filled (neither kernel uses one) and [marker_off, marker_off +
+// marker_bytes) filled with 0xff
 // bytes before every launch.
 struct WsLayout {
   size_t total, zero_bytes, marker_off, marker_bytes;

@@ -1,0 +1,45 @@
+"""Run a few verify calls on one preset workload (a target for profilers).
+
+    python -m speculative_decoding_verification_36_gb300.run_case c4 [--batch B] [--calls N]
+
+Builds the library if needed, generates the preset's synthetic inputs on
+cuda:0 and makes N calls of the entry point the preset exercises
+(spec_verify for c1-c4, spec_tree_verify_greedy for c5), then synchronises.
+"""
+from __future__ import annotations
+
+import argparse
+import sys
+
+
+def main(argv=None) -> int:
+    ap = argparse.ArgumentParser()
+    ap.add_argument("preset", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("--batch", type=int, default=0, help="sequences (default: the preset's B)")
+    ap.add_argument("--calls", type=int, default=3)
+    args = ap.parse_args(argv)
+
+    import torch
+
+    from . import build, spec_get_status, spec_tree_verify_greedy, spec_verify
+    from . import workloads as wl
+
+    build.build()
+    dev = torch.device("cuda", 0)
+    p = wl.preset(args.preset, B=args.batch) if args.batch else wl.preset(args.preset)
+    if args.preset == "c5":
+        x = wl.make_tree(p, device=dev, seed=0)
+        for _ in range(args.calls):
+            spec_tree_verify_greedy(x["target"], x["tokens"], x["parents"])
+    else:
+        x = wl.make_chain(p, device=dev, seed=0)
+        for i in range(args.calls):
+            spec_verify(x["target"], x["draft"], x["tokens"], x["temperature"], i)
+    torch.cuda.synchronize()
+    flags = spec_get_status()
+    print(f"{args.preset} B={p.B}: {args.calls} calls, status flags {flags}")
+    return 0 if flags == 0 else 1
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -65,15 +65,18 @@ def barrier(world: int):
         dist.barrier()
 
 
+# The sources that make up the sampling kernel and its launch configuration.
+SAMPLE_SOURCES = ("api.cu", "sample_kernel.cu", "sv_common.cuh", "sv_kernels.h")
+
+
 def source_hash() -> str:
-    """sha256 over the CUDA sources (ties a stored ncu traffic figure to the
-    kernel it was measured on)."""
+    """sha256 over the sampling kernel's sources (ties a stored ncu traffic
+    figure to the kernel it was measured on)."""
     csrc = os.path.join(ROOT, "speculative_decoding_verification_36_gb300", "csrc")
     h = hashlib.sha256()
-    for name in sorted(os.listdir(csrc)):
-        if name.endswith((".cu", ".cuh", ".h")):
-            h.update(name.encode())
-            h.update(open(os.path.join(csrc, name), "rb").read())
+    for name in SAMPLE_SOURCES:
+        h.update(name.encode())
+        h.update(open(os.path.join(csrc, name), "rb").read())
     return h.hexdigest()
 
 

@@ -203,6 +203,28 @@ int spec_tree_verify_greedy_bf16(const uint16_t *target_logits, const int32_t *t
                                  cudaStream_t stream);
 
 /*
+ * Acceptance statistics of a batch of verify outputs ([P2] "How much speedup
+ * to expect": the per-position acceptance rate and the expected tokens per
+ * iteration, measured instead of predicted).
+ *
+ *   n_accepted       [B] int32 counts as written by spec_verify (-1 = bad
+ *                    sequence).  For tree outputs pass out_len - 1.
+ *   K                drafts per sequence, 0 <= K <= 1024.
+ *   out_hist         [K+2] uint64 (required): out_hist[j] = #(n == j) for
+ *                    j = 0..K; out_hist[K+1] counts every other value.
+ *   out_alpha        [K] double or NULL: #(n > i) / #(n >= i), the fraction of
+ *                    sequences whose position i was tested that accepted it
+ *                    (NaN if none reached position i).
+ *   out_mean_tokens  [1] double or NULL: mean of n + 1 over the counted
+ *                    sequences (NaN if none).
+ * All pointers are device pointers; counts are exact.  Returns SPEC_OK,
+ * SPEC_ERR_NULL (out_hist NULL, or n_accepted NULL with B > 0),
+ * SPEC_ERR_SHAPE (B < 0, K outside [0, 1024]) or SPEC_ERR_CUDA.
+ */
+int spec_acceptance_stats(const int32_t *n_accepted, int B, int K, uint64_t *out_hist,
+                          double *out_alpha, double *out_mean_tokens, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns in *flags_out (may be NULL) the device
  * status word of the current device (an OR of SPEC_FLAG_* set by every call
  * since the last read) and clears it.  Returns SPEC_OK or SPEC_ERR_CUDA.

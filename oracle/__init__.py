@@ -63,6 +63,8 @@ def _load():
     lib.oracle_spec_verify_greedy.restype = i32
     lib.oracle_tree_verify_greedy.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P]
     lib.oracle_tree_verify_greedy.restype = i32
+    lib.oracle_acceptance_stats.argtypes = [P, i32, i32, P, P, P]
+    lib.oracle_acceptance_stats.restype = None
     _lib = lib
     return lib
 
@@ -218,3 +220,16 @@ def tree_verify_greedy(target, tree_tokens, parent_idx):
     if rc != 0:
         raise MemoryError("oracle_tree_verify_greedy failed to allocate")
     return dict(path=path, length=length, mask=mask)
+
+
+def acceptance_stats(n_accepted, K: int):
+    """Histogram of accepted counts, per-position acceptance rate and mean
+    tokens per iteration.  n_accepted [B] int32 (-1 marks a bad sequence)."""
+    lib = _load()
+    n = np.ascontiguousarray(np.asarray(n_accepted, dtype=np.int32).reshape(-1))
+    hist = np.zeros(K + 2, dtype=np.uint64)
+    alpha = np.zeros(max(K, 1), dtype=np.float64)
+    mean = np.zeros(1, dtype=np.float64)
+    n_buf = n if n.size else np.zeros(1, dtype=np.int32)
+    lib.oracle_acceptance_stats(_ptr(n_buf), int(n.size), int(K), _ptr(hist), _ptr(alpha), _ptr(mean))
+    return dict(hist=hist, alpha=alpha[:K], mean_tokens=float(mean[0]))

@@ -486,3 +486,43 @@ int oracle_tree_verify_greedy(const void *target, int dtype, const int32_t *tree
     free(g); free(acc); free(depth); free(walk);
     return 0;
 }
+
+/*
+ * Acceptance statistics over a batch of verify outputs
+ *   [P2] "How much speedup to expect": the per-position acceptance rate alpha
+ *   and the expected number of tokens per draft-and-verify iteration.
+ * hist[j] = number of sequences with n_accepted == j (j = 0..K); hist[K+1]
+ * counts the rest (bad sequences, n = -1, or values outside [0, K]).
+ * alpha[i] = #(n > i) / #(n >= i) over the counted sequences: of the sequences
+ * whose position i was tested, the fraction that accepted it (NaN when none
+ * reached position i).  *mean_tokens = mean of n + 1 over the counted
+ * sequences (NaN when there are none).
+ */
+void oracle_acceptance_stats(const int32_t *n_accepted, int B, int K, uint64_t *hist,
+                             double *alpha, double *mean_tokens)
+{
+    for (int j = 0; j <= K + 1; ++j)
+        hist[j] = 0;
+    for (int b = 0; b < B; ++b) {
+        int n = n_accepted[b];
+        if (n >= 0 && n <= K)
+            hist[n] += 1;
+        else
+            hist[K + 1] += 1;
+    }
+    for (int i = 0; i < K; ++i) {
+        uint64_t reached = 0, accepted = 0;
+        for (int j = i; j <= K; ++j)
+            reached += hist[j];
+        for (int j = i + 1; j <= K; ++j)
+            accepted += hist[j];
+        alpha[i] = reached ? (double)accepted / (double)reached : NAN;
+    }
+    uint64_t count = 0;
+    double total = 0.0;
+    for (int j = 0; j <= K; ++j) {
+        count += hist[j];
+        total += (double)hist[j] * (double)(j + 1);
+    }
+    *mean_tokens = count ? total / (double)count : NAN;
+}

@@ -21,7 +21,7 @@ from ._lib import SPEC_FLAG_BAD_DATA, SPEC_FLAG_TIMEOUT, SpecError
 
 __all__ = [
     "spec_verify", "spec_verify_static_scratch", "spec_verify_stats", "spec_verify_greedy_argmax",
-    "spec_tree_verify_greedy", "spec_get_status", "SpecError",
+    "spec_tree_verify_greedy", "spec_acceptance_stats", "spec_get_status", "SpecError",
     "SPEC_FLAG_BAD_DATA", "SPEC_FLAG_TIMEOUT",
 ]
 
@@ -192,6 +192,26 @@ def spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx, out_path=Non
                       _ptr(parent_idx) if N > 0 else None, B, N, V, _ptr(out_path), _ptr(out_len),
                       _ptr(out_mask), _stream(stream)))
     return out_path, out_len, out_mask
+
+
+def spec_acceptance_stats(n_accepted, K: int, stream=None):
+    """Acceptance statistics of verify outputs on the device.
+
+    n_accepted: int32 [B] (-1 = bad sequence).  Returns dict(hist uint64-valued
+    int64 [K+2], alpha float64 [K], mean_tokens float64 scalar tensor)."""
+    if n_accepted.dtype != torch.int32 or n_accepted.dim() != 1 or not n_accepted.is_contiguous():
+        raise TypeError("n_accepted must be a contiguous 1-D int32 tensor")
+    dev = n_accepted.device
+    B = n_accepted.shape[0]
+    hist = torch.empty((K + 2,), dtype=torch.int64, device=dev)
+    alpha = torch.empty((max(K, 0),), dtype=torch.float64, device=dev)
+    mean = torch.empty((1,), dtype=torch.float64, device=dev)
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        _lib.check(lib.spec_acceptance_stats(_ptr(n_accepted) if B > 0 else None, B, int(K),
+                                             _ptr(hist), _ptr(alpha) if K > 0 else None, _ptr(mean),
+                                             _stream(stream)))
+    return dict(hist=hist, alpha=alpha, mean_tokens=mean[0])
 
 
 def spec_get_status(stream=None, device=None) -> int:

@@ -412,6 +412,20 @@ int spec_tree_verify_greedy_bf16(const uint16_t* target_logits, const int32_t* t
                    out_mask, stream);
 }
 
+int spec_acceptance_stats(const int32_t* n_accepted, int B, int K, uint64_t* out_hist,
+                          double* out_alpha, double* out_mean_tokens, cudaStream_t stream) {
+  if (!out_hist || (B > 0 && !n_accepted)) return SPEC_ERR_NULL;
+  if (B < 0 || K < 0 || K > sv::kMaxTreeNodes) return SPEC_ERR_SHAPE;
+  DeviceState* d = nullptr;
+  const int rc = get_device_state(&d);
+  if (rc) return rc;
+  const cudaError_t e = sv::launch_acceptance(n_accepted, B, K, (unsigned long long*)out_hist,
+                                              K > 0 ? out_alpha : nullptr, out_mean_tokens, d->sms,
+                                              stream);
+  if (e != cudaSuccess) return cuda_fail(e, "acceptance statistics launch");
+  return SPEC_OK;
+}
+
 int spec_get_status(cudaStream_t stream, uint32_t* flags_out) {
   DeviceState* d = nullptr;
   int rc = get_device_state(&d);

@@ -157,6 +157,11 @@ cudaError_t launch_sample(const SampleArgs& a, bool bf16, bool vec, int grid, cu
 cudaError_t launch_greedy(const GreedyArgs& a, bool bf16, bool vec, int grid, cudaStream_t s);
 cudaError_t launch_tree(const GreedyArgs& a, bool bf16, bool vec, int grid, cudaStream_t s);
 
+// Acceptance statistics: zeroes hist[0..K+1], counts n_accepted into it and,
+// when alpha / mean_tokens are given, derives them (acceptance_kernel.cu).
+cudaError_t launch_acceptance(const int32_t* n, int B, int K, unsigned long long* hist, double* alpha,
+                              double* mean_tokens, int sms, cudaStream_t s);
+
 // Resident CTAs per SM for each kernel (occupancy calculator).
 int sample_blocks_per_sm(bool bf16, bool vec);
 int greedy_blocks_per_sm(bool bf16, bool vec);

@@ -52,6 +52,7 @@ SAMPLING_CASES = [
     ("c2", dict(B=4, K=0, V=2048)),       # no drafts: the bonus token only
     ("c1", dict(B=3, K=31, V=600)),       # acceptance scan across a 32-lane boundary
     ("c1", dict(B=2, K=40, V=300)),
+    ("c1", dict(B=2, K=255, V=64)),       # the largest K: 511 rows, eight 32-position chunks
 ]
 
 
@@ -202,7 +203,7 @@ def test_gpu_chi_square_losslessness():
 # greedy chain
 # --------------------------------------------------------------------------
 @pytest.mark.parametrize("over", [dict(B=64), dict(B=16, V=1001), dict(B=8, V=1, K=3),
-                                  dict(B=8, K=0, V=512)])
+                                  dict(B=8, K=0, V=512), dict(B=3, K=255, V=96)])
 def test_greedy_parity(over):
     p = wl.preset("c4", **over)
     x = wl.make_chain(p, seed=21)

@@ -431,3 +431,45 @@ def test_tree_bad_parent_is_flagged():
     out = oracle.tree_verify_greedy(target, np.zeros((1, 3), np.int32),
                                     np.array([[-1, 0, 2]], np.int32))
     assert out["length"][0] == -1 and (out["path"] == -1).all() and (out["mask"] == 0).all()
+
+
+# --------------------------------------------------------------------------
+# acceptance statistics (page 2, "How much speedup to expect")
+# --------------------------------------------------------------------------
+def test_acceptance_stats_worked_example():
+    """Counted by hand: n = 0, 1, 2, 4, 4, bad, 3, 0 with K = 4."""
+    r = oracle.acceptance_stats([0, 1, 2, 4, 4, -1, 3, 0], 4)
+    assert r["hist"].tolist() == [2, 1, 1, 1, 2, 1]
+    # position i tested by #(n >= i) sequences, accepted by #(n > i)
+    assert np.allclose(r["alpha"], [5 / 7, 4 / 5, 3 / 4, 2 / 3], rtol=0, atol=1e-15)
+    assert r["mean_tokens"] == (2 * 1 + 1 * 2 + 1 * 3 + 1 * 4 + 2 * 5) / 7
+
+
+def test_acceptance_stats_edge_cases():
+    empty = oracle.acceptance_stats([], 3)
+    assert empty["hist"].tolist() == [0, 0, 0, 0, 0]
+    assert np.isnan(empty["alpha"]).all() and math.isnan(empty["mean_tokens"])
+    bad = oracle.acceptance_stats([-1, 7, -5], 3)  # every value outside [0, K]
+    assert bad["hist"].tolist() == [0, 0, 0, 0, 3] and math.isnan(bad["mean_tokens"])
+    none = oracle.acceptance_stats([0, 0, 2], 0)  # K = 0: only n == 0 counts
+    assert none["hist"].tolist() == [2, 1] and none["alpha"].size == 0
+    assert none["mean_tokens"] == 1.0
+
+
+@pytest.mark.parametrize("alpha", [0.7, 0.9])
+def test_acceptance_stats_recover_alpha_and_closed_form(alpha):
+    """Positions accepted independently with probability alpha: the histogram is
+    numpy.bincount, every alpha_i estimates alpha, and the mean tokens per
+    iteration approaches the page's (1 - alpha^(K+1)) / (1 - alpha)."""
+    K, B = 4, 400000
+    rng = np.random.default_rng(5)
+    acc = rng.random((B, K)) < alpha
+    n = np.where(acc.all(axis=1), K, np.argmin(acc, axis=1)).astype(np.int32)
+    r = oracle.acceptance_stats(n, K)
+    assert r["hist"][:K + 1].tolist() == np.bincount(n, minlength=K + 1).tolist()
+    assert r["hist"][K + 1] == 0
+    for i in range(K):
+        reached = int((n >= i).sum())
+        assert abs(r["alpha"][i] - alpha) < 5 * math.sqrt(alpha * (1 - alpha) / reached)
+    expect = (1 - alpha ** (K + 1)) / (1 - alpha)
+    assert abs(r["mean_tokens"] - expect) < 5 * (n + 1).std() / math.sqrt(B)

@@ -146,6 +146,12 @@ int spec_verify_bf16_static_scratch(const uint16_t *target_logits,
  *   out_resid_mass [B] float: total mass of the distribution the token at n
  *                  was drawn from (sum max(0, p_n - q_n), or about 1 for the
  *                  bonus row).
+ *   out_row_entropy [B, 2K+1] float: entropy in nats, -sum_v p(v) ln p(v), of
+ *                  each row's softmax(z / tau), rows in the order of
+ *                  out_row_stats, computed in the same streaming pass ([P3]
+ *                  sec. 3 "Engineering Recommendations": choose the
+ *                  speculation depth from how uncertain the distribution is).
+ *                  Unspecified for the rows of a sequence flagged bad.
  * With temperature == 0 the extra outputs are not written (the greedy argmax
  * of every target row comes from spec_verify_greedy_argmax_*).
  */
@@ -153,12 +159,12 @@ int spec_verify_stats_f32(const float *target_logits, const float *draft_logits,
                           const int32_t *draft_tokens, int B, int K, int V, float temperature,
                           uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
                           float *out_row_stats, float *out_pq, float *out_resid_mass,
-                          cudaStream_t stream);
+                          float *out_row_entropy, cudaStream_t stream);
 int spec_verify_stats_bf16(const uint16_t *target_logits, const uint16_t *draft_logits,
                            const int32_t *draft_tokens, int B, int K, int V, float temperature,
                            uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
                            float *out_row_stats, float *out_pq, float *out_resid_mass,
-                           cudaStream_t stream);
+                           float *out_row_entropy, cudaStream_t stream);
 
 /*
  * Greedy verification (temperature 0) that also writes the lowest-id argmax of

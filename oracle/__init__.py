@@ -65,6 +65,8 @@ def _load():
     lib.oracle_tree_verify_greedy.restype = i32
     lib.oracle_acceptance_stats.argtypes = [P, i32, i32, P, P, P]
     lib.oracle_acceptance_stats.restype = None
+    lib.oracle_row_entropy.argtypes = [P, i32, i64, i32, f64, P]
+    lib.oracle_row_entropy.restype = None
     _lib = lib
     return lib
 
@@ -233,3 +235,17 @@ def acceptance_stats(n_accepted, K: int):
     n_buf = n if n.size else np.zeros(1, dtype=np.int32)
     lib.oracle_acceptance_stats(_ptr(n_buf), int(n.size), int(K), _ptr(hist), _ptr(alpha), _ptr(mean))
     return dict(hist=hist, alpha=alpha[:K], mean_tokens=float(mean[0]))
+
+
+def row_entropy(logits, temperature: float):
+    """Entropy (nats) of softmax(logits / temperature) along the last axis;
+    the leading axes are kept.  NaN for a bad row."""
+    lib = _load()
+    t, dt = _as_logits(logits)
+    shape = t.shape[:-1]
+    V = t.shape[-1]
+    rows = int(np.prod(shape)) if len(shape) else 1
+    out = np.zeros(max(rows, 1), dtype=np.float64)
+    t_buf = t if t.size else np.zeros(1, dtype=t.dtype)
+    lib.oracle_row_entropy(_ptr(t_buf), dt, rows, V, float(temperature), _ptr(out))
+    return out[:rows].reshape(shape)

@@ -526,3 +526,33 @@ void oracle_acceptance_stats(const int32_t *n_accepted, int B, int K, uint64_t *
     }
     *mean_tokens = count ? total / (double)count : NAN;
 }
+
+/*
+ * Entropy (nats) of p = softmax(z / tau) for each of `rows` rows of V logits
+ *   [P3] "Speculative Decoding at Scale: Latency Reduction in Distributed LLM
+ *   Serving", sec. 3 "Engineering Recommendations" (speculation depth chosen
+ *   from how uncertain the distribution is); the entropy H = -sum_v p(v) ln p(v)
+ *   is the plain measure of that uncertainty.
+ * Terms with p(v) == 0 contribute 0.  A row with a NaN or +inf logit or no
+ * finite logit gets NaN.
+ */
+void oracle_row_entropy(const void *logits, int dtype, long long rows, int V, double tau,
+                        double *out)
+{
+    double *p = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    for (long long r = 0; r < rows; ++r) {
+        const char *row = (const char *)logits + (size_t)r * (size_t)V * (dtype == ORC_DTYPE_F32 ? 4 : 2);
+        if (row_is_bad(row, dtype, V)) {
+            out[r] = NAN;
+            continue;
+        }
+        double m, ssum;
+        softmax_row(row, dtype, V, tau, p, &m, &ssum);
+        double h = 0.0;
+        for (int v = 0; v < V; ++v)
+            if (p[v] > 0.0)
+                h -= p[v] * log(p[v]);
+        out[r] = h;
+    }
+    free(p);
+}

@@ -125,11 +125,12 @@ def spec_verify_static_scratch(target_logits, draft_logits, draft_tokens, temper
 
 
 def spec_verify_stats(target_logits, draft_logits, draft_tokens, temperature: float, seed: int,
-                      stream=None):
+                      stream=None, entropy: bool = False):
     """spec_verify plus the intermediate probabilities (temperature > 0).
 
     Returns dict(tokens [B,K+1], n [B], row_stats [B,2K+1,2] (max z/tau, sum
-    exp(z/tau - max)), pq [B,K,2] (p_i(x_i), q_i(x_i)), resid_mass [B])."""
+    exp(z/tau - max)), pq [B,K,2] (p_i(x_i), q_i(x_i)), resid_mass [B]) and,
+    with entropy=True, row_entropy [B,2K+1] (nats)."""
     if not temperature > 0:
         raise ValueError("spec_verify_stats needs temperature > 0")
     bf16, B, K, V = _chain_args(target_logits, draft_logits, draft_tokens, temperature)
@@ -139,13 +140,18 @@ def spec_verify_stats(target_logits, draft_logits, draft_tokens, temperature: fl
     row_stats = torch.empty((B, 2 * K + 1, 2), dtype=torch.float32, device=dev)
     pq = torch.empty((B, K, 2), dtype=torch.float32, device=dev)
     resid = torch.empty((B,), dtype=torch.float32, device=dev)
+    ent = torch.empty((B, 2 * K + 1), dtype=torch.float32, device=dev) if entropy else None
     lib = _lib.load()
     fn = lib.spec_verify_stats_bf16 if bf16 else lib.spec_verify_stats_f32
     with torch.cuda.device(dev):
         _lib.check(fn(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens) if K > 0 else None,
                       B, K, V, float(temperature), int(seed) & (2**64 - 1), _ptr(tokens), _ptr(n),
-                      _ptr(row_stats), _ptr(pq), _ptr(resid), _stream(stream)))
-    return dict(tokens=tokens, n=n, row_stats=row_stats, pq=pq, resid_mass=resid)
+                      _ptr(row_stats), _ptr(pq), _ptr(resid), _ptr(ent) if entropy else None,
+                      _stream(stream)))
+    out = dict(tokens=tokens, n=n, row_stats=row_stats, pq=pq, resid_mass=resid)
+    if entropy:
+        out["row_entropy"] = ent
+    return out
 
 
 def spec_verify_greedy_argmax(target_logits, draft_tokens, stream=None):

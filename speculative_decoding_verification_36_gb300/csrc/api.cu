@@ -255,7 +255,8 @@ int greedy_impl(bool bf16, const void* target, const int32_t* tokens, int B, int
 
 int verify_impl(bool bf16, const void* target, const void* draft, const int32_t* tokens, int B,
                 int K, int V, float temperature, uint64_t seed, int32_t* out_tokens, int32_t* out_n,
-                float* out_row_stats, float* out_pq, float* out_resid, cudaStream_t stream,
+                float* out_row_stats, float* out_pq, float* out_resid, float* out_entropy,
+                cudaStream_t stream,
                 bool use_static = false) {
   if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-30f))
     return SPEC_ERR_TEMPERATURE;
@@ -312,9 +313,11 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.out_row_stats = out_row_stats;
   a.out_pq = out_pq;
   a.out_resid = out_resid;
+  a.out_entropy = out_entropy;
   a.status = d->status;
   void* ws = nullptr;
-  rc = get_scratch(d, use_static, sv::sample_workspace(B, K, a.CS, a.TC, a.P), stream, &ws);
+  rc = get_scratch(d, use_static, sv::sample_workspace(B, K, a.CS, a.TC, a.P, out_entropy != nullptr),
+                   stream, &ws);
   if (rc) return rc;
   sv::sample_bind_workspace(a, ws);
   cudaError_t e = sv::launch_sample(a, bf16, vec, grid, stream);
@@ -345,7 +348,7 @@ int spec_verify_f32(const float* target_logits, const float* draft_logits,
                     uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
                     cudaStream_t stream) {
   return verify_impl(false, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
-                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream);
+                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 int spec_verify_bf16(const uint16_t* target_logits, const uint16_t* draft_logits,
@@ -353,7 +356,7 @@ int spec_verify_bf16(const uint16_t* target_logits, const uint16_t* draft_logits
                      uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
                      cudaStream_t stream) {
   return verify_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
-                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream);
+                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 int spec_verify_bf16_static_scratch(const uint16_t* target_logits, const uint16_t* draft_logits,
@@ -361,25 +364,27 @@ int spec_verify_bf16_static_scratch(const uint16_t* target_logits, const uint16_
                                     float temperature, uint64_t seed, int32_t* out_tokens,
                                     int32_t* out_n_accepted, cudaStream_t stream) {
   return verify_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
-                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, stream, true);
+                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, nullptr, stream, true);
 }
 
 int spec_verify_stats_f32(const float* target_logits, const float* draft_logits,
                           const int32_t* draft_tokens, int B, int K, int V, float temperature,
                           uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
                           float* out_row_stats, float* out_pq, float* out_resid_mass,
-                          cudaStream_t stream) {
+                          float* out_row_entropy, cudaStream_t stream) {
   return verify_impl(false, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
-                     out_tokens, out_n_accepted, out_row_stats, out_pq, out_resid_mass, stream);
+                     out_tokens, out_n_accepted, out_row_stats, out_pq, out_resid_mass,
+                     out_row_entropy, stream);
 }
 
 int spec_verify_stats_bf16(const uint16_t* target_logits, const uint16_t* draft_logits,
                            const int32_t* draft_tokens, int B, int K, int V, float temperature,
                            uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
                            float* out_row_stats, float* out_pq, float* out_resid_mass,
-                           cudaStream_t stream) {
+                           float* out_row_entropy, cudaStream_t stream) {
   return verify_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
-                     out_tokens, out_n_accepted, out_row_stats, out_pq, out_resid_mass, stream);
+                     out_tokens, out_n_accepted, out_row_stats, out_pq, out_resid_mass,
+                     out_row_entropy, stream);
 }
 
 int spec_verify_greedy_argmax_f32(const float* target_logits, const int32_t* draft_tokens, int B,

@@ -248,17 +248,30 @@ __device__ __noinline__ void stats_finisher(const SampleArgs& a, int b, FinIn pr
 // The sequence ticket is taken with a predicated atomic, and the finisher's
 // inputs for positions 0..31 are loaded while it is in flight, so the last
 // row goes on to the finisher without another round trip.
-template <class E>
+template <class E, bool ENT>
 __device__ __noinline__ void row_finisher(const SampleArgs& a, int b, int r) {
   const int lane = threadIdx.x & 31;
   const int C = a.CS;
   const float2* pp = a.part + ((size_t)b * a.R + r) * C;
-  float m = neg_inf(), s = 0.f;
+  float m = neg_inf(), s = 0.f, t = 0.f;
   for (int c = lane; c < C; c += 32) {
     const uint2 w = wait_u2(pp + c, a.status);
-    ms_merge(m, s, __uint_as_float(w.x), __uint_as_float(w.y), a.c_hi);
+    if constexpr (ENT) {
+      const float tc = wait_f32(a.part_t + ((size_t)b * a.R + r) * C + c, a.status);
+      mst_merge(m, s, t, __uint_as_float(w.x), __uint_as_float(w.y), tc, a.c_hi);
+    } else {
+      ms_merge(m, s, __uint_as_float(w.x), __uint_as_float(w.y), a.c_hi);
+    }
   }
-  warp_ms(m, s, a.c_hi);
+  if constexpr (ENT) {
+    warp_mst(m, s, t, a.c_hi);
+    // nats: ln s - ln 2 * t / s (NaN for a row without mass or with NaN)
+    if (lane == 0)
+      a.out_entropy[(size_t)b * a.R + r] =
+          (float)(log((double)s) - 0.69314718055994530942 * (double)t / (double)s);
+  } else {
+    warp_ms(m, s, a.c_hi);
+  }
   if (lane == 0) st_relaxed_u2(a.rowstat + (size_t)b * a.R + r, __float_as_uint(m), __float_as_uint(s));
   int old = ticket_take_if(lane == 0, &a.seqticket[b]);
   const FinIn pre = load_fin_inputs(a, b, 0);
@@ -649,34 +662,50 @@ __device__ __forceinline__ void load_batch(Raw<E, VEC> (&z)[kUnroll], const type
 
 // One batch into the lane's running (m, s): the batch max first, one rescale
 // if it rose, then 2^{(z - m) c} summed with packed pair arithmetic.
-template <class E, int VEC>
+template <class E, int VEC, bool ENT>
 __device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], float& m, f2_t& acc,
-                                            float cc) {
+                                            f2_t& tacc, float cc) {
   const float bm = batch_max<E, VEC>(z);
   if (bm > m) {
-    const float f = ex2((m - bm) * cc);
+    const float delta = (m - bm) * cc;
+    const float f = ex2(delta);
+    if constexpr (ENT) {
+      // t' = 2^delta (t + delta s); an empty accumulator stays empty
+      tacc = m == neg_inf() ? f2(0.f, 0.f) : f2mul(f2(f, f), f2fma(f2(delta, delta), acc, tacc));
+    }
     acc = f2mul(acc, f2(f, f));
     m = bm;
   }
   const float base = (m == neg_inf()) ? 0.f : m;
   if constexpr (VEC == 1) {
-    float lo = f2lo(acc);
+    float lo = f2lo(acc), tlo = f2lo(tacc);
 #pragma unroll
-    for (int u = 0; u < kUnroll; ++u) lo += ex2((z[u].f - base) * cc);
+    for (int u = 0; u < kUnroll; ++u) {
+      const float d = (z[u].f - base) * cc;
+      const float e = ex2(d);
+      lo += e;
+      if constexpr (ENT) tlo = fmaf(e, fmaxf(d, -126.f), tlo);
+    }
     acc = f2(lo, f2hi(acc));
+    if constexpr (ENT) tacc = f2(tlo, f2hi(tacc));
   } else {
     const f2_t b2 = f2(base, base), c2 = f2(cc, cc);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
-      for (int p = 0; p < VEC / 2; ++p) f2_exp_acc(acc, elem_pair<E, VEC>(z[u], p), b2, c2);
+      for (int p = 0; p < VEC / 2; ++p) {
+        if constexpr (ENT)
+          f2_exp_acc_ent(acc, tacc, elem_pair<E, VEC>(z[u], p), b2, c2);
+        else
+          f2_exp_acc(acc, elem_pair<E, VEC>(z[u], p), b2, c2);
+      }
   }
 }
 
 // Statistics slice s of row r of sequence b: the row's (m, s) over the slice,
 // then the row's ticket.  Returns the ticket's old value (lane 0).  Kept out
 // of line so that the stream loop has the register file to itself.
-template <class E, int VEC>
+template <class E, int VEC, bool ENT>
 __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int r, int s) {
   using S = typename E::storage;
   constexpr int BATCH = 32 * VEC * kUnroll;
@@ -690,7 +719,7 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int r, int s
   const uint32_t xt = ld_relaxed_if(lane == 0 && ti >= 0, a.tokens + (size_t)b * a.K + ti, kMarker);
   const float cc = a.c_hi;
   float m = neg_inf();
-  f2_t acc = f2(0.f, 0.f);
+  f2_t acc = f2(0.f, 0.f), tacc = f2(0.f, 0.f);
   // two register buffers: the next batch is in flight while one is reduced
   const int nb = v1 > v0 ? (v1 - v0 + BATCH - 1) / BATCH : 0;
   int e = v0 + lane * VEC;
@@ -701,16 +730,23 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int r, int s
   if (nb > 0) load_batch<E, VEC>(z0, row, e, v1);
   for (int bt = 0; bt < nb; bt += 2, e += 2 * BATCH) {
     if (bt + 1 < nb) load_batch<E, VEC>(z1, row, e + BATCH, v1);
-    stats_batch<E, VEC>(z0, m, acc, cc);
+    stats_batch<E, VEC, ENT>(z0, m, acc, tacc, cc);
     if (bt + 1 < nb) {
       if (bt + 2 < nb) load_batch<E, VEC>(z0, row, e + 2 * BATCH, v1);
-      stats_batch<E, VEC>(z1, m, acc, cc);
+      stats_batch<E, VEC, ENT>(z1, m, acc, tacc, cc);
     }
   }
   float sum = f2lo(acc) + f2hi(acc);
-  warp_ms(m, sum, cc);
+  float tsum = 0.f;
+  if constexpr (ENT) {
+    tsum = f2lo(tacc) + f2hi(tacc);
+    warp_mst(m, sum, tsum, cc);
+  } else {
+    warp_ms(m, sum, cc);
+  }
   int old = 0;
   if (lane == 0) {
+    if constexpr (ENT) st_relaxed_f32(a.part_t + ((size_t)b * a.R + r) * a.CS + s, tsum);
     st_relaxed_u2(a.part + ((size_t)b * a.R + r) * a.CS + s, __float_as_uint(m), __float_as_uint(sum));
     old = ticket_take(&a.rowticket[((size_t)b * a.R + r) * kTicketStride]);
     const int xi = (int)xt;
@@ -763,7 +799,7 @@ __device__ __forceinline__ int next_live_counter(int ctr, unsigned dead) {
 // decided once its statistics slices are done.  So every queue entry is
 // eventually written and every wait ends, whatever part of the grid is
 // resident.
-template <class E, int VEC>
+template <class E, int VEC, bool ENT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __grid_constant__ SampleArgs a) {
   const int lane = threadIdx.x & 31;
   const int w = slice_of_warp();
@@ -804,8 +840,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
       }
       if (!tail_ready) seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
       const int b = fdiv(f, a.div_seq), rs = f - b * per_seq, r = fdiv(rs, a.div_cs), s = rs - r * a.CS;
-      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC>(a, b, r, s), 0);
-      if (old == a.CS - 1) row_finisher<E>(a, b, r);
+      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC, ENT>(a, b, r, s), 0);
+      if (old == a.CS - 1) row_finisher<E, ENT>(a, b, r);
       if (ahead) {
         f = bcast(next) * kSlices + nctr;
         ctr = nctr;
@@ -848,9 +884,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: [counters, tickets, queue count (all start at -1)][marker-filled
-// result slots: part, rowstat, tailsum, queue, pieces, zx]; one 0xff fill
-// initialises both parts.
-static void sample_layout(int B, int R, int CS, int TC, int P, size_t* off) {
+// result slots: part, rowstat, tailsum, queue, pieces, zx, and part_t when the
+// entropy is asked for]; one 0xff fill initialises both parts.
+static void sample_layout(int B, int R, int CS, int TC, int P, bool ent, size_t* off) {
   size_t o = 0;
   off[0] = o; o += kCounterBytes;                                          // counter
   off[1] = o; o += align_up((size_t)B * R * kTicketStride * 4, 16);       // rowticket
@@ -865,13 +901,14 @@ static void sample_layout(int B, int R, int CS, int TC, int P, size_t* off) {
   off[10] = o; o += align_up((size_t)B * sizeof(SeqInfo), 256);           // queue
   off[11] = o; o += align_up((size_t)B * TC * P * sizeof(float), 256);    // pieces
   off[13] = o; o += align_up((size_t)B * R * sizeof(float), 256);         // zx
+  off[14] = o; if (ent) o += align_up((size_t)B * R * CS * sizeof(float), 256);  // part_t
   off[9] = o;                                                              // end of marker region
   off[12] = o;
 }
 
-WsLayout sample_workspace(int B, int K, int CS, int TC, int P) {
-  size_t off[14];
-  sample_layout(B, 2 * K + 1, CS, TC, P, off);
+WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
+  size_t off[15];
+  sample_layout(B, 2 * K + 1, CS, TC, P, ent, off);
   WsLayout l;
   l.total = off[12];
   l.zero_bytes = 0;  // counters and tickets start at -1: one 0xff fill covers everything
@@ -881,8 +918,8 @@ WsLayout sample_workspace(int B, int K, int CS, int TC, int P) {
 }
 
 void sample_bind_workspace(SampleArgs& a, void* ws) {
-  size_t off[14];
-  sample_layout(a.B, a.R, a.CS, a.TC, a.P, off);
+  size_t off[15];
+  sample_layout(a.B, a.R, a.CS, a.TC, a.P, a.out_entropy != nullptr, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
   a.rowticket = (int*)(p + off[1]);
@@ -895,11 +932,15 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.queue = (SeqInfo*)(p + off[10]);
   a.pieces = (float*)(p + off[11]);
   a.zx = (float*)(p + off[13]);
+  a.part_t = a.out_entropy ? (float*)(p + off[14]) : nullptr;
 }
 
 template <class E, int VEC>
 static cudaError_t launch_sample_t(const SampleArgs& a, int grid, cudaStream_t s) {
-  sample_kernel<E, VEC><<<grid, kThreads, 0, s>>>(a);
+  if (a.out_entropy)
+    sample_kernel<E, VEC, true><<<grid, kThreads, 0, s>>>(a);
+  else
+    sample_kernel<E, VEC, false><<<grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -911,7 +952,8 @@ cudaError_t launch_sample(const SampleArgs& a, bool bf16, bool vec, int grid, cu
 template <class E, int VEC>
 static int blocks_sample_t() {
   int n = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sample_kernel<E, VEC>, kThreads, 0) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, sample_kernel<E, VEC, false>, kThreads, 0) !=
+      cudaSuccess)
     return 1;
   return n > 0 ? n : 1;
 }

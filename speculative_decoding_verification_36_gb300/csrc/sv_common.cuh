@@ -67,6 +67,16 @@ __device__ __forceinline__ void f2_exp_acc(f2_t& acc, f2_t z, f2_t base, f2_t c)
   acc = f2add(acc, f2(ex2(f2lo(t)), ex2(f2hi(t))));
 }
 
+// The same with the entropy accumulator tacc += 2^t t (t <= 0: exponents are
+// taken relative to the running maximum).  t is clamped at -126 for the
+// product, so masked (-inf) elements and underflowed terms add 0, not NaN.
+__device__ __forceinline__ void f2_exp_acc_ent(f2_t& acc, f2_t& tacc, f2_t z, f2_t base, f2_t c) {
+  const f2_t t = f2mul(f2sub(z, base), c);
+  const f2_t e = f2(ex2(f2lo(t)), ex2(f2hi(t)));
+  acc = f2add(acc, e);
+  tacc = f2fma(e, f2(fmaxf(f2lo(t), -126.f), fmaxf(f2hi(t), -126.f)), tacc);
+}
+
 __device__ __forceinline__ uint32_t bf16x2_max(uint32_t a, uint32_t b) {
   uint32_t r;
   asm("max.bf16x2 %0, %1, %2;" : "=r"(r) : "r"(a), "r"(b));
@@ -374,6 +384,42 @@ __device__ __forceinline__ void warp_ms(float& m, float& s, float c) {
   for (int off = 16; off > 0; off >>= 1) t += __shfl_xor_sync(0xffffffffu, t, off);
   m = mx;
   s = t;
+}
+
+// Entropy statistics (m, s, t) with t = sum 2^d d over the same terms as s,
+// d = (z - m) c.  Moving the reference maximum from m to m' shifts every
+// exponent by delta = (m - m') c <= 0, and 2^(d + delta) (d + delta) =
+// 2^delta (2^d d + delta 2^d), so t' = 2^delta (t + delta s); an empty
+// accumulator (m = -inf) has t = 0.  The entropy of the row in nats is then
+// ln s - ln 2 * t / s.  s is updated with exactly the expressions of ms_merge
+// and warp_ms, so asking for the entropy changes no other result.
+__device__ __forceinline__ float t_rescaled(float m, float s, float t, float base, float c) {
+  if (m == neg_inf()) return 0.f;
+  const float delta = (m - base) * c;
+  return ex2(delta) * (t + delta * s);
+}
+__device__ __forceinline__ void mst_merge(float& m, float& s, float& t, float m2, float s2, float t2, float c) {
+  const float mn = fmaxf(m, m2);
+  const float base = (mn == neg_inf()) ? 0.f : mn;
+  t = t_rescaled(m, s, t, base, c) + t_rescaled(m2, s2, t2, base, c);
+  s = s * ex2((m - base) * c) + s2 * ex2((m2 - base) * c);
+  m = mn;
+}
+__device__ __forceinline__ void warp_mst(float& m, float& s, float& t, float c) {
+  float mx = m;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+  const float base = (mx == neg_inf()) ? 0.f : mx;
+  float u = s * ex2((m - base) * c);
+  float v = t_rescaled(m, s, t, base, c);
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    u += __shfl_xor_sync(0xffffffffu, u, off);
+    v += __shfl_xor_sync(0xffffffffu, v, off);
+  }
+  m = mx;
+  s = u;
+  t = v;
 }
 
 // Argmax with the lowest index winning ties.

@@ -94,6 +94,7 @@ struct SampleArgs {
   float* out_row_stats;  // optional [B, R, 2]: max(z)/tau, sum exp(z/tau - max)
   float* out_pq;         // optional [B, K, 2]: p_i(x_i), q_i(x_i)
   float* out_resid;      // optional [B]: mass of the replacement distribution
+  float* out_entropy;    // optional [B, R]: entropy (nats) of each row's softmax
   // workspace, filled with all-ones bytes before the launch: the counters and
   // tickets (counter, rowticket, seqticket, tailticket, qcount) then start at
   // -1, and the result slots (part, rowstat, zx, tailsum, queue, pieces) hold
@@ -106,6 +107,7 @@ struct SampleArgs {
   float2* part;     // [B, R, CS] per-slice (m, s)
   float2* rowstat;  // [B, R] merged (m, s) of each row
   float* zx;        // [B, R] logit at the drafted token, written by the slice holding it
+  float* part_t;    // [B, R, CS] per-slice entropy accumulator (only with out_entropy)
   float* tailsum;   // [B, TC] per tail-slice mass
   SeqInfo* queue;   // [B] decisions in the order they were made
   float* pieces;    // [B, TC, P] per-piece mass
@@ -144,7 +146,7 @@ struct GreedyArgs {
 struct WsLayout {
   size_t total, zero_bytes, marker_off, marker_bytes;
 };
-WsLayout sample_workspace(int B, int K, int CS, int TC, int P);
+WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent);
 WsLayout greedy_workspace(int B, int R, int CU);
 
 // Bind workspace pointers into the argument blocks.

@@ -92,6 +92,28 @@ def test_sampling_probabilities(name, over):
     assert e_sum <= 1e-5 and e_p <= 1e-5 and e_q <= 1e-5 and e_z <= 1e-5
 
 
+@pytest.mark.parametrize("name,over", [("c1", {}), ("c3", dict(B=8)), ("c2", dict(B=4, V=1001)),
+                                       ("c2", dict(B=4, K=0, V=2048)), ("c1", dict(B=3, K=40, V=300))])
+def test_row_entropy(name, over):
+    """Entropy of every row's softmax from the statistics pass, against the
+    oracle; asking for it leaves the tokens unchanged."""
+    p = wl.preset(name, **over)
+    x = wl.make_chain(p, seed=8)
+    if name == "c1":  # masked vocabulary entries in the first target row
+        x["target"][0, 0, ::7] = -float("inf")
+    out = sv.spec_verify_stats(_dev(x["target"]), _dev(x["draft"]), _dev(x["tokens"]),
+                               p.temperature, 9, entropy=True)
+    plain_t, plain_n = run_chain(x, seed=9)
+    h = out["row_entropy"].cpu().numpy()
+    rows = torch.cat([x["target"], x["draft"]], dim=1) if p.K > 0 else x["target"]
+    ref = oracle.row_entropy(rows, p.temperature)
+    err = np.abs(h - ref) / np.maximum(1.0, np.abs(ref))
+    print(f"{name}: entropy err {err.max():.2e}")
+    assert err.max() <= 1e-5
+    assert np.array_equal(out["tokens"].cpu().numpy(), plain_t)
+    assert np.array_equal(out["n"].cpu().numpy(), plain_n)
+
+
 @pytest.mark.parametrize("name,sel", [("c3", [0, 1, 77, 128, 201, 255]),
                                       ("c2", [0, 13, 31, 63])])
 def test_full_size_sampled_sequences(name, sel):

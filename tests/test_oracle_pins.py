@@ -473,3 +473,35 @@ def test_acceptance_stats_recover_alpha_and_closed_form(alpha):
         assert abs(r["alpha"][i] - alpha) < 5 * math.sqrt(alpha * (1 - alpha) / reached)
     expect = (1 - alpha ** (K + 1)) / (1 - alpha)
     assert abs(r["mean_tokens"] - expect) < 5 * (n + 1).std() / math.sqrt(B)
+
+
+# --------------------------------------------------------------------------
+# per-row entropy (page 3, sec. 3: speculation depth from the distribution's
+# uncertainty)
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("dtype", [torch.float32, torch.bfloat16])
+@pytest.mark.parametrize("tau", [0.5, 1.0, 1.7])
+def test_row_entropy_matches_torch_categorical(dtype, tau):
+    g = torch.Generator().manual_seed(31)
+    z = (torch.randn(4, 3, 513, generator=g) * 3).to(dtype)
+    h = oracle.row_entropy(z, tau)
+    ref = torch.distributions.Categorical(logits=z.double() / tau).entropy().numpy()
+    assert np.abs(h - ref).max() < 1e-12
+
+
+def test_row_entropy_closed_forms():
+    V = 1000
+    assert abs(oracle.row_entropy(torch.zeros(1, V), 1.0)[0] - math.log(V)) < 1e-12  # uniform
+    one_hot = torch.full((1, V), -float("inf"))
+    one_hot[0, 17] = 3.0
+    assert oracle.row_entropy(one_hot, 0.9)[0] == 0.0
+    two = torch.full((1, V), -float("inf"))  # two admissible tokens
+    two[0, 0], two[0, 1] = math.log(0.3), math.log(0.7)
+    l0, l1 = float(two[0, 0]), float(two[0, 1])  # the fp32-rounded logits
+    a = 1.0 / (1.0 + math.exp(l1 - l0))
+    expect = -a * math.log(a) - (1 - a) * math.log(1 - a)
+    assert abs(oracle.row_entropy(two, 1.0)[0] - expect) < 1e-12
+    bad = torch.zeros(2, 8)
+    bad[0, 3] = float("nan")
+    bad[1, :] = -float("inf")
+    assert np.isnan(oracle.row_entropy(bad, 1.0)).all()

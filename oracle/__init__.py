@@ -67,6 +67,8 @@ def _load():
     lib.oracle_acceptance_stats.restype = None
     lib.oracle_row_entropy.argtypes = [P, i32, i64, i32, f64, P]
     lib.oracle_row_entropy.restype = None
+    lib.oracle_tree_verify_sampling.argtypes = [P, P, i32, P, P, i32, i32, i32, f64, u64, P, P, P]
+    lib.oracle_tree_verify_sampling.restype = i32
     _lib = lib
     return lib
 
@@ -249,3 +251,29 @@ def row_entropy(logits, temperature: float):
     t_buf = t if t.size else np.zeros(1, dtype=t.dtype)
     lib.oracle_row_entropy(_ptr(t_buf), dt, rows, V, float(temperature), _ptr(out))
     return out[:rows].reshape(shape)
+
+
+def tree_verify_sampling(target, draft, tree_tokens, parent_idx, temperature: float, seed: int):
+    """Stochastic verification of a token tree.  target, draft [B, N+1, V];
+    tokens, parents [B, N].  Returns dict(path [B, N+1], length [B],
+    boundary [B] (1 when some draw lay within 1e-6 of its decision boundary))."""
+    lib = _load()
+    t, dt = _as_logits(target)
+    d, dd = _as_logits(draft)
+    if dd != dt or d.shape != t.shape:
+        raise ValueError("target and draft must share dtype and shape")
+    tok = _as_i32(tree_tokens)
+    par = _as_i32(parent_idx)
+    B, N1, V = t.shape
+    N = N1 - 1
+    path = np.full((B, N1), -1, dtype=np.int32)
+    length = np.zeros(B, dtype=np.int32)
+    boundary = np.zeros(B, dtype=np.int32)
+    tok_buf = tok if tok.size else np.zeros(1, dtype=np.int32)
+    par_buf = par if par.size else np.zeros(1, dtype=np.int32)
+    rc = lib.oracle_tree_verify_sampling(_ptr(t), _ptr(d), dt, _ptr(tok_buf), _ptr(par_buf), B, N, V,
+                                         float(temperature), int(seed) & (2**64 - 1), _ptr(path),
+                                         _ptr(length), _ptr(boundary))
+    if rc != 0:
+        raise MemoryError("oracle_tree_verify_sampling failed to allocate")
+    return dict(path=path, length=length, boundary=boundary)

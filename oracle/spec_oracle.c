@@ -556,3 +556,118 @@ void oracle_row_entropy(const void *logits, int dtype, long long rows, int V, do
     }
     free(p);
 }
+
+/*
+ * Stochastic (temperature > 0) verification of a token tree per sequence.
+ *   [P4] sec. 4 "Tree-Based Speculative Verification & Custom 2D Attention
+ *   Masks" (a tree of candidates verified in one target pass, the longest
+ *   accepted path kept) with the acceptance rule and residual of [P1] sec. 2 /
+ *   [P2] "The correctness guarantee", applied node by node: the children of the
+ *   current node are tried in index order, each against the current target
+ *   distribution P; a rejected child replaces P by norm(max(0, P - Q)) before the
+ *   next sibling is tried.  When no child is accepted (or the node is a leaf) one
+ *   token is drawn from the current P.
+ *
+ * target, draft: B x (N+1) x V; row 0 is the root, row i+1 node i.  At node u,
+ *   P = softmax(target row u / tau) and Q = softmax(draft row u / tau), Q being
+ *   the distribution u's children were drawn from.
+ * tree_tokens, parents: B x N; parents[i] in [-1, i) (-1: the root).
+ * Draws: child c's acceptance uniform uses counter (b, c, 0, 0); the final draw
+ *   at the stopping node uses (b, row of the node, 1, 0).
+ * out_path: B x (N+1): accepted tokens root to leaf, then the drawn token, -1
+ *   after; out_len: B, the number of entries written (depth + 1).
+ * boundary (may be NULL): B, 1 when some draw of the sequence lies within 1e-6
+ *   of its decision boundary (|u - min(1, P(x)/Q(x))|, or the distance of w * Z
+ *   to the nearest cumulative sum relative to Z).
+ * Bad data (any bad row of the sequence, a token outside [0, V), a parent not in
+ * [-1, i)) gives out_len = -1 and -1 everywhere.  Returns 0, or -1 if memory
+ * could not be allocated.
+ */
+int oracle_tree_verify_sampling(const void *target, const void *draft, int dtype,
+                                const int32_t *tree_tokens, const int32_t *parents, int B, int N,
+                                int V, double tau, uint64_t seed, int32_t *out_path,
+                                int32_t *out_len, int32_t *boundary)
+{
+    const size_t esz = dtype == ORC_DTYPE_F32 ? 4 : 2;
+    const size_t rowb = (size_t)V * esz;
+    double *P = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    double *Q = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    double *R = (double *)malloc(sizeof(double) * (size_t)(V > 0 ? V : 1));
+    if (!P || !Q || !R) {
+        free(P); free(Q); free(R);
+        return -1;
+    }
+    for (int b = 0; b < B; ++b) {
+        const char *T = (const char *)target + (size_t)b * (size_t)(N + 1) * rowb;
+        const char *D = (const char *)draft + (size_t)b * (size_t)(N + 1) * rowb;
+        const int32_t *tok = tree_tokens + (size_t)b * N;
+        const int32_t *par = parents + (size_t)b * N;
+        int32_t *path = out_path + (size_t)b * (N + 1);
+        for (int j = 0; j <= N; ++j)
+            path[j] = -1;
+        if (boundary)
+            boundary[b] = 0;
+        int bad = 0;
+        for (int r = 0; r <= N; ++r)
+            if (row_is_bad(T + r * rowb, dtype, V) || row_is_bad(D + r * rowb, dtype, V))
+                bad = 1;
+        for (int i = 0; i < N; ++i)
+            if (tok[i] < 0 || tok[i] >= V || par[i] < -1 || par[i] >= i)
+                bad = 1;
+        if (bad) {
+            out_len[b] = -1;
+            continue;
+        }
+        int u = -1, len = 0;
+        double m, s;
+        softmax_row(T, dtype, V, tau, P, &m, &s);
+        softmax_row(D, dtype, V, tau, Q, &m, &s);
+        for (;;) {
+            int accepted = -1;
+            for (int c = 0; c < N; ++c) {
+                if (par[c] != u)
+                    continue;
+                const int x = tok[c];
+                const double r = oracle_uniform(seed, (uint64_t)b, (uint64_t)c, 0);
+                const int ok = P[x] >= Q[x] || r * Q[x] < P[x];
+                if (boundary && Q[x] > 0.0) {
+                    double a = P[x] / Q[x];
+                    if (a > 1.0)
+                        a = 1.0;
+                    if (fabs(r - a) < 1e-6)
+                        boundary[b] = 1;
+                }
+                if (ok) {
+                    accepted = c;
+                    break;
+                }
+                /* rejected: P <- norm(max(0, P - Q)) for the next sibling */
+                double z = 0.0;
+                for (int v = 0; v < V; ++v) {
+                    R[v] = P[v] > Q[v] ? P[v] - Q[v] : 0.0;
+                    z += R[v];
+                }
+                if (z > 0.0)
+                    for (int v = 0; v < V; ++v)
+                        P[v] = R[v] / z;
+            }
+            if (accepted < 0)
+                break;
+            path[len++] = tok[accepted];
+            u = accepted;
+            softmax_row(T + (size_t)(u + 1) * rowb, dtype, V, tau, P, &m, &s);
+            softmax_row(D + (size_t)(u + 1) * rowb, dtype, V, tau, Q, &m, &s);
+        }
+        double z = 0.0;
+        for (int v = 0; v < V; ++v)
+            z += P[v];
+        const double w = oracle_uniform(seed, (uint64_t)b, (uint64_t)(u + 1), 1);
+        double dist;
+        path[len++] = inverse_cdf(P, V, w * z, &dist);
+        if (boundary && dist < 1e-6 * z)
+            boundary[b] = 1;
+        out_len[b] = len;
+    }
+    free(P); free(Q); free(R);
+    return 0;
+}

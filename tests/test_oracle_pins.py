@@ -505,3 +505,91 @@ def test_row_entropy_closed_forms():
     bad[0, 3] = float("nan")
     bad[1, :] = -float("inf")
     assert np.isnan(oracle.row_entropy(bad, 1.0)).all()
+
+
+# --------------------------------------------------------------------------
+# stochastic tree verification (page 4, sec. 4, with the page 1 sec. 2 rule)
+# --------------------------------------------------------------------------
+def test_tree_sampling_on_a_chain_is_the_chain_verify():
+    """A tree whose nodes form one chain is verified exactly like the chain."""
+    g = torch.Generator().manual_seed(3)
+    B, K, V = 64, 5, 50
+    T = torch.randn(B, K + 1, V, generator=g) * 2
+    D = T + torch.randn(B, K + 1, V, generator=g)
+    x = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    par = torch.arange(-1, K - 1, dtype=torch.int32).expand(B, K).contiguous()
+    tr = oracle.tree_verify_sampling(T, D, x, par, 0.8, 5)
+    ch = oracle.spec_verify(T, D[:, :K].contiguous(), x, 0.8, 5)
+    assert np.array_equal(tr["length"], ch["n"] + 1)
+    assert np.array_equal(tr["path"], ch["tokens"])
+
+
+def test_tree_sampling_without_nodes_draws_the_bonus():
+    g = torch.Generator().manual_seed(4)
+    T = torch.randn(32, 1, 40, generator=g)
+    D = torch.randn(32, 1, 40, generator=g)
+    tr = oracle.tree_verify_sampling(T, D, torch.zeros(32, 0, dtype=torch.int32),
+                                     torch.zeros(32, 0, dtype=torch.int32), 1.3, 8)
+    ch = oracle.spec_verify(T, torch.zeros(32, 0, 40), torch.zeros(32, 0, dtype=torch.int32), 1.3, 8)
+    assert (tr["length"] == 1).all() and np.array_equal(tr["path"][:, 0], ch["tokens"][:, 0])
+
+
+def test_tree_sampling_is_lossless():
+    """Root with two children drawn from Q_root, each with one child drawn from
+    Q1[token].  Target rows depend only on the token prefix, so every emitted
+    position, given its prefix and that it exists, must follow the target's
+    conditional distribution, whichever sibling was accepted or resampled."""
+    from scipy import stats
+    V, B = 4, 200000
+    rng = np.random.default_rng(11)
+
+    def dist(k):
+        p = rng.random(k) + 0.05
+        return p / p.sum()
+    P0, Q0 = dist(V), dist(V)
+    P1 = np.stack([dist(V) for _ in range(V)])
+    Q1 = np.stack([dist(V) for _ in range(V)])
+    P2 = np.stack([[dist(V) for _ in range(V)] for _ in range(V)])
+    c = np.stack([rng.choice(V, size=B, p=Q0), rng.choice(V, size=B, p=Q0)], axis=1)
+    gch = np.stack([np.array([rng.choice(V, p=Q1[a]) for a in col]) for col in c.T], axis=1)
+    tokens = np.concatenate([c, gch], axis=1).astype(np.int32)
+    parents = np.tile(np.array([-1, -1, 0, 1], dtype=np.int32), (B, 1))
+    lg = lambda p: np.log(p).astype(np.float32)
+    T = np.empty((B, 5, V), dtype=np.float32)
+    D = np.empty((B, 5, V), dtype=np.float32)
+    T[:, 0] = lg(P0)
+    D[:, 0] = lg(Q0)
+    for k in range(2):
+        T[:, 1 + k] = lg(P1[c[:, k]])
+        D[:, 1 + k] = lg(Q1[c[:, k]])
+        T[:, 3 + k] = lg(P2[c[:, k], gch[:, k]])
+        D[:, 3 + k] = lg(np.full(V, 1.0 / V))  # leaves: their Q is never used
+    out = oracle.tree_verify_sampling(T, D, tokens, parents, 1.0, 21)
+    path, length = out["path"], out["length"]
+    assert length.min() >= 1 and length.max() <= 3
+    P0e = np.exp(T[0, 0].astype(np.float64)); P0e /= P0e.sum()
+    assert stats.chisquare(np.bincount(path[:, 0], minlength=V), P0e * B).pvalue > 1e-3
+    for a in range(V):
+        sel = (length >= 2) & (path[:, 0] == a)
+        if sel.sum() > 500:
+            p = np.exp(lg(P1[a]).astype(np.float64)); p /= p.sum()
+            assert stats.chisquare(np.bincount(path[sel, 1], minlength=V), p * sel.sum()).pvalue > 1e-3
+        for b2 in range(V):
+            sel3 = (length == 3) & (path[:, 0] == a) & (path[:, 1] == b2)
+            if sel3.sum() > 500:
+                p = np.exp(lg(P2[a, b2]).astype(np.float64)); p /= p.sum()
+                assert stats.chisquare(np.bincount(path[sel3, 2], minlength=V),
+                                       p * sel3.sum()).pvalue > 1e-3
+    # the second sibling is really tested (after a residual update)
+    first_rejected = path[:, 0] != c[:, 0]
+    assert ((length >= 2) & first_rejected & (path[:, 0] == c[:, 1])).sum() > 1000
+
+
+def test_tree_sampling_bad_data():
+    T = torch.zeros(3, 3, 8)
+    D = torch.zeros(3, 3, 8)
+    tok = torch.tensor([[1, 2], [1, 9], [1, 2]], dtype=torch.int32)  # sequence 1: token out of range
+    par = torch.tensor([[-1, 0], [-1, 0], [-1, 1]], dtype=torch.int32)  # sequence 2: parent not < i
+    out = oracle.tree_verify_sampling(T, D, tok, par, 1.0, 0)
+    assert out["length"].tolist()[1:] == [-1, -1] and (out["path"][1:] == -1).all()
+    assert out["length"][0] >= 1

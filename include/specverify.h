@@ -209,6 +209,45 @@ int spec_tree_verify_greedy_bf16(const uint16_t *target_logits, const int32_t *t
                                  cudaStream_t stream);
 
 /*
+ * Stochastic verification of a candidate tree per sequence (temperature > 0).
+ * The tree of "Speculative Decoding in Production: How Small Draft Models &
+ * Medusa Heads Deliver 2x-3x LLM Speedups Without Accuracy Loss", sec. 4,
+ * checked with the acceptance rule and residual of "Speculative Decoding &
+ * Draft Model Topologies: Slashing Enterprise LLM Latency by 3.5x in 2026",
+ * sec. 2, one node at a time.
+ *
+ *   target_logits [B, N+1, V]  row 0: the root; row i+1: node i.
+ *   draft_logits  [B, N+1, V]  row u+1: the draft distribution the children
+ *                              of node u (row 0: of the root) were drawn from.
+ *   tree_tokens, parent_idx    as for spec_tree_verify_greedy_*.
+ *   temperature   > 0: p = softmax(target / T), q = softmax(draft / T).
+ *   seed          Philox-4x64-10 key word as for spec_verify_*: node c's
+ *                 acceptance uniform uses counter (b, c, 0, 0); the final
+ *                 draw at node u uses counter (b, u + 1, 1, 0).
+ *   out_path      [B, N+1] int32: the accepted tokens from the root down, then
+ *                 the token drawn at the last accepted node, then -1 padding.
+ *   out_len       [B] int32: accepted nodes + 1, or -1 for bad data.
+ * At the current node (the root first) with current distribution P = p of its
+ * row, the children are tried in node-index order: child x is accepted with
+ * probability min(1, P(x) / q(x)) (always when q(x) == 0) and becomes the
+ * current node; a rejected child replaces P by norm(max(0, P - q)) for the
+ * next sibling.  When no child is accepted, or the node is a leaf, one token
+ * is drawn from the current P by inverse CDF in vocabulary order.  Each
+ * emitted token is then distributed exactly as p at its position.  Every row
+ * of both inputs is checked for bad data, leaves' draft rows included.
+ * N <= 1024.  temperature 0 is SPEC_ERR_TEMPERATURE here (the greedy tree is
+ * spec_tree_verify_greedy_*).
+ */
+int spec_tree_verify_sampling_f32(const float *target_logits, const float *draft_logits,
+                                  const int32_t *tree_tokens, const int32_t *parent_idx, int B,
+                                  int N, int V, float temperature, uint64_t seed,
+                                  int32_t *out_path, int32_t *out_len, cudaStream_t stream);
+int spec_tree_verify_sampling_bf16(const uint16_t *target_logits, const uint16_t *draft_logits,
+                                   const int32_t *tree_tokens, const int32_t *parent_idx, int B,
+                                   int N, int V, float temperature, uint64_t seed,
+                                   int32_t *out_path, int32_t *out_len, cudaStream_t stream);
+
+/*
  * Acceptance statistics of a batch of verify outputs ([P2] "How much speedup
  * to expect": the per-position acceptance rate and the expected tokens per
  * iteration, measured instead of predicted).

@@ -10,6 +10,8 @@ library's CUDA kernels.  There is no CPU fallback.
     spec_verify_stats(...)            # plus row statistics, p(x), q(x), mass
     spec_verify_greedy_argmax(...)    # greedy chain plus every row's argmax
     spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx)
+    spec_tree_verify_sampling(target_logits, draft_logits, tree_tokens, parent_idx, T, seed)
+    spec_acceptance_stats(n_accepted, K)  # histogram, alpha, mean tokens
     spec_get_status()                 # device status word (bad data, timeouts)
 """
 from __future__ import annotations
@@ -21,7 +23,7 @@ from ._lib import SPEC_FLAG_BAD_DATA, SPEC_FLAG_TIMEOUT, SpecError
 
 __all__ = [
     "spec_verify", "spec_verify_static_scratch", "spec_verify_stats", "spec_verify_greedy_argmax",
-    "spec_tree_verify_greedy", "spec_acceptance_stats", "spec_get_status", "SpecError",
+    "spec_tree_verify_greedy", "spec_tree_verify_sampling", "spec_acceptance_stats", "spec_get_status", "SpecError",
     "SPEC_FLAG_BAD_DATA", "SPEC_FLAG_TIMEOUT",
 ]
 
@@ -198,6 +200,40 @@ def spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx, out_path=Non
                       _ptr(parent_idx) if N > 0 else None, B, N, V, _ptr(out_path), _ptr(out_len),
                       _ptr(out_mask), _stream(stream)))
     return out_path, out_len, out_mask
+
+
+def spec_tree_verify_sampling(target_logits, draft_logits, tree_tokens, parent_idx, temperature: float,
+                              seed: int, out_path=None, out_len=None, stream=None):
+    """Stochastic verification of a candidate tree per sequence (temperature > 0).
+
+    target_logits, draft_logits [B, N+1, V] (draft row u+1: the distribution
+    node u's children were drawn from); tree_tokens, parent_idx [B, N] int32.
+    Returns (out_path [B, N+1], out_len [B])."""
+    if not temperature > 0:
+        raise ValueError("spec_tree_verify_sampling needs temperature > 0 (spec_tree_verify_greedy is T = 0)")
+    bf16 = _is_bf16(target_logits, "target_logits")
+    if target_logits.dim() != 3:
+        raise ValueError("target_logits must be [B, N+1, V]")
+    if _is_bf16(draft_logits, "draft_logits") != bf16:
+        raise TypeError("target_logits and draft_logits must share a dtype")
+    if tuple(draft_logits.shape) != tuple(target_logits.shape):
+        raise ValueError(f"draft_logits has shape {tuple(draft_logits.shape)}, expected "
+                         f"{tuple(target_logits.shape)}")
+    B, N1, V = target_logits.shape
+    N = N1 - 1
+    if N > 0:
+        _i32(tree_tokens, (B, N), "tree_tokens")
+        _i32(parent_idx, (B, N), "parent_idx")
+    dev = target_logits.device
+    out_path = _out(out_path, (B, N + 1), torch.int32, dev, "out_path")
+    out_len = _out(out_len, (B,), torch.int32, dev, "out_len")
+    lib = _lib.load()
+    fn = lib.spec_tree_verify_sampling_bf16 if bf16 else lib.spec_tree_verify_sampling_f32
+    with torch.cuda.device(dev):
+        _lib.check(fn(_ptr(target_logits), _ptr(draft_logits), _ptr(tree_tokens) if N > 0 else None,
+                      _ptr(parent_idx) if N > 0 else None, B, N, V, float(temperature),
+                      int(seed) & (2**64 - 1), _ptr(out_path), _ptr(out_len), _stream(stream)))
+    return out_path, out_len
 
 
 def spec_acceptance_stats(n_accepted, K: int, stream=None):

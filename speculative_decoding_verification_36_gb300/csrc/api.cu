@@ -46,6 +46,8 @@ struct DeviceState {
   int occ_sample[2][2] = {{0, 0}, {0, 0}};  // [bf16][vec]
   int occ_greedy[2][2] = {{0, 0}, {0, 0}};
   int occ_tree[2][2] = {{0, 0}, {0, 0}};
+  int occ_tree_stats[2][2] = {{0, 0}, {0, 0}};
+  int walk_clusters[2][2][4] = {};  // [bf16][vec][log2 C]: walk clusters resident at once
 };
 
 constexpr int kMaxDevices = 64;
@@ -76,6 +78,8 @@ int get_device_state(DeviceState** out) {
         d.occ_sample[bf][v] = sv::sample_blocks_per_sm(bf, v);
         d.occ_greedy[bf][v] = sv::greedy_blocks_per_sm(bf, v);
         d.occ_tree[bf][v] = sv::tree_blocks_per_sm(bf, v);
+        d.occ_tree_stats[bf][v] = sv::tree_stats_blocks_per_sm(bf, v);
+        for (int c = 0; c < 4; ++c) d.walk_clusters[bf][v][c] = sv::tree_walk_clusters(bf, v, 1 << c);
       }
     d.init = true;
   }
@@ -339,6 +343,72 @@ int tree_impl(bool bf16, const void* target, const int32_t* tree_tokens, const i
                      nullptr, stream);
 }
 
+// Stochastic tree verification: row statistics of all 2 (N + 1) rows of every
+// sequence, then one CTA per sequence walks its tree.
+int tree_sample_impl(bool bf16, const void* target, const void* draft, const int32_t* tree_tokens,
+                     const int32_t* parents, int B, int N, int V, float temperature, uint64_t seed,
+                     int32_t* out_path, int32_t* out_len, cudaStream_t stream) {
+  if (!(temperature >= 1e-30f)) return SPEC_ERR_TEMPERATURE;
+  if (!target || !draft || !out_path || !out_len || (N > 0 && (!tree_tokens || !parents)))
+    return SPEC_ERR_NULL;
+  if (B < 0 || N < 0 || N > sv::kMaxTreeNodes || V < 1 || !sizes_ok(B, 2 * (N + 1), V))
+    return SPEC_ERR_SHAPE;
+  if (B == 0) return SPEC_OK;
+  DeviceState* d = nullptr;
+  int rc = get_device_state(&d);
+  if (rc) return rc;
+  const size_t esz = bf16 ? 2 : 4;
+  const bool vec = aligned16(target) && aligned16(draft) && ((size_t)V * esz) % 16 == 0;
+  const int vec_elems = vec ? (bf16 ? 8 : 4) : 1;
+  sv::TreeSampleArgs a;
+  memset(&a, 0, sizeof a);
+  a.target = target;
+  a.draft = draft;
+  a.tokens = tree_tokens;
+  a.parents = parents;
+  a.B = B;
+  a.N = N;
+  a.V = V;
+  a.RR = 2 * (N + 1);
+  int CU = 0;
+  static const int slice_bytes = env_int("SPECVERIFY_SLICE_BYTES", 12288);
+  choose_slices(V, vec_elems, esz, slice_bytes, &a.SL, &a.CS, &CU);
+  a.F = (long long)B * a.RR * a.CS;
+  // walk: the widest cluster (8, 4, 2 CTAs) for which every sequence's
+  // cluster is resident at once, else one CTA per sequence; each pass gives
+  // every warp of the cluster one contiguous run of whole warp steps
+  a.C = 1;
+  for (int c = 3; c >= 1; --c)
+    if (B <= d->walk_clusters[bf16][vec][c]) {
+      a.C = 1 << c;
+      break;
+    }
+  const long long step = 32LL * vec_elems;
+  const long long warps = (long long)a.C * (sv::kWalkThreads / 32);
+  const long long per_warp = ((long long)V + warps - 1) / warps;
+  a.chunk = (int)((per_warp + step - 1) / step * step);
+  const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
+  a.c64 = c;
+  a.c_hi = (float)c;
+  a.c_lo = (float)(c - (double)a.c_hi);
+  a.seed = seed;
+  a.out_path = out_path;
+  a.out_len = out_len;
+  a.status = d->status;
+  void* ws = nullptr;
+  rc = get_scratch(d, false, sv::tree_sample_workspace(B, a.RR, a.CS), stream, &ws);
+  if (rc) return rc;
+  sv::tree_sample_bind_workspace(a, ws);
+  const long long capacity = (long long)d->sms * d->occ_tree_stats[bf16][vec];
+  const long long want = (a.F + sv::kWarps - 1) / sv::kWarps;  // one slice per warp
+  const int stats_grid = (int)(want < capacity ? want : capacity);
+  cudaError_t e = sv::launch_tree_sample(a, bf16, vec, stats_grid, stream);
+  cudaError_t e2 = put_scratch(false, ws, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "tree sampling verify launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
+  return SPEC_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -415,6 +485,22 @@ int spec_tree_verify_greedy_bf16(const uint16_t* target_logits, const int32_t* t
                                  cudaStream_t stream) {
   return tree_impl(true, target_logits, tree_tokens, parent_idx, B, N, V, out_path, out_len,
                    out_mask, stream);
+}
+
+int spec_tree_verify_sampling_f32(const float* target_logits, const float* draft_logits,
+                                  const int32_t* tree_tokens, const int32_t* parent_idx, int B, int N,
+                                  int V, float temperature, uint64_t seed, int32_t* out_path,
+                                  int32_t* out_len, cudaStream_t stream) {
+  return tree_sample_impl(false, target_logits, draft_logits, tree_tokens, parent_idx, B, N, V,
+                          temperature, seed, out_path, out_len, stream);
+}
+
+int spec_tree_verify_sampling_bf16(const uint16_t* target_logits, const uint16_t* draft_logits,
+                                   const int32_t* tree_tokens, const int32_t* parent_idx, int B,
+                                   int N, int V, float temperature, uint64_t seed, int32_t* out_path,
+                                   int32_t* out_len, cudaStream_t stream) {
+  return tree_sample_impl(true, target_logits, draft_logits, tree_tokens, parent_idx, B, N, V,
+                          temperature, seed, out_path, out_len, stream);
 }
 
 int spec_acceptance_stats(const int32_t* n_accepted, int B, int K, uint64_t* out_hist,

@@ -34,98 +34,6 @@
 
 namespace sv {
 
-// ---------------------------------------------------------------------------
-// Replacement / bonus weights.  Both are scaled by the target row's sum sT so
-// that no division is needed: the inverse CDF only sees ratios.
-//   bonus:     w(v) = 2^{(zT - mT) c}                        = sT * p(v)
-//   residual:  w(v) = 2^{(zT - mT) c} * (1 - 2^{-delta})     = sT * max(0, p(v) - q(v))
-//              delta = (dT - dD) c - log2(sT / sD)          (> 0 iff p(v) > q(v))
-// The form 2^{aT}(1 - 2^{-delta}) has no cancellation (see resid_factor).
-// Explicit round-to-nearest operations (no contraction) keep the arithmetic
-// identical in the tail units and in the final rescan.
-// ---------------------------------------------------------------------------
-struct TailConsts {
-  float mT, mD, c_hi, c_lo, lam_hi, lam_lo;
-  int residual;
-};
-
-// max(0, 1 - 2^{-d}) without cancellation and without branches.  With
-// eh = 2^{-d/2} (ex2) and x = d ln2 / 2:
-//   d >= 1.4:  1 - eh^2                                   (>= 0.62, nothing cancels)
-//   d <  1.4:  1 - e^{-2x} = 2 sinh(x) e^{-x} = x (2 + x^2/3 + x^4/60 + x^6/2520) eh
-// (|x| < 0.49 there, so the first omitted term is below 1e-8 relative).  For
-// d <= 0 the second form is <= 0 and the clamp returns 0.  Both forms are
-// evaluated and one is selected, so the packed version below can share every
-// instruction between the two elements of a pair.
-__device__ __forceinline__ float resid_factor(float d) {
-  const float eh = ex2(__fmul_rn(d, -0.5f));
-  const float A = __fsub_rn(1.f, __fmul_rn(eh, eh));
-  const float x = __fmul_rn(d, 0.346573590279972655f);
-  const float xx = __fmul_rn(x, x);
-  float p = __fmaf_rn(xx, 1.f / 2520.f, 1.f / 60.f);
-  p = __fmaf_rn(xx, p, 1.f / 3.f);
-  p = __fmaf_rn(xx, p, 2.f);
-  const float Bv = __fmul_rn(__fmul_rn(x, p), eh);
-  return fmaxf(d >= 1.4f ? A : Bv, 0.f);
-}
-
-// resid_factor on both elements of a pair, with every operation rounding as
-// in the scalar version (bit-identical results).
-__device__ __forceinline__ f2_t resid_factor2(f2_t d) {
-  const f2_t hd = f2mul(d, f2(-0.5f, -0.5f));
-  const f2_t eh = f2(ex2(f2lo(hd)), ex2(f2hi(hd)));
-  const f2_t A = f2sub(f2(1.f, 1.f), f2mul(eh, eh));
-  const f2_t x = f2mul(d, f2(0.346573590279972655f, 0.346573590279972655f));
-  const f2_t xx = f2mul(x, x);
-  f2_t p = f2fma(xx, f2(1.f / 2520.f, 1.f / 2520.f), f2(1.f / 60.f, 1.f / 60.f));
-  p = f2fma(xx, p, f2(1.f / 3.f, 1.f / 3.f));
-  p = f2fma(xx, p, f2(2.f, 2.f));
-  const f2_t Bv = f2mul(f2mul(x, p), eh);
-  const float r0 = fmaxf(f2lo(d) >= 1.4f ? f2lo(A) : f2lo(Bv), 0.f);
-  const float r1 = fmaxf(f2hi(d) >= 1.4f ? f2hi(A) : f2hi(Bv), 0.f);
-  return f2(r0, r1);
-}
-
-__device__ __forceinline__ float tail_weight(float zT, float zD, const TailConsts& k) {
-  const float dT = __fsub_rn(zT, k.mT);
-  const float eT = ex2(__fmul_rn(dT, k.c_hi));
-  if (!k.residual) return eT;
-  const float dD = __fsub_rn(zD, k.mD);
-  const float D = __fsub_rn(dT, dD);
-  const float delta = __fadd_rn(__fmaf_rn(D, k.c_hi, -k.lam_hi), __fmaf_rn(D, k.c_lo, -k.lam_lo));
-  return __fmul_rn(eT, resid_factor(delta));
-}
-
-// The same weights for an element pair with packed f32x2 arithmetic: every
-// operation rounds exactly as the scalar version above.
-__device__ __forceinline__ f2_t tail_weight2(f2_t zT, f2_t zD, const TailConsts& k) {
-  const f2_t dT = f2sub(zT, f2(k.mT, k.mT));
-  const f2_t aT = f2mul(dT, f2(k.c_hi, k.c_hi));
-  const f2_t eT = f2(ex2(f2lo(aT)), ex2(f2hi(aT)));
-  if (!k.residual) return eT;
-  const f2_t dD = f2sub(zD, f2(k.mD, k.mD));
-  const f2_t D = f2sub(dT, dD);
-  const f2_t delta = f2add(f2fma(D, f2(k.c_hi, k.c_hi), f2(-k.lam_hi, -k.lam_hi)),
-                           f2fma(D, f2(k.c_lo, k.c_lo), f2(-k.lam_lo, -k.lam_lo)));
-  return f2mul(eT, resid_factor2(delta));
-}
-
-// The VEC weights of one lane's vector, in element order.
-template <class E, int VEC>
-__device__ __forceinline__ void lane_weights(const Raw<E, VEC>& zt, const Raw<E, VEC>& zd,
-                                             const TailConsts& k, float (&w)[VEC]) {
-  if constexpr (VEC == 1) {
-    w[0] = tail_weight(elem(zt, 0), elem(zd, 0), k);
-  } else {
-#pragma unroll
-    for (int p = 0; p < VEC / 2; ++p) {
-      const f2_t wp = tail_weight2(elem_pair<E, VEC>(zt, p), elem_pair<E, VEC>(zd, p), k);
-      w[2 * p] = f2lo(wp);
-      w[2 * p + 1] = f2hi(wp);
-    }
-  }
-}
-
 template <class E>
 __device__ __forceinline__ const typename E::storage* target_row(const SampleArgs& a, int b, int r) {
   return (const typename E::storage*)a.target + ((size_t)b * (a.K + 1) + r) * (size_t)a.V;
@@ -413,16 +321,6 @@ __device__ __noinline__ void stats_finisher(const SampleArgs& a, int b, FinIn pr
 // starting at v0 + q * 32 * VEC; its mass is the butterfly sum over lanes of
 // each lane's sequential sum of its VEC weights.
 // ---------------------------------------------------------------------------
-template <class E, int VEC>
-__device__ __forceinline__ float lane_mass(const Raw<E, VEC>& zt, const Raw<E, VEC>& zd,
-                                           const TailConsts& k) {
-  float w[VEC];
-  lane_weights<E, VEC>(zt, zd, k, w);
-  float ls = 0.f;
-#pragma unroll
-  for (int q = 0; q < VEC; ++q) ls = __fadd_rn(ls, w[q]);
-  return ls;
-}
 
 // One warp: the pieces of tail slice s of the tail row(s) into the workspace
 // and the slice's mass, the fp32 sum of its pieces in order (every lane).
@@ -652,56 +550,6 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
 // ---------------------------------------------------------------------------
 // statistics unit (one warp)
 // ---------------------------------------------------------------------------
-template <class E, int VEC>
-__device__ __forceinline__ void load_batch(Raw<E, VEC> (&z)[kUnroll], const typename E::storage* row,
-                                           int e, int v1) {
-  constexpr int STEPW = 32 * VEC;
-#pragma unroll
-  for (int u = 0; u < kUnroll; ++u) z[u] = load_raw<E, VEC>(row, e + u * STEPW, v1);
-}
-
-// One batch into the lane's running (m, s): the batch max first, one rescale
-// if it rose, then 2^{(z - m) c} summed with packed pair arithmetic.
-template <class E, int VEC, bool ENT>
-__device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], float& m, f2_t& acc,
-                                            f2_t& tacc, float cc) {
-  const float bm = batch_max<E, VEC>(z);
-  if (bm > m) {
-    const float delta = (m - bm) * cc;
-    const float f = ex2(delta);
-    if constexpr (ENT) {
-      // t' = 2^delta (t + delta s); an empty accumulator stays empty
-      tacc = m == neg_inf() ? f2(0.f, 0.f) : f2mul(f2(f, f), f2fma(f2(delta, delta), acc, tacc));
-    }
-    acc = f2mul(acc, f2(f, f));
-    m = bm;
-  }
-  const float base = (m == neg_inf()) ? 0.f : m;
-  if constexpr (VEC == 1) {
-    float lo = f2lo(acc), tlo = f2lo(tacc);
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u) {
-      const float d = (z[u].f - base) * cc;
-      const float e = ex2(d);
-      lo += e;
-      if constexpr (ENT) tlo = fmaf(e, fmaxf(d, -126.f), tlo);
-    }
-    acc = f2(lo, f2hi(acc));
-    if constexpr (ENT) tacc = f2(tlo, f2hi(tacc));
-  } else {
-    const f2_t b2 = f2(base, base), c2 = f2(cc, cc);
-#pragma unroll
-    for (int u = 0; u < kUnroll; ++u)
-#pragma unroll
-      for (int p = 0; p < VEC / 2; ++p) {
-        if constexpr (ENT)
-          f2_exp_acc_ent(acc, tacc, elem_pair<E, VEC>(z[u], p), b2, c2);
-        else
-          f2_exp_acc(acc, elem_pair<E, VEC>(z[u], p), b2, c2);
-      }
-  }
-}
-
 // Statistics slice s of row r of sequence b: the row's (m, s) over the slice,
 // then the row's ticket.  Returns the ticket's old value (lane 0).  Kept out
 // of line so that the stream loop has the register file to itself.

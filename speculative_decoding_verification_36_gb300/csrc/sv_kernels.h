@@ -149,6 +149,40 @@ struct WsLayout {
 WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent);
 WsLayout greedy_workspace(int B, int R, int CU);
 
+// Stochastic tree verification (tree_sample_kernel.cu).  Rows per sequence:
+// target rows 0..N (row 0 the root, row i+1 node i), then draft rows 0..N.
+struct TreeSampleArgs {
+  const void* target;
+  const void* draft;
+  const int32_t* tokens;   // [B, N]
+  const int32_t* parents;  // [B, N]
+  int B, N, V;
+  int RR;   // rows per sequence, both models: 2 (N + 1)
+  int SL;   // statistics slice length in elements
+  int CS;   // statistics slices per row
+  long long F;  // statistics slices in all: B * RR * CS
+  int C;        // CTAs (one cluster) per sequence in the walk: 1, 2, 4 or 8
+  int chunk;    // elements per warp of the cluster in the walk passes (whole warp steps)
+  float c_hi, c_lo;  // log2(e) / temperature as a float pair
+  double c64;
+  uint64_t seed;
+  int32_t* out_path;  // [B, N+1]
+  int32_t* out_len;   // [B]
+  // workspace, filled with all-ones bytes: row tickets start at -1, part and
+  // rowstat hold the "not yet written" marker
+  int* rowticket;    // [B * RR] (kTicketStride apart)
+  float2* part;      // [B * RR, CS] per-slice (m, s)
+  float2* rowstat;   // [B * RR] merged (m, s)
+  unsigned* status;
+};
+constexpr int kWalkThreads = 512;  // threads per walk CTA (a cluster of C per sequence)
+WsLayout tree_sample_workspace(int B, int RR, int CS);
+void tree_sample_bind_workspace(TreeSampleArgs& a, void* ws);
+cudaError_t launch_tree_sample(const TreeSampleArgs& a, bool bf16, bool vec, int stats_grid, cudaStream_t s);
+int tree_stats_blocks_per_sm(bool bf16, bool vec);
+int tree_walk_clusters(bool bf16, bool vec, int C);
+
+
 // Bind workspace pointers into the argument blocks.
 void sample_bind_workspace(SampleArgs& a, void* ws);
 void greedy_bind_workspace(GreedyArgs& a, void* ws);

@@ -4,7 +4,9 @@
 
 Builds the library if needed, generates the preset's synthetic inputs on
 cuda:0 and makes N calls of the entry point the preset exercises
-(spec_verify for c1-c4, spec_tree_verify_greedy for c5), then synchronises.
+(spec_verify for c1-c4, spec_tree_verify_greedy for c5,
+spec_tree_verify_sampling at tau = 1 on the c5 tree for c5s), then
+synchronises.
 """
 from __future__ import annotations
 
@@ -14,20 +16,25 @@ import sys
 
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
-    ap.add_argument("preset", choices=["c1", "c2", "c3", "c4", "c5"])
+    ap.add_argument("preset", choices=["c1", "c2", "c3", "c4", "c5", "c5s"])
     ap.add_argument("--batch", type=int, default=0, help="sequences (default: the preset's B)")
     ap.add_argument("--calls", type=int, default=3)
     args = ap.parse_args(argv)
 
     import torch
 
-    from . import build, spec_get_status, spec_tree_verify_greedy, spec_verify
+    from . import build, spec_get_status, spec_tree_verify_greedy, spec_tree_verify_sampling, spec_verify
     from . import workloads as wl
 
     build.build()
     dev = torch.device("cuda", 0)
-    p = wl.preset(args.preset, B=args.batch) if args.batch else wl.preset(args.preset)
-    if args.preset == "c5":
+    name = "c5" if args.preset == "c5s" else args.preset
+    p = wl.preset(name, B=args.batch) if args.batch else wl.preset(name)
+    if args.preset == "c5s":
+        x = wl.make_tree_sampling(p, 1.0, device=dev, seed=0)
+        for i in range(args.calls):
+            spec_tree_verify_sampling(x["target"], x["draft"], x["tokens"], x["parents"], 1.0, i)
+    elif args.preset == "c5":
         x = wl.make_tree(p, device=dev, seed=0)
         for _ in range(args.calls):
             spec_tree_verify_greedy(x["target"], x["tokens"], x["parents"])

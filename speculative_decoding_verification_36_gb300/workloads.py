@@ -23,6 +23,11 @@ them):
       V=128256, bf16: target N(0, 4^2) for the root and every node; the two
       children of a node carry the top-2 ids of (that node's row + N(0, 1^2)).
 
+The stochastic tree workload (spec_tree_verify_sampling) takes a tree preset's
+shapes and a temperature: target N(0, 4^2) for the root and every node, draft
+= target + N(0, 1.5^2) row by row, and the children of a node drawn i.i.d.
+(with replacement) from softmax(that node's draft row / tau).
+
 Logits are generated in fp32 and rounded to the preset's dtype before the
 draft tokens are drawn, so tokens come from exactly the bits the verifier
 reads.  Drafted chain tokens are drawn from softmax(draft / tau).
@@ -168,3 +173,30 @@ def make_tree(p: TreePreset, device="cpu", seed: int | None = None, parents=None
             tokens[:, node] = top[:, j]
     parents_b = par.to(device).unsqueeze(0).expand(B, N).contiguous()
     return dict(target=target, tokens=tokens.contiguous(), parents=parents_b)
+
+
+def make_tree_sampling(p: TreePreset, temperature: float = 1.0, device="cpu", seed: int | None = None,
+                       parents=None):
+    """Inputs of the stochastic tree workload: dict(target, draft [B,N+1,V],
+    tokens, parents [B,N], temperature).  ``parents`` overrides the complete
+    binary tree with any BFS-ordered parent list."""
+    seed = p.seed if seed is None else seed
+    g = _gen(device, "c5s", seed)
+    par = complete_binary_parents(p.depth) if parents is None else torch.as_tensor(
+        parents, dtype=torch.int32)
+    N = int(par.numel())
+    B, V = p.B, p.V
+    target = (4.0 * _randn((B, N + 1, V), g, device)).to(p.dtype).contiguous()
+    draft = (target.float() + 1.5 * _randn((B, N + 1, V), g, device)).to(p.dtype).contiguous()
+    tokens = torch.empty((B, N), dtype=torch.int32, device=device)
+    children = {}
+    for i, pr in enumerate(par.tolist()):
+        children.setdefault(pr, []).append(i)
+    for pr, kids in children.items():
+        probs = torch.softmax(draft[:, pr + 1].float() / temperature, dim=-1)
+        drawn = torch.multinomial(probs, len(kids), replacement=True, generator=g).to(torch.int32)
+        for j, node in enumerate(kids):
+            tokens[:, node] = drawn[:, j]
+    parents_b = par.to(device).unsqueeze(0).expand(B, N).contiguous()
+    return dict(target=target, draft=draft, tokens=tokens.contiguous(), parents=parents_b,
+                temperature=float(temperature))

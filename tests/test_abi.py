@@ -91,6 +91,29 @@ def test_tree_checks(lib):
     assert f(FAKE, FAKE, FAKE, 0, 3, 8, FAKE, FAKE, FAKE, None) == _lib.SPEC_OK
 
 
+@pytest.mark.parametrize("fn", ["spec_tree_verify_sampling_f32", "spec_tree_verify_sampling_bf16"])
+def test_tree_sampling_checks(lib, fn):
+    f = getattr(lib, fn)
+
+    def call(t=FAKE, d=FAKE, tok=FAKE, par=FAKE, B=1, N=3, V=8, tau=1.0, path=FAKE, ln=FAKE):
+        return f(t, d, tok, par, B, N, V, tau, 0, path, ln, None)
+
+    assert call(t=None) == _lib.SPEC_ERR_NULL
+    assert call(d=None) == _lib.SPEC_ERR_NULL
+    assert call(tok=None) == _lib.SPEC_ERR_NULL
+    assert call(par=None) == _lib.SPEC_ERR_NULL
+    assert call(path=None) == _lib.SPEC_ERR_NULL
+    assert call(ln=None) == _lib.SPEC_ERR_NULL
+    assert call(tok=None, par=None, N=0, B=0) == _lib.SPEC_OK  # no nodes: no tree arrays needed
+    for tau in (0.0, -1.0, math.nan, 1e-35):
+        assert call(tau=tau) == _lib.SPEC_ERR_TEMPERATURE
+    assert call(N=1025) == _lib.SPEC_ERR_SHAPE
+    assert call(N=-1) == _lib.SPEC_ERR_SHAPE
+    assert call(V=0) == _lib.SPEC_ERR_SHAPE
+    assert call(B=-1) == _lib.SPEC_ERR_SHAPE
+    assert call(B=0) == _lib.SPEC_OK
+
+
 def test_python_binding_rejects_cpu_tensors():
     import torch
     import speculative_decoding_verification_36_gb300 as sv

@@ -47,7 +47,7 @@ struct DeviceState {
   int occ_greedy[2][2] = {{0, 0}, {0, 0}};
   int occ_tree[2][2] = {{0, 0}, {0, 0}};
   int occ_tree_stats[2][2] = {{0, 0}, {0, 0}};
-  int walk_clusters[2][2][4] = {};  // [bf16][vec][log2 C]: walk clusters resident at once
+  int walk_clusters[2][2][5] = {};  // [bf16][vec][log2 C]: walk clusters resident at once
 };
 
 constexpr int kMaxDevices = 64;
@@ -79,7 +79,7 @@ int get_device_state(DeviceState** out) {
         d.occ_greedy[bf][v] = sv::greedy_blocks_per_sm(bf, v);
         d.occ_tree[bf][v] = sv::tree_blocks_per_sm(bf, v);
         d.occ_tree_stats[bf][v] = sv::tree_stats_blocks_per_sm(bf, v);
-        for (int c = 0; c < 4; ++c) d.walk_clusters[bf][v][c] = sv::tree_walk_clusters(bf, v, 1 << c);
+        for (int c = 0; c < 5; ++c) d.walk_clusters[bf][v][c] = sv::tree_walk_clusters(bf, v, 1 << c);
       }
     d.init = true;
   }
@@ -374,11 +374,11 @@ int tree_sample_impl(bool bf16, const void* target, const void* draft, const int
   static const int slice_bytes = env_int("SPECVERIFY_SLICE_BYTES", 12288);
   choose_slices(V, vec_elems, esz, slice_bytes, &a.SL, &a.CS, &CU);
   a.F = (long long)B * a.RR * a.CS;
-  // walk: the widest cluster (8, 4, 2 CTAs) for which every sequence's
+  // walk: the widest cluster (16, 8, 4, 2 CTAs) for which every sequence's
   // cluster is resident at once, else one CTA per sequence; each pass gives
   // every warp of the cluster one contiguous run of whole warp steps
   a.C = 1;
-  for (int c = 3; c >= 1; --c)
+  for (int c = 4; c >= 1; --c)
     if (B <= d->walk_clusters[bf16][vec][c]) {
       a.C = 1 << c;
       break;

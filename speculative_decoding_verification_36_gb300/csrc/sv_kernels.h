@@ -161,7 +161,7 @@ struct TreeSampleArgs {
   int SL;   // statistics slice length in elements
   int CS;   // statistics slices per row
   long long F;  // statistics slices in all: B * RR * CS
-  int C;        // CTAs (one cluster) per sequence in the walk: 1, 2, 4 or 8
+  int C;        // CTAs (one cluster) per sequence in the walk: 1, 2, 4, 8 or 16
   int chunk;    // elements per warp of the cluster in the walk passes (whole warp steps)
   float c_hi, c_lo;  // log2(e) / temperature as a float pair
   double c64;

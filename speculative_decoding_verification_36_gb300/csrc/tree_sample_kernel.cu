@@ -110,10 +110,11 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) tree_stats_kernel(const 
 constexpr int kWalkWarps = kWalkThreads / 32;
 constexpr int kWalkSteps = 128;  // step sums kept per warp for the final search
 constexpr int kWalkU = 4;        // warp steps per load group
+constexpr int kMaxWalkCluster = 16;  // CTAs per sequence at most (a non-portable cluster size)
 
-// Mass of one warp's chunk [v0, v1) of the current weights: the fp64 sum, in
-// step order, of the fp32 step sums (each the butterfly sum of the lanes'
-// element-order sums).  Step sums 0 .. kWalkSteps-1 are also left in `steps`
+// Mass of one warp's chunk [v0, v1) of the current weights (in lane 0): the
+// fp64 sum, in step order, of the fp32 step sums (each the butterfly sum of
+// the lanes' element-order sums).  Step sums 0 .. kWalkSteps-1 are also left in `steps`
 // for chunk_select.  Loads run kWalkU steps ahead of the arithmetic.
 template <class E, int VEC>
 __device__ double chunk_mass(const typename E::storage* rowT, const typename E::storage* rowD, int v0,
@@ -139,7 +140,7 @@ __device__ double chunk_mass(const typename E::storage* rowT, const typename E::
     for (int i = 0; i < U; ++i) {
       if (q0 + i < nsteps) {
         const float sq = warp_sum(lane_mass<E, VEC>(t[i], d[i], k));
-        total += (double)sq;
+        if (lane == 0) total += (double)sq;  // fp64 in one lane: the result is lane 0's
         if (lane == 0 && q0 + i < kWalkSteps) steps[q0 + i] = sq;
       }
     }
@@ -262,36 +263,29 @@ __device__ int chunk_select(const typename E::storage* rowT, const typename E::s
 }
 
 struct WalkShared {
-  double A, B, L;      // residual state of the current node
+  // residual state of the current node (thread 0 keeps it; fp64 stays in thread 0)
+  double A, B, L, lam, sT;
+  float mT, mD;        // row maxima of the current node's target and draft rows
+  float lam_hi, lam_lo;  // log2(sT / sD) + L of the next pass, as a float pair
+  int residual;        // the next pass weighs the residual (1) or P itself (0)
   int k;               // rejections at the current node
   int u;               // current node (-1: the root)
   int len;             // path entries written
   int decision;        // 1: accept the child under test
-  int pick;            // warp of the cluster whose chunk holds the final draw (-1: none)
+  int current;         // the last pass's masses are those of the current distribution
+  int pick;            // warp of the cluster whose chunk holds the final draw (-1: none here)
   int tok_out;         // rank 0 only: the drawn token, written by the picking CTA
   double pick_before;
   double theta;
 };
 
-// Residual constants of the current node with the threshold moved by L.
-__device__ __forceinline__ TailConsts walk_consts(float mT, float mD, const TreeSampleArgs& a, double lam,
-                                                  double L, bool residual) {
-  TailConsts k;
-  k.mT = mT;
-  k.mD = mD;
-  k.c_hi = a.c_hi;
-  k.c_lo = a.c_lo;
-  const double shifted = lam + L;
-  k.lam_hi = (float)shifted;
-  k.lam_lo = (float)(shifted - (double)k.lam_hi);
-  k.residual = residual ? 1 : 0;
-  return k;
-}
-
 // One cluster of a.C CTAs per sequence.  Every CTA runs the same control
-// flow: after each pass over the row pair the warp masses of all CTAs are read
-// through distributed shared memory in the same order, so every CTA holds the
-// same sums and takes the same decisions; rank 0 alone writes the outputs.
+// flow: after each pass over the row pair every CTA pushes its fp64 mass into
+// the shared memory of all CTAs of the cluster, so after the cluster barrier
+// every CTA holds the same per-CTA masses, forms the same sums in the same
+// order and takes the same decisions; rank 0 alone writes the outputs.  All
+// fp64 arithmetic runs in one thread (or one lane per warp): the fp64 rate of
+// the part is a small fraction of its fp32 rate.
 template <class E, int VEC>
 __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid_constant__ TreeSampleArgs a) {
   using S = typename E::storage;
@@ -299,7 +293,11 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
   __shared__ WalkShared sh;
   __shared__ int s_par[kMaxTreeNodes];
   __shared__ int s_tok[kMaxTreeNodes];
-  __shared__ double s_wm[2][NW];
+  __shared__ float s_zt[kMaxTreeNodes];  // node i's token: its logit in the parent's target row
+  __shared__ float s_zd[kMaxTreeNodes];  // ... and in the parent's draft row
+  __shared__ float s_u[kMaxTreeNodes];   // node i's acceptance uniform (exact in fp32)
+  __shared__ double s_wm[NW];                 // this CTA's warp masses of the last pass
+  __shared__ double s_cta[2][kMaxWalkCluster];  // every CTA's mass, pushed by its owner
   __shared__ float s_steps[NW][kWalkSteps];
   cg::cluster_group cluster = cg::this_cluster();
   const int C = a.C;
@@ -332,6 +330,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
     }
     return;
   }
+  // every node's decision inputs at once, off the walk's serial path
+  for (int i = tid; i < N; i += kWalkThreads) {
+    const int x = s_tok[i], pr = s_par[i];
+    s_zt[i] = E::load1(tree_row<E>(a, b, pr + 1) + x);
+    s_zd[i] = E::load1(tree_row<E>(a, b, N1 + pr + 1) + x);
+    s_u[i] = (float)uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0);
+  }
   if (tid == 0) {
     sh.u = -1;
     sh.len = 0;
@@ -342,19 +347,33 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
   const int gw = rank * NW + warp;  // warp index within the cluster
   const int v0 = (int)min((long long)gw * a.chunk, (long long)a.V);
   const int v1 = (int)min((long long)v0 + a.chunk, (long long)a.V);
-  int buf = 0;  // s_wm buffer of the next pass
-  // one pass: every warp's chunk mass, then the cluster-wide sum (fp64, in
-  // rank-major warp order) in thread 0 of every CTA
-  auto pass = [&](const S* rowT, const S* rowD, const TailConsts& k) -> double {
+  int buf = 0;  // s_cta buffer of the next pass
+  // One pass with the constants in sh: returns (in thread 0) the cluster's
+  // mass, the fp64 sum of the per-CTA masses in rank order, each the fp64 sum
+  // of its warp masses in warp order.
+  auto pass = [&](const S* rowT, const S* rowD) -> double {
+    TailConsts k;
+    k.mT = sh.mT;
+    k.mD = sh.mD;
+    k.c_hi = a.c_hi;
+    k.c_lo = a.c_lo;
+    k.lam_hi = sh.lam_hi;
+    k.lam_lo = sh.lam_lo;
+    k.residual = sh.residual;
     const double wm = chunk_mass<E, VEC>(rowT, rowD, v0, v1, k, s_steps[warp]);
-    if (lane == 0) s_wm[buf][warp] = wm;
+    if (lane == 0) s_wm[warp] = wm;
+    __syncthreads();
+    if (warp == 0) {
+      double cs = 0.0;
+      if (lane == 0)
+        for (int j = 0; j < NW; ++j) cs += s_wm[j];
+      cs = __shfl_sync(0xffffffffu, cs, 0);
+      if (lane < C) *cluster.map_shared_rank(&s_cta[buf][rank], lane) = cs;
+    }
     cluster.sync();
     double sum = 0.0;
     if (tid == 0)
-      for (int r = 0; r < C; ++r) {
-        const double* w = cluster.map_shared_rank(&s_wm[buf][0], r);
-        for (int j = 0; j < NW; ++j) sum += w[j];
-      }
+      for (int r = 0; r < C; ++r) sum += s_cta[buf][r];
     buf ^= 1;  // the next pass writes the other buffer while this one may still be read
     return sum;
   };
@@ -365,37 +384,45 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
     const int row = u + 1;
     const S* rowT = tree_row<E>(a, b, row);
     const S* rowD = tree_row<E>(a, b, N1 + row);
-    const float2 st = __ldcg(rs + row), sd = __ldcg(rs + N1 + row);
-    const double lam = log2((double)st.y) - log2((double)sd.y);  // log2(sT / sD)
     if (tid == 0) {
+      const float2 st = __ldcg(rs + row), sd = __ldcg(rs + N1 + row);
+      sh.mT = st.x;
+      sh.mD = sd.x;
+      sh.sT = (double)st.y;
+      sh.lam = log2((double)st.y) - log2((double)sd.y);  // log2(sT / sD)
       sh.k = 0;
       sh.A = 0.0;
       sh.B = 1.0;
       sh.L = 0.0;
+      sh.current = 0;
     }
     __syncthreads();
     bool moved = false;
-    bool masses_current = false;  // the last pass's buffer holds the current distribution's masses
     for (int c = 0; c < N && !moved; ++c) {
       if (s_par[c] != u) continue;
       if (tid == 0) {
         const int x = s_tok[c];
-        const float zT = E::load1(rowT + x), zD = E::load1(rowD + x);
+        const float zT = s_zt[c], zD = s_zd[c];
         bool accept;
         if (zD == neg_inf()) {
           accept = true;  // Q(x) = 0
         } else {
-          const double delta = (((double)zT - st.x) - ((double)zD - sd.x)) * a.c64 - lam;
+          const double delta = (((double)zT - sh.mT) - ((double)zD - sh.mD)) * a.c64 - sh.lam;
           const double rho = exp2(delta);
           const double g = sh.k == 0 ? rho : fmax(0.0, rho - sh.A) / sh.B;  // P_k(x) / Q(x)
-          const double r = uniform_draw(a.seed, (uint64_t)b, (uint64_t)c, 0);
-          accept = g >= 1.0 || r < g;
+          accept = g >= 1.0 || (double)s_u[c] < g;
         }
         sh.decision = accept;
         if (accept) {
           if (rank == 0) path[sh.len] = x;
           sh.len += 1;
           sh.u = c;
+        } else {
+          // constants of the pass for B_{k+1}: threshold moved by L_{k+1} = log2(A_k + B_k)
+          const double shifted = sh.lam + log2(sh.A + sh.B);
+          sh.lam_hi = (float)shifted;
+          sh.lam_lo = (float)(shifted - (double)sh.lam_hi);
+          sh.residual = 1;
         }
       }
       __syncthreads();
@@ -404,61 +431,91 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
         break;
       }
       // rejected: the next residual's mass, B_{k+1} = sum P0 (1 - 2^{-(delta - L)})_+
-      const double A1 = sh.A + sh.B;
-      const double L1 = log2(A1);
-      const double sum = pass(rowT, rowD, walk_consts(st.x, sd.x, a, lam, L1, true));
+      const double sum = pass(rowT, rowD);
       if (tid == 0) {
-        const double Bk = sum / (double)st.y;  // weights are sT * P0 (...)
+        const double Bk = sum / sh.sT;  // weights are sT * P0 (...)
+        sh.current = Bk > 0.0;
         if (Bk > 0.0) {  // else only rounding emptied the residual: keep P
+          const double A1 = sh.A + sh.B;
+          sh.L = log2(A1);
           sh.A = A1;
           sh.B = Bk;
-          sh.L = L1;
           sh.k += 1;
         }
       }
       __syncthreads();
-      masses_current = sh.k > 0 && sh.L == L1;
     }
     if (moved) continue;
 
     // no child accepted (or a leaf): one token from the current distribution
-    const TailConsts k = walk_consts(st.x, sd.x, a, lam, sh.L, sh.k > 0);
-    if (!masses_current) pass(rowT, rowD, k);
-    const int last = buf ^ 1;  // buffer of the pass that matches k
+    if (!sh.current) {
+      if (tid == 0) {
+        const double shifted = sh.lam + sh.L;
+        sh.lam_hi = (float)shifted;
+        sh.lam_lo = (float)(shifted - (double)sh.lam_hi);
+        sh.residual = sh.k > 0;
+      }
+      __syncthreads();
+      pass(rowT, rowD);
+    }
+    const int last = buf ^ 1;  // buffer of the pass that matches the current distribution
     if (tid == 0) {
       double Z = 0.0;
-      for (int r = 0; r < C; ++r) {
-        const double* w = cluster.map_shared_rank(&s_wm[last][0], r);
-        for (int j = 0; j < NW; ++j) Z += w[j];
-      }
+      for (int r = 0; r < C; ++r) Z += s_cta[last][r];
       const double theta = uniform_draw(a.seed, (uint64_t)b, (uint64_t)row, 1) * Z;
-      // the warp whose chunk holds the crossing (positive mass only)
+      // the CTA, then the warp, whose chunk holds the crossing (positive mass only)
       double run = 0.0, last_before = 0.0;
-      int pick = -1, lastw = -1;
-      for (int r = 0; r < C && pick < 0; ++r) {
-        const double* w = cluster.map_shared_rank(&s_wm[last][0], r);
+      int pr = -1, lastr = -1;
+      for (int r = 0; r < C; ++r) {
+        const double m = s_cta[last][r];
+        if (!(m > 0.0)) continue;
+        if (run + m > theta) {
+          pr = r;
+          break;
+        }
+        lastr = r;
+        last_before = run;
+        run += m;
+      }
+      if (pr < 0) {
+        pr = lastr;
+        run = last_before;
+      }
+      int pick = -1;
+      if (pr == rank) {
+        double wrun = run, wlast_before = run;
+        int lastw = -1;
         for (int j = 0; j < NW; ++j) {
-          const double m = w[j];
+          const double m = s_wm[j];
           if (!(m > 0.0)) continue;
-          if (run + m > theta) {
-            pick = r * NW + j;
+          if (wrun + m > theta) {
+            pick = j;
             break;
           }
-          lastw = r * NW + j;
-          last_before = run;
-          run += m;
+          lastw = j;
+          wlast_before = wrun;
+          wrun += m;
         }
-      }
-      if (pick < 0) {
-        pick = lastw;
-        run = last_before;
+        if (pick < 0) {
+          pick = lastw;
+          wrun = wlast_before;
+        }
+        run = wrun;
       }
       sh.pick = pick;
       sh.pick_before = run;
       sh.theta = theta;
     }
     __syncthreads();
-    if (gw == sh.pick) {
+    if (warp == sh.pick) {
+      TailConsts k;
+      k.mT = sh.mT;
+      k.mD = sh.mD;
+      k.c_hi = a.c_hi;
+      k.c_lo = a.c_lo;
+      k.lam_hi = sh.lam_hi;
+      k.lam_lo = sh.lam_lo;
+      k.residual = sh.residual;
       const int tok = chunk_select<E, VEC>(rowT, rowD, v0, v1, k, sh.theta, sh.pick_before, s_steps[warp]);
       if (lane == 0) *cluster.map_shared_rank(&sh.tok_out, 0) = tok;
     }
@@ -560,6 +617,12 @@ static int walk_clusters_t(int C) {
   cfg.attrs = at;
   cfg.numAttrs = 1;
   int n = 0;
+  if (C > 8 &&
+      cudaFuncSetAttribute(tree_walk_kernel<E, VEC>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) !=
+          cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
   if (cudaOccupancyMaxActiveClusters(&n, tree_walk_kernel<E, VEC>, &cfg) != cudaSuccess) {
     cudaGetLastError();
     return 0;

@@ -300,7 +300,9 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.TL = a.P * step;
   a.TC = (int)(((long long)V + a.TL - 1) / a.TL);
   a.F = B * a.R * a.CS;
-  a.div_seq = sv::make_fastdiv((uint32_t)(a.R * a.CS));
+  a.FP = K * B * 2 * a.CS;
+  a.div_pos = sv::make_fastdiv((uint32_t)(B * 2 * a.CS));
+  a.div_pair = sv::make_fastdiv((uint32_t)(2 * a.CS));
   a.div_cs = sv::make_fastdiv((uint32_t)a.CS);
   a.div_tc = sv::make_fastdiv((uint32_t)a.TC);
   const int grid = grid_for((a.F + sv::kSlices - 1) / sv::kSlices, capacity);

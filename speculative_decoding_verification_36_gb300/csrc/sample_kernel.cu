@@ -119,49 +119,165 @@ __device__ __noinline__ SeqInfo read_decision(const SampleArgs& a, int pos) {
 }
 
 // ---------------------------------------------------------------------------
-// Inputs of the statistics finisher for one chunk of 32 positions (lane i:
-// position i0 + i): target row i's and draft row i's (m, s), the drafted token
-// and the logits at it.  One round of independent relaxed loads; slots still
-// holding the marker are waited for by the finisher.
+// Position units.  Unit (b, i) is the row pair of draft position i of
+// sequence b (target row i and draft row i), or target row K alone for i = K.
+// The warp that takes a unit's last slice ticket merges the slice partials of
+// its rows, tests position i and records the verdict in the sequence's
+// resolution word.  A sequence is decided as soon as positions 0..n are
+// resolved with 0..n-1 accepted and n rejected (or 0..K resolved and all K
+// accepted): the rows of the positions after n never delay the decision.
+// Its outputs are committed once every row has also been checked for bad data.
 // ---------------------------------------------------------------------------
-struct FinIn {
-  uint2 st, sd;
-  int xi;
-  float zT, zD;
-};
+constexpr int kVerdictAccept = 0;
+constexpr int kVerdictReject = 1;
+constexpr int kVerdictBad = 2;
+constexpr int kMaskMaxK = 31;       // resolution words hold positions 0..31 (K <= 31)
+constexpr int kUnitBad = 0x10000;   // added to the sequence's unit count by a unit with bad data
+constexpr uint32_t kResultBad = 0x7ffffffeu;  // result slot field: no value (never kMarker)
 
-__device__ __forceinline__ FinIn load_fin_inputs(const SampleArgs& a, int b, int i0) {
-  const int K = a.K, R = a.R;
-  const int i = i0 + (threadIdx.x & 31);
-  const bool hasT = i <= K, hasD = i < K;
-  const float2* rs = a.rowstat + (size_t)b * R;
-  const float* zx = a.zx + (size_t)b * R;
-  FinIn in;
-  in.st = hasT ? ld_relaxed_u2(rs + i) : make_uint2(0u, 0u);
-  in.sd = hasD ? ld_relaxed_u2(rs + K + 1 + i) : make_uint2(0u, 0u);
-  in.xi = hasD ? __ldg(a.tokens + (size_t)b * K + i) : 0;
-  in.zT = hasD ? ld_relaxed_f32(zx + i) : 0.f;
-  in.zD = hasD ? ld_relaxed_f32(zx + K + 1 + i) : 0.f;
-  return in;
+__device__ __forceinline__ int unit_slices(const SampleArgs& a, int i) { return i < a.K ? 2 * a.CS : a.CS; }
+
+// Decided count n for the set of resolved / rejected positions `set` (bit i:
+// position i resolved; bit 32 + i: position i rejected, i < K), or -1 while
+// the prefix that fixes n is incomplete.
+__device__ __forceinline__ int decided_n(unsigned long long set, int K) {
+  const unsigned rej = K > 0 ? (unsigned)(set >> 32) & (0xffffffffu >> (32 - K)) : 0u;
+  const int r = rej ? __ffs(rej) - 1 : K;
+  const unsigned long long need = (2ull << r) - 1ull;
+  return (set & need) == need ? r : -1;
 }
 
-// ---------------------------------------------------------------------------
-// row finisher (one warp): merges the slice partials of row r in slice order
-// (lane-strided, then the fixed warp merge) into rowstat; the last row of a
-// sequence then runs the statistics finisher.
-// ---------------------------------------------------------------------------
-template <class E>
-__device__ __noinline__ void stats_finisher(const SampleArgs& a, int b, FinIn pre);
+// Lane 0: record the verdict of position i of sequence b.  Returns n (lane 0)
+// if this resolution is the one that decides the sequence, else -1.  With
+// K <= 31 the resolved and rejected positions live in one 64-bit word per
+// sequence (stored complemented, so that the all-ones fill is the empty set)
+// and the one atomic whose result crosses into "decided" identifies the
+// decider.  With larger K the sequence is decided by its last resolution,
+// which scans the verdicts in position order.
+__device__ __forceinline__ int resolve_position(const SampleArgs& a, int b, int i, int verdict) {
+  if (a.K <= kMaskMaxK) {
+    unsigned long long bits = 1ull << i;
+    if (verdict != kVerdictAccept && i < a.K) bits |= 1ull << (32 + i);
+    const unsigned long long old_set = ~atomicAnd(a.resword + b, ~bits);
+    const int was = decided_n(old_set, a.K), now = decided_n(old_set | bits, a.K);
+    return (was < 0 && now >= 0) ? now : -1;
+  }
+  return ticket_take(a.posticket + b) == a.K ? a.K + 1 : -1;  // K + 1: scan the verdicts
+}
 
-// The sequence ticket is taken with a predicated atomic, and the finisher's
-// inputs for positions 0..31 are loaded while it is in flight, so the last
-// row goes on to the finisher without another round trip.
-template <class E, bool ENT>
-__device__ __noinline__ void row_finisher(const SampleArgs& a, int b, int r) {
+// Commit (one warp, the second of the sequence's two commit arrivals: "every
+// unit checked" and "token drawn / decided bad"): writes out_tokens, out_n and
+// out_resid from the workspace slots.
+__device__ __noinline__ void commit_sequence(const SampleArgs& a, int b) {
+  const int lane = threadIdx.x & 31;
+  const int K = a.K;
+  const int sb = wait_s32(a.seqbad + b, a.status);
+  const uint4 res = wait_result(a.result + b, a.status);
+  const bool bad = sb != 0 || res.x == kResultBad;
+  int32_t* out = a.out_tokens + (size_t)b * (K + 1);
+  const int32_t* x = a.tokens + (size_t)b * K;
+  if (bad) {
+    for (int j = lane; j <= K; j += 32) out[j] = -1;
+    if (lane == 0) {
+      a.out_n[b] = -1;
+      atomicOr(a.status, kStatusBadData);
+      if (a.out_resid) a.out_resid[b] = NAN;
+    }
+  } else {
+    const int n = (int)res.x;
+    const int token = res.y == kResultBad ? -1 : (int)res.y;
+    for (int j = lane; j <= K; j += 32) out[j] = j < n ? __ldg(x + j) : (j == n ? token : -1);
+    if (lane == 0) {
+      a.out_n[b] = n;
+      if (a.out_resid) a.out_resid[b] = __uint_as_float(res.z);
+    }
+  }
+  __syncwarp();
+}
+
+// One of the two commit arrivals of sequence b (lane 0 takes the ticket); the
+// second runs the commit.
+__device__ __forceinline__ void commit_arrive(const SampleArgs& a, int b) {
+  const int lane = threadIdx.x & 31;
+  int old = 0;
+  if (lane == 0) old = ticket_take(a.committicket + b);
+  old = __shfl_sync(0xffffffffu, old, 0);
+  if (old == 1) commit_sequence(a, b);
+}
+
+// Decision of sequence b at n (one warp): the tail constants of row n, the
+// decision queue entry, and for a bad position the result-side commit arrival.
+// (mT, sT, mD, sD, verdict) are those of position n when `have` holds (the
+// caller resolved it), else they are read from the workspace.
+__device__ __noinline__ void decide_sequence(const SampleArgs& a, int b, int n, bool have, uint2 stT,
+                                             uint2 stD, int verdict) {
+  const int lane = threadIdx.x & 31;
+  const int K = a.K, R = a.R;
+  const int qpos = reserve_decision(a, lane);
+  if (n > K) {  // K > 31: every position resolved; n = the first verdict that is not an accept
+    n = K;
+    for (int i0 = 0; i0 < K; i0 += 32) {
+      const int i = i0 + lane;
+      const int v = i < K ? wait_s32(a.verdict + (size_t)b * (K + 1) + i, a.status) : kVerdictAccept;
+      const unsigned bal = __ballot_sync(0xffffffffu, v != kVerdictAccept);
+      if (bal) {
+        n = i0 + __ffs(bal) - 1;
+        break;
+      }
+    }
+    have = false;
+  }
+  if (!have) {
+    const float2* rs = a.rowstat + (size_t)b * R;
+    stT = wait_u2(rs + n, a.status);
+    stD = n < K ? wait_u2(rs + K + 1 + n, a.status) : make_uint2(0u, 0u);
+    verdict = wait_s32(a.verdict + (size_t)b * (K + 1) + n, a.status);
+  }
+  SeqInfo si;
+  si.b = b;
+  si.n = n;
+  if (verdict == kVerdictBad) {
+    si.mode = kModeBad;
+    si.mT = si.mD = si.lam_hi = si.lam_lo = si.sT = 0.f;
+  } else {
+    si.mT = __uint_as_float(stT.x);
+    si.sT = __uint_as_float(stT.y);
+    if (n < K) {
+      si.mode = kModeResidual;
+      si.mD = __uint_as_float(stD.x);
+      const double lam = log2((double)si.sT) - log2((double)__uint_as_float(stD.y));
+      si.lam_hi = (float)lam;
+      si.lam_lo = (float)(lam - (double)si.lam_hi);
+    } else {
+      si.mode = kModeBonus;
+      si.mD = 0.f;
+      si.lam_hi = si.lam_lo = 0.f;
+    }
+  }
+  if (lane == 0) publish_decision(a, qpos, si);
+  if (si.mode == kModeBad) {  // no token will be drawn: the result side arrives now
+    if (lane == 0) st_relaxed_v4(a.result + b, kResultBad, kResultBad, 0x7fc00000u, 0u);
+    commit_arrive(a, b);
+  }
+  __syncwarp();
+}
+
+__device__ __forceinline__ bool row_ok(uint2 w) {
+  const float m = __uint_as_float(w.x), sum = __uint_as_float(w.y);
+  return sum > 0.f && sum < INFINITY && m < INFINITY && m > neg_inf();
+}
+
+// Merge (in slice order: lane-strided, then the fixed warp merge) the slice
+// partials of row r of sequence b from the values already loaded for slice c
+// = lane, lane + 32, ...; every lane ends with the row's (m, s) (and t).
+template <bool ENT>
+__device__ __forceinline__ void merge_row(const SampleArgs& a, int b, int r, float& m, float& s, float& t) {
   const int lane = threadIdx.x & 31;
   const int C = a.CS;
   const float2* pp = a.part + ((size_t)b * a.R + r) * C;
-  float m = neg_inf(), s = 0.f, t = 0.f;
+  m = neg_inf();
+  s = 0.f;
+  t = 0.f;
   for (int c = lane; c < C; c += 32) {
     const uint2 w = wait_u2(pp + c, a.status);
     if constexpr (ENT) {
@@ -173,145 +289,81 @@ __device__ __noinline__ void row_finisher(const SampleArgs& a, int b, int r) {
   }
   if constexpr (ENT) {
     warp_mst(m, s, t, a.c_hi);
-    // nats: ln s - ln 2 * t / s (NaN for a row without mass or with NaN)
-    if (lane == 0)
-      a.out_entropy[(size_t)b * a.R + r] =
-          (float)(log((double)s) - 0.69314718055994530942 * (double)t / (double)s);
   } else {
     warp_ms(m, s, a.c_hi);
   }
-  if (lane == 0) st_relaxed_u2(a.rowstat + (size_t)b * a.R + r, __float_as_uint(m), __float_as_uint(s));
-  int old = ticket_take_if(lane == 0, &a.seqticket[b]);
-  const FinIn pre = load_fin_inputs(a, b, 0);
-  old = __shfl_sync(0xffffffffu, old, 0);
-  if (old == a.R - 1) stats_finisher<E>(a, b, pre);
 }
 
-// ---------------------------------------------------------------------------
-// statistics finisher (one warp): steps 2-4 for sequence b
-// ---------------------------------------------------------------------------
-__device__ __forceinline__ bool row_ok(uint2 w) {
-  const float m = __uint_as_float(w.x), sum = __uint_as_float(w.y);
-  return sum > 0.f && sum < INFINITY && m < INFINITY && m > neg_inf();
-}
-__device__ __forceinline__ uint2 shfl_u2(uint2 v, int src) {
-  return make_uint2(__shfl_sync(0xffffffffu, v.x, src), __shfl_sync(0xffffffffu, v.y, src));
+// Row r's merged statistics into the workspace and the optional outputs (lane 0).
+template <bool ENT>
+__device__ __forceinline__ void store_row(const SampleArgs& a, int b, int r, float m, float s, float t) {
+  const size_t k = (size_t)b * a.R + r;
+  st_relaxed_u2(a.rowstat + k, __float_as_uint(m), __float_as_uint(s));
+  if (a.out_row_stats) {
+    a.out_row_stats[k * 2 + 0] = (float)((double)m * a.inv_tau);
+    a.out_row_stats[k * 2 + 1] = s;
+  }
+  // nats: ln s - ln 2 * t / s (NaN for a row without mass or with NaN)
+  if constexpr (ENT) a.out_entropy[k] = (float)(log((double)s) - 0.69314718055994530942 * (double)t / (double)s);
 }
 
-// Position i of a chunk is lane i: target row i, draft row i, the drafted
-// token x_i and the two logits at x_i (recorded by the statistics slices that
-// hold them).  Target row K rides along as position K.  Every chunk issues one
-// round of independent loads; the decision is published before the output
-// tokens are written, and its queue position is taken first so that the
-// atomic's round trip overlaps the loads.
-template <class E>
-__device__ __noinline__ void stats_finisher(const SampleArgs& a, int b, FinIn pre) {
-  const int R = a.R, K = a.K;
+// Unit finisher (one warp): position i of sequence b.
+template <class E, bool ENT>
+__device__ __noinline__ void unit_finisher(const SampleArgs& a, int b, int i) {
   const int lane = threadIdx.x & 31;
-  const float2* rs = a.rowstat + (size_t)b * R;
-  const float* zx = a.zx + (size_t)b * R;
-  const int32_t* x = a.tokens + (size_t)b * K;
-  const int qpos = reserve_decision(a, lane);
-  bool bad = false;
-  int n = K;
-  uint2 stn = make_uint2(0u, 0u), sdn = make_uint2(0u, 0u);
-  for (int i0 = 0; i0 <= K; i0 += 32) {
-    const int i = i0 + lane;
-    const bool hasT = i <= K, hasD = i < K;
-    const FinIn in = i0 == 0 ? pre : load_fin_inputs(a, b, i0);
-    uint2 st = in.st, sd = in.sd;
-    const int xi = in.xi;
-    float zT = in.zT, zD = in.zD;
-    if (hasT && st.x == kMarker) st = wait_u2(rs + i, a.status);
-    if (hasD && sd.x == kMarker) sd = wait_u2(rs + K + 1 + i, a.status);
-    if (a.out_row_stats) {
-      if (hasT) {
-        a.out_row_stats[((size_t)b * R + i) * 2 + 0] = (float)((double)__uint_as_float(st.x) * a.inv_tau);
-        a.out_row_stats[((size_t)b * R + i) * 2 + 1] = __uint_as_float(st.y);
-      }
-      if (hasD) {
-        a.out_row_stats[((size_t)b * R + K + 1 + i) * 2 + 0] =
-            (float)((double)__uint_as_float(sd.x) * a.inv_tau);
-        a.out_row_stats[((size_t)b * R + K + 1 + i) * 2 + 1] = __uint_as_float(sd.y);
-      }
-    }
-    bool ok = !hasT || row_ok(st);
-    if (hasD) ok = ok && row_ok(sd) && xi >= 0 && xi < a.V;
-    bad |= !ok;
-    bool reject = false;
-    if (hasD && ok) {
-      // the slice holding x_i writes these; a valid token always has one
-      if (__float_as_uint(zT) == kMarker) zT = wait_f32(zx + i, a.status);
-      if (__float_as_uint(zD) == kMarker) zD = wait_f32(zx + K + 1 + i, a.status);
-      const double mT = __uint_as_float(st.x), sT = __uint_as_float(st.y);
-      const double mD = __uint_as_float(sd.x), sD = __uint_as_float(sd.y);
-      // log2 of the unnormalised probabilities, from exact differences
-      const double lp = ((double)zT - mT) * a.c64;
-      const double lq = ((double)zD - mD) * a.c64;
+  const int K = a.K, R = a.R;
+  const bool pair = i < K;
+  const int rT = i, rD = K + 1 + i;
+  // the drafted token and the logits at it (written by the slices holding it)
+  const int xi = pair ? __ldg(a.tokens + (size_t)b * K + i) : 0;
+  float zT = pair ? ld_relaxed_f32(a.zx + (size_t)b * R + rT) : 0.f;
+  float zD = pair ? ld_relaxed_f32(a.zx + (size_t)b * R + rD) : 0.f;
+  float mT, sT, tT, mD = 0.f, sD = 0.f, tD = 0.f;
+  merge_row<ENT>(a, b, rT, mT, sT, tT);
+  if (pair) merge_row<ENT>(a, b, rD, mD, sD, tD);
+  const uint2 stT = make_uint2(__float_as_uint(mT), __float_as_uint(sT));
+  const uint2 stD = make_uint2(__float_as_uint(mD), __float_as_uint(sD));
+  if (lane == 0) {
+    store_row<ENT>(a, b, rT, mT, sT, tT);
+    if (pair) store_row<ENT>(a, b, rD, mD, sD, tD);
+  }
+  bool bad = !row_ok(stT);
+  if (pair) bad = bad || !row_ok(stD) || xi < 0 || xi >= a.V;
+  int verdict = bad ? kVerdictBad : kVerdictAccept;
+  if (pair && !bad) {
+    // a valid token always has a slice that records the logits at it
+    if (__float_as_uint(zT) == kMarker) zT = wait_f32(a.zx + (size_t)b * R + rT, a.status);
+    if (__float_as_uint(zD) == kMarker) zD = wait_f32(a.zx + (size_t)b * R + rD, a.status);
+    // log2 of the unnormalised probabilities, from exact differences
+    const double lp = ((double)zT - (double)mT) * a.c64;
+    const double lq = ((double)zD - (double)mD) * a.c64;
+    bool accept = true;  // q(x) = 0 <= p(x)
+    if (zD != neg_inf()) {
       const double u = uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0);
-      bool accept;
-      if (zD == neg_inf()) {
-        accept = true;  // q(x) = 0 <= p(x)
-      } else {
-        const double ratio = exp2(lp - lq) * (sD / sT);  // p(x) / q(x)
-        accept = u < ratio;
-      }
-      reject = !accept;
-      if (a.out_pq) {
-        a.out_pq[((size_t)b * K + i) * 2 + 0] = (float)(exp2(lp) / sT);
-        a.out_pq[((size_t)b * K + i) * 2 + 1] = (float)(exp2(lq) / sD);
-      }
+      accept = u < exp2(lp - lq) * ((double)sD / (double)sT);  // u < p(x) / q(x)
     }
-    const unsigned bal = __ballot_sync(0xffffffffu, reject);
-    if (n == K && bal) {
-      const int L = __ffs(bal) - 1;
-      n = i0 + L;
-      stn = shfl_u2(st, L);
-      sdn = shfl_u2(sd, L);
-    } else if (n == K && K - i0 < 32) {  // the chunk holding position K, nothing rejected
-      stn = shfl_u2(st, K - i0);
+    verdict = accept ? kVerdictAccept : kVerdictReject;
+    if (a.out_pq && lane == 0) {
+      a.out_pq[((size_t)b * K + i) * 2 + 0] = (float)(exp2(lp) / (double)sT);
+      a.out_pq[((size_t)b * K + i) * 2 + 1] = (float)(exp2(lq) / (double)sD);
     }
   }
-  bad = __any_sync(0xffffffffu, bad);
-
-  SeqInfo si;
-  si.b = b;
-  if (bad) {
-    si.n = 0;
-    si.mode = kModeBad;
-    si.mT = si.mD = si.lam_hi = si.lam_lo = si.sT = 0.f;
-  } else {
-    si.n = n;
-    si.mT = __uint_as_float(stn.x);
-    si.sT = __uint_as_float(stn.y);
-    if (n < K) {
-      si.mode = kModeResidual;
-      si.mD = __uint_as_float(sdn.x);
-      const double lam = log2((double)si.sT) - log2((double)__uint_as_float(sdn.y));
-      si.lam_hi = (float)lam;
-      si.lam_lo = (float)(lam - (double)si.lam_hi);
-    } else {
-      si.mode = kModeBonus;
-      si.mD = 0.f;
-      si.lam_hi = si.lam_lo = 0.f;
-    }
+  // the verdict slot, the resolution and the sequence's unit count, issued
+  // together from lane 0
+  int n = -1, units = 0;
+  if (lane == 0) {
+    st_relaxed_s32(a.verdict + (size_t)b * (K + 1) + i, verdict);
+    n = resolve_position(a, b, i, verdict);
+    units = atom_add_relaxed(a.seqticket + b, bad ? kUnitBad + 1 : 1) + 1;
   }
-  if (lane == 0) publish_decision(a, qpos, si);
-
-  int32_t* out = a.out_tokens + (size_t)b * (K + 1);
-  if (bad) {
-    for (int j = lane; j <= K; j += 32) out[j] = -1;
-    if (lane == 0) {
-      a.out_n[b] = -1;
-      atomicOr(a.status, kStatusBadData);
-      if (a.out_resid) a.out_resid[b] = NAN;
-    }
-  } else {
-    for (int j = lane; j <= K; j += 32) {
-      if (j < n) out[j] = __ldg(x + j);
-      else if (j > n) out[j] = -1;
-    }
-    if (lane == 0) a.out_n[b] = n;
+  n = __shfl_sync(0xffffffffu, n, 0);
+  units = __shfl_sync(0xffffffffu, units, 0);
+  if (n >= 0) decide_sequence(a, b, n, n == i, stT, stD, verdict);
+  // (the count starts at -1: `units` is the number of earlier arrivals, with
+  // kUnitBad added once per unit that had bad data)
+  if ((units & (kUnitBad - 1)) == K) {  // every unit of the sequence is checked
+    if (lane == 0) st_relaxed_s32(a.seqbad + b, (units >= kUnitBad || bad) ? 1 : 0);
+    commit_arrive(a, b);
   }
   __syncwarp();
 }
@@ -480,10 +532,10 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
       warp_cdf_search(C, theta, 0.0, [&](int t) { return (double)ld_relaxed_f32(ts + t); }, &acc);
   if (tsel < 0) {  // no slice with mass: only an expired wait can cause this
     if (lane == 0) {
-      a.out_tokens[(size_t)b * (a.K + 1) + n] = -1;
       atomicOr(a.status, kStatusTimeout);
+      st_relaxed_v4(a.result + b, (uint32_t)n, kResultBad, __float_as_uint((float)(Z / (double)si.sT)), 0u);
     }
-    __syncwarp();
+    commit_arrive(a, b);
     return;
   }
   const int v0 = tsel * a.TL, v1 = min(a.V, v0 + a.TL);
@@ -494,10 +546,10 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
       np, theta, acc, [&](int q) { return (double)wait_f32(gp + q, a.status); }, &acc2);
   if (psel < 0) {  // pieces inconsistent with their slice mass (expired wait)
     if (lane == 0) {
-      a.out_tokens[(size_t)b * (a.K + 1) + n] = -1;
       atomicOr(a.status, kStatusTimeout);
+      st_relaxed_v4(a.result + b, (uint32_t)n, kResultBad, __float_as_uint((float)(Z / (double)si.sT)), 0u);
     }
-    __syncwarp();
+    commit_arrive(a, b);
     return;
   }
 
@@ -540,21 +592,49 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
     token = pick >= 0 ? base + pick : -1;
   }
   token = __shfl_sync(0xffffffffu, token, L);
-  if (lane == 0) {
-    a.out_tokens[(size_t)b * (a.K + 1) + n] = token;
-    if (a.out_resid) a.out_resid[b] = (float)(Z / (double)si.sT);
+  if (lane == 0)
+    st_relaxed_v4(a.result + b, (uint32_t)n, token >= 0 ? (uint32_t)token : kResultBad,
+                  __float_as_uint((float)(Z / (double)si.sT)), 0u);
+  commit_arrive(a, b);
+}
+
+// Flat statistics slice f, position-major: the slices of position 0 of every
+// sequence come first (for each sequence its target row, then its draft
+// row), then position 1, and so on; position K (the bonus rows) comes last.
+// Every sequence is then decided early in the stream (after its first
+// rejection's pair), and the rows streamed at the end gate few decisions.
+struct SliceId {
+  int b, i, r, s;
+};
+__device__ __forceinline__ SliceId decode_slice(const SampleArgs& a, int f) {
+  SliceId id;
+  int h = 0;
+  if (f < a.FP) {
+    id.i = fdiv(f, a.div_pos);
+    const int rem = f - id.i * a.B * 2 * a.CS;
+    id.b = fdiv(rem, a.div_pair);
+    const int r2 = rem - id.b * 2 * a.CS;
+    h = r2 >= a.CS ? 1 : 0;
+    id.s = r2 - h * a.CS;
+  } else {
+    id.i = a.K;
+    const int rem = f - a.FP;
+    id.b = fdiv(rem, a.div_cs);
+    id.s = rem - id.b * a.CS;
   }
-  __syncwarp();
+  id.r = h ? a.K + 1 + id.i : id.i;
+  return id;
 }
 
 // ---------------------------------------------------------------------------
 // statistics unit (one warp)
 // ---------------------------------------------------------------------------
-// Statistics slice s of row r of sequence b: the row's (m, s) over the slice,
-// then the row's ticket.  Returns the ticket's old value (lane 0).  Kept out
-// of line so that the stream loop has the register file to itself.
+// Statistics slice s of row r (position i) of sequence b: the row's (m, s)
+// over the slice, then the ticket of unit (b, i).  Returns the ticket's old
+// value (lane 0).  Kept out of line so that the stream loop has the register
+// file to itself.
 template <class E, int VEC, bool ENT>
-__device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int r, int s) {
+__device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int i, int r, int s) {
   using S = typename E::storage;
   constexpr int BATCH = 32 * VEC * kUnroll;
   const int lane = threadIdx.x & 31;
@@ -562,7 +642,7 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int r, int s
   const int v0 = s * a.SL, v1 = min(a.V, v0 + a.SL);
   // the drafted token scored by this row (target rows 0..K-1 and every draft
   // row); its load overlaps the stream, and the slice holding it records the
-  // logit there for the statistics finisher
+  // logit there for the unit finisher
   const int ti = r < a.K ? r : (r > a.K ? r - a.K - 1 : -1);
   const uint32_t xt = ld_relaxed_if(lane == 0 && ti >= 0, a.tokens + (size_t)b * a.K + ti, kMarker);
   const float cc = a.c_hi;
@@ -596,7 +676,7 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int r, int s
   if (lane == 0) {
     if constexpr (ENT) st_relaxed_f32(a.part_t + ((size_t)b * a.R + r) * a.CS + s, tsum);
     st_relaxed_u2(a.part + ((size_t)b * a.R + r) * a.CS + s, __float_as_uint(m), __float_as_uint(sum));
-    old = ticket_take(&a.rowticket[((size_t)b * a.R + r) * kTicketStride]);
+    old = ticket_take(&a.unitticket[((size_t)b * (a.K + 1) + i) * kTicketStride]);
     const int xi = (int)xt;
     if (ti >= 0 && xi >= v0 && xi < v1) st_relaxed_f32(a.zx + (size_t)b * a.R + r, E::load1(row + xi));
   }
@@ -608,7 +688,7 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int r, int s
 template <class E, int VEC>
 __device__ __noinline__ void tail_slice(const SampleArgs& a, const SeqInfo& si, int s) {
   const int lane = threadIdx.x & 31;
-  if (si.mode == kModeBad) return;  // outputs already written by the statistics finisher
+  if (si.mode == kModeBad) return;  // no draw: the decision made the result-side commit arrival
   const int b = si.b;
   const float tot = tail_slice_mass<E, VEC>(a, b, s, si);
   int old = 0;
@@ -644,26 +724,24 @@ __device__ __forceinline__ int next_live_counter(int ctr, unsigned dead) {
 // Progress: statistics slices and the finishers they trigger wait only for
 // stores that other warps have already issued (their tickets were counted), a
 // warp holding a claimed statistics slice never waits, and every sequence is
-// decided once its statistics slices are done.  So every queue entry is
-// eventually written and every wait ends, whatever part of the grid is
-// resident.
+// decided once the statistics slices of its positions up to the first
+// rejection are done.  So every queue entry is eventually written and every
+// wait ends, whatever part of the grid is resident.
 template <class E, int VEC, bool ENT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __grid_constant__ SampleArgs a) {
   const int lane = threadIdx.x & 31;
   const int w = slice_of_warp();
-  const int per_seq = a.R * a.CS;
   const int TT = a.B * a.TC;                       // tail items in all
   const int W = kSlices * (int)gridDim.x;          // warps in the grid
   int t = w * (int)gridDim.x + (int)blockIdx.x;    // this warp's next tail item
   // Statistics claims rotate over the eight counters (warp slot w starts at
   // counter w), so every warp draws equally from every counter and the
-  // counters advance together: a sequence's slices, spread over all eight,
-  // are then processed close together in time.  A claim past a counter's end
-  // marks that counter dead for this warp; the warp leaves the statistics
-  // work only when it has seen all eight dead, so no slice is ever left
-  // unclaimed.  A claimed slice is processed before a tail item that became
-  // ready (other warps' decisions may wait on it); the claim after it is then
-  // deferred until the tail item is done.
+  // counters advance together.  A claim past a counter's end marks that
+  // counter dead for this warp; the warp leaves the statistics work only when
+  // it has seen all eight dead, so no slice is ever left unclaimed.  A claimed
+  // slice is processed before a tail item that became ready (other warps'
+  // decisions may wait on it); the claim after it is then deferred until the
+  // tail item is done.
   unsigned dead = 0;
   int ctr = w;
   int f = bcast(claim_from(a.counter, ctr, lane)) * kSlices + ctr;
@@ -687,9 +765,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
         next = claim_from(a.counter, nctr, lane);
       }
       if (!tail_ready) seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
-      const int b = fdiv(f, a.div_seq), rs = f - b * per_seq, r = fdiv(rs, a.div_cs), s = rs - r * a.CS;
-      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC, ENT>(a, b, r, s), 0);
-      if (old == a.CS - 1) row_finisher<E, ENT>(a, b, r);
+      const SliceId id = decode_slice(a, f);
+      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC, ENT>(a, id.b, id.i, id.r, id.s), 0);
+      if (old == unit_slices(a, id.i) - 1) unit_finisher<E, ENT>(a, id.b, id.i);
       if (ahead) {
         f = bcast(next) * kSlices + nctr;
         ctr = nctr;
@@ -731,32 +809,40 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
 // ---------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [counters, tickets, queue count (all start at -1)][marker-filled
-// result slots: part, rowstat, tailsum, queue, pieces, zx, and part_t when the
-// entropy is asked for]; one 0xff fill initialises both parts.
-static void sample_layout(int B, int R, int CS, int TC, int P, bool ent, size_t* off) {
+// Workspace: [counters, tickets, resolution words, queue count (all start at
+// all-ones)][marker-filled result slots: part, rowstat, tailsum, queue,
+// pieces, zx, verdict, seqbad, result, and part_t when the entropy is asked
+// for]; one 0xff fill initialises both parts.
+static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t* off) {
+  const int R = 2 * K + 1;
   size_t o = 0;
-  off[0] = o; o += kCounterBytes;                                          // counter
-  off[1] = o; o += align_up((size_t)B * R * kTicketStride * 4, 16);       // rowticket
-  off[2] = o; o += align_up((size_t)B * 4, 16);                           // seqticket
-  off[3] = o; o += align_up((size_t)B * 4, 16);                           // tailticket
-  off[4] = o; o += 16;                                                     // qcount
+  off[0] = o; o += kCounterBytes;                                            // counter
+  off[1] = o; o += align_up((size_t)B * (K + 1) * kTicketStride * 4, 16);   // unitticket
+  off[2] = o; o += align_up((size_t)B * 4, 16);                             // seqticket
+  off[3] = o; o += align_up((size_t)B * 4, 16);                             // tailticket
+  off[4] = o; o += 16;                                                       // qcount
+  off[15] = o; o += align_up((size_t)B * 4, 16);                            // posticket
+  off[16] = o; o += align_up((size_t)B * 4, 16);                            // committicket
+  off[17] = o; o += align_up((size_t)B * 8, 16);                            // resword
   o = align_up(o, 256);
-  off[5] = o;                                                              // end of zero region
-  off[6] = o; o += align_up((size_t)B * R * CS * sizeof(float2), 256);    // part
-  off[7] = o; o += align_up((size_t)B * R * sizeof(float2), 256);         // rowstat
-  off[8] = o; o += align_up((size_t)B * TC * sizeof(float), 256);         // tailsum
-  off[10] = o; o += align_up((size_t)B * sizeof(SeqInfo), 256);           // queue
-  off[11] = o; o += align_up((size_t)B * TC * P * sizeof(float), 256);    // pieces
-  off[13] = o; o += align_up((size_t)B * R * sizeof(float), 256);         // zx
+  off[5] = o;                                                                // end of counter region
+  off[6] = o; o += align_up((size_t)B * R * CS * sizeof(float2), 256);      // part
+  off[7] = o; o += align_up((size_t)B * R * sizeof(float2), 256);           // rowstat
+  off[8] = o; o += align_up((size_t)B * TC * sizeof(float), 256);           // tailsum
+  off[10] = o; o += align_up((size_t)B * sizeof(SeqInfo), 256);             // queue
+  off[11] = o; o += align_up((size_t)B * TC * P * sizeof(float), 256);      // pieces
+  off[13] = o; o += align_up((size_t)B * R * sizeof(float), 256);           // zx
+  off[18] = o; o += align_up((size_t)B * (K + 1) * 4, 256);                 // verdict
+  off[19] = o; o += align_up((size_t)B * 4, 256);                           // seqbad
+  off[20] = o; o += align_up((size_t)B * sizeof(uint4), 256);               // result
   off[14] = o; if (ent) o += align_up((size_t)B * R * CS * sizeof(float), 256);  // part_t
-  off[9] = o;                                                              // end of marker region
+  off[9] = o;                                                                // end of marker region
   off[12] = o;
 }
 
 WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
-  size_t off[15];
-  sample_layout(B, 2 * K + 1, CS, TC, P, ent, off);
+  size_t off[21];
+  sample_layout(B, K, CS, TC, P, ent, off);
   WsLayout l;
   l.total = off[12];
   l.zero_bytes = 0;  // counters and tickets start at -1: one 0xff fill covers everything
@@ -766,20 +852,26 @@ WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
 }
 
 void sample_bind_workspace(SampleArgs& a, void* ws) {
-  size_t off[15];
-  sample_layout(a.B, a.R, a.CS, a.TC, a.P, a.out_entropy != nullptr, off);
+  size_t off[21];
+  sample_layout(a.B, a.K, a.CS, a.TC, a.P, a.out_entropy != nullptr, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
-  a.rowticket = (int*)(p + off[1]);
+  a.unitticket = (int*)(p + off[1]);
   a.seqticket = (int*)(p + off[2]);
   a.tailticket = (int*)(p + off[3]);
   a.qcount = (int*)(p + off[4]);
+  a.posticket = (int*)(p + off[15]);
+  a.committicket = (int*)(p + off[16]);
+  a.resword = (unsigned long long*)(p + off[17]);
   a.part = (float2*)(p + off[6]);
   a.rowstat = (float2*)(p + off[7]);
   a.tailsum = (float*)(p + off[8]);
   a.queue = (SeqInfo*)(p + off[10]);
   a.pieces = (float*)(p + off[11]);
   a.zx = (float*)(p + off[13]);
+  a.verdict = (int*)(p + off[18]);
+  a.seqbad = (int*)(p + off[19]);
+  a.result = (uint4*)(p + off[20]);
   a.part_t = a.out_entropy ? (float*)(p + off[14]) : nullptr;
 }
 

@@ -309,6 +309,18 @@ __device__ __forceinline__ float wait_f32_acquire(const float* p, unsigned* stat
   return v;
 }
 
+// A 16-byte result slot whose first three words have all been written.
+__device__ __forceinline__ uint4 wait_result(const void* p, unsigned* status) {
+  uint4 v = ld_relaxed_v4(p);
+  unsigned it = 0;
+  while ((v.x == kMarker || v.y == kMarker || v.z == kMarker) && ++it < kSpinLimit) {
+    __nanosleep(64);
+    v = ld_relaxed_v4(p);
+  }
+  if (v.x == kMarker || v.y == kMarker || v.z == kMarker) atomicOr(status, kStatusTimeout);
+  return v;
+}
+
 // n / d for 0 <= n < 2^31 with d's FastDiv constants.
 __device__ __forceinline__ int fdiv(int n, const FastDiv& f) {
   return (int)(((unsigned long long)(unsigned)n * f.m) >> f.shift);

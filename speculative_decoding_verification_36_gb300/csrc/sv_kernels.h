@@ -83,8 +83,9 @@ struct SampleArgs {
   int TC;  // tail slices per row = ceil(V / TL)
   int P;   // pieces (warp steps) per tail slice
   int F;   // statistics slices in all: B * R * CS
+  int FP;  // slices of positions 0..K-1 (row pairs), which come first: K * B * 2 * CS
   int claim_tail;  // within this many slices of the end, claims are not made ahead
-  FastDiv div_seq, div_cs, div_tc;  // division by R * CS, CS and TC
+  FastDiv div_pos, div_pair, div_cs, div_tc;  // division by B * 2 * CS, 2 * CS, CS and TC
   float c_hi, c_lo;  // log2(e)/temperature as a float pair
   double c64;        // the same in double
   double inv_tau;    // 1 / temperature
@@ -96,12 +97,20 @@ struct SampleArgs {
   float* out_resid;      // optional [B]: mass of the replacement distribution
   float* out_entropy;    // optional [B, R]: entropy (nats) of each row's softmax
   // workspace, filled with all-ones bytes before the launch: the counters and
-  // tickets (counter, rowticket, seqticket, tailticket, qcount) then start at
-  // -1, and the result slots (part, rowstat, zx, tailsum, queue, pieces) hold
-  // the kMarker "not yet written" pattern.
+  // tickets (counter, unitticket, seqticket, posticket, committicket,
+  // tailticket, qcount) then start at -1, the resolution words at the empty
+  // set (stored complemented), and the result slots (part, rowstat, zx,
+  // verdict, seqbad, result, tailsum, queue, pieces) hold the kMarker "not yet
+  // written" pattern.
   unsigned long long* counter;  // kSlices claim counters, kCounterStride apart
-  int* rowticket;   // [B, R] (kTicketStride apart) finished slices of a row
-  int* seqticket;   // [B] finished rows of a sequence
+  int* unitticket;  // [B, K+1] (kTicketStride apart) finished slices of a position unit
+  int* seqticket;   // [B] finished units of a sequence (+ 0x10000 per unit with bad data)
+  int* posticket;   // [B] resolved positions (K > 31 only)
+  int* committicket;  // [B] commit arrivals (units checked; token drawn or decided bad)
+  unsigned long long* resword;  // [B] resolved / rejected positions, complemented (K <= 31)
+  int* verdict;     // [B, K+1] accept / reject / bad of each position
+  int* seqbad;      // [B] 1 if any unit of the sequence had bad data
+  uint4* result;    // [B] (n, token, residual mass bits, 0) for the commit
   int* tailticket;  // [B] finished tail slices
   int* qcount;      // decision-queue positions taken so far
   float2* part;     // [B, R, CS] per-slice (m, s)

@@ -122,7 +122,7 @@ int spec_verify_bf16(const uint16_t *target_logits, const uint16_t *draft_logits
  * cudaMalloc/cudaFree or other allocating call.
  *   - A problem whose scratch exceeds SPEC_STATIC_SCRATCH_BYTES returns
  *     SPEC_ERR_SCRATCH and launches nothing (for K = 8, V = 152064, B = 256
- *     needs about 1.8 MB).
+ *     needs about 1.7 MB).
  *   - The buffer's address is looked up on the first call on each device
  *     (cudaGetSymbolAddress, which may load the module): make that first call
  *     before any stream capture on that device.

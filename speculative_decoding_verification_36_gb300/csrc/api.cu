@@ -115,18 +115,35 @@ int ensure_pool(DeviceState* d) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Tuning knobs (environment, read once per process): SPECVERIFY_SLICE_BYTES,
-// the bytes of logits per statistics slice of the sampling kernel (default
-// 12288); SPECVERIFY_ARGMAX_SLICE_BYTES, the same for the greedy and tree
-// kernels (default 8192);
-// SPECVERIFY_TAIL_BYTES, the bytes of one row per tail slice (default half a
-// statistics slice); SPECVERIFY_CLAIM_TAIL, the number of final statistics
-// slices that are not claimed ahead (default one per warp of the grid).
+// Tuning knobs (environment, read once per process), defaults measured on
+// GB300 with the c3 workload:
+//   SPECVERIFY_SLICE_BYTES        bytes of logits per statistics slice of the
+//                                 sampling kernel (12288)
+//   SPECVERIFY_ARGMAX_SLICE_BYTES the same for the greedy and tree kernels (8192)
+//   SPECVERIFY_TAIL_BYTES         bytes of one row per tail slice (half a
+//                                 statistics slice)
+//   SPECVERIFY_CLAIM_TAIL         final statistics slices not claimed ahead (1)
+//   SPECVERIFY_FRONT_POS          draft positions whose row pairs are spread
+//                                 through the stream (1)
+//   SPECVERIFY_FRONT_SPAN         percent of the stream they are spread over
+//                                 (60; 0 gives plain position-major order)
+//   SPECVERIFY_L2_KEEP            positions whose rows are prefetched into L2
+//                                 with evict_last, as likely tail rows (2)
+//   SPECVERIFY_L2_OTHER           prefetch policy of the other rows: 0 the
+//                                 default, 1 evict_first, 2 evict_normal (0)
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
   const long x = strtol(v, nullptr, 10);
   return (x > 0 && x < (1L << 30)) ? (int)x : dflt;
+}
+
+// The same for a knob that may be zero or negative.
+int env_int_signed(const char* name, int dflt) {
+  const char* v = getenv(name);
+  if (!v || !*v) return dflt;
+  const long x = strtol(v, nullptr, 10);
+  return (x > -(1L << 30) && x < (1L << 30)) ? (int)x : dflt;
 }
 
 // Slice length: a whole number of warp load batches (32 lanes x kUnroll
@@ -305,9 +322,33 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.div_pair = sv::make_fastdiv((uint32_t)(2 * a.CS));
   a.div_cs = sv::make_fastdiv((uint32_t)a.CS);
   a.div_tc = sv::make_fastdiv((uint32_t)a.TC);
+  // Stream order: the front positions' slices are spread over the first
+  // `front_span` percent of the stream (100 or more, or a span shorter than
+  // their own share: position-major order).
+  {
+    static const int front_pos = env_int_signed("SPECVERIFY_FRONT_POS", 1);
+    static const int front_span = env_int_signed("SPECVERIFY_FRONT_SPAN", 60);
+    const int fp = front_pos < 0 ? 0 : (front_pos > K ? K : front_pos);
+    a.NA = fp * B * 2 * a.CS;
+    a.FQ = 64;
+    const double span = (double)front_span / 100.0 * (double)a.F;
+    int fa = a.FQ;
+    if (a.NA > 0 && span > (double)a.NA) fa = (int)ceil((double)a.FQ * (double)a.NA / span);
+    a.FA = fa < 1 ? 1 : (fa > a.FQ ? a.FQ : fa);
+    // every front slice must land inside the stream: the claim index of the
+    // last one, ((NA-1) / FA) * FQ + (NA-1) % FA, below F (FA = FQ always is)
+    while (a.NA > 0 && a.FA < a.FQ &&
+           (long long)((a.NA - 1) / a.FA) * a.FQ + (a.NA - 1) % a.FA >= (long long)a.F)
+      ++a.FA;
+    a.div_fq = sv::make_fastdiv((uint32_t)a.FQ);
+  }
   const int grid = grid_for((a.F + sv::kSlices - 1) / sv::kSlices, capacity);
-  static const int claim_tail_env = env_int("SPECVERIFY_CLAIM_TAIL", 0);
-  a.claim_tail = claim_tail_env > 0 ? claim_tail_env : grid * sv::kSlices;  // one slice per warp
+  static const int claim_tail = env_int("SPECVERIFY_CLAIM_TAIL", 1);
+  a.claim_tail = claim_tail;
+  static const int l2_keep = env_int_signed("SPECVERIFY_L2_KEEP", 2);
+  static const int l2_other = env_int_signed("SPECVERIFY_L2_OTHER", 0);
+  a.l2_keep = l2_keep;
+  a.l2_other = l2_other;
   const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
   a.c64 = c;
   a.c_hi = (float)c;

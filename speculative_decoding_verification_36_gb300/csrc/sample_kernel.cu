@@ -15,17 +15,23 @@
 // Work decomposition: one persistent grid of independent warps (sv_kernels.h).
 //   * statistics slice = SL elements of one row: an online (max, sum of
 //     exp2) pass with 16-byte streaming loads and packed f32x2 arithmetic,
-//     reduced to one (m, s) pair in the workspace.  The warp that takes a
-//     sequence's last statistics ticket merges the slice pairs, runs steps
-//     2-4 in fp64 and appends the sequence's decision to the decision queue.
-//   * tail slice = SL elements of the tail row (pair) of a decided sequence:
+//     reduced to one (m, s) pair in the workspace.  Slices are streamed by
+//     draft position (position-major, with position 0 spread through the
+//     first part of the stream).  The warp that takes the last ticket of a
+//     position's row pair merges both rows, runs steps 2-3 for that position
+//     in fp64 and records the verdict; the verdict that completes the prefix
+//     0..n fixes n (step 4) and appends the sequence's decision to the
+//     decision queue, without waiting for the rows after the first rejection.
+//   * tail slice = a segment of the tail row (pair) of a decided sequence:
 //     the mass of every warp step ("piece") of the replacement / bonus
-//     distribution.  Tail items are owned by fixed warps; a warp polls its
-//     next item's queue entry while it streams statistics slices and takes
-//     the item as soon as the entry is there, so no warp ever waits for a decision while
-//     statistics work is left, and the re-read rows are still in L2.  The warp
-//     that takes the last tail ticket finds the CDF crossing from the slice
-//     and piece masses and rescans one piece.
+//     distribution, streamed through a per-warp shared-memory ring.  Tail
+//     items are owned by fixed warps; a warp polls its next item's queue entry
+//     while it streams statistics slices and takes the item once the entry is
+//     there, so no warp ever waits for a decision while statistics work is
+//     left.  The warp that takes the last tail ticket finds the CDF crossing
+//     from the slice and piece masses and rescans one piece (step 6).
+//   * commit: a sequence's outputs are written once its token is drawn and
+//     every one of its rows has been checked for bad data.
 // Every reduction runs in a fixed order, so results are run-to-run identical.
 #include "sv_common.cuh"
 #include "sv_kernels.h"
@@ -376,9 +382,17 @@ __device__ __noinline__ void unit_finisher(const SampleArgs& a, int b, int i) {
 
 // One warp: the pieces of tail slice s of the tail row(s) into the workspace
 // and the slice's mass, the fp32 sum of its pieces in order (every lane).
-// The loads of the next warp step are issued before the current step's
-// arithmetic (two register buffers).
-template <class E, int VEC>
+// RING (the vector path): the loads run kTailStages - 1 warp steps ahead of
+// the arithmetic through a per-warp ring in shared memory (16-byte cp.async
+// per lane and row), so that a warp keeps three steps of both rows in flight
+// without holding them in registers.  With one step in flight a tail warp
+// moved its bytes at half the rate of a statistics warp (its loads wait on a
+// loaded memory system for about a microsecond), and the tail items of the
+// sequences decided together held the grid for tens of microseconds.  The
+// scalar path double-buffers in registers.
+constexpr int kTailStages = 4;
+
+template <class E, int VEC, bool RING>
 __device__ float tail_slice_mass(const SampleArgs& a, int b, int s, const SeqInfo& si) {
   using S = typename E::storage;
   constexpr int STEPW = 32 * VEC;
@@ -389,36 +403,78 @@ __device__ float tail_slice_mass(const SampleArgs& a, int b, int s, const SeqInf
   const int v0 = s * a.TL, v1 = min(a.V, v0 + a.TL);
   const int nsteps = v1 > v0 ? (v1 - v0 + STEPW - 1) / STEPW : 0;
   float* gp = a.pieces + ((size_t)b * a.TC + s) * a.P;
+  float total = 0.f;
+  const int e0 = v0 + lane * VEC;
   if constexpr (VEC > 1) {
+    if constexpr (RING) {
+    // [warp][stage][row][lane]: 8 x 4 x 2 x 32 x 16 B = 32 KB per CTA
+    __shared__ uint4 ring[kWarps][kTailStages][2][32];
+    uint4(*my)[2][32] = ring[threadIdx.x >> 5];
+    if (lane == 0 && v1 > v0) {
+      prefetch_l2(rowT + v0, (unsigned)((v1 - v0) * sizeof(S)));
+      if (k.residual) prefetch_l2(rowD + v0, (unsigned)((v1 - v0) * sizeof(S)));
+    }
+    // group q holds step q's copies (an empty group past the end keeps the
+    // count uniform); elements past v1 fill whole vectors (V * esz % 16 == 0)
+    auto issue = [&](int q) {
+      const int e = e0 + q * STEPW;
+      if (q < nsteps && e < v1) {
+        cp_async16(&my[q % kTailStages][0][lane], rowT + e);
+        if (k.residual) cp_async16(&my[q % kTailStages][1][lane], rowD + e);
+      }
+      cp_async_commit();
+    };
+#pragma unroll
+    for (int q = 0; q < kTailStages - 1; ++q) issue(q);
+    for (int q = 0; q < nsteps; ++q) {
+      issue(q + kTailStages - 1);  // refills the stage step q - 1 used
+      cp_async_wait<kTailStages - 1>();  // step q's group has landed
+      const int e = e0 + q * STEPW;
+      Raw<E, VEC> t, d;
+      if (e < v1) {
+        t.w = ld_shared16(&my[q % kTailStages][0][lane]);
+        d.w = k.residual ? ld_shared16(&my[q % kTailStages][1][lane]) : t.w;
+      } else {
+        t.w = make_uint4(E::kNegInfWord, E::kNegInfWord, E::kNegInfWord, E::kNegInfWord);
+        d.w = t.w;
+      }
+      const float ps = warp_sum(lane_mass<E, VEC>(t, d, k));
+      if (lane == 0) st_relaxed_f32(gp + q, ps);
+      total += ps;
+    }
+    cp_async_wait<0>();
+    return total;
+    }
     if (lane == 0 && v1 > v0) {
       prefetch_l2(rowT + v0, (unsigned)((v1 - v0) * sizeof(S)));
       if (k.residual) prefetch_l2(rowD + v0, (unsigned)((v1 - v0) * sizeof(S)));
     }
   }
-  float total = 0.f;
-  int e = v0 + lane * VEC;
-  Raw<E, VEC> t0{}, d0{}, t1{}, d1{};
-  if (nsteps > 0) {
-    t0 = load_raw<E, VEC>(rowT, e, v1);
-    d0 = k.residual ? load_raw<E, VEC>(rowD, e, v1) : t0;
-  }
-  for (int q = 0; q < nsteps; q += 2, e += 2 * STEPW) {
-    const bool has1 = q + 1 < nsteps;
-    if (has1) {
-      t1 = load_raw<E, VEC>(rowT, e + STEPW, v1);
-      d1 = k.residual ? load_raw<E, VEC>(rowD, e + STEPW, v1) : t1;
+  {
+    Raw<E, VEC> t0{}, d0{}, t1{}, d1{};
+    int e = e0;
+    if (nsteps > 0) {
+      t0 = load_raw<E, VEC>(rowT, e, v1);
+      d0 = k.residual ? load_raw<E, VEC>(rowD, e, v1) : t0;
     }
-    float ps = warp_sum(lane_mass<E, VEC>(t0, d0, k));
-    if (lane == 0) st_relaxed_f32(gp + q, ps);
-    total += ps;
-    if (has1) {
-      if (q + 2 < nsteps) {
-        t0 = load_raw<E, VEC>(rowT, e + 2 * STEPW, v1);
-        d0 = k.residual ? load_raw<E, VEC>(rowD, e + 2 * STEPW, v1) : t0;
+    for (int q = 0; q < nsteps; q += 2, e += 2 * STEPW) {
+      const bool has1 = q + 1 < nsteps;
+      if (has1) {
+        t1 = load_raw<E, VEC>(rowT, e + STEPW, v1);
+        d1 = k.residual ? load_raw<E, VEC>(rowD, e + STEPW, v1) : t1;
       }
-      ps = warp_sum(lane_mass<E, VEC>(t1, d1, k));
-      if (lane == 0) st_relaxed_f32(gp + q + 1, ps);
+      float ps = warp_sum(lane_mass<E, VEC>(t0, d0, k));
+      if (lane == 0) st_relaxed_f32(gp + q, ps);
       total += ps;
+      if (has1) {
+        if (q + 2 < nsteps) {
+          t0 = load_raw<E, VEC>(rowT, e + 2 * STEPW, v1);
+          d0 = k.residual ? load_raw<E, VEC>(rowD, e + 2 * STEPW, v1) : t0;
+        }
+        ps = warp_sum(lane_mass<E, VEC>(t1, d1, k));
+        if (lane == 0) st_relaxed_f32(gp + q + 1, ps);
+        total += ps;
+      }
     }
   }
   return total;
@@ -480,7 +536,7 @@ __device__ __forceinline__ int warp_cdf_search(int count, double theta, double r
   return last;
 }
 
-template <class E, int VEC>
+template <class E, int VEC, bool RING>
 __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   using S = typename E::storage;
   constexpr int STEPW = 32 * VEC;
@@ -514,7 +570,7 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
     si.mode = kModeBonus;
     z = 0.0;
     for (int t = 0; t < C; ++t) {
-      const float tot = tail_slice_mass<E, VEC>(a, b, t, si);
+      const float tot = tail_slice_mass<E, VEC, RING>(a, b, t, si);
       if (lane == 0) st_relaxed_f32(ts + t, tot);
       if (lane == (t & 31)) z += (double)tot;
     }
@@ -598,6 +654,21 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   commit_arrive(a, b);
 }
 
+// Stream order.  Claim index f is first mapped to a position-major index:
+// the NA slices of the front positions (the row pairs of positions below
+// the front count, every sequence) are spread through the stream, FA of every
+// FQ claims, and the rest of the position-major order fills the other claims
+// and the end of the stream.  Decisions (which mostly come from the front
+// positions) then arrive at a steady rate instead of in one burst, so their
+// tail work interleaves with the statistics stream, while the end of the
+// stream holds later positions, which gate few decisions.
+__device__ __forceinline__ int stream_to_pm(const SampleArgs& a, int f) {
+  const int blk = fdiv(f, a.div_fq), r = f - blk * a.FQ;
+  const int before = blk * a.FA;  // front slices in earlier blocks (before the cap)
+  if (r < a.FA && before + r < a.NA) return before + r;
+  return a.NA + f - min(a.NA, before + min(r, a.FA));
+}
+
 // Flat statistics slice f, position-major: the slices of position 0 of every
 // sequence come first (for each sequence its target row, then its draft
 // row), then position 1, and so on; position K (the bonus rows) comes last.
@@ -653,7 +724,17 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int i, int r
   int e = v0 + lane * VEC;
   Raw<E, VEC> z0[kUnroll], z1[kUnroll];
   if constexpr (VEC > 1) {
-    if (lane == 0 && v1 > v0) prefetch_l2(row + v0, (unsigned)((v1 - v0) * sizeof(S)));
+    if (lane == 0 && v1 > v0) {
+      const unsigned bytes = (unsigned)((v1 - v0) * sizeof(S));
+      if (i < a.l2_keep)
+        prefetch_l2_pol(row + v0, bytes, l2_policy_evict_last());
+      else if (a.l2_other == 1)
+        prefetch_l2_pol(row + v0, bytes, l2_policy_evict_first());
+      else if (a.l2_other == 2)
+        prefetch_l2_pol(row + v0, bytes, l2_policy_evict_normal());
+      else
+        prefetch_l2(row + v0, bytes);
+    }
   }
   if (nb > 0) load_batch<E, VEC>(z0, row, e, v1);
   for (int bt = 0; bt < nb; bt += 2, e += 2 * BATCH) {
@@ -685,12 +766,12 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int i, int r
 
 // Tail slice s of a decided sequence: the slice's pieces and mass, then the
 // sequence's tail ticket; the last ticket runs the select finisher.
-template <class E, int VEC>
+template <class E, int VEC, bool RING>
 __device__ __noinline__ void tail_slice(const SampleArgs& a, const SeqInfo& si, int s) {
   const int lane = threadIdx.x & 31;
   if (si.mode == kModeBad) return;  // no draw: the decision made the result-side commit arrival
   const int b = si.b;
-  const float tot = tail_slice_mass<E, VEC>(a, b, s, si);
+  const float tot = tail_slice_mass<E, VEC, RING>(a, b, s, si);
   int old = 0;
   if (lane == 0) {
     // pieces and mass are marker-validated by the reader: no ordering needed
@@ -698,7 +779,7 @@ __device__ __noinline__ void tail_slice(const SampleArgs& a, const SeqInfo& si, 
     old = ticket_take(&a.tailticket[b]);
   }
   old = __shfl_sync(0xffffffffu, old, 0);
-  if (old == a.TC - 1) select_finisher<E, VEC>(a, si);
+  if (old == a.TC - 1) select_finisher<E, VEC, RING>(a, si);
 }
 
 // The next counter after ctr (cyclically) that this warp has not seen run dry.
@@ -765,7 +846,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
         next = claim_from(a.counter, nctr, lane);
       }
       if (!tail_ready) seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
-      const SliceId id = decode_slice(a, f);
+      const SliceId id = decode_slice(a, stream_to_pm(a, f));
       const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC, ENT>(a, id.b, id.i, id.r, id.s), 0);
       if (old == unit_slices(a, id.i) - 1) unit_finisher<E, ENT>(a, id.b, id.i);
       if (ahead) {
@@ -777,7 +858,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
     if (tail_ready) {
       const int pos = fdiv(t, a.div_tc);
       const SeqInfo si = read_decision(a, pos);
-      tail_slice<E, VEC>(a, si, t - pos * a.TC);
+      tail_slice<E, VEC, (VEC > 1)>(a, si, t - pos * a.TC);
       t += W;
       seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
       continue;

@@ -2,14 +2,15 @@
 // (api.cu) and the kernel translation units.  Internal to the library.
 //
 // Work decomposition (all three kernels): a persistent grid of independent
-// warps.  A row is cut into slices of SL elements.  Slices are numbered flat,
-// sequence-major (sequence, row, slice), and slice f is handed out by claim
-// counter f % kSlices; warp w of every CTA claims from counter w, so each
+// warps.  A row is cut into slices of SL elements.  Slices are numbered flat
+// (the argmax kernels: sequence-major; the sampling kernel: by draft
+// position) and slice f is handed out by claim counter f % kSlices, so each
 // counter sees one eighth of the claims and every counter has the same amount
 // of work.  A slice is reduced to one partial result in the workspace; the
-// warp that takes a row's (and then a sequence's) last ticket runs the
-// finisher.  There are no CTA-wide barriers: a warp that finishes a row or a
-// sequence stalls only itself.
+// warp that takes the last ticket of a row (argmax kernels) or of a
+// position's row pair (sampling kernel) runs the finisher.  There are no
+// CTA-wide barriers: a warp that finishes a row or a sequence stalls only
+// itself.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -84,7 +85,12 @@ struct SampleArgs {
   int P;   // pieces (warp steps) per tail slice
   int F;   // statistics slices in all: B * R * CS
   int FP;  // slices of positions 0..K-1 (row pairs), which come first: K * B * 2 * CS
+  int NA;  // slices of the front positions (spread through the stream)
+  int FA, FQ;  // FA front slices in every block of FQ claims
+  FastDiv div_fq;
   int claim_tail;  // within this many slices of the end, claims are not made ahead
+  int l2_keep;     // rows of positions < l2_keep are prefetched into L2 with evict_last
+  int l2_other;    // the other rows: 0 default prefetch, 1 evict_first, 2 evict_normal
   FastDiv div_pos, div_pair, div_cs, div_tc;  // division by B * 2 * CS, 2 * CS, CS and TC
   float c_hi, c_lo;  // log2(e)/temperature as a float pair
   double c64;        // the same in double

@@ -69,6 +69,8 @@ def _load():
     lib.oracle_row_entropy.restype = None
     lib.oracle_tree_verify_sampling.argtypes = [P, P, i32, P, P, i32, i32, i32, f64, u64, P, P, P]
     lib.oracle_tree_verify_sampling.restype = i32
+    lib.oracle_ngram_draft.argtypes = [P, i64, P, i32, i32, i32, i32, P, P, P]
+    lib.oracle_ngram_draft.restype = i32
     _lib = lib
     return lib
 
@@ -277,3 +279,27 @@ def tree_verify_sampling(target, draft, tree_tokens, parent_idx, temperature: fl
     if rc != 0:
         raise MemoryError("oracle_tree_verify_sampling failed to allocate")
     return dict(path=path, length=length, boundary=boundary)
+
+
+def ngram_draft(tokens, lengths, n_min: int, n_max: int, K: int):
+    """N-gram (prompt-lookup) drafts.  tokens [B, Lmax] int32 histories (row b
+    holds lengths[b] valid tokens), lengths [B].  Returns dict(drafts [B, K]
+    (-1 padded), n_drafts [B], match_len [B]); a length outside [0, Lmax]
+    gives n_drafts = match_len = -1."""
+    lib = _load()
+    tok = _as_i32(tokens)
+    if tok.ndim != 2:
+        raise ValueError("tokens must be [B, Lmax]")
+    B, Lmax = tok.shape
+    ln = np.ascontiguousarray(np.asarray(lengths, dtype=np.int32).reshape(-1))
+    if ln.size != B:
+        raise ValueError("lengths must have B entries")
+    drafts = np.full((B, max(K, 0)), -1, dtype=np.int32)
+    n_drafts = np.zeros(B, dtype=np.int32)
+    match_len = np.zeros(B, dtype=np.int32)
+    tok_buf = tok if tok.size else np.zeros(1, dtype=np.int32)
+    ln_buf = ln if ln.size else np.zeros(1, dtype=np.int32)
+    d_buf = drafts if drafts.size else np.zeros(1, dtype=np.int32)
+    lib.oracle_ngram_draft(_ptr(tok_buf), int(Lmax), _ptr(ln_buf), int(B), int(n_min), int(n_max), int(K),
+                           _ptr(d_buf), _ptr(n_drafts), _ptr(match_len))
+    return dict(drafts=drafts, n_drafts=n_drafts, match_len=match_len)

@@ -671,3 +671,69 @@ int oracle_tree_verify_sampling(const void *target, const void *draft, int dtype
     free(P); free(Q); free(R);
     return 0;
 }
+
+/*
+ * N-gram (prompt-lookup) drafting
+ *   [P2] "Speculative Decoding for LLM Inference: How Draft-and-Verify
+ *   Accelerates Token Generation", sections "The variant landscape" and
+ *   "Support in production systems", and the FAQ "Do all variants require a
+ *   separate draft model?": candidate continuations are copied from the prompt
+ *   or the output so far through an n-gram lookup, with no drafter weights.
+ * Reading (the pages fix no rule): for each sequence b with history
+ * tokens[b][0 .. L-1], try the match length m = n_max, n_max - 1, ..., n_min.
+ * For the first m that occurs, take the latest earlier occurrence of the last
+ * m tokens: the largest end e (exclusive, e <= L - 1, so at least one token
+ * follows it) with tokens[e - m .. e - 1] == tokens[L - m .. L - 1].  The
+ * drafts are the tokens that follow it, tokens[e .. e + d - 1] with
+ * d = min(K, L - e).  Outputs: drafts [B, K] (-1 past d), n_drafts [B] = d
+ * (0 when nothing matches), match_len [B] = m (0 when nothing matches).  A
+ * length outside [0, stride] marks the sequence bad: n_drafts = match_len = -1
+ * and every draft -1.  Token values are compared and copied as given.
+ */
+int oracle_ngram_draft(const int32_t *tokens, long long stride, const int32_t *lengths, int B, int n_min,
+                       int n_max, int K, int32_t *drafts, int32_t *n_drafts, int32_t *match_len)
+{
+    for (int b = 0; b < B; ++b) {
+        const int32_t *h = tokens + (long long)b * stride;
+        const long long L = lengths[b];
+        for (int i = 0; i < K; ++i)
+            drafts[(long long)b * K + i] = -1;
+        if (L < 0 || L > stride) {
+            n_drafts[b] = -1;
+            match_len[b] = -1;
+            continue;
+        }
+        n_drafts[b] = 0;
+        match_len[b] = 0;
+        long long found_e = -1;
+        int found_m = 0;
+        for (int m = n_max; m >= n_min && found_e < 0; --m) {
+            if (L < (long long)m + 1)
+                continue;  /* no room for the suffix and one earlier token */
+            for (long long e = L - 1; e >= m; --e) {
+                int same = 1;
+                for (int t = 0; t < m; ++t) {
+                    if (h[e - m + t] != h[L - m + t]) {
+                        same = 0;
+                        break;
+                    }
+                }
+                if (same) {
+                    found_e = e;
+                    found_m = m;
+                    break;
+                }
+            }
+        }
+        if (found_e < 0)
+            continue;
+        long long d = L - found_e;
+        if (d > K)
+            d = K;
+        for (long long i = 0; i < d; ++i)
+            drafts[(long long)b * K + i] = h[found_e + i];
+        n_drafts[b] = (int32_t)d;
+        match_len[b] = found_m;
+    }
+    return 0;
+}

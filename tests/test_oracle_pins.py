@@ -593,3 +593,90 @@ def test_tree_sampling_bad_data():
     out = oracle.tree_verify_sampling(T, D, tok, par, 1.0, 0)
     assert out["length"].tolist()[1:] == [-1, -1] and (out["path"][1:] == -1).all()
     assert out["length"][0] >= 1
+
+
+# --------------------------------------------------------------------------
+# n-gram (prompt-lookup) drafting
+# --------------------------------------------------------------------------
+def _ngram_by_index(h, n_min, n_max, K):
+    """The same reading by a different route: for each match length m a
+    dictionary from every m-gram of the history to the end (exclusive) of its
+    latest occurrence that still has a following token, then one lookup of
+    the last m tokens."""
+    L = len(h)
+    for m in range(n_max, n_min - 1, -1):
+        if L < m + 1:
+            continue
+        last_end = {}
+        for e in range(m, L):  # e <= L - 1: one token follows
+            last_end[tuple(h[e - m:e])] = e
+        e = last_end.get(tuple(h[L - m:L]))
+        if e is not None:
+            d = min(K, L - e)
+            return list(h[e:e + d]), d, m
+    return [], 0, 0
+
+
+def test_ngram_worked_cases():
+    cases = [
+        # suffix (5,6,7) also ends at 3; the three tokens after it are 8,5,6
+        ([5, 6, 7, 8, 5, 6, 7], 2, 3, 3, [8, 5, 6], 3),
+        # a run: the latest earlier (9,9) ends at 3, one token (9) follows
+        ([9, 9, 9, 9], 1, 2, 4, [9], 2),
+        # (9,3,4) never occurred before; (3,4) ends at 4; drafts 9,3,4
+        ([1, 2, 3, 4, 9, 3, 4], 1, 3, 3, [9, 3, 4], 2),
+        # two earlier (1,2): the latest one (end 5) wins, then 7 and the 1,2
+        ([1, 2, 3, 1, 2, 7, 1, 2], 2, 2, 4, [7, 1, 2], 2),
+        # nothing repeats
+        ([1, 2, 3, 4, 5], 1, 3, 2, [], 0),
+        # K = 0: a match, no drafts
+        ([4, 4, 4], 1, 1, 0, [], 1),
+    ]
+    for h, n_min, n_max, K, want, m in cases:
+        out = oracle.ngram_draft(np.array([h], dtype=np.int32), [len(h)], n_min, n_max, K)
+        d = int(out["n_drafts"][0])
+        assert d == len(want) and out["drafts"][0, :d].tolist() == want, (h, out)
+        assert (out["drafts"][0, d:] == -1).all()
+        assert int(out["match_len"][0]) == m, (h, out)
+
+
+def test_ngram_matches_the_dictionary_index():
+    rng = np.random.default_rng(7)
+    for trial in range(400):
+        B = int(rng.integers(1, 6))
+        Lmax = int(rng.integers(1, 60))
+        alphabet = int(rng.integers(2, 6))
+        toks = rng.integers(0, alphabet, size=(B, Lmax)).astype(np.int32)
+        lengths = rng.integers(0, Lmax + 1, size=B).astype(np.int32)
+        n_min = int(rng.integers(1, 4))
+        n_max = n_min + int(rng.integers(0, 4))
+        K = int(rng.integers(0, 7))
+        out = oracle.ngram_draft(toks, lengths, n_min, n_max, K)
+        for b in range(B):
+            want, d, m = _ngram_by_index(toks[b, :lengths[b]].tolist(), n_min, n_max, K)
+            assert int(out["n_drafts"][b]) == d and int(out["match_len"][b]) == m
+            assert out["drafts"][b, :d].tolist() == want
+            assert (out["drafts"][b, d:] == -1).all()
+
+
+def test_ngram_copy_property_and_bad_lengths():
+    rng = np.random.default_rng(11)
+    toks = rng.integers(0, 3, size=(8, 200)).astype(np.int32)
+    lengths = np.array([200, 150, 3, 2, 1, 0, -1, 201], dtype=np.int32)
+    out = oracle.ngram_draft(toks, lengths, 2, 5, 6)
+    for b in range(6):
+        L, m, d = int(lengths[b]), int(out["match_len"][b]), int(out["n_drafts"][b])
+        if m == 0:
+            assert d == 0
+            continue
+        h = toks[b, :L]
+        # the drafts continue an earlier copy of the last m tokens
+        e = next(e for e in range(L - 1, m - 1, -1)
+                 if (h[e - m:e] == h[L - m:L]).all() and (h[e:e + d] == out["drafts"][b, :d]).all())
+        assert d == min(6, L - e)
+        # no longer match exists anywhere earlier
+        if m < 5:
+            mm = m + 1
+            assert not any((h[e2 - mm:e2] == h[L - mm:L]).all() for e2 in range(mm, L)) or L < mm + 1
+    for b in (6, 7):
+        assert out["n_drafts"][b] == -1 and out["match_len"][b] == -1 and (out["drafts"][b] == -1).all()

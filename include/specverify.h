@@ -270,6 +270,41 @@ int spec_acceptance_stats(const int32_t *n_accepted, int B, int K, uint64_t *out
                           double *out_alpha, double *out_mean_tokens, cudaStream_t stream);
 
 /*
+ * N-gram (prompt-lookup) drafting: for every sequence, draft up to K tokens by
+ * copying what followed an earlier occurrence of the history's last tokens
+ * ([P2] "Speculative Decoding for LLM Inference: How Draft-and-Verify
+ * Accelerates Token Generation", sections "The variant landscape" and
+ * "Support in production systems", FAQ "Do all variants require a separate
+ * draft model?": candidates copied from the prompt or prior output through an
+ * n-gram lookup, no drafter weights).
+ *   tokens        [B, stride] int32, device: row b holds the history of
+ *                 sequence b (prompt and output so far) in its first
+ *                 lengths[b] entries; the rest is never read.
+ *   lengths       [B] int32, device.
+ *   n_min, n_max  match lengths tried, longest first: 1 <= n_min <= n_max <= 32.
+ *   K             drafts per sequence, 0 <= K <= 4096.
+ *   out_drafts    [B, K] int32, device: the drafts, -1 past the last one.
+ *   out_n_drafts  [B] int32, device: the number of drafts (0 when nothing
+ *                 matches).
+ *   out_match_len [B] int32, device (may be NULL): the match length m used (0
+ *                 when nothing matches).
+ * Rule: the longest m in [n_min, n_max] whose last-m-token suffix occurred
+ * earlier wins; of its occurrences the latest one with at least one token
+ * after it (end e <= L - 1) is copied: drafts = h[e .. e + d - 1],
+ * d = min(K, L - e).  Token values are compared and copied as given.
+ * Bad data: a length outside [0, stride] gives n_drafts = match_len = -1 and
+ * -1 drafts for that sequence and sets SPEC_FLAG_BAD_DATA.
+ * Each history token is read from device memory once; scratch (8 bytes per
+ * sequence) comes from the library's stream-ordered pool.  Returns SPEC_OK,
+ * SPEC_ERR_NULL (an output, or tokens / lengths with B > 0, is NULL),
+ * SPEC_ERR_SHAPE (B < 0, stride < 1 or above 2^30, bad n_min / n_max / K) or
+ * SPEC_ERR_CUDA.  Asynchronous on `stream`.
+ */
+int spec_ngram_draft(const int32_t *tokens, const int32_t *lengths, int B, int stride, int n_min,
+                     int n_max, int K, int32_t *out_drafts, int32_t *out_n_drafts,
+                     int32_t *out_match_len, cudaStream_t stream);
+
+/*
  * Synchronises `stream`, then returns in *flags_out (may be NULL) the device
  * status word of the current device (an OR of SPEC_FLAG_* set by every call
  * since the last read) and clears it.  Returns SPEC_OK or SPEC_ERR_CUDA.

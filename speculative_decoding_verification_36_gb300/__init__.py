@@ -23,7 +23,8 @@ from ._lib import SPEC_FLAG_BAD_DATA, SPEC_FLAG_TIMEOUT, SpecError
 
 __all__ = [
     "spec_verify", "spec_verify_static_scratch", "spec_verify_stats", "spec_verify_greedy_argmax",
-    "spec_tree_verify_greedy", "spec_tree_verify_sampling", "spec_acceptance_stats", "spec_get_status", "SpecError",
+    "spec_tree_verify_greedy", "spec_tree_verify_sampling", "spec_acceptance_stats", "spec_ngram_draft",
+    "spec_get_status", "SpecError",
     "SPEC_FLAG_BAD_DATA", "SPEC_FLAG_TIMEOUT",
 ]
 
@@ -254,6 +255,29 @@ def spec_acceptance_stats(n_accepted, K: int, stream=None):
                                              _ptr(hist), _ptr(alpha) if K > 0 else None, _ptr(mean),
                                              _stream(stream)))
     return dict(hist=hist, alpha=alpha, mean_tokens=mean[0])
+
+
+def spec_ngram_draft(tokens, lengths, n_min: int, n_max: int, K: int, out_drafts=None, out_n_drafts=None,
+                     out_match_len=None, stream=None):
+    """N-gram (prompt-lookup) drafts from token histories on the device.
+
+    tokens: int32 [B, Lmax] (row b's first lengths[b] entries are its history);
+    lengths: int32 [B].  Returns (drafts int32 [B, K] (-1 padded), n_drafts
+    int32 [B], match_len int32 [B])."""
+    if tokens.dim() != 2:
+        raise ValueError("tokens must be [B, Lmax]")
+    B, Lmax = tokens.shape
+    _i32(tokens, (B, Lmax), "tokens")
+    _i32(lengths, (B,), "lengths")
+    dev = tokens.device
+    drafts = _out(out_drafts, (B, max(int(K), 0)), torch.int32, dev, "out_drafts")  # K < 0: the C layer refuses
+    n_drafts = _out(out_n_drafts, (B,), torch.int32, dev, "out_n_drafts")
+    match_len = _out(out_match_len, (B,), torch.int32, dev, "out_match_len")
+    lib = _lib.load()
+    with torch.cuda.device(dev):
+        _lib.check(lib.spec_ngram_draft(_ptr(tokens), _ptr(lengths), B, Lmax, int(n_min), int(n_max), int(K),
+                                        _ptr(drafts), _ptr(n_drafts), _ptr(match_len), _stream(stream)))
+    return drafts, n_drafts, match_len
 
 
 def spec_get_status(stream=None, device=None) -> int:

@@ -47,6 +47,7 @@ SIGNATURES = {
     "spec_tree_verify_sampling_f32": [_P, _P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_tree_verify_sampling_bf16": [_P, _P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_acceptance_stats": [_P, _I, _I, _P, _P, _P, _P],
+    "spec_ngram_draft": [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P],
     "spec_get_status": [_P, _P],
     "spec_status_string": [_I],
 }

@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD_DIR = os.path.join(PKG, "_build")
 LIB_PATH = os.path.join(PKG, "libspecverify.so")
 SOURCES = ["api.cu", "sample_kernel.cu", "greedy_kernel.cu", "acceptance_kernel.cu",
-           "tree_sample_kernel.cu"]
+           "tree_sample_kernel.cu", "ngram_kernel.cu"]
 HEADERS = ["sv_common.cuh", "sv_kernels.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

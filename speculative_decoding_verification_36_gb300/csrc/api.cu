@@ -560,6 +560,52 @@ int spec_acceptance_stats(const int32_t* n_accepted, int B, int K, uint64_t* out
   return SPEC_OK;
 }
 
+int spec_ngram_draft(const int32_t* tokens, const int32_t* lengths, int B, int stride, int n_min, int n_max,
+                     int K, int32_t* out_drafts, int32_t* out_n_drafts, int32_t* out_match_len,
+                     cudaStream_t stream) {
+  if (B < 0 || stride < 1 || stride > (1 << 30) || n_min < 1 || n_max < n_min || n_max > sv::kNgramMaxN ||
+      K < 0 || K > 4096)
+    return SPEC_ERR_SHAPE;
+  if (B == 0) return SPEC_OK;
+  if (!tokens || !lengths || !out_n_drafts || (K > 0 && !out_drafts)) return SPEC_ERR_NULL;
+  const long long chunks = ((long long)stride + sv::ngram_chunk() - 1) / sv::ngram_chunk();
+  if ((long long)B * chunks >= (1LL << 31)) return SPEC_ERR_SHAPE;
+  DeviceState* d = nullptr;
+  int rc = get_device_state(&d);
+  if (rc) return rc;
+  sv::NgramArgs a;
+  memset(&a, 0, sizeof a);
+  a.tokens = tokens;
+  a.stride = stride;
+  a.lengths = lengths;
+  a.B = B;
+  a.n_min = n_min;
+  a.n_max = n_max;
+  a.K = K;
+  a.chunks = (int)chunks;
+  a.vec = aligned16(tokens) && stride % 4 == 0;
+  a.drafts = out_drafts;
+  a.n_drafts = out_n_drafts;
+  a.status = d->status;
+  // match_len is optional: without it the kernel writes into scratch
+  sv::WsLayout l;
+  const size_t keys = ((size_t)B * 8 + 255) / 256 * 256;
+  l.total = keys + (out_match_len ? 0 : ((size_t)B * 4 + 255) / 256 * 256);
+  l.zero_bytes = 0;
+  l.marker_off = 0;
+  l.marker_bytes = keys;  // all-ones: empty keys (stored complemented)
+  void* ws = nullptr;
+  rc = get_scratch(d, false, l, stream, &ws);
+  if (rc) return rc;
+  a.key = (unsigned long long*)ws;
+  a.match_len = out_match_len ? out_match_len : (int32_t*)((char*)ws + keys);
+  cudaError_t e = sv::launch_ngram(a, stream);
+  cudaError_t e2 = put_scratch(false, ws, stream);
+  if (e != cudaSuccess) return cuda_fail(e, "n-gram drafting launch");
+  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
+  return SPEC_OK;
+}
+
 int spec_get_status(cudaStream_t stream, uint32_t* flags_out) {
   DeviceState* d = nullptr;
   int rc = get_device_state(&d);

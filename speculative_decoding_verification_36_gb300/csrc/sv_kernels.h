@@ -208,6 +208,27 @@ cudaError_t launch_sample(const SampleArgs& a, bool bf16, bool vec, int grid, cu
 cudaError_t launch_greedy(const GreedyArgs& a, bool bf16, bool vec, int grid, cudaStream_t s);
 cudaError_t launch_tree(const GreedyArgs& a, bool bf16, bool vec, int grid, cudaStream_t s);
 
+// N-gram (prompt-lookup) drafting (ngram_kernel.cu).  CTA (b, c) scans chunk
+// c of sequence b's candidate match ends; a second launch writes the drafts.
+// Workspace (filled with all-ones bytes): key [B] (the best (m << 32) | e,
+// stored complemented).
+constexpr int kNgramMaxN = 32;  // longest n-gram matched
+struct NgramArgs {
+  const int32_t* tokens;   // [B, stride] histories
+  long long stride;        // row stride and the largest valid length
+  const int32_t* lengths;  // [B]
+  int B, n_min, n_max, K;
+  int chunks;              // CTAs per sequence: ceil((stride) / chunk)
+  int vec;                 // every row starts on a 16-byte boundary (16-byte loads)
+  int32_t* drafts;         // [B, K]
+  int32_t* n_drafts;       // [B]
+  int32_t* match_len;      // [B]
+  unsigned long long* key;
+  unsigned* status;
+};
+int ngram_chunk();
+cudaError_t launch_ngram(const NgramArgs& a, cudaStream_t s);
+
 // Acceptance statistics: zeroes hist[0..K+1], counts n_accepted into it and,
 // when alpha / mean_tokens are given, derives them (acceptance_kernel.cu).
 cudaError_t launch_acceptance(const int32_t* n, int B, int K, unsigned long long* hist, double* alpha,

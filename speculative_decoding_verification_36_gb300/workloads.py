@@ -200,3 +200,35 @@ def make_tree_sampling(p: TreePreset, temperature: float = 1.0, device="cpu", se
     parents_b = par.to(device).unsqueeze(0).expand(B, N).contiguous()
     return dict(target=target, draft=draft, tokens=tokens.contiguous(), parents=parents_b,
                 temperature=float(temperature))
+
+
+def make_ngram_histories(B: int, Lmax: int, V: int = 128256, seed: int = 0, copy_prob: float = 0.5,
+                         device="cpu", alphabet: int | None = None):
+    """Token histories for n-gram drafting: dict(tokens [B, Lmax] int32,
+    lengths [B] int32).
+
+    The pages place n-gram lookup on input-grounded, repetitive work
+    (summaries and code edits that echo their input), so each history is
+    built from segments: with probability copy_prob a segment copies a span
+    of 8-64 tokens from earlier in the same history, otherwise it is 8-64
+    fresh tokens drawn uniformly from [0, V) (or [0, alphabet) when given, for
+    dense small-vocabulary cases).  Lengths are uniform in [Lmax / 2, Lmax];
+    entries past a row's length are -7 (never read)."""
+    g = torch.Generator(device="cpu")
+    g.manual_seed(12345 + 1000 * 7 + int(seed))
+    hi = V if alphabet is None else alphabet
+    tokens = torch.full((B, Lmax), -7, dtype=torch.int32)
+    lengths = torch.randint(max(Lmax // 2, 0), Lmax + 1, (B,), generator=g, dtype=torch.int32)
+    for b in range(B):
+        L = int(lengths[b])
+        row = []
+        while len(row) < L:
+            n = int(torch.randint(8, 65, (1,), generator=g))
+            if row and float(torch.rand((1,), generator=g)) < copy_prob:
+                start = int(torch.randint(0, len(row), (1,), generator=g))
+                seg = row[start:start + n]
+            else:
+                seg = torch.randint(0, hi, (n,), generator=g, dtype=torch.int32).tolist()
+            row.extend(seg)
+        tokens[b, :L] = torch.tensor(row[:L], dtype=torch.int32)
+    return dict(tokens=tokens.to(device), lengths=lengths.to(device))

@@ -20,6 +20,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -119,7 +120,7 @@ class ClockSampler:
     def __init__(self, uuid: str | None):
         self.uuid = uuid
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_{os.getpid()}.csv")
+        self.path = os.path.join(tempfile.gettempdir(), f"specverify_clocks_{os.getpid()}.csv")
 
     def __enter__(self):
         try:

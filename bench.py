@@ -245,10 +245,37 @@ def run_reference(args):
     return 0
 
 
+def gpu_local_cpus(dev):
+    """CPUs on the host socket the GPU is attached to (from the PCI device's
+    local_cpulist), or None when the system does not say."""
+    import torch
+    try:
+        pr = torch.cuda.get_device_properties(dev)
+        path = "/sys/bus/pci/devices/%04x:%02x:%02x.0/local_cpulist" % (
+            pr.pci_domain_id, pr.pci_bus_id, pr.pci_device_id)
+        cpus = set()
+        for part in open(path).read().strip().split(","):
+            if "-" in part:
+                lo, hi = part.split("-")
+                cpus.update(range(int(lo), int(hi) + 1))
+            elif part:
+                cpus.add(int(part))
+        usable = cpus & os.sched_getaffinity(0)
+        return usable or None
+    except Exception:
+        return None
+
+
 def run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps):
     """The same metric through the public API with the inputs copied from
-    pinned host memory and the outputs read back, every step."""
+    pinned host memory and the outputs read back, every step.  The process is
+    first bound to the CPUs of the GPU's own socket, so that the pinned
+    buffers are allocated (first touch) in the memory next to the GPU, as a
+    serving process would place them."""
     import torch
+    local = gpu_local_cpus(dev)
+    if local:
+        os.sched_setaffinity(0, local)
     host = [{k: sets[i][k].cpu().pin_memory() for k in ("target", "draft", "tokens")}
             for i in range(len(sets))]
     host_out = (torch.empty((p.B, p.K + 1), dtype=torch.int32).pin_memory(),
@@ -279,7 +306,7 @@ def run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps):
     barrier(world)
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_value = world * p.B * e2e_steps / (e2e_ms / 1e3)
-    return e2e_value, h2d, d2h
+    return e2e_value, h2d, d2h, (len(local) if local else None)
 
 
 def run_gpu(args):
@@ -343,9 +370,9 @@ def run_gpu(args):
 
     # end to end through the public API from pinned host buffers
     e2e_steps = min(args.steps, args.e2e_steps)
-    e2e_value, h2d, d2h = None, 0, 0
+    e2e_value, h2d, d2h, e2e_cpus = None, 0, 0, None
     if e2e_steps > 0:
-        e2e_value, h2d, d2h = run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps)
+        e2e_value, h2d, d2h, e2e_cpus = run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps)
 
     if rank != 0:
         if world > 1:
@@ -369,7 +396,9 @@ def run_gpu(args):
                      if peak_kind == "measured" else "fallback 6.8 TB/s",
                      "avg_launch_ms": avg_launch_ms, "bytes_per_launch": abytes},
         "e2e": ({"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
-                 "d2h_bytes_per_step": d2h, "steps": e2e_steps} if e2e_steps > 0 else None),
+                 "d2h_bytes_per_step": d2h, "steps": e2e_steps,
+                 "host_buffers": ("pinned, allocated from the %d CPUs of the GPU's socket" % e2e_cpus)
+                 if e2e_cpus else "pinned"} if e2e_steps > 0 else None),
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "status_flags": flags,

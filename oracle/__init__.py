@@ -56,7 +56,7 @@ def _load():
     lib.oracle_philox4x64_10.restype = None
     lib.oracle_uniform.argtypes = [u64, u64, u64, u64]
     lib.oracle_uniform.restype = f64
-    lib.oracle_spec_verify.argtypes = [P, P, i32, i64, i64, P, i64, i32, i32, i32, f64, u64, P,
+    lib.oracle_spec_verify.argtypes = [P, P, i32, i64, i64, P, i64, i32, i32, i32, f64, u64, P, i32,
                                        P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.oracle_spec_verify.restype = i32
     lib.oracle_spec_verify_greedy.argtypes = [P, i32, i64, P, i64, i32, i32, i32, P, P, P]
@@ -129,7 +129,8 @@ def uniform(seed: int, b: int, position: int, stream: int) -> float:
 
 
 def spec_verify(target, draft, draft_tokens, temperature: float, seed: int,
-                broadcast: bool = False, n_seq: int | None = None, seq_ids=None):
+                broadcast: bool = False, n_seq: int | None = None, seq_ids=None,
+                used_rows_only: bool = False):
     """Speculative-sampling verification of a batch (temperature > 0).
 
     target: [B, K+1, V]; draft: [B, K, V]; draft_tokens: [B, K].  With
@@ -137,7 +138,10 @@ def spec_verify(target, draft, draft_tokens, temperature: float, seed: int,
     is shared by all ``n_seq`` batch entries (each entry still draws its own
     uniforms through its batch index).  ``seq_ids`` (optional, [B]) gives the
     sequence number each batch entry draws its uniforms with, so that a subset
-    of a larger batch reproduces that batch's draws.  Returns a dict of numpy arrays:
+    of a larger batch reproduces that batch's draws.  ``used_rows_only``
+    checks for bad data only the rows the result depends on (positions 0..n,
+    and target row K when every draft is accepted), as the early-exit verify
+    does.  Returns a dict of numpy arrays:
     tokens [B, K+1], n [B] and the per-sequence diagnostics documented in
     spec_oracle.c.
     """
@@ -180,7 +184,7 @@ def spec_verify(target, draft, draft_tokens, temperature: float, seed: int,
     rc = lib.oracle_spec_verify(
         _ptr(t), _ptr(d_buf), dt, t_stride, d_stride, _ptr(x_buf), tok_stride,
         B, K, V, float(temperature), int(seed) & (2**64 - 1),
-        _ptr(ids) if ids is not None else None,
+        _ptr(ids) if ids is not None else None, int(bool(used_rows_only)),
         _ptr(out["tokens"]), _ptr(out["n"]), _ptr(out["row_logmax"]), _ptr(out["row_sum"]),
         _ptr(out["px"]), _ptr(out["qx"]), _ptr(out["u"]), _ptr(out["acc_margin"]),
         _ptr(out["resid_mass"]), _ptr(out["theta"]), _ptr(out["w"]),

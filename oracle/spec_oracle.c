@@ -211,11 +211,19 @@ static int inverse_cdf(const double *r, int V, double theta, double *dist_out)
  *
  * Returns 0; sequences with bad data get n = -1 and -1 everywhere.
  */
+/*
+ * used_rows_only selects the early-exit reading of the bad-data rule: only
+ * the rows the result depends on are checked, in position order -- target
+ * and draft rows 0..n and the drafted tokens x_0..x_n, plus target row K when
+ * all K drafts are accepted.  A bad position stops the scan and marks the
+ * sequence bad; rows after the first rejection never matter.  Otherwise (the
+ * default) every row and every drafted token is checked before anything else.
+ */
 int oracle_spec_verify(const void *target, const void *draft, int dtype,
                        long long t_stride_b, long long d_stride_b,
                        const int32_t *tokens, long long tok_stride_b,
                        int B, int K, int V, double tau, uint64_t seed,
-                       const long long *seq_ids,
+                       const long long *seq_ids, int used_rows_only,
                        int32_t *out_tokens, int32_t *out_n,
                        double *row_logmax, double *row_sum,
                        double *px_out, double *qx_out, double *u_out, double *acc_margin,
@@ -226,9 +234,11 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype,
     const int R = 2 * K + 1;
     double *probs = (double *)malloc(sizeof(double) * (size_t)R * (size_t)V);
     double *r = (double *)malloc(sizeof(double) * (size_t)V);
-    if (!probs || !r) {
+    int *rowbad = (int *)malloc(sizeof(int) * (size_t)R);
+    if (!probs || !r || !rowbad) {
         free(probs);
         free(r);
+        free(rowbad);
         return -1;
     }
     for (int b = 0; b < B; ++b) {
@@ -255,22 +265,26 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype,
 
         /* bad data: any unusable row or an out-of-range drafted token */
         int bad = 0;
-        for (int rr = 0; rr < R && !bad; ++rr) {
+        for (int rr = 0; rr < R; ++rr) {
             const char *row = rr <= K ? tb + (size_t)rr * V * esz : db + (size_t)(rr - K - 1) * V * esz;
-            bad = row_is_bad(row, dtype, V);
+            rowbad[rr] = row_is_bad(row, dtype, V);
+            if (!used_rows_only)
+                bad = bad || rowbad[rr];
         }
-        for (int i = 0; i < K && !bad; ++i)
+        for (int i = 0; i < K && !bad && !used_rows_only; ++i)
             bad = x[i] < 0 || x[i] >= V;
         if (bad) {
             out_n[b] = -1;
             continue;
         }
 
-        /* step 1: temperature softmax of every target row and draft row */
+        /* step 1: temperature softmax of every target row and draft row
+         * (an unusable row is only ever used when it makes the sequence bad) */
         for (int rr = 0; rr < R; ++rr) {
             const char *row = rr <= K ? tb + (size_t)rr * V * esz : db + (size_t)(rr - K - 1) * V * esz;
-            double m, s;
-            softmax_row(row, dtype, V, tau, probs + (size_t)rr * V, &m, &s);
+            double m = NAN, s = NAN;
+            if (!rowbad[rr])
+                softmax_row(row, dtype, V, tau, probs + (size_t)rr * V, &m, &s);
             if (row_logmax) row_logmax[(size_t)b * R + rr] = m;
             if (row_sum) row_sum[(size_t)b * R + rr] = s;
         }
@@ -281,6 +295,10 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype,
          * min(1, p/q); stop at the first rejection */
         int n = K;
         for (int i = 0; i < K; ++i) {
+            if (used_rows_only && (rowbad[i] || rowbad[K + 1 + i] || x[i] < 0 || x[i] >= V)) {
+                bad = 1;
+                break;
+            }
             double p = p_rows[(size_t)i * V + x[i]];
             double q = q_rows[(size_t)i * V + x[i]];
             double u = oracle_uniform(seed, seq, (uint64_t)i, 0);
@@ -297,6 +315,15 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype,
                 break;
             }
             out[i] = x[i];
+        }
+
+        if (used_rows_only && !bad && n == K && rowbad[K])
+            bad = 1;
+        if (bad) {
+            for (int j = 0; j <= K; ++j)
+                out[j] = -1;
+            out_n[b] = -1;
+            continue;
         }
 
         /* step 5: the replacement distribution max(0, p_n - q_n) after a
@@ -336,6 +363,7 @@ int oracle_spec_verify(const void *target, const void *draft, int dtype,
     }
     free(probs);
     free(r);
+    free(rowbad);
     return 0;
 }
 

@@ -324,3 +324,37 @@ def test_tree_bad_parent_is_flagged():
     assert np.array_equal(path, ref["path"]) and np.array_equal(length, ref["length"])
     assert np.array_equal(mask, ref["mask"])
     assert length[1] == -1
+
+
+def test_bad_data_after_the_first_rejection_still_flags_the_sequence():
+    """Decisions are taken as soon as positions 0..n are resolved; the rows
+    after n are still checked before the outputs are written."""
+    B, K, V = 6, 4, 512
+    g = torch.Generator().manual_seed(5)
+    t = 2.0 * torch.randn(B, K + 1, V, generator=g)
+    d = t[:, :K].clone()
+    x = torch.randint(0, V, (B, K), generator=g, dtype=torch.int32)
+    # position 0 rejects for certain: q(x_0) near 1, p(x_0) near 0
+    for b in range(B):
+        d[b, 0, x[b, 0]] = 40.0
+        t[b, 0, x[b, 0]] = -40.0
+    t[0, 3, 11] = float("nan")         # a target row after n = 0
+    d[1, 2, :] = float("-inf")          # a draft row with no mass after n = 0
+    x[2, 3] = V                          # a token out of range after n = 0
+    t[3, K, 5] = float("inf")           # the bonus row (never drawn from here)
+    # sequence 4: clean; sequence 5: every draft accepted (q = p), bad bonus row
+    d[5] = t[5, :K]
+    x[5] = torch.argmax(t[5, :K], dim=-1).to(torch.int32)
+    t[5, K, 0] = float("nan")
+    sv.spec_get_status()
+    for dt in (torch.float32, torch.bfloat16):
+        tt, dd = t.to(dt), d.to(dt)
+        tokens, n = sv.spec_verify(tt.to(DEV), dd.to(DEV), x.to(DEV), 1.0, 17)
+        torch.cuda.synchronize()
+        assert sv.spec_get_status() & sv.SPEC_FLAG_BAD_DATA
+        tokens, n = tokens.cpu().numpy(), n.cpu().numpy()
+        ref = oracle.spec_verify(tt, dd, x, 1.0, 17)
+        assert list(ref["n"][[0, 1, 2, 3, 5]]) == [-1] * 5 and ref["n"][4] == 0
+        assert list(n) == list(ref["n"])
+        assert np.array_equal(tokens, ref["tokens"]), (tokens, ref["tokens"])
+    assert sv.spec_get_status() == 0

@@ -680,3 +680,48 @@ def test_ngram_copy_property_and_bad_lengths():
             assert not any((h[e2 - mm:e2] == h[L - mm:L]).all() for e2 in range(mm, L)) or L < mm + 1
     for b in (6, 7):
         assert out["n_drafts"][b] == -1 and out["match_len"][b] == -1 and (out["drafts"][b] == -1).all()
+
+
+# --------------------------------------------------------------------------
+# the early-exit reading of the bad-data rule
+# --------------------------------------------------------------------------
+def test_used_rows_only_agrees_on_clean_data_and_ignores_rows_after_n():
+    rng = np.random.default_rng(21)
+    B, K, V = 40, 5, 64
+    t = torch.tensor(2.0 * rng.standard_normal((B, K + 1, V)), dtype=torch.float32)
+    d = t[:, :K] + torch.tensor(1.5 * rng.standard_normal((B, K, V)), dtype=torch.float32)
+    x = torch.tensor(rng.integers(0, V, (B, K)), dtype=torch.int32)
+    full = oracle.spec_verify(t, d, x, 1.0, 9)
+    used = oracle.spec_verify(t, d, x, 1.0, 9, used_rows_only=True)
+    assert np.array_equal(full["tokens"], used["tokens"]) and np.array_equal(full["n"], used["n"])
+    # spoil every row and token after each sequence's first rejection: the
+    # used-rows result must not move, while the full rule flags the sequence
+    t2, d2, x2 = t.clone(), d.clone(), x.clone()
+    spoiled = []
+    for b in range(B):
+        n = int(full["n"][b])
+        if n < K - 1:
+            t2[b, n + 1, 3] = float("nan")
+            d2[b, K - 1, :] = float("-inf")
+            x2[b, K - 1] = V + 5
+            spoiled.append(b)
+        if n < K:
+            t2[b, K, 0] = float("inf")  # the bonus row is not used after a rejection
+    assert spoiled
+    used2 = oracle.spec_verify(t2, d2, x2, 1.0, 9, used_rows_only=True)
+    assert np.array_equal(used2["tokens"], full["tokens"]) and np.array_equal(used2["n"], full["n"])
+    full2 = oracle.spec_verify(t2, d2, x2, 1.0, 9)
+    assert (full2["n"][spoiled] == -1).all()
+
+
+def test_used_rows_only_flags_bad_rows_it_uses():
+    B, K, V = 4, 3, 16
+    t = torch.zeros(B, K + 1, V)
+    d = torch.zeros(B, K, V)
+    x = torch.zeros(B, K, dtype=torch.int32)  # q = p: every draft accepted
+    t[0, 0, 2] = float("nan")       # position 0
+    d[1, 2, :] = float("-inf")      # position 2 (reached: all accepted)
+    x[2, 1] = -3                     # position 1
+    t[3, K, 4] = float("nan")       # the bonus row, used since all are accepted
+    out = oracle.spec_verify(t, d, x, 1.0, 0, used_rows_only=True)
+    assert out["n"].tolist() == [-1, -1, -1, -1] and (out["tokens"] == -1).all()

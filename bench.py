@@ -368,6 +368,30 @@ def run_gpu(args):
     value = world * p.B * args.steps / (total_ms / 1e3)
     flags = sv.spec_get_status()
 
+    # the early-exit verify on the same inputs (reads only the rows the result
+    # depends on): reported beside the full-read number, same timing rules
+    ee_ms = None
+    if args.early_exit_steps > 0:
+        def ee_step(i):
+            x = sets[i % len(sets)]
+            o = outs[i % 2]
+            sv.spec_verify_early_exit(x["target"], x["draft"], x["tokens"], p.temperature,
+                                      rank_seed(rank, i), out_tokens=o[0], out_n_accepted=o[1],
+                                      stream=stream)
+        for i in range(max(args.warmup, 3)):
+            ee_step(i)
+        barrier(world)
+        torch.cuda.synchronize(dev)
+        a0 = torch.cuda.Event(enable_timing=True)
+        a1 = torch.cuda.Event(enable_timing=True)
+        a0.record(stream)
+        for i in range(args.early_exit_steps):
+            ee_step(i)
+        a1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier(world)
+        ee_ms = max_over_ranks(a0.elapsed_time(a1), world) / args.early_exit_steps
+
     # end to end through the public API from pinned host buffers
     e2e_steps = min(args.steps, args.e2e_steps)
     e2e_value, h2d, d2h, e2e_cpus = None, 0, 0, None
@@ -399,6 +423,12 @@ def run_gpu(args):
                  "d2h_bytes_per_step": d2h, "steps": e2e_steps,
                  "host_buffers": ("pinned, allocated from the %d CPUs of the GPU's socket" % e2e_cpus)
                  if e2e_cpus else "pinned"} if e2e_steps > 0 else None),
+        "early_exit": ({"value": world * p.B / (ee_ms / 1e3), "unit": UNIT, "ms_per_step": ee_ms,
+                        "steps": args.early_exit_steps,
+                        "entry_point": "spec_verify_early_exit_bf16",
+                        "note": "reads only target/draft rows 0..n (and row K when all drafts are "
+                                "accepted); identical tokens on valid inputs; bad data checked on "
+                                "the rows used"} if ee_ms else None),
         "gpu_launches": args.steps,
         "clocks": clk.summary(),
         "status_flags": flags,
@@ -425,6 +455,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=20,
                     help="steps of the end-to-end (host buffers) measurement; 0 skips it")
+    ap.add_argument("--early-exit-steps", type=int, default=500,
+                    help="timed steps of the early-exit verify reported beside the main number; 0 skips it")
     ap.add_argument("--batch", type=int, default=0,
                     help="sequences per rank (default: the workload's B); for profiling runs")
     ap.add_argument("--sets", type=int, default=2, choices=[1, 2],

@@ -105,6 +105,33 @@ int spec_verify_bf16(const uint16_t *target_logits, const uint16_t *draft_logits
                      cudaStream_t stream);
 
 /*
+ * spec_verify with early exit: the same arguments, layouts and outputs, but
+ * only the rows the result depends on are read -- the target and draft rows
+ * of positions 0..n (n the first rejection) and target row K when all K
+ * drafts are accepted.  A sequence is decided as soon as its positions 0..n
+ * are resolved, and the statistics slices of its later rows that have not
+ * started by then are skipped, so far fewer logits are read when drafts are
+ * rejected early ([P2] "The draft-and-verify loop": the tokens after the
+ * first rejection are discarded, so their rows cannot change the result).
+ * Tokens and counts equal spec_verify's on every sequence whose inputs are
+ * valid.  Bad data is checked, in position order, only on what is used: a
+ * NaN / +inf logit or an empty row among target/draft rows 0..n, a drafted
+ * token x_0..x_n outside [0, V), or a bad target row K when n == K; then
+ * n = -1, the sequence's outputs are -1 and SPEC_FLAG_BAD_DATA is set.  Bad
+ * data after the first rejection is not reported (spec_verify reports it).
+ * With K > 31 every row is read (the sequence is decided once all positions
+ * are resolved); temperature 0 runs the greedy verify of spec_verify.
+ */
+int spec_verify_early_exit_f32(const float *target_logits, const float *draft_logits,
+                               const int32_t *draft_tokens, int B, int K, int V, float temperature,
+                               uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
+                               cudaStream_t stream);
+int spec_verify_early_exit_bf16(const uint16_t *target_logits, const uint16_t *draft_logits,
+                                const int32_t *draft_tokens, int B, int K, int V, float temperature,
+                                uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
+                                cudaStream_t stream);
+
+/*
  * spec_verify_bf16 without any device allocation.  The pages describe the
  * verify step only; they have no counterpart of this entry point, which exists
  * for callers that cannot let the library allocate: a serving process that

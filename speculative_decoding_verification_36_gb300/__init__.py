@@ -22,7 +22,7 @@ from . import _lib
 from ._lib import SPEC_FLAG_BAD_DATA, SPEC_FLAG_TIMEOUT, SpecError
 
 __all__ = [
-    "spec_verify", "spec_verify_static_scratch", "spec_verify_stats", "spec_verify_greedy_argmax",
+    "spec_verify", "spec_verify_early_exit", "spec_verify_static_scratch", "spec_verify_stats", "spec_verify_greedy_argmax",
     "spec_tree_verify_greedy", "spec_tree_verify_sampling", "spec_acceptance_stats", "spec_ngram_draft",
     "spec_get_status", "SpecError",
     "SPEC_FLAG_BAD_DATA", "SPEC_FLAG_TIMEOUT",
@@ -98,6 +98,26 @@ def spec_verify(target_logits, draft_logits, draft_tokens, temperature: float, s
     out_n_accepted = _out(out_n_accepted, (B,), torch.int32, dev, "out_n_accepted")
     lib = _lib.load()
     fn = lib.spec_verify_bf16 if bf16 else lib.spec_verify_f32
+    with torch.cuda.device(dev):
+        _lib.check(fn(_ptr(target_logits), _ptr(draft_logits) if temperature > 0 else None,
+                      _ptr(draft_tokens) if K > 0 else None, B, K, V, float(temperature),
+                      int(seed) & (2**64 - 1), _ptr(out_tokens), _ptr(out_n_accepted),
+                      _stream(stream)))
+    return out_tokens, out_n_accepted
+
+
+def spec_verify_early_exit(target_logits, draft_logits, draft_tokens, temperature: float, seed: int,
+                           out_tokens=None, out_n_accepted=None, stream=None):
+    """spec_verify that reads only the rows its result depends on (positions
+    up to the first rejection, and the bonus row when every draft is
+    accepted); bad data is checked on those rows only.  Returns (out_tokens
+    [B,K+1], n [B])."""
+    bf16, B, K, V = _chain_args(target_logits, draft_logits, draft_tokens, temperature)
+    dev = target_logits.device
+    out_tokens = _out(out_tokens, (B, K + 1), torch.int32, dev, "out_tokens")
+    out_n_accepted = _out(out_n_accepted, (B,), torch.int32, dev, "out_n_accepted")
+    lib = _lib.load()
+    fn = lib.spec_verify_early_exit_bf16 if bf16 else lib.spec_verify_early_exit_f32
     with torch.cuda.device(dev):
         _lib.check(fn(_ptr(target_logits), _ptr(draft_logits) if temperature > 0 else None,
                       _ptr(draft_tokens) if K > 0 else None, B, K, V, float(temperature),

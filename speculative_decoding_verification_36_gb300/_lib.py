@@ -38,6 +38,8 @@ SIGNATURES = {
     "spec_verify_f32": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_verify_bf16": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_verify_bf16_static_scratch": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
+    "spec_verify_early_exit_f32": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
+    "spec_verify_early_exit_bf16": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_verify_stats_f32": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P, _P, _P, _P, _P],
     "spec_verify_stats_bf16": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P, _P, _P, _P, _P],
     "spec_verify_greedy_argmax_f32": [_P, _P, _I, _I, _I, _P, _P, _P, _P],

@@ -278,7 +278,7 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
                 int K, int V, float temperature, uint64_t seed, int32_t* out_tokens, int32_t* out_n,
                 float* out_row_stats, float* out_pq, float* out_resid, float* out_entropy,
                 cudaStream_t stream,
-                bool use_static = false) {
+                bool use_static = false, bool early_exit = false) {
   if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-30f))
     return SPEC_ERR_TEMPERATURE;
   if (temperature == 0.f)
@@ -328,7 +328,9 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   {
     static const int front_pos = env_int_signed("SPECVERIFY_FRONT_POS", 1);
     static const int front_span = env_int_signed("SPECVERIFY_FRONT_SPAN", 60);
-    const int fp = front_pos < 0 ? 0 : (front_pos > K ? K : front_pos);
+    // early exit keeps plain position-major order: a sequence's later rows
+    // then come after its decision, so they can be skipped
+    const int fp = early_exit ? 0 : (front_pos < 0 ? 0 : (front_pos > K ? K : front_pos));
     a.NA = fp * B * 2 * a.CS;
     a.FQ = 64;
     const double span = (double)front_span / 100.0 * (double)a.F;
@@ -349,6 +351,7 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   static const int l2_other = env_int_signed("SPECVERIFY_L2_OTHER", 0);
   a.l2_keep = l2_keep;
   a.l2_other = l2_other;
+  a.early_exit = early_exit ? 1 : 0;
   const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
   a.c64 = c;
   a.c_hi = (float)c;
@@ -470,6 +473,22 @@ int spec_verify_bf16(const uint16_t* target_logits, const uint16_t* draft_logits
                      cudaStream_t stream) {
   return verify_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
                      out_tokens, out_n_accepted, nullptr, nullptr, nullptr, nullptr, stream);
+}
+
+int spec_verify_early_exit_f32(const float* target_logits, const float* draft_logits,
+                               const int32_t* draft_tokens, int B, int K, int V, float temperature,
+                               uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
+                               cudaStream_t stream) {
+  return verify_impl(false, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
+                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, nullptr, stream, false, true);
+}
+
+int spec_verify_early_exit_bf16(const uint16_t* target_logits, const uint16_t* draft_logits,
+                                const int32_t* draft_tokens, int B, int K, int V, float temperature,
+                                uint64_t seed, int32_t* out_tokens, int32_t* out_n_accepted,
+                                cudaStream_t stream) {
+  return verify_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
+                     out_tokens, out_n_accepted, nullptr, nullptr, nullptr, nullptr, stream, false, true);
 }
 
 int spec_verify_bf16_static_scratch(const uint16_t* target_logits, const uint16_t* draft_logits,

@@ -177,7 +177,8 @@ __device__ __forceinline__ int resolve_position(const SampleArgs& a, int b, int 
 __device__ __noinline__ void commit_sequence(const SampleArgs& a, int b) {
   const int lane = threadIdx.x & 31;
   const int K = a.K;
-  const int sb = wait_s32(a.seqbad + b, a.status);
+  // early exit: only the rows the decision used were checked (by the decider)
+  const int sb = a.early_exit ? 0 : wait_s32(a.seqbad + b, a.status);
   const uint4 res = wait_result(a.result + b, a.status);
   const bool bad = sb != 0 || res.x == kResultBad;
   int32_t* out = a.out_tokens + (size_t)b * (K + 1);
@@ -202,13 +203,14 @@ __device__ __noinline__ void commit_sequence(const SampleArgs& a, int b) {
 }
 
 // One of the two commit arrivals of sequence b (lane 0 takes the ticket); the
-// second runs the commit.
+// second runs the commit.  In early-exit mode the result side is the only
+// arrival: the rows after the decision are not all read.
 __device__ __forceinline__ void commit_arrive(const SampleArgs& a, int b) {
   const int lane = threadIdx.x & 31;
   int old = 0;
   if (lane == 0) old = ticket_take(a.committicket + b);
   old = __shfl_sync(0xffffffffu, old, 0);
-  if (old == 1) commit_sequence(a, b);
+  if (old == (a.early_exit ? 0 : 1)) commit_sequence(a, b);
 }
 
 // Decision of sequence b at n (one warp): the tail constants of row n, the
@@ -239,6 +241,7 @@ __device__ __noinline__ void decide_sequence(const SampleArgs& a, int b, int n, 
     stD = n < K ? wait_u2(rs + K + 1 + n, a.status) : make_uint2(0u, 0u);
     verdict = wait_s32(a.verdict + (size_t)b * (K + 1) + n, a.status);
   }
+  if (a.early_exit && lane == 0) st_relaxed_s32(a.decided + b, n);  // later slices of b may skip
   SeqInfo si;
   si.b = b;
   si.n = n;
@@ -367,7 +370,7 @@ __device__ __noinline__ void unit_finisher(const SampleArgs& a, int b, int i) {
   if (n >= 0) decide_sequence(a, b, n, n == i, stT, stD, verdict);
   // (the count starts at -1: `units` is the number of earlier arrivals, with
   // kUnitBad added once per unit that had bad data)
-  if ((units & (kUnitBad - 1)) == K) {  // every unit of the sequence is checked
+  if ((units & (kUnitBad - 1)) == K && !a.early_exit) {  // every unit of the sequence is checked
     if (lane == 0) st_relaxed_s32(a.seqbad + b, (units >= kUnitBad || bad) ? 1 : 0);
     commit_arrive(a, b);
   }
@@ -847,8 +850,17 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
       }
       if (!tail_ready) seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
       const SliceId id = decode_slice(a, stream_to_pm(a, f));
-      const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC, ENT>(a, id.b, id.i, id.r, id.s), 0);
-      if (old == unit_slices(a, id.i) - 1) unit_finisher<E, ENT>(a, id.b, id.i);
+      // early exit: a row after a decided sequence's first rejection (or its
+      // bonus row after a rejection) cannot change the result; it is not read
+      bool skip = false;
+      if (a.early_exit && id.i > 0) {
+        const int dn = (int)ld_relaxed_if(lane == 0, a.decided + id.b, kMarker);
+        skip = bcast(dn) >= 0 && bcast(dn) < id.i;
+      }
+      if (!skip) {
+        const int old = __shfl_sync(0xffffffffu, stats_slice<E, VEC, ENT>(a, id.b, id.i, id.r, id.s), 0);
+        if (old == unit_slices(a, id.i) - 1) unit_finisher<E, ENT>(a, id.b, id.i);
+      }
       if (ahead) {
         f = bcast(next) * kSlices + nctr;
         ctr = nctr;
@@ -916,13 +928,14 @@ static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t*
   off[18] = o; o += align_up((size_t)B * (K + 1) * 4, 256);                 // verdict
   off[19] = o; o += align_up((size_t)B * 4, 256);                           // seqbad
   off[20] = o; o += align_up((size_t)B * sizeof(uint4), 256);               // result
+  off[21] = o; o += align_up((size_t)B * 4, 256);                           // decided
   off[14] = o; if (ent) o += align_up((size_t)B * R * CS * sizeof(float), 256);  // part_t
   off[9] = o;                                                                // end of marker region
   off[12] = o;
 }
 
 WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
-  size_t off[21];
+  size_t off[22];
   sample_layout(B, K, CS, TC, P, ent, off);
   WsLayout l;
   l.total = off[12];
@@ -933,7 +946,7 @@ WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
 }
 
 void sample_bind_workspace(SampleArgs& a, void* ws) {
-  size_t off[21];
+  size_t off[22];
   sample_layout(a.B, a.K, a.CS, a.TC, a.P, a.out_entropy != nullptr, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
@@ -953,6 +966,7 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.verdict = (int*)(p + off[18]);
   a.seqbad = (int*)(p + off[19]);
   a.result = (uint4*)(p + off[20]);
+  a.decided = (int*)(p + off[21]);
   a.part_t = a.out_entropy ? (float*)(p + off[14]) : nullptr;
 }
 

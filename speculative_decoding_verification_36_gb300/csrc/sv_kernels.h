@@ -91,6 +91,7 @@ struct SampleArgs {
   int claim_tail;  // within this many slices of the end, claims are not made ahead
   int l2_keep;     // rows of positions < l2_keep are prefetched into L2 with evict_last
   int l2_other;    // the other rows: 0 default prefetch, 1 evict_first, 2 evict_normal
+  int early_exit;  // read only the rows the result depends on (positions 0..n, row K if n = K)
   FastDiv div_pos, div_pair, div_cs, div_tc;  // division by B * 2 * CS, 2 * CS, CS and TC
   float c_hi, c_lo;  // log2(e)/temperature as a float pair
   double c64;        // the same in double
@@ -117,6 +118,7 @@ struct SampleArgs {
   int* verdict;     // [B, K+1] accept / reject / bad of each position
   int* seqbad;      // [B] 1 if any unit of the sequence had bad data
   uint4* result;    // [B] (n, token, residual mass bits, 0) for the commit
+  int* decided;     // [B] n once the sequence is decided (early exit), kMarker before
   int* tailticket;  // [B] finished tail slices
   int* qcount;      // decision-queue positions taken so far
   float2* part;     // [B, R, CS] per-slice (m, s)

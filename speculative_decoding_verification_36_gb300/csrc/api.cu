@@ -42,6 +42,8 @@ struct DeviceState {
   int sms = 0;
   cudaMemPool_t pool = nullptr;  // created by the first call that allocates
   void* static_scratch = nullptr;  // looked up by the first static-scratch call
+  cudaStream_t side = nullptr;     // scratch is allocated and filled here, off the caller's stream
+  cudaEvent_t side_done = nullptr;
   unsigned* status = nullptr;
   int occ_sample[2][2] = {{0, 0}, {0, 0}};  // [bf16][vec]
   int occ_greedy[2][2] = {{0, 0}, {0, 0}};
@@ -105,6 +107,11 @@ int ensure_pool(DeviceState* d) {
   if (e != cudaSuccess) return cuda_fail(e, "cudaMemPoolCreate");
   uint64_t keep = UINT64_MAX;  // keep freed scratch in the pool between calls
   e = cudaMemPoolSetAttribute(pool, cudaMemPoolAttrReleaseThreshold, &keep);
+  // an allocation never waits for the stream that freed a block: the pool
+  // hands out another block instead, so a call's scratch can be prepared
+  // while the previous call's kernel still runs
+  int no_wait = 0;
+  if (e == cudaSuccess) e = cudaMemPoolSetAttribute(pool, cudaMemPoolReuseAllowInternalDependencies, &no_wait);
   if (e != cudaSuccess) {
     cudaMemPoolDestroy(pool);
     return cuda_fail(e, "cudaMemPoolSetAttribute");
@@ -173,12 +180,39 @@ bool sizes_ok(int B, int rows, int V) {
   return V <= 0x7fff0000 && total < 4.0e18 && units < 2.0e9;
 }
 
-// Stream-ordered scratch from the library's pool, with the zero region and
-// the "not yet written" marker region initialised on the stream.
+// Scratch from the library's pool with the zero region and the "not yet
+// written" marker region initialised.  Outside stream capture the allocation
+// and fills run on the device's side stream and the caller's stream waits for
+// them through an event: they do not depend on the caller's earlier work, so
+// they can run while the previous kernel drains, and the caller's stream sees
+// one launch per call instead of a fill, a gap and a launch.  (The caller's
+// stream returns the scratch with cudaFreeAsync after the kernel.)
 int run_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, void** ws) {
   const int rc = ensure_pool(d);
   if (rc) return rc;
-  cudaError_t e = cudaMallocFromPoolAsync(ws, l.total, d->pool, stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t e = cudaStreamIsCapturing(stream, &cap);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
+  if (cap == cudaStreamCaptureStatusNone) {
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!d->side) {
+      e = cudaStreamCreateWithFlags(&d->side, cudaStreamNonBlocking);
+      if (e == cudaSuccess) e = cudaEventCreateWithFlags(&d->side_done, cudaEventDisableTiming);
+      if (e != cudaSuccess) return cuda_fail(e, "side stream");
+    }
+    e = cudaMallocFromPoolAsync(ws, l.total, d->pool, d->side);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
+    if (l.zero_bytes) e = cudaMemsetAsync(*ws, 0, l.zero_bytes, d->side);
+    if (e == cudaSuccess) e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, d->side);
+    if (e == cudaSuccess) e = cudaEventRecord(d->side_done, d->side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, d->side_done, 0);
+    if (e != cudaSuccess) {
+      cudaFreeAsync(*ws, d->side);
+      return cuda_fail(e, "scratch preparation");
+    }
+    return SPEC_OK;
+  }
+  e = cudaMallocFromPoolAsync(ws, l.total, d->pool, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
   if (l.zero_bytes) e = cudaMemsetAsync(*ws, 0, l.zero_bytes, stream);
   if (e == cudaSuccess) e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, stream);

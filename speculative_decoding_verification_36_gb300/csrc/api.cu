@@ -138,6 +138,9 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 //                                 with evict_last, as likely tail rows (2)
 //   SPECVERIFY_L2_OTHER           prefetch policy of the other rows: 0 the
 //                                 default, 1 evict_first, 2 evict_normal (0)
+//   SPECVERIFY_LATE_TAILS         percent of the decision queue (the latest
+//                                 decisions) whose tail items free warps claim
+//                                 instead of fixed owners (6; 25 with early exit)
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
@@ -386,6 +389,18 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.l2_keep = l2_keep;
   a.l2_other = l2_other;
   a.early_exit = early_exit ? 1 : 0;
+  // the tail items of the last late_tails percent of queue positions (the
+  // latest decisions) go to whichever warps are free
+  // (measured on c3: 6 % with the full read, 25 % with early exit, where
+  // most of the grid is free once the first position has been streamed)
+  static const int late_tails = env_int_signed("SPECVERIFY_LATE_TAILS", -1);
+  {
+    const int want = late_tails >= 0 ? late_tails : (early_exit ? 25 : 6);
+    const int pct = want > 100 ? 100 : want;
+    int late = (int)(((long long)B * pct + 99) / 100);
+    if (late > B) late = B;
+    a.TTo = (B - late) * a.TC;
+  }
   const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
   a.c64 = c;
   a.c_hi = (float)c;

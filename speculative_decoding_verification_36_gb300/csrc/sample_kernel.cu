@@ -797,13 +797,17 @@ __device__ __forceinline__ int next_live_counter(int ctr, unsigned dead) {
 // Scheduling.  Statistics slices come from eight claim counters: the k-th
 // claim on counter c is flat slice f = k * kSlices + c.  The next claim
 // is issued before the current slice is processed, so the atomic's latency
-// hides behind the stream.  Tail slices are owned, not claimed: tail item j
-// (queue position j / TC, tail slice j % TC) belongs to global warp j % W,
-// where warp slot w of CTA c is global warp w * grid + c and W = 8 * grid.  A
-// warp takes its items in order and polls the queue entry of its next item
-// with a relaxed load issued before each statistics slice; a published item
-// is taken before the next statistics slice.  Only when a warp has no
-// statistics slice left does it wait (bounded) for its next entry.
+// hides behind the stream.  Tail slices of the first TTo / TC queue positions
+// are owned, not claimed: tail item j (queue position j / TC, tail slice
+// j % TC) belongs to global warp j % W, where warp slot w of CTA c is global
+// warp w * grid + c and W = 8 * grid.  A warp takes its items in order and
+// polls the queue entry of its next item with a relaxed load issued before
+// each statistics slice; a published item is taken before the next
+// statistics slice.  Only when a warp has no statistics slice left does it
+// wait (bounded) for its next entry.  The tail items of the last queue
+// positions -- the latest decisions, which come near the end of the stream
+// -- are claimed in order by warps that have nothing else left, so that no
+// late tail waits for a busy owner.
 //
 // Progress: statistics slices and the finishers they trigger wait only for
 // stores that other warps have already issued (their tickets were counted), a
@@ -816,8 +820,10 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
   const int lane = threadIdx.x & 31;
   const int w = slice_of_warp();
   const int TT = a.B * a.TC;                       // tail items in all
+  const int TO = a.TTo;                            // owned tail items: the first TTo
   const int W = kSlices * (int)gridDim.x;          // warps in the grid
-  int t = w * (int)gridDim.x + (int)blockIdx.x;    // this warp's next tail item
+  int t = w * (int)gridDim.x + (int)blockIdx.x;    // this warp's next owned tail item
+  if (t >= TO) t = TT;
   // Statistics claims rotate over the eight counters (warp slot w starts at
   // counter w), so every warp draws equally from every counter and the
   // counters advance together.  A claim past a counter's end marks that
@@ -830,9 +836,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
   int ctr = w;
   int f = bcast(claim_from(a.counter, ctr, lane)) * kSlices + ctr;
   bool held = true;  // f is the result of a claim on counter ctr
-  uint32_t seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
+  uint32_t seen = poll_decision(a, lane == 0 && t < TO, fdiv(t, a.div_tc));
   for (;;) {
-    const bool tail_ready = t < TT && word_set(bcast((int)seen));
+    const bool tail_ready = t < TO && word_set(bcast((int)seen));
     if (held && f >= a.F) {  // the claim came back past the counter's end
       dead |= 1u << ctr;
       held = false;
@@ -848,7 +854,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
         nctr = next_live_counter(ctr, dead);
         next = claim_from(a.counter, nctr, lane);
       }
-      if (!tail_ready) seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
+      if (!tail_ready) seen = poll_decision(a, lane == 0 && t < TO, fdiv(t, a.div_tc));
       const SliceId id = decode_slice(a, stream_to_pm(a, f));
       // early exit: a row after a decided sequence's first rejection (or its
       // bonus row after a rejection) cannot change the result; it is not read
@@ -872,7 +878,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
       const SeqInfo si = read_decision(a, pos);
       tail_slice<E, VEC, (VEC > 1)>(a, si, t - pos * a.TC);
       t += W;
-      seen = poll_decision(a, lane == 0 && t < TT, fdiv(t, a.div_tc));
+      if (t >= TO) t = TT;
+      seen = poll_decision(a, lane == 0 && t < TO, fdiv(t, a.div_tc));
       continue;
     }
     if (dead != 0xffu) {  // nothing held: claim from the next live counter
@@ -881,8 +888,31 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
       held = true;
       continue;
     }
-    if (t >= TT) break;
-    // no statistics work left: wait for this warp's next decision
+    if (t >= TT) {
+      // No statistics work and no owned tail item left: take the tail items
+      // of the latest decisions (queue positions from TTo / TC on) in claim
+      // order, so that they run at once on warps that are free instead of
+      // waiting for owners that may still be streaming.
+      const int j = TO + bcast(ticket_take_if(lane == 0, a.dclaim));
+      if (j >= TT) break;
+      uint32_t dseen = kMarker;
+      if (lane == 0) {
+        unsigned it = 0, nap = 64;
+        dseen = poll_decision(a, true, fdiv(j, a.div_tc));
+        while (!word_set(dseen) && ++it < kSpinLimit) {
+          __nanosleep(nap);
+          if (nap < 1024) nap <<= 1;
+          dseen = poll_decision(a, true, fdiv(j, a.div_tc));
+        }
+        if (!word_set(dseen)) atomicOr(a.status, kStatusTimeout);
+      }
+      if (!word_set(bcast((int)dseen))) break;
+      const int pos = fdiv(j, a.div_tc);
+      const SeqInfo si = read_decision(a, pos);
+      tail_slice<E, VEC, (VEC > 1)>(a, si, j - pos * a.TC);
+      continue;
+    }
+    // no statistics work left: wait for this warp's next owned decision
     if (lane == 0) {
       unsigned it = 0, nap = 64;
       seen = poll_decision(a, true, fdiv(t, a.div_tc));
@@ -913,7 +943,8 @@ static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t*
   off[1] = o; o += align_up((size_t)B * (K + 1) * kTicketStride * 4, 16);   // unitticket
   off[2] = o; o += align_up((size_t)B * 4, 16);                             // seqticket
   off[3] = o; o += align_up((size_t)B * 4, 16);                             // tailticket
-  off[4] = o; o += 16;                                                       // qcount
+  off[4] = o; o += 128;                                                      // qcount
+  off[22] = o; o += 128;                                                     // dclaim
   off[15] = o; o += align_up((size_t)B * 4, 16);                            // posticket
   off[16] = o; o += align_up((size_t)B * 4, 16);                            // committicket
   off[17] = o; o += align_up((size_t)B * 8, 16);                            // resword
@@ -935,7 +966,7 @@ static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t*
 }
 
 WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
-  size_t off[22];
+  size_t off[23];
   sample_layout(B, K, CS, TC, P, ent, off);
   WsLayout l;
   l.total = off[12];
@@ -946,7 +977,7 @@ WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
 }
 
 void sample_bind_workspace(SampleArgs& a, void* ws) {
-  size_t off[22];
+  size_t off[23];
   sample_layout(a.B, a.K, a.CS, a.TC, a.P, a.out_entropy != nullptr, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
@@ -954,6 +985,7 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.seqticket = (int*)(p + off[2]);
   a.tailticket = (int*)(p + off[3]);
   a.qcount = (int*)(p + off[4]);
+  a.dclaim = (int*)(p + off[22]);
   a.posticket = (int*)(p + off[15]);
   a.committicket = (int*)(p + off[16]);
   a.resword = (unsigned long long*)(p + off[17]);

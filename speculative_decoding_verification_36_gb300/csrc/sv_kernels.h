@@ -92,6 +92,7 @@ struct SampleArgs {
   int l2_keep;     // rows of positions < l2_keep are prefetched into L2 with evict_last
   int l2_other;    // the other rows: 0 default prefetch, 1 evict_first, 2 evict_normal
   int early_exit;  // read only the rows the result depends on (positions 0..n, row K if n = K)
+  int TTo;         // owned tail items (the first TTo); the rest are claimed by free warps
   FastDiv div_pos, div_pair, div_cs, div_tc;  // division by B * 2 * CS, 2 * CS, CS and TC
   float c_hi, c_lo;  // log2(e)/temperature as a float pair
   double c64;        // the same in double
@@ -105,7 +106,7 @@ struct SampleArgs {
   float* out_entropy;    // optional [B, R]: entropy (nats) of each row's softmax
   // workspace, filled with all-ones bytes before the launch: the counters and
   // tickets (counter, unitticket, seqticket, posticket, committicket,
-  // tailticket, qcount) then start at -1, the resolution words at the empty
+  // tailticket, qcount, dclaim) then start at -1, the resolution words at the empty
   // set (stored complemented), and the result slots (part, rowstat, zx,
   // verdict, seqbad, result, tailsum, queue, pieces) hold the kMarker "not yet
   // written" pattern.
@@ -121,6 +122,7 @@ struct SampleArgs {
   int* decided;     // [B] n once the sequence is decided (early exit), kMarker before
   int* tailticket;  // [B] finished tail slices
   int* qcount;      // decision-queue positions taken so far
+  int* dclaim;      // tail items of the last queue positions claimed so far
   float2* part;     // [B, R, CS] per-slice (m, s)
   float2* rowstat;  // [B, R] merged (m, s) of each row
   float* zx;        // [B, R] logit at the drafted token, written by the slice holding it

@@ -125,7 +125,8 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 // Tuning knobs (environment, read once per process), defaults measured on
 // GB300 with the c3 workload:
 //   SPECVERIFY_SLICE_BYTES        bytes of logits per statistics slice of the
-//                                 sampling kernel (12288)
+//                                 sampling kernel (12288; 8192 for a batch
+//                                 with fewer than ~6 slices per warp)
 //   SPECVERIFY_ARGMAX_SLICE_BYTES the same for the greedy and tree kernels (8192)
 //   SPECVERIFY_TAIL_BYTES         bytes of one row per tail slice (half a
 //                                 statistics slice)
@@ -140,7 +141,8 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 //                                 default, 1 evict_first, 2 evict_normal (0)
 //   SPECVERIFY_LATE_TAILS         percent of the decision queue (the latest
 //                                 decisions) whose tail items free warps claim
-//                                 instead of fixed owners (6; 25 with early exit)
+//                                 instead of fixed owners (6; 25 with early
+//                                 exit; 100 for a small batch)
 int env_int(const char* name, int dflt) {
   const char* v = getenv(name);
   if (!v || !*v) return dflt;
@@ -341,8 +343,16 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.R = 2 * K + 1;
   const int vec_elems = vec ? (bf16 ? 8 : 4) : 1;
   int CU = 0;
-  static const int slice_bytes = env_int("SPECVERIFY_SLICE_BYTES", 12288);
-  choose_slices(V, vec_elems, esz, slice_bytes, &a.SL, &a.CS, &CU);
+  // 12 KB statistics slices; a batch too small to give every warp of the grid
+  // about six of them streams 8 KB slices and lets free warps take all of its
+  // tail items (c2: 68 us instead of 75 us per call)
+  static const int slice_bytes_env = env_int("SPECVERIFY_SLICE_BYTES", 0);
+  choose_slices(V, vec_elems, esz, slice_bytes_env > 0 ? slice_bytes_env : 12288, &a.SL, &a.CS, &CU);
+  bool small = false;
+  if (slice_bytes_env <= 0 && (long long)B * a.R * a.CS < 6LL * capacity * sv::kWarps) {
+    small = true;
+    choose_slices(V, vec_elems, esz, 8192, &a.SL, &a.CS, &CU);
+  }
   // tail slices: whole warp steps, half a statistics slice per row, so that a
   // tail item (target and draft slice) carries as many bytes as a statistics
   // slice
@@ -395,7 +405,7 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   // most of the grid is free once the first position has been streamed)
   static const int late_tails = env_int_signed("SPECVERIFY_LATE_TAILS", -1);
   {
-    const int want = late_tails >= 0 ? late_tails : (early_exit ? 25 : 6);
+    const int want = late_tails >= 0 ? late_tails : (small ? 100 : (early_exit ? 25 : 6));
     const int pct = want > 100 ? 100 : want;
     int late = (int)(((long long)B * pct + 99) / 100);
     if (late > B) late = B;

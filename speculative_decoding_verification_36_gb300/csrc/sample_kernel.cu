@@ -171,16 +171,19 @@ __device__ __forceinline__ int resolve_position(const SampleArgs& a, int b, int 
   return ticket_take(a.posticket + b) == a.K ? a.K + 1 : -1;  // K + 1: scan the verdicts
 }
 
-// Commit (one warp, the second of the sequence's two commit arrivals: "every
-// unit checked" and "token drawn / decided bad"): writes out_tokens, out_n and
-// out_resid from the workspace slots.
-__device__ __noinline__ void commit_sequence(const SampleArgs& a, int b) {
+// Commit (one warp): writes out_tokens, out_n and out_resid.  A sequence's
+// commit count gathers K + 2 arrivals: one per position unit (with kUnitBad
+// added when the unit saw bad data) and one for the result (the drawn token,
+// or a bad decision).  Whichever arrives last commits, with the bad-data
+// verdict of every unit in the count's high bits.  The result comes in `res`
+// when the committer is the result side, else from the result slot.  In
+// early-exit mode the rows after the decision are not all read: the result
+// side commits at once, and only the rows the decision used were checked.
+__device__ __noinline__ void commit_sequence(const SampleArgs& a, int b, bool seqbad, bool have, uint4 res) {
   const int lane = threadIdx.x & 31;
   const int K = a.K;
-  // early exit: only the rows the decision used were checked (by the decider)
-  const int sb = a.early_exit ? 0 : wait_s32(a.seqbad + b, a.status);
-  const uint4 res = wait_result(a.result + b, a.status);
-  const bool bad = sb != 0 || res.x == kResultBad;
+  if (!have) res = wait_result(a.result + b, a.status);
+  const bool bad = seqbad || res.x == kResultBad;
   int32_t* out = a.out_tokens + (size_t)b * (K + 1);
   const int32_t* x = a.tokens + (size_t)b * K;
   if (bad) {
@@ -202,15 +205,17 @@ __device__ __noinline__ void commit_sequence(const SampleArgs& a, int b) {
   __syncwarp();
 }
 
-// One of the two commit arrivals of sequence b (lane 0 takes the ticket); the
-// second runs the commit.  In early-exit mode the result side is the only
-// arrival: the rows after the decision are not all read.
-__device__ __forceinline__ void commit_arrive(const SampleArgs& a, int b) {
+// The result side's arrival: the result slot has been stored (lane 0) before.
+__device__ __forceinline__ void commit_result(const SampleArgs& a, int b, uint4 res) {
   const int lane = threadIdx.x & 31;
+  if (a.early_exit) {
+    commit_sequence(a, b, false, true, res);
+    return;
+  }
   int old = 0;
-  if (lane == 0) old = ticket_take(a.committicket + b);
+  if (lane == 0) old = atom_add_relaxed(a.seqticket + b, 1) + 1;  // arrivals before this one
   old = __shfl_sync(0xffffffffu, old, 0);
-  if (old == (a.early_exit ? 0 : 1)) commit_sequence(a, b);
+  if ((old & (kUnitBad - 1)) == a.K + 1) commit_sequence(a, b, old >= kUnitBad, true, res);
 }
 
 // Decision of sequence b at n (one warp): the tail constants of row n, the
@@ -265,8 +270,9 @@ __device__ __noinline__ void decide_sequence(const SampleArgs& a, int b, int n, 
   }
   if (lane == 0) publish_decision(a, qpos, si);
   if (si.mode == kModeBad) {  // no token will be drawn: the result side arrives now
-    if (lane == 0) st_relaxed_v4(a.result + b, kResultBad, kResultBad, 0x7fc00000u, 0u);
-    commit_arrive(a, b);
+    const uint4 res = make_uint4(kResultBad, kResultBad, 0x7fc00000u, 0u);
+    if (lane == 0) st_relaxed_v4(a.result + b, res.x, res.y, res.z, res.w);
+    commit_result(a, b, res);
   }
   __syncwarp();
 }
@@ -363,17 +369,16 @@ __device__ __noinline__ void unit_finisher(const SampleArgs& a, int b, int i) {
   if (lane == 0) {
     st_relaxed_s32(a.verdict + (size_t)b * (K + 1) + i, verdict);
     n = resolve_position(a, b, i, verdict);
-    units = atom_add_relaxed(a.seqticket + b, bad ? kUnitBad + 1 : 1) + 1;
+    if (!a.early_exit) units = atom_add_relaxed(a.seqticket + b, bad ? kUnitBad + 1 : 1) + 1;
   }
   n = __shfl_sync(0xffffffffu, n, 0);
   units = __shfl_sync(0xffffffffu, units, 0);
   if (n >= 0) decide_sequence(a, b, n, n == i, stT, stD, verdict);
   // (the count starts at -1: `units` is the number of earlier arrivals, with
-  // kUnitBad added once per unit that had bad data)
-  if ((units & (kUnitBad - 1)) == K && !a.early_exit) {  // every unit of the sequence is checked
-    if (lane == 0) st_relaxed_s32(a.seqbad + b, (units >= kUnitBad || bad) ? 1 : 0);
-    commit_arrive(a, b);
-  }
+  // kUnitBad added once per unit that had bad data; K + 1 earlier arrivals
+  // means every other unit and the result are in)
+  if ((units & (kUnitBad - 1)) == K + 1 && !a.early_exit)
+    commit_sequence(a, b, units >= kUnitBad || bad, false, make_uint4(0u, 0u, 0u, 0u));
   __syncwarp();
 }
 
@@ -590,11 +595,12 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   const int tsel =
       warp_cdf_search(C, theta, 0.0, [&](int t) { return (double)ld_relaxed_f32(ts + t); }, &acc);
   if (tsel < 0) {  // no slice with mass: only an expired wait can cause this
+    const uint4 res = make_uint4((uint32_t)n, kResultBad, __float_as_uint((float)(Z / (double)si.sT)), 0u);
     if (lane == 0) {
       atomicOr(a.status, kStatusTimeout);
-      st_relaxed_v4(a.result + b, (uint32_t)n, kResultBad, __float_as_uint((float)(Z / (double)si.sT)), 0u);
+      st_relaxed_v4(a.result + b, res.x, res.y, res.z, res.w);
     }
-    commit_arrive(a, b);
+    commit_result(a, b, res);
     return;
   }
   const int v0 = tsel * a.TL, v1 = min(a.V, v0 + a.TL);
@@ -604,11 +610,12 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   const int psel = warp_cdf_search(
       np, theta, acc, [&](int q) { return (double)wait_f32(gp + q, a.status); }, &acc2);
   if (psel < 0) {  // pieces inconsistent with their slice mass (expired wait)
+    const uint4 res = make_uint4((uint32_t)n, kResultBad, __float_as_uint((float)(Z / (double)si.sT)), 0u);
     if (lane == 0) {
       atomicOr(a.status, kStatusTimeout);
-      st_relaxed_v4(a.result + b, (uint32_t)n, kResultBad, __float_as_uint((float)(Z / (double)si.sT)), 0u);
+      st_relaxed_v4(a.result + b, res.x, res.y, res.z, res.w);
     }
-    commit_arrive(a, b);
+    commit_result(a, b, res);
     return;
   }
 
@@ -651,10 +658,10 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
     token = pick >= 0 ? base + pick : -1;
   }
   token = __shfl_sync(0xffffffffu, token, L);
-  if (lane == 0)
-    st_relaxed_v4(a.result + b, (uint32_t)n, token >= 0 ? (uint32_t)token : kResultBad,
-                  __float_as_uint((float)(Z / (double)si.sT)), 0u);
-  commit_arrive(a, b);
+  const uint4 res = make_uint4((uint32_t)n, token >= 0 ? (uint32_t)token : kResultBad,
+                               __float_as_uint((float)(Z / (double)si.sT)), 0u);
+  if (lane == 0) st_relaxed_v4(a.result + b, res.x, res.y, res.z, res.w);
+  commit_result(a, b, res);
 }
 
 // Stream order.  Claim index f is first mapped to a position-major index:
@@ -832,9 +839,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
   // slice is processed before a tail item that became ready (other warps'
   // decisions may wait on it); the claim after it is then deferred until the
   // tail item is done.
+  // The first claim of every warp is static (claim index blockIdx.x on
+  // counter w), so the first slices start streaming without a round trip;
+  // claims made through the counters are offset by the grid size.
+  const int k0 = (int)gridDim.x;
   unsigned dead = 0;
   int ctr = w;
-  int f = bcast(claim_from(a.counter, ctr, lane)) * kSlices + ctr;
+  int f = (int)blockIdx.x * kSlices + ctr;
   bool held = true;  // f is the result of a claim on counter ctr
   uint32_t seen = poll_decision(a, lane == 0 && t < TO, fdiv(t, a.div_tc));
   for (;;) {
@@ -868,7 +879,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
         if (old == unit_slices(a, id.i) - 1) unit_finisher<E, ENT>(a, id.b, id.i);
       }
       if (ahead) {
-        f = bcast(next) * kSlices + nctr;
+        f = (bcast(next) + k0) * kSlices + nctr;
         ctr = nctr;
       }
       continue;
@@ -884,7 +895,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
     }
     if (dead != 0xffu) {  // nothing held: claim from the next live counter
       ctr = next_live_counter(ctr, dead);
-      f = bcast(claim_from(a.counter, ctr, lane)) * kSlices + ctr;
+      f = (bcast(claim_from(a.counter, ctr, lane)) + k0) * kSlices + ctr;
       held = true;
       continue;
     }
@@ -934,7 +945,7 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: [counters, tickets, resolution words, queue count (all start at
 // all-ones)][marker-filled result slots: part, rowstat, tailsum, queue,
-// pieces, zx, verdict, seqbad, result, and part_t when the entropy is asked
+// pieces, zx, verdict, result, and part_t when the entropy is asked
 // for]; one 0xff fill initialises both parts.
 static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t* off) {
   const int R = 2 * K + 1;
@@ -946,7 +957,6 @@ static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t*
   off[4] = o; o += 128;                                                      // qcount
   off[22] = o; o += 128;                                                     // dclaim
   off[15] = o; o += align_up((size_t)B * 4, 16);                            // posticket
-  off[16] = o; o += align_up((size_t)B * 4, 16);                            // committicket
   off[17] = o; o += align_up((size_t)B * 8, 16);                            // resword
   o = align_up(o, 256);
   off[5] = o;                                                                // end of counter region
@@ -957,7 +967,6 @@ static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t*
   off[11] = o; o += align_up((size_t)B * TC * P * sizeof(float), 256);      // pieces
   off[13] = o; o += align_up((size_t)B * R * sizeof(float), 256);           // zx
   off[18] = o; o += align_up((size_t)B * (K + 1) * 4, 256);                 // verdict
-  off[19] = o; o += align_up((size_t)B * 4, 256);                           // seqbad
   off[20] = o; o += align_up((size_t)B * sizeof(uint4), 256);               // result
   off[21] = o; o += align_up((size_t)B * 4, 256);                           // decided
   off[14] = o; if (ent) o += align_up((size_t)B * R * CS * sizeof(float), 256);  // part_t
@@ -987,7 +996,6 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.qcount = (int*)(p + off[4]);
   a.dclaim = (int*)(p + off[22]);
   a.posticket = (int*)(p + off[15]);
-  a.committicket = (int*)(p + off[16]);
   a.resword = (unsigned long long*)(p + off[17]);
   a.part = (float2*)(p + off[6]);
   a.rowstat = (float2*)(p + off[7]);
@@ -996,7 +1004,6 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.pieces = (float*)(p + off[11]);
   a.zx = (float*)(p + off[13]);
   a.verdict = (int*)(p + off[18]);
-  a.seqbad = (int*)(p + off[19]);
   a.result = (uint4*)(p + off[20]);
   a.decided = (int*)(p + off[21]);
   a.part_t = a.out_entropy ? (float*)(p + off[14]) : nullptr;

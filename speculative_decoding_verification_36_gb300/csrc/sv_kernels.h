@@ -105,19 +105,17 @@ struct SampleArgs {
   float* out_resid;      // optional [B]: mass of the replacement distribution
   float* out_entropy;    // optional [B, R]: entropy (nats) of each row's softmax
   // workspace, filled with all-ones bytes before the launch: the counters and
-  // tickets (counter, unitticket, seqticket, posticket, committicket,
-  // tailticket, qcount, dclaim) then start at -1, the resolution words at the empty
+  // tickets (counter, unitticket, seqticket, posticket, tailticket, qcount,
+  // dclaim) then start at -1, the resolution words at the empty
   // set (stored complemented), and the result slots (part, rowstat, zx,
-  // verdict, seqbad, result, tailsum, queue, pieces) hold the kMarker "not yet
+  // verdict, result, tailsum, queue, pieces) hold the kMarker "not yet
   // written" pattern.
   unsigned long long* counter;  // kSlices claim counters, kCounterStride apart
   int* unitticket;  // [B, K+1] (kTicketStride apart) finished slices of a position unit
-  int* seqticket;   // [B] finished units of a sequence (+ 0x10000 per unit with bad data)
+  int* seqticket;   // [B] commit count: finished units (+ 0x10000 per unit with bad data) and the result
   int* posticket;   // [B] resolved positions (K > 31 only)
-  int* committicket;  // [B] commit arrivals (units checked; token drawn or decided bad)
   unsigned long long* resword;  // [B] resolved / rejected positions, complemented (K <= 31)
   int* verdict;     // [B, K+1] accept / reject / bad of each position
-  int* seqbad;      // [B] 1 if any unit of the sequence had bad data
   uint4* result;    // [B] (n, token, residual mass bits, 0) for the commit
   int* decided;     // [B] n once the sequence is decided (early exit), kMarker before
   int* tailticket;  // [B] finished tail slices

@@ -62,9 +62,9 @@ __device__ __forceinline__ TailConsts tail_consts(const SampleArgs& a, const Seq
 }
 
 // ---------------------------------------------------------------------------
-// decision queue.  The statistics finisher of a sequence takes the next queue
-// position and writes its SeqInfo there with two relaxed 16-byte stores; a
-// reader validates each field against kMarker (a NaN no field ever holds).
+// decision queue.  The decider of a sequence takes the next queue position
+// and writes its SeqInfo there with two relaxed 16-byte stores; a reader
+// validates each field against kMarker (a NaN no field ever holds).
 // ---------------------------------------------------------------------------
 // Lane 0 takes the next queue position (a predicated atomic: nothing waits
 // for it until the entry is written).
@@ -179,11 +179,11 @@ __device__ __forceinline__ int resolve_position(const SampleArgs& a, int b, int 
 // when the committer is the result side, else from the result slot.  In
 // early-exit mode the rows after the decision are not all read: the result
 // side commits at once, and only the rows the decision used were checked.
-__device__ __noinline__ void commit_sequence(const SampleArgs& a, int b, bool seqbad, bool have, uint4 res) {
+__device__ __noinline__ void commit_sequence(const SampleArgs& a, int b, bool rows_bad, bool have, uint4 res) {
   const int lane = threadIdx.x & 31;
   const int K = a.K;
   if (!have) res = wait_result(a.result + b, a.status);
-  const bool bad = seqbad || res.x == kResultBad;
+  const bool bad = rows_bad || res.x == kResultBad;
   int32_t* out = a.out_tokens + (size_t)b * (K + 1);
   const int32_t* x = a.tokens + (size_t)b * K;
   if (bad) {
@@ -802,9 +802,10 @@ __device__ __forceinline__ int next_live_counter(int ctr, unsigned dead) {
 }
 
 // Scheduling.  Statistics slices come from eight claim counters: the k-th
-// claim on counter c is flat slice f = k * kSlices + c.  The next claim
-// is issued before the current slice is processed, so the atomic's latency
-// hides behind the stream.  Tail slices of the first TTo / TC queue positions
+// claim on counter c is flat slice f = k * kSlices + c, where claims
+// 0 .. grid-1 of every counter are the warps' static first claims and the
+// counters hand out the rest.  The next claim is issued before the current
+// slice is processed, so the atomic's latency hides behind the stream.  Tail slices of the first TTo / TC queue positions
 // are owned, not claimed: tail item j (queue position j / TC, tail slice
 // j % TC) belongs to global warp j % W, where warp slot w of CTA c is global
 // warp w * grid + c and W = 8 * grid.  A warp takes its items in order and
@@ -817,8 +818,9 @@ __device__ __forceinline__ int next_live_counter(int ctr, unsigned dead) {
 // late tail waits for a busy owner.
 //
 // Progress: statistics slices and the finishers they trigger wait only for
-// stores that other warps have already issued (their tickets were counted), a
-// warp holding a claimed statistics slice never waits, and every sequence is
+// stores that other warps have already issued (their tickets were counted); a
+// warp holding a claimed statistics slice never waits, and a warp waits for a
+// queue entry only when it has no statistics work left; every sequence is
 // decided once the statistics slices of its positions up to the first
 // rejection are done.  So every queue entry is eventually written and every
 // wait ends, whatever part of the grid is resident.

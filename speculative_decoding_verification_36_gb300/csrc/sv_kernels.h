@@ -46,7 +46,7 @@ inline FastDiv make_fastdiv(uint32_t d) {
   return f;
 }
 
-// Per-sequence decision, published by the statistics finisher as one 32-byte
+// Per-sequence decision, published by the sequence's decider as one 32-byte
 // entry of the decision queue.  Entries start filled with kMarker words and
 // every field is written once with a value that is never kMarker (n >= 0, and
 // the floats are finite), so a reader knows a field has arrived from its value

@@ -16,6 +16,7 @@ from __future__ import annotations
 import argparse
 import hashlib
 import json
+import math
 import os
 import statistics
 import subprocess
@@ -189,20 +190,46 @@ def algorithmic_bytes(p) -> int:
 
 def oracle_seq_per_s(x_cpu, p, budget_s: float, max_seq: int):
     """The fp64 oracle timed on this host's cores on a bounded sample of the
-    same inputs (sequence by sequence until the time budget is used)."""
+    same inputs (sequence by sequence until the time budget is used).  Also
+    returns the oracle's result for the first pass over the sample (seed 0,
+    sequence ids 0..B-1), for the parity check of the bench line."""
     import oracle
     oracle.build()
     done = 0
+    first = {}
     t0 = time.perf_counter()
     while done < max_seq:
         b = done % p.B
-        oracle.spec_verify(x_cpu["target"][b:b + 1], x_cpu["draft"][b:b + 1], x_cpu["tokens"][b:b + 1],
-                           p.temperature, 0, seq_ids=[b])
+        r = oracle.spec_verify(x_cpu["target"][b:b + 1], x_cpu["draft"][b:b + 1], x_cpu["tokens"][b:b + 1],
+                               p.temperature, 0, seq_ids=[b])
+        if b not in first:
+            first[b] = r
         done += 1
         if time.perf_counter() - t0 > budget_s:
             break
     dt = time.perf_counter() - t0
-    return done / dt, done, dt
+    return done / dt, done, dt, first
+
+
+def parity_sample(gpu_tokens, gpu_n, first):
+    """GPU outputs against the oracle's on the sequences the CPU leg ran:
+    exact matches, sequences that differ only at a draw within 1e-6 of its
+    decision boundary, other mismatches, and the oracle's boundary draws."""
+    import numpy as np
+    same = boundary = other = draws = 0
+    for b, r in first.items():
+        am, sm = r["acc_margin"][0], r["sample_margin"][0]
+        draws += int(np.sum(am[np.isfinite(am)] < 1e-6)) + int(np.isfinite(sm) and sm < 1e-6)
+        if int(gpu_n[b]) == int(r["n"][0]) and np.array_equal(gpu_tokens[b], r["tokens"][0]):
+            same += 1
+        elif (int(gpu_n[b]) != int(r["n"][0]) and min(int(gpu_n[b]), int(r["n"][0])) >= 0
+              and am[min(int(gpu_n[b]), int(r["n"][0]))] < 1e-6) or (
+                int(gpu_n[b]) == int(r["n"][0]) and np.isfinite(sm) and sm < 1e-6):
+            boundary += 1
+        else:
+            other += 1
+    return {"sequences": len(first), "identical": same, "boundary_only": boundary,
+            "mismatch": other, "oracle_boundary_draws": draws}
 
 
 # --------------------------------------------------------------------------
@@ -436,10 +463,27 @@ def run_gpu(args):
     if world == 1 and not args.no_cpu_baseline:
         x_cpu = {k: sets[0][k][:64].cpu() for k in ("target", "draft", "tokens")}
         pp = wl.preset(WORKLOAD, B=64)
-        v, done, dt = oracle_seq_per_s(x_cpu, pp, args.cpu_budget, 1 << 30)
+        v, done, dt, first = oracle_seq_per_s(x_cpu, pp, args.cpu_budget, 1 << 30)
         line["cpu_baseline"] = {"value": v, "unit": UNIT, "cores": 1, "kind": "oracle",
                                 "sample": f"{done} c3 sequences (cycling over the first 64 of "
                                           f"the batch) in {dt:.1f} s, fp64 C oracle, single thread"}
+        # the verify of input set 0 with seed 0, checked against the oracle
+        # on the sequences above
+        x = sets[0]
+        tok0, n0 = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 0, stream=stream)
+        torch.cuda.synchronize(dev)
+        line["parity_sample"] = parity_sample(tok0.cpu().numpy(), n0.cpu().numpy(), first)
+    if world == 1:
+        # acceptance statistics of one batch (spec_acceptance_stats on the GPU)
+        x = sets[0]
+        _, n0 = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 0, stream=stream)
+        st = sv.spec_acceptance_stats(n0, p.K, stream=stream)
+        torch.cuda.synchronize(dev)
+        line["acceptance"] = {"mean_tokens_per_step": float(st["mean_tokens"]),
+                              # null where no sequence reached the position
+                              "alpha_per_position": [round(float(a), 4) if math.isfinite(float(a)) else None
+                                                     for a in st["alpha"].cpu()],
+                              "accepted_histogram": [int(h) for h in st["hist"].cpu()]}
     print(json.dumps(line), flush=True)
     if world > 1:
         import torch.distributed as dist

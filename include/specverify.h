@@ -332,6 +332,17 @@ int spec_ngram_draft(const int32_t *tokens, const int32_t *lengths, int B, int s
                      int32_t *out_match_len, cudaStream_t stream);
 
 /*
+ * Test hook, for fault-injection tests: the next n scratch allocations from
+ * the library's pool (any device, any entry point that allocates) fail as if
+ * the pool were exhausted.  The call then returns SPEC_ERR_CUDA before
+ * launching anything, and spec_status_string(SPEC_ERR_CUDA) says so.  n <= 0
+ * clears it.  Returns the count that was pending.  The pages have no
+ * counterpart; it exists so that the error path can be tested without a real
+ * allocation failure.
+ */
+int spec_test_fail_allocations(int n);
+
+/*
  * Synchronises `stream`, then returns in *flags_out (may be NULL) the device
  * status word of the current device (an OR of SPEC_FLAG_* set by every call
  * since the last read) and clears it.  Returns SPEC_OK or SPEC_ERR_CUDA.

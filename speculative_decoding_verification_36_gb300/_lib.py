@@ -50,6 +50,7 @@ SIGNATURES = {
     "spec_tree_verify_sampling_bf16": [_P, _P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_acceptance_stats": [_P, _I, _I, _P, _P, _P, _P],
     "spec_ngram_draft": [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P],
+    "spec_test_fail_allocations": [_I],
     "spec_get_status": [_P, _P],
     "spec_status_string": [_I],
 }

@@ -13,6 +13,7 @@
 
 #include <stdlib.h>
 
+#include <atomic>
 #include <mutex>
 
 // Sticky per-device status word (SPEC_FLAG_* bits), read and cleared by
@@ -192,9 +193,15 @@ bool sizes_ok(int B, int rows, int V) {
 // they can run while the previous kernel drains, and the caller's stream sees
 // one launch per call instead of a fill, a gap and a launch.  (The caller's
 // stream returns the scratch with cudaFreeAsync after the kernel.)
+// Scratch allocations still to be failed on purpose (spec_test_fail_allocations).
+std::atomic<int> g_fail_allocs{0};
+
 int run_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, void** ws) {
   const int rc = ensure_pool(d);
   if (rc) return rc;
+  for (int k = g_fail_allocs.load(); k > 0; k = g_fail_allocs.load())
+    if (g_fail_allocs.compare_exchange_weak(k, k - 1))
+      return cuda_fail(cudaErrorMemoryAllocation, "cudaMallocFromPoolAsync (failed on request)");
   cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
   cudaError_t e = cudaStreamIsCapturing(stream, &cap);
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamIsCapturing");
@@ -683,6 +690,8 @@ int spec_ngram_draft(const int32_t* tokens, const int32_t* lengths, int B, int s
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
   return SPEC_OK;
 }
+
+int spec_test_fail_allocations(int n) { return g_fail_allocs.exchange(n < 0 ? 0 : n); }
 
 int spec_get_status(cudaStream_t stream, uint32_t* flags_out) {
   DeviceState* d = nullptr;

@@ -1,0 +1,117 @@
+"""Output guards and an injected allocation failure on the GPU.
+
+Every output buffer is surrounded by canary words: a call must write its
+outputs and nothing next to them.  A scratch allocation that fails (forced
+through the library's test hook) must return SPEC_ERR_CUDA without touching
+the outputs, and the next call must work."""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+import speculative_decoding_verification_36_gb300 as sv
+from speculative_decoding_verification_36_gb300 import _lib
+from speculative_decoding_verification_36_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+G = 64  # guard elements on each side
+CANARY_I = 0x5A5A1234
+CANARY_F = -12345.25
+
+
+class Guarded:
+    """An output tensor with canary words on both sides."""
+
+    def __init__(self, shape, dtype):
+        n = int(np.prod(shape)) if len(shape) else 1
+        self.buf = torch.empty(n + 2 * G, dtype=dtype, device=DEV)
+        self.fill = CANARY_I if dtype in (torch.int32, torch.int64) else CANARY_F
+        self.buf.fill_(self.fill)
+        self.t = self.buf[G:G + n].view(shape)
+
+    def intact(self):
+        b = self.buf.cpu()
+        return bool((b[:G] == self.fill).all() and (b[-G:] == self.fill).all())
+
+
+def _chain(name, **over):
+    p = wl.preset(name, **over)
+    x = wl.make_chain(p, device=DEV, seed=2)
+    return p, x
+
+
+def test_chain_outputs_are_guarded():
+    for name, over in (("c2", dict(B=5, K=5, V=1000)), ("c1", dict(B=3, K=2, V=257)), ("c4", dict(B=7, V=999))):
+        p, x = _chain(name, **over)
+        tok, n = Guarded((p.B, p.K + 1), torch.int32), Guarded((p.B,), torch.int32)
+        sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 1, out_tokens=tok.t, out_n_accepted=n.t)
+        if p.temperature > 0:
+            tok2, n2 = Guarded((p.B, p.K + 1), torch.int32), Guarded((p.B,), torch.int32)
+            sv.spec_verify_early_exit(x["target"], x["draft"], x["tokens"], p.temperature, 1,
+                                      out_tokens=tok2.t, out_n_accepted=n2.t)
+            torch.cuda.synchronize()
+            assert tok2.intact() and n2.intact()
+            assert torch.equal(tok.t, tok2.t)
+        torch.cuda.synchronize()
+        assert tok.intact() and n.intact(), name
+        assert (n.t >= 0).all()
+    assert sv.spec_get_status() == 0
+
+
+def test_stats_outputs_are_guarded():
+    p, x = _chain("c2", B=4, K=3, V=2048)
+    B, K, R = p.B, p.K, 2 * p.K + 1
+    outs = dict(tok=Guarded((B, K + 1), torch.int32), n=Guarded((B,), torch.int32),
+                rs=Guarded((B, R, 2), torch.float32), pq=Guarded((B, K, 2), torch.float32),
+                res=Guarded((B,), torch.float32), ent=Guarded((B, R), torch.float32))
+    lib = _lib.load()
+    with torch.cuda.device(DEV):
+        _lib.check(lib.spec_verify_stats_bf16(
+            x["target"].data_ptr(), x["draft"].data_ptr(), x["tokens"].data_ptr(), B, K, p.V,
+            ctypes.c_float(p.temperature), 1, outs["tok"].t.data_ptr(), outs["n"].t.data_ptr(),
+            outs["rs"].t.data_ptr(), outs["pq"].t.data_ptr(), outs["res"].t.data_ptr(),
+            outs["ent"].t.data_ptr(), torch.cuda.current_stream().cuda_stream))
+    torch.cuda.synchronize()
+    for k, g in outs.items():
+        assert g.intact(), k
+
+
+def test_tree_and_ngram_outputs_are_guarded():
+    tr = wl.make_tree(wl.preset("c5", B=3, V=777), device=DEV, seed=5)
+    B, N = 3, tr["tokens"].shape[1]
+    path, ln, mask = Guarded((B, N + 1), torch.int32), Guarded((B,), torch.int32), Guarded((B, N, 1), torch.int32)
+    sv.spec_tree_verify_greedy(tr["target"], tr["tokens"], tr["parents"], out_path=path.t, out_len=ln.t,
+                               out_mask=mask.t)
+    torch.cuda.synchronize()
+    assert path.intact() and ln.intact() and mask.intact()
+    h = wl.make_ngram_histories(6, 5000, V=50, seed=3)
+    d, nd, ml = Guarded((6, 7), torch.int32), Guarded((6,), torch.int32), Guarded((6,), torch.int32)
+    sv.spec_ngram_draft(h["tokens"].to(DEV), h["lengths"].to(DEV), 1, 5, 7, out_drafts=d.t, out_n_drafts=nd.t,
+                        out_match_len=ml.t)
+    torch.cuda.synchronize()
+    assert d.intact() and nd.intact() and ml.intact()
+    assert sv.spec_get_status() == 0
+
+
+def test_a_failed_scratch_allocation_is_reported_and_harmless():
+    lib = _lib.load()
+    p, x = _chain("c2", B=6, K=4, V=3000)
+    ref_tok, ref_n = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 9)
+    torch.cuda.synchronize()
+    tok, n = Guarded((p.B, p.K + 1), torch.int32), Guarded((p.B,), torch.int32)
+    assert lib.spec_test_fail_allocations(1) == 0
+    with pytest.raises(sv.SpecError) as err:
+        sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 9, out_tokens=tok.t,
+                       out_n_accepted=n.t)
+    assert "failed on request" in str(err.value)
+    torch.cuda.synchronize()
+    # nothing was launched: the outputs keep their canary fill
+    assert (tok.buf.cpu() == CANARY_I).all() and (n.buf.cpu() == CANARY_I).all()
+    # the next call allocates normally and gives the same result as before
+    sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 9, out_tokens=tok.t, out_n_accepted=n.t)
+    torch.cuda.synchronize()
+    assert torch.equal(tok.t, ref_tok) and torch.equal(n.t, ref_n) and tok.intact()
+    assert lib.spec_test_fail_allocations(0) == 0
+    assert sv.spec_get_status() == 0

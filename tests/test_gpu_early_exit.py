@@ -22,7 +22,7 @@ def _dev(x):
 @pytest.mark.parametrize("name,over", [
     ("c1", {}), ("c2", dict(B=24)), ("c3", dict(B=32)), ("c3", dict(B=6, V=4093, K=1)),
     ("c2", dict(B=4, K=0, V=2048)), ("c1", dict(B=5, V=7, K=3)), ("c1", dict(B=3, K=31, V=600)),
-    ("c1", dict(B=2, K=40, V=300)),
+    ("c1", dict(B=2, K=40, V=300)), ("c3", dict(B=3, K=2, V=1048576)), ("c2", dict(B=2100, K=3, V=6400)),
 ])
 def test_early_exit_parity(name, over):
     p = wl.preset(name, **over)

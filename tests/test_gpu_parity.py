@@ -53,6 +53,10 @@ SAMPLING_CASES = [
     ("c1", dict(B=3, K=31, V=600)),       # acceptance scan across a 32-lane boundary
     ("c1", dict(B=2, K=40, V=300)),
     ("c1", dict(B=2, K=255, V=64)),       # the largest K: 511 rows, eight 32-position chunks
+    ("c3", dict(B=3, K=2, V=1048576)),    # 342 tail slices per row: the CDF search takes 3 rounds
+    ("c1", dict(B=2, K=2, V=999999)),     # fp32 scalar path, 652 tail slices per row
+    ("c2", dict(B=2048, K=2, V=512)),     # many short sequences (small-batch scheduling)
+    ("c2", dict(B=2100, K=3, V=6400)),    # 2100 queue entries with the full-size scheduling
 ]
 
 

@@ -74,6 +74,7 @@ CASES = [
     ("1024 nodes", 2, 64, torch.float32, "rand1024", 1.0),
     ("single node", 8, 9, torch.float32, [-1], 1.0),
     ("tiny vocabulary", 8, 1, torch.float32, [-1, 0, 0], 1.0),
+    ("binary depth 2, V=2^20", 2, 1 << 20, torch.bfloat16, [-1, -1, 0, 0, 1, 1], 1.0),
 ]
 
 

@@ -198,6 +198,32 @@ def test_bad_data_is_flagged_not_trapped():
     assert sv.spec_get_status() == 0
 
 
+def test_gpu_adversarial_draft_is_lossless():
+    """A draft that puts almost all of its mass where the target has almost
+    none: 10^6 replicas match the oracle and the emitted tokens follow p."""
+    from scipy import stats
+    K, V, R = 2, 6, 1_000_000
+    target = torch.zeros(K + 1, V)
+    target[:, 0], target[:, 1], target[:, V - 1] = 3.0, 2.5, -6.0
+    draft = torch.zeros(K, V)
+    draft[:, V - 1] = 8.0
+    P = torch.softmax(target.double(), -1).numpy()
+    Q = torch.softmax(draft.double(), -1)
+    g = torch.Generator().manual_seed(8)
+    x = torch.stack([torch.multinomial(Q[i], R, replacement=True, generator=g) for i in range(K)],
+                    dim=1).int()
+    tokens, n = sv.spec_verify(target.to(DEV).expand(R, K + 1, V).contiguous(),
+                               draft.to(DEV).expand(R, K, V).contiguous(), x.to(DEV), 1.0, 77)
+    torch.cuda.synchronize()
+    tokens, n = tokens.cpu().numpy(), n.cpu().numpy()
+    for j in range(K + 1):
+        reached = n >= j
+        counts = np.bincount(tokens[reached, j], minlength=V)
+        assert stats.chisquare(counts, P[j] * reached.sum()).pvalue > 1e-4
+    ref = oracle.spec_verify(target, draft, x, 1.0, 77, broadcast=True, n_seq=R)
+    assert not chain_report(tokens, n, ref)["mismatch"]
+
+
 def test_gpu_chi_square_losslessness():
     """V = 8, K = 3, 10^6 replicas of one sequence with drafts drawn from q:
     the token emitted at each reached position follows p (chi-square), and

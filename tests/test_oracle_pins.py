@@ -275,6 +275,42 @@ def test_chi_square_losslessness(K, V, seed):
         assert abs(reached.mean() - pr) < 5 * sig
 
 
+def _adversarial_rows(K, V):
+    """Target rows with their mass on the low ids and a draft that puts almost
+    all of its mass on the last id, where the target has almost none."""
+    target = torch.zeros(K + 1, V)
+    target[:, 0], target[:, 1], target[:, V - 1] = 3.0, 2.5, -6.0
+    draft = torch.zeros(K, V)
+    draft[:, V - 1] = 8.0
+    return target, draft
+
+
+def test_adversarial_draft_is_still_lossless():
+    """The output distribution does not depend on how good the draft is
+    (page 2 'The correctness guarantee'): a draft concentrated where the
+    target is nearly zero is rejected almost always, and the emitted tokens
+    still follow p, by exact enumeration and by chi-square over 10^6
+    replicas; the acceptance rate is the (small) sum of min(p, q)."""
+    from scipy import stats
+    K, V, n_rep = 2, 6, 1000000
+    target, draft = _adversarial_rows(K, V)
+    P = torch.softmax(target.double(), -1).numpy()
+    Q = torch.softmax(draft.double(), -1).numpy()
+    M = _exact_output_marginals(P, Q)
+    np.testing.assert_allclose(M / M.sum(axis=1, keepdims=True), P, atol=1e-12)
+    rng = np.random.default_rng(8)
+    x = np.stack([rng.choice(V, size=n_rep, p=Q[i]) for i in range(K)], axis=1).astype(np.int32)
+    out = oracle.spec_verify(target, draft, x, 1.0, 77, broadcast=True, n_seq=n_rep)
+    alpha = np.minimum(P[0], Q[0]).sum()
+    assert alpha < 0.05
+    acc0 = (out["n"] >= 1).mean()
+    assert abs(acc0 - alpha) < 5 * math.sqrt(alpha * (1 - alpha) / n_rep)
+    for j in range(K + 1):
+        reached = out["n"] >= j
+        counts = np.bincount(out["tokens"][reached, j], minlength=V)
+        assert stats.chisquare(counts, P[j] * reached.sum()).pvalue > 1e-4
+
+
 def test_expected_tokens_closed_form_and_page_example():
     """Page 2: E[tokens] = (1 - alpha^(gamma+1)) / (1 - alpha); worked example
     0.7 -> about 2.8, 0.9 -> about 4.1 for gamma = 4 (tests/golden)."""

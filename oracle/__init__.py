@@ -59,7 +59,7 @@ def _load():
     lib.oracle_spec_verify.argtypes = [P, P, i32, i64, i64, P, i64, i32, i32, i32, f64, u64, P, i32,
                                        P, P, P, P, P, P, P, P, P, P, P, P, P]
     lib.oracle_spec_verify.restype = i32
-    lib.oracle_spec_verify_greedy.argtypes = [P, i32, i64, P, i64, i32, i32, i32, P, P, P]
+    lib.oracle_spec_verify_greedy.argtypes = [P, i32, i64, P, i64, i32, i32, i32, i32, P, P, P]
     lib.oracle_spec_verify_greedy.restype = i32
     lib.oracle_tree_verify_greedy.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P]
     lib.oracle_tree_verify_greedy.restype = i32
@@ -194,8 +194,11 @@ def spec_verify(target, draft, draft_tokens, temperature: float, seed: int,
     return out
 
 
-def spec_verify_greedy(target, draft_tokens):
-    """Greedy verification (temperature 0).  target [B, K+1, V]; tokens [B, K]."""
+def spec_verify_greedy(target, draft_tokens, used_rows_only: bool = False):
+    """Greedy verification (temperature 0).  target [B, K+1, V]; tokens [B, K].
+    ``used_rows_only`` checks for bad data only what the result depends on,
+    in position order (rows 0..n, tokens x_0..x_n, row K when all match), as
+    the early-exit verify does."""
     lib = _load()
     t, dt = _as_logits(target)
     x = _as_i32(draft_tokens)
@@ -205,7 +208,7 @@ def spec_verify_greedy(target, draft_tokens):
     tokens = np.full((B, K1), -1, dtype=np.int32)
     n = np.zeros(B, dtype=np.int32)
     argmax = np.zeros((B, K1), dtype=np.int32)
-    lib.oracle_spec_verify_greedy(_ptr(t), dt, K1 * V, _ptr(x_buf), K, B, K, V,
+    lib.oracle_spec_verify_greedy(_ptr(t), dt, K1 * V, _ptr(x_buf), K, B, K, V, int(bool(used_rows_only)),
                                   _ptr(tokens), _ptr(n), _ptr(argmax))
     return dict(tokens=tokens, n=n, row_argmax=argmax)
 

@@ -389,10 +389,19 @@ static int row_argmax(const void *row, int dtype, int V)
  * target row, which is the bonus token when all K match.
  * Layouts as in oracle_spec_verify; draft logits are not read.
  */
+/*
+ * used_rows_only: the early-exit reading, as for the sampled verify above --
+ * positions are examined in order and only what the result uses is checked:
+ * target row i (NaN / +inf / no finite maximum), then x_i outside [0, V), then
+ * x_i against the argmax of row i; the first mismatch is n, and target row K
+ * is checked only when all K drafts match.  A bad position stops the scan and
+ * marks the sequence bad.  row_argmax_out then holds the argmax of rows 0..n
+ * and -1 after n.
+ */
 int oracle_spec_verify_greedy(const void *target, int dtype, long long t_stride_b,
                               const int32_t *tokens, long long tok_stride_b,
-                              int B, int K, int V, int32_t *out_tokens, int32_t *out_n,
-                              int32_t *row_argmax_out)
+                              int B, int K, int V, int used_rows_only,
+                              int32_t *out_tokens, int32_t *out_n, int32_t *row_argmax_out)
 {
     const size_t esz = dtype == ORC_DTYPE_F32 ? 4 : 2;
     for (int b = 0; b < B; ++b) {
@@ -401,6 +410,40 @@ int oracle_spec_verify_greedy(const void *target, int dtype, long long t_stride_
         int32_t *out = out_tokens + (size_t)b * (size_t)(K + 1);
         for (int j = 0; j <= K; ++j)
             out[j] = -1;
+        if (used_rows_only) {
+            int n = K, bad = 0, last = -1;
+            for (int i = 0; i <= K; ++i) {
+                const char *row = tb + (size_t)i * V * esz;
+                if (row_is_bad(row, dtype, V)) {
+                    bad = 1;
+                    break;
+                }
+                const int a = row_argmax(row, dtype, V);
+                if (row_argmax_out) row_argmax_out[(size_t)b * (K + 1) + i] = a;
+                last = i;
+                if (i == K)
+                    break;
+                if (x[i] < 0 || x[i] >= V) {
+                    bad = 1;
+                    break;
+                }
+                if (x[i] != a) {
+                    n = i;
+                    break;
+                }
+            }
+            for (int rr = last + 1; rr <= K && row_argmax_out; ++rr)
+                row_argmax_out[(size_t)b * (K + 1) + rr] = -1;
+            if (bad) {
+                out_n[b] = -1;
+                continue;
+            }
+            for (int i = 0; i < n; ++i)
+                out[i] = x[i];
+            out[n] = row_argmax(tb + (size_t)n * V * esz, dtype, V);
+            out_n[b] = n;
+            continue;
+        }
         int bad = 0;
         for (int rr = 0; rr <= K && !bad; ++rr)
             bad = row_is_bad(tb + (size_t)rr * V * esz, dtype, V);

@@ -761,3 +761,56 @@ def test_used_rows_only_flags_bad_rows_it_uses():
     t[3, K, 4] = float("nan")       # the bonus row, used since all are accepted
     out = oracle.spec_verify(t, d, x, 1.0, 0, used_rows_only=True)
     assert out["n"].tolist() == [-1, -1, -1, -1] and (out["tokens"] == -1).all()
+
+
+def test_greedy_used_rows_only():
+    """The early-exit reading of the greedy verify: on clean data the result
+    equals the full greedy verify (argmax of torch, lowest id on ties); rows
+    and tokens after the first mismatch never matter; a bad row or token at
+    or before it marks the sequence bad, and target row K matters only when
+    every draft matches."""
+    rng = np.random.default_rng(31)
+    B, K, V = 60, 4, 32
+    t = torch.tensor(2.0 * rng.standard_normal((B, K + 1, V)), dtype=torch.float32)
+    g = torch.argmax(t, dim=-1).numpy()
+    # drafts match the argmax with probability 0.6 per position
+    x = np.where(rng.random((B, K)) < 0.6, g[:, :K], rng.integers(0, V, (B, K))).astype(np.int32)
+    full = oracle.spec_verify_greedy(t, x)
+    used = oracle.spec_verify_greedy(t, x, used_rows_only=True)
+    assert np.array_equal(full["tokens"], used["tokens"]) and np.array_equal(full["n"], used["n"])
+    for b in range(B):
+        n = int(used["n"][b])
+        assert np.array_equal(used["row_argmax"][b, :n + 1], g[b, :n + 1])
+        assert (used["row_argmax"][b, n + 1:] == -1).all()
+    assert (full["n"] < K).any() and (full["n"] == K).any()
+    # spoil every row and token after each sequence's first mismatch
+    t2, x2 = t.clone(), x.copy()
+    for b in range(B):
+        n = int(full["n"][b])
+        if n < K:
+            t2[b, n + 1:, 5] = float("nan")
+            x2[b, n + 1:] = V + 7
+    used2 = oracle.spec_verify_greedy(t2, x2, used_rows_only=True)
+    assert np.array_equal(used2["tokens"], used["tokens"]) and np.array_equal(used2["n"], used["n"])
+    full2 = oracle.spec_verify_greedy(t2, x2)
+    assert all(full2["n"][b] == -1 for b in range(B) if full["n"][b] < K - 1)
+    # a bad row at or before n, or an out-of-range x_n, marks the sequence bad
+    for b in range(B):
+        n = int(full["n"][b])
+        t3, x3 = t.clone(), x.copy()
+        j = int(rng.integers(0, n + 1))
+        t3[b, j, 0] = float("inf")
+        assert oracle.spec_verify_greedy(t3, x3, used_rows_only=True)["n"][b] == -1
+        if n < K:
+            x3 = x.copy()
+            x3[b, n] = -5
+            r = oracle.spec_verify_greedy(t, x3, used_rows_only=True)
+            assert r["n"][b] == -1 and (r["tokens"][b] == -1).all()
+    # target row K is used only when every draft matches
+    allm = [b for b in range(B) if full["n"][b] == K]
+    some = [b for b in range(B) if full["n"][b] < K]
+    t4 = t.clone()
+    t4[:, K, :] = float("-inf")
+    r = oracle.spec_verify_greedy(t4, x, used_rows_only=True)
+    assert all(r["n"][b] == -1 for b in allm)
+    assert all(r["n"][b] == full["n"][b] for b in some)

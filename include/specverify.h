@@ -120,7 +120,14 @@ int spec_verify_bf16(const uint16_t *target_logits, const uint16_t *draft_logits
  * n = -1, the sequence's outputs are -1 and SPEC_FLAG_BAD_DATA is set.  Bad
  * data after the first rejection is not reported (spec_verify reports it).
  * With K > 31 every row is read (the sequence is decided once all positions
- * are resolved); temperature 0 runs the greedy verify of spec_verify.
+ * are resolved).
+ * Temperature 0 (draft_logits may be NULL): the greedy verify of spec_verify
+ * with the same early exit -- target rows are read by position and a row
+ * after a decided sequence's first mismatch n is skipped.  Bad data is
+ * checked in position order on what is used: target row i (NaN, +inf, no
+ * finite maximum), then x_i outside [0, V), for i = 0..n, and target row K
+ * when all K drafts match.  (1 <= K <= 31; otherwise every row is read, as in
+ * spec_verify.)
  */
 int spec_verify_early_exit_f32(const float *target_logits, const float *draft_logits,
                                const int32_t *draft_tokens, int B, int K, int V, float temperature,

@@ -110,8 +110,9 @@ def spec_verify_early_exit(target_logits, draft_logits, draft_tokens, temperatur
                            out_tokens=None, out_n_accepted=None, stream=None):
     """spec_verify that reads only the rows its result depends on (positions
     up to the first rejection, and the bonus row when every draft is
-    accepted); bad data is checked on those rows only.  Returns (out_tokens
-    [B,K+1], n [B])."""
+    accepted); bad data is checked on those rows only.  Temperature 0 is the
+    greedy verify with the same early exit (draft_logits may be None).
+    Returns (out_tokens [B,K+1], n [B])."""
     bf16, B, K, V = _chain_args(target_logits, draft_logits, draft_tokens, temperature)
     dev = target_logits.device
     out_tokens = _out(out_tokens, (B, K + 1), torch.int32, dev, "out_tokens")

@@ -272,7 +272,7 @@ cudaError_t put_scratch(bool use_static, void* ws, cudaStream_t stream) {
 int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
                 const int32_t* parents, int B, int K, int V, int32_t* out_tokens, int32_t* out_n,
                 uint32_t* out_mask, int32_t* out_row_argmax, cudaStream_t stream,
-                bool use_static = false) {
+                bool use_static = false, bool early_exit = false) {
   DeviceState* d = nullptr;
   int rc = get_device_state(&d);
   if (rc) return rc;
@@ -296,6 +296,8 @@ int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
   a.out_n = out_n;
   a.out_mask = out_mask;
   a.out_row_argmax = out_row_argmax;
+  // early exit for the chain (the resolution word holds positions 0..31)
+  a.early_exit = (early_exit && !tree && K >= 1 && K <= sv::kMaskMaxK && !out_row_argmax) ? 1 : 0;
   a.status = d->status;
   void* ws = nullptr;
   rc = get_scratch(d, use_static, sv::greedy_workspace(B, a.R, a.CU), stream, &ws);
@@ -312,12 +314,12 @@ int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
 
 int greedy_impl(bool bf16, const void* target, const int32_t* tokens, int B, int K, int V,
                 int32_t* out_tokens, int32_t* out_n, int32_t* out_row_argmax, cudaStream_t stream,
-                bool use_static = false) {
+                bool use_static = false, bool early_exit = false) {
   if (!target || !out_tokens || !out_n || (K > 0 && !tokens)) return SPEC_ERR_NULL;
   if (B < 0 || K < 0 || K > sv::kMaxK || V < 1 || !sizes_ok(B, K + 1, V)) return SPEC_ERR_SHAPE;
   if (B == 0) return SPEC_OK;
   return argmax_impl(false, bf16, target, tokens, nullptr, B, K, V, out_tokens, out_n, nullptr,
-                     out_row_argmax, stream, use_static);
+                     out_row_argmax, stream, use_static, early_exit);
 }
 
 int verify_impl(bool bf16, const void* target, const void* draft, const int32_t* tokens, int B,
@@ -329,7 +331,7 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
     return SPEC_ERR_TEMPERATURE;
   if (temperature == 0.f)
     return greedy_impl(bf16, target, tokens, B, K, V, out_tokens, out_n, nullptr, stream,
-                       use_static);
+                       use_static, early_exit);
   if (!target || !out_tokens || !out_n || (K > 0 && (!tokens || !draft))) return SPEC_ERR_NULL;
   if (B < 0 || K < 0 || K > sv::kMaxK || V < 1 || !sizes_ok(B, 2 * K + 1, V)) return SPEC_ERR_SHAPE;
   if (B == 0) return SPEC_OK;

@@ -159,6 +159,62 @@ __device__ __noinline__ bool row_argmax_finisher(const GreedyArgs& a, int b, int
   return old == a.R - 1;
 }
 
+// Early-exit row finisher (one warp): the argmax of row r of sequence b, the
+// verdict of position r (bad row or token, match, mismatch), its resolution
+// and, when that resolution decides the sequence, the sequence's outputs.
+// Only what the result uses is checked, in position order: a bad row or token
+// after the first mismatch is never read.
+__device__ __noinline__ void ee_row_finisher(const GreedyArgs& a, int b, int r) {
+  const int lane = threadIdx.x & 31;
+  const int K = a.K;
+  const int C = a.CU * kSlices;
+  const uint2* pp = a.part + ((size_t)b * a.R + r) * C;
+  float v = neg_inf();
+  int i = INT_MAX;
+  bool nan = false;
+  for (int c = lane; c < C; c += 32) {
+    const uint2 w = wait_u2(pp + c, a.status);
+    am_merge(v, i, __uint_as_float(w.x), (int)(w.y & 0x7fffffffu));
+    nan |= (w.y >> 31) != 0;
+  }
+  warp_am(v, i);
+  nan = __any_sync(0xffffffffu, nan);
+  const int gv = (nan || !(v > neg_inf()) || !(v < INFINITY) || i == INT_MAX) ? -2 : i;
+  int verdict = gv < 0 ? kVerdictBad : kVerdictAccept;
+  if (r < K && verdict == kVerdictAccept) {
+    const int x = __ldg(a.tokens + (size_t)b * K + r);
+    verdict = (x < 0 || x >= a.V) ? kVerdictBad : (x == gv ? kVerdictAccept : kVerdictReject);
+  }
+  int n = -1;
+  if (lane == 0) {
+    st_relaxed_s32(a.g + (size_t)b * a.R + r, gv);
+    st_relaxed_s32(a.verdict + (size_t)b * a.R + r, verdict);
+    unsigned long long bits = 1ull << r;
+    if (verdict != kVerdictAccept && r < K) bits |= 1ull << (32 + r);
+    const unsigned long long old_set = ~atomicAnd(a.resword + b, ~bits);
+    const int was = decided_n(old_set, K), now = decided_n(old_set | bits, K);
+    if (was < 0 && now >= 0) {
+      n = now;
+      st_relaxed_s32(a.decided + b, n);  // later rows of b may skip
+    }
+  }
+  n = __shfl_sync(0xffffffffu, n, 0);
+  if (n < 0) return;
+  // decided at n: positions 0..n-1 matched; position n mismatched, was bad,
+  // or is the bonus row
+  const int vn = n == r ? verdict : wait_s32(a.verdict + (size_t)b * a.R + n, a.status);
+  const bool bad = vn == kVerdictBad;
+  const int gn = bad ? -1 : (n == r ? gv : wait_s32(a.g + (size_t)b * a.R + n, a.status));
+  const int32_t* x = a.tokens + (size_t)b * K;
+  int32_t* out = a.out_tokens + (size_t)b * (K + 1);
+  for (int j = lane; j <= K; j += 32) out[j] = bad ? -1 : (j < n ? __ldg(x + j) : (j == n ? gn : -1));
+  if (lane == 0) {
+    a.out_n[b] = bad ? -1 : n;
+    if (bad) atomicOr(a.status, kStatusBadData);
+  }
+  __syncwarp();
+}
+
 // The finished argmax of row r (waits for the row finisher's store).
 __device__ __forceinline__ int row_g(const GreedyArgs& a, int b, int r) {
   return wait_s32(a.g + (size_t)b * a.R + r, a.status);
@@ -321,7 +377,11 @@ __device__ __noinline__ void tree_finisher(const GreedyArgs& a, int b) {
 // The warp taking a row's last ticket merges the row; the one merging a
 // sequence's last row runs its finisher.  The only waits are for stores that
 // are already issued (slots leaving the marker state).
-template <class E, int VEC, bool TREE>
+//
+// Early exit (EE, chain only): units are taken by position (row 0 of every
+// sequence, then row 1, ...), each row's finisher resolves its position, and
+// a unit of row r of a sequence already decided at n < r is skipped.
+template <class E, int VEC, bool TREE, bool EE>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) argmax_kernel(const __grid_constant__ GreedyArgs a) {
   const int lane = threadIdx.x & 31;
   const int w = slice_of_warp();
@@ -329,13 +389,33 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) argmax_kernel(const __gr
   int unit = bcast(claim_unit(a.counter, lane));
   while (unit < a.map.total) {
     const int next = claim_unit(a.counter, lane);
-    const int b = unit / a.map.A, idx = unit - (unit / a.map.A) * a.map.A;
-    const int old = __shfl_sync(0xffffffffu, argmax_slice<E, VEC>(a, b, idx, w), 0);
-    if (old == last && row_argmax_finisher(a, b, idx / a.CU)) {
-      if (TREE)
-        tree_finisher(a, b);
-      else
-        chain_finisher(a, b);
+    int b, idx;
+    bool skip = false;
+    if constexpr (EE) {
+      const int per_pos = a.B * a.CU;
+      const int r = unit / per_pos, rem = unit - r * per_pos;
+      b = rem / a.CU;
+      idx = r * a.CU + (rem - b * a.CU);
+      if (r > 0) {
+        const int dn = bcast((int)ld_relaxed_if(lane == 0, a.decided + b, kMarker));
+        skip = dn >= 0 && dn < r;
+      }
+    } else {
+      b = unit / a.map.A;
+      idx = unit - b * a.map.A;
+    }
+    if (!skip) {
+      const int old = __shfl_sync(0xffffffffu, argmax_slice<E, VEC>(a, b, idx, w), 0);
+      if (old == last) {
+        if constexpr (EE) {
+          ee_row_finisher(a, b, idx / a.CU);
+        } else if (row_argmax_finisher(a, b, idx / a.CU)) {
+          if (TREE)
+            tree_finisher(a, b);
+          else
+            chain_finisher(a, b);
+        }
+      }
     }
     unit = bcast(next);
   }
@@ -346,18 +426,22 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) argmax_kernel(const __gr
 // ---------------------------------------------------------------------------
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
-// Workspace: [counters, tickets (start at -1)][marker-filled: part, g][depth,
-// acc]; one 0xff fill initialises the first two parts.
+// Workspace: [counters, tickets (start at -1), resolution words (all-ones:
+// empty)][marker-filled: part, g, decided, verdict][depth, acc]; one 0xff
+// fill initialises the first two parts.
 static void greedy_layout(int B, int R, int CU, size_t* off) {
   const size_t C = (size_t)CU * kSlices;
   size_t o = 0;
   off[0] = o; o += kCounterBytes;                                     // counter
   off[1] = o; o += align_up((size_t)B * R * kTicketStride * 4, 16);  // rowticket
   off[2] = o; o += align_up((size_t)B * 4, 16);                      // seqticket
+  off[10] = o; o += align_up((size_t)B * 8, 16);                     // resword
   o = align_up(o, 256);
   off[3] = o;                                                         // end of zero region
   off[4] = o; o += align_up((size_t)B * R * C * sizeof(uint2), 256);  // part
   off[5] = o; o += align_up((size_t)B * R * 4, 256);                  // g
+  off[11] = o; o += align_up((size_t)B * 4, 256);                     // decided
+  off[12] = o; o += align_up((size_t)B * R * 4, 256);                 // verdict
   off[6] = o;                                                         // end of marker region
   off[7] = o; o += align_up((size_t)B * R * 4, 256);                  // depth
   off[8] = o; o += align_up((size_t)B * R * 4, 256);                  // acc
@@ -365,7 +449,7 @@ static void greedy_layout(int B, int R, int CU, size_t* off) {
 }
 
 WsLayout greedy_workspace(int B, int R, int CU) {
-  size_t off[10];
+  size_t off[13];
   greedy_layout(B, R, CU, off);
   WsLayout l;
   l.total = off[9];
@@ -376,7 +460,7 @@ WsLayout greedy_workspace(int B, int R, int CU) {
 }
 
 void greedy_bind_workspace(GreedyArgs& a, void* ws) {
-  size_t off[10];
+  size_t off[13];
   greedy_layout(a.B, a.R, a.CU, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
@@ -386,11 +470,17 @@ void greedy_bind_workspace(GreedyArgs& a, void* ws) {
   a.g = (int*)(p + off[5]);
   a.depth = (int*)(p + off[7]);
   a.acc = (int*)(p + off[8]);
+  a.resword = (unsigned long long*)(p + off[10]);
+  a.decided = (int*)(p + off[11]);
+  a.verdict = (int*)(p + off[12]);
 }
 
 template <class E, int VEC, bool TREE>
 static cudaError_t launch_t(const GreedyArgs& a, int grid, cudaStream_t s) {
-  argmax_kernel<E, VEC, TREE><<<grid, kThreads, 0, s>>>(a);
+  if (!TREE && a.early_exit)
+    argmax_kernel<E, VEC, false, true><<<grid, kThreads, 0, s>>>(a);
+  else
+    argmax_kernel<E, VEC, TREE, false><<<grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 
@@ -411,12 +501,12 @@ static int occ(K kernel) {
 }
 
 int greedy_blocks_per_sm(bool bf16, bool vec) {
-  if (bf16) return vec ? occ(argmax_kernel<BF16, 8, false>) : occ(argmax_kernel<BF16, 1, false>);
-  return vec ? occ(argmax_kernel<F32, 4, false>) : occ(argmax_kernel<F32, 1, false>);
+  if (bf16) return vec ? occ(argmax_kernel<BF16, 8, false, false>) : occ(argmax_kernel<BF16, 1, false, false>);
+  return vec ? occ(argmax_kernel<F32, 4, false, false>) : occ(argmax_kernel<F32, 1, false, false>);
 }
 int tree_blocks_per_sm(bool bf16, bool vec) {
-  if (bf16) return vec ? occ(argmax_kernel<BF16, 8, true>) : occ(argmax_kernel<BF16, 1, true>);
-  return vec ? occ(argmax_kernel<F32, 4, true>) : occ(argmax_kernel<F32, 1, true>);
+  if (bf16) return vec ? occ(argmax_kernel<BF16, 8, true, false>) : occ(argmax_kernel<BF16, 1, true, false>);
+  return vec ? occ(argmax_kernel<F32, 4, true, false>) : occ(argmax_kernel<F32, 1, true, false>);
 }
 
 }  // namespace sv

@@ -134,24 +134,10 @@ __device__ __noinline__ SeqInfo read_decision(const SampleArgs& a, int pos) {
 // accepted): the rows of the positions after n never delay the decision.
 // Its outputs are committed once every row has also been checked for bad data.
 // ---------------------------------------------------------------------------
-constexpr int kVerdictAccept = 0;
-constexpr int kVerdictReject = 1;
-constexpr int kVerdictBad = 2;
-constexpr int kMaskMaxK = 31;       // resolution words hold positions 0..31 (K <= 31)
 constexpr int kUnitBad = 0x10000;   // added to the sequence's unit count by a unit with bad data
 constexpr uint32_t kResultBad = 0x7ffffffeu;  // result slot field: no value (never kMarker)
 
 __device__ __forceinline__ int unit_slices(const SampleArgs& a, int i) { return i < a.K ? 2 * a.CS : a.CS; }
-
-// Decided count n for the set of resolved / rejected positions `set` (bit i:
-// position i resolved; bit 32 + i: position i rejected, i < K), or -1 while
-// the prefix that fixes n is incomplete.
-__device__ __forceinline__ int decided_n(unsigned long long set, int K) {
-  const unsigned rej = K > 0 ? (unsigned)(set >> 32) & (0xffffffffu >> (32 - K)) : 0u;
-  const int r = rej ? __ffs(rej) - 1 : K;
-  const unsigned long long need = (2ull << r) - 1ull;
-  return (set & need) == need ? r : -1;
-}
 
 // Lane 0: record the verdict of position i of sequence b.  Returns n (lane 0)
 // if this resolution is the one that decides the sequence, else -1.  With

@@ -415,6 +415,26 @@ __device__ __forceinline__ uint32_t ld_relaxed_if(bool pred, const void* p, uint
 __device__ __forceinline__ int bcast(int v) { return __shfl_sync(0xffffffffu, v, 0); }
 
 // ---------------------------------------------------------------------------
+// Position verdicts and the per-sequence resolution word of the chain
+// verifies: a sequence is decided once positions 0..n are resolved with
+// 0..n-1 accepted and n rejected (or bad), or 0..K resolved with all K
+// accepted.
+// ---------------------------------------------------------------------------
+constexpr int kVerdictAccept = 0;
+constexpr int kVerdictReject = 1;
+constexpr int kVerdictBad = 2;
+
+// Decided count n for the set of resolved / rejected positions `set` (bit i:
+// position i resolved; bit 32 + i: position i rejected, i < K), or -1 while
+// the prefix that fixes n is incomplete.
+__device__ __forceinline__ int decided_n(unsigned long long set, int K) {
+  const unsigned rej = K > 0 ? (unsigned)(set >> 32) & (0xffffffffu >> (32 - K)) : 0u;
+  const int r = rej ? __ffs(rej) - 1 : K;
+  const unsigned long long need = (2ull << r) - 1ull;
+  return (set & need) == need ? r : -1;
+}
+
+// ---------------------------------------------------------------------------
 // Online softmax statistics: (m, s) with m the running max of the raw logits
 // and s = sum exp2((z - m) * c), c = log2(e) / temperature.  Terms are always
 // taken relative to the current max, so the dominant terms carry exponent 0.

@@ -27,6 +27,7 @@ constexpr int kTicketStride = 8;    // per-row tickets 32 bytes apart (no same-a
 constexpr int kMinBlocks = 4;  // resident CTAs per SM the register budget allows (64 regs)
 constexpr int kUnroll = 2;     // 16-byte vectors per lane per load batch; two batches in flight
 constexpr int kMaxK = 255;
+constexpr int kMaskMaxK = 31;  // resolution words hold positions 0..31 (K <= 31)
 constexpr int kMaxTreeNodes = 1024;
 
 // Division by a per-launch constant d >= 1 for dividends below 2^31, as one
@@ -153,6 +154,13 @@ struct GreedyArgs {
   int* g;          // [B, R] row argmax, -2 for an unusable row
   int* depth;     // [B, R] tree finisher scratch
   int* acc;       // [B, R] tree finisher scratch
+  // early exit (chain, 1 <= K <= 31): rows streamed by position; the row
+  // finisher resolves its position and the resolution that decides the
+  // sequence writes its outputs; rows after a decided sequence's n are skipped
+  int early_exit;
+  unsigned long long* resword;  // [B] resolution words, stored complemented (all-ones: empty)
+  int* decided;                 // [B] n once decided (marker before)
+  int* verdict;                 // [B, R] position verdicts (marker before)
   unsigned* status;
 };
 

@@ -84,3 +84,66 @@ def test_early_exit_full_size_c3_sampled():
                              p.temperature, 4, seq_ids=sel, used_rows_only=True)
     rep = chain_report(tok_e[sel].cpu().numpy(), n_e[sel].cpu().numpy(), ref)
     assert not rep["mismatch"], rep
+
+
+# --------------------------------------------------------------------------
+# greedy (temperature 0): rows after the first mismatch are not read
+# --------------------------------------------------------------------------
+@pytest.mark.parametrize("over", [dict(B=64), dict(B=16, V=1001), dict(B=8, K=1, V=512),
+                                  dict(B=5, K=31, V=300), dict(B=3, K=40, V=96), dict(B=6, K=0, V=128),
+                                  dict(B=700, K=3, V=2048)])
+def test_greedy_early_exit_parity(over):
+    p = wl.preset("c4", **over)
+    x = wl.make_chain(p, seed=12)
+    t, k = _dev(x["target"]), _dev(x["tokens"])
+    tok_e, n_e = sv.spec_verify_early_exit(t, None, k, 0.0, 0)
+    tok_f, n_f = sv.spec_verify(t, None, k, 0.0, 0)
+    torch.cuda.synchronize()
+    assert sv.spec_get_status() == 0
+    assert torch.equal(tok_e, tok_f) and torch.equal(n_e, n_f)
+    ref = oracle.spec_verify_greedy(x["target"], x["tokens"], used_rows_only=True)
+    assert np.array_equal(tok_e.cpu().numpy(), ref["tokens"]) and np.array_equal(n_e.cpu().numpy(), ref["n"])
+
+
+def test_greedy_early_exit_ignores_rows_after_the_first_mismatch():
+    B, K, V = 10, 4, 640
+    g = torch.Generator().manual_seed(9)
+    t = 3.0 * torch.randn(B, K + 1, V, generator=g)
+    am = torch.argmax(t, dim=-1).to(torch.int32)
+    x = am[:, :K].clone()
+    x[:, 1] = (am[:, 1] + 1) % V  # every sequence mismatches at position 1
+    t[0, 2, 9] = float("nan")      # after n: ignored
+    t[1, 3, :] = float("-inf")     # after n: ignored
+    x[2, 3] = V + 5                 # after n: ignored
+    t[3, K, 4] = float("inf")      # bonus row after n: ignored
+    t[4, 1, 2] = float("nan")      # at n: used
+    x[5, 1] = -3                    # the mismatching token itself is out of range: used
+    t[6, 0, 0] = float("inf")      # before n: used
+    x[7] = am[7, :K]                # all match, the bonus row is used ...
+    t[7, K, 1] = float("nan")      # ... and bad
+    x[8] = am[8, :K]                # all match, clean: n = K
+    sv.spec_get_status()
+    for dt in (torch.float32, torch.bfloat16):
+        tt = t.to(dt)
+        ref = oracle.spec_verify_greedy(tt, x, used_rows_only=True)
+        assert ref["n"].tolist() == [1, 1, 1, 1, -1, -1, -1, -1, K, 1]
+        tokens, n = sv.spec_verify_early_exit(_dev(tt), None, _dev(x), 0.0, 0)
+        torch.cuda.synchronize()
+        assert sv.spec_get_status() & sv.SPEC_FLAG_BAD_DATA
+        assert n.cpu().tolist() == ref["n"].tolist()
+        assert np.array_equal(tokens.cpu().numpy(), ref["tokens"])
+    assert sv.spec_get_status() == 0
+
+
+def test_greedy_early_exit_full_size_c4():
+    p = wl.preset("c4")
+    x = wl.make_chain(p, device=DEV, seed=5)
+    tok_e, n_e = sv.spec_verify_early_exit(x["target"], None, x["tokens"], 0.0, 0)
+    tok_f, n_f = sv.spec_verify(x["target"], None, x["tokens"], 0.0, 0)
+    torch.cuda.synchronize()
+    assert sv.spec_get_status() == 0
+    assert torch.equal(tok_e, tok_f) and torch.equal(n_e, n_f)
+    sel = list(range(0, p.B, 64))
+    ref = oracle.spec_verify_greedy(x["target"][sel].cpu(), x["tokens"][sel].cpu(), used_rows_only=True)
+    assert np.array_equal(tok_e[sel].cpu().numpy(), ref["tokens"])
+    assert np.array_equal(n_e[sel].cpu().numpy(), ref["n"])

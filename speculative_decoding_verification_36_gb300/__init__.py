@@ -7,11 +7,14 @@ the same name on the current stream; every step of the verify path runs in the
 library's CUDA kernels.  There is no CPU fallback.
 
     spec_verify(target_logits, draft_logits, draft_tokens, temperature, seed)
+    spec_verify_early_exit(...)       # reads only the rows the result depends on
+    spec_verify_static_scratch(...)   # no allocation: a fixed per-device scratch buffer
     spec_verify_stats(...)            # plus row statistics, p(x), q(x), mass
     spec_verify_greedy_argmax(...)    # greedy chain plus every row's argmax
     spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx)
     spec_tree_verify_sampling(target_logits, draft_logits, tree_tokens, parent_idx, T, seed)
     spec_acceptance_stats(n_accepted, K)  # histogram, alpha, mean tokens
+    spec_ngram_draft(tokens, lengths, n_min, n_max, K)  # prompt-lookup drafts
     spec_get_status()                 # device status word (bad data, timeouts)
 """
 from __future__ import annotations
@@ -55,11 +58,19 @@ def _ptr(t):
     return t.data_ptr()
 
 
-def _i32(t: torch.Tensor, shape, name: str):
-    if t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
+def _same_device(t: torch.Tensor, device, name: str):
+    # a pointer into another GPU's memory is not readable by this device's kernels
+    if t.device != device:
+        raise ValueError(f"{name} is on {t.device}, expected {device} (all tensors of a call share one GPU)")
+
+
+def _i32(t: torch.Tensor, shape, name: str, device=None):
+    if not isinstance(t, torch.Tensor) or t.dtype != torch.int32 or not t.is_cuda or not t.is_contiguous():
         raise ValueError(f"{name} must be a contiguous int32 CUDA tensor")
     if tuple(t.shape) != tuple(shape):
         raise ValueError(f"{name} has shape {tuple(t.shape)}, expected {tuple(shape)}")
+    if device is not None:
+        _same_device(t, device, name)
     return t
 
 
@@ -84,8 +95,9 @@ def _chain_args(target_logits, draft_logits, draft_tokens, temperature):
             raise TypeError("target_logits and draft_logits must share a dtype")
         if tuple(draft_logits.shape) != (B, K, V):
             raise ValueError(f"draft_logits has shape {tuple(draft_logits.shape)}, expected {(B, K, V)}")
+        _same_device(draft_logits, target_logits.device, "draft_logits")
     if K > 0:
-        _i32(draft_tokens, (B, K), "draft_tokens")
+        _i32(draft_tokens, (B, K), "draft_tokens", target_logits.device)
     return bf16, B, K, V
 
 
@@ -207,10 +219,10 @@ def spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx, out_path=Non
     B, N1, V = target_logits.shape
     N = N1 - 1
     W = (N + 31) // 32
-    if N > 0:
-        _i32(tree_tokens, (B, N), "tree_tokens")
-        _i32(parent_idx, (B, N), "parent_idx")
     dev = target_logits.device
+    if N > 0:
+        _i32(tree_tokens, (B, N), "tree_tokens", dev)
+        _i32(parent_idx, (B, N), "parent_idx", dev)
     out_path = _out(out_path, (B, N + 1), torch.int32, dev, "out_path")
     out_len = _out(out_len, (B,), torch.int32, dev, "out_len")
     # torch has no uint32 arithmetic on every version: the mask words travel as int32 bits
@@ -243,10 +255,11 @@ def spec_tree_verify_sampling(target_logits, draft_logits, tree_tokens, parent_i
                          f"{tuple(target_logits.shape)}")
     B, N1, V = target_logits.shape
     N = N1 - 1
-    if N > 0:
-        _i32(tree_tokens, (B, N), "tree_tokens")
-        _i32(parent_idx, (B, N), "parent_idx")
     dev = target_logits.device
+    _same_device(draft_logits, dev, "draft_logits")
+    if N > 0:
+        _i32(tree_tokens, (B, N), "tree_tokens", dev)
+        _i32(parent_idx, (B, N), "parent_idx", dev)
     out_path = _out(out_path, (B, N + 1), torch.int32, dev, "out_path")
     out_len = _out(out_len, (B,), torch.int32, dev, "out_len")
     lib = _lib.load()
@@ -263,8 +276,9 @@ def spec_acceptance_stats(n_accepted, K: int, stream=None):
 
     n_accepted: int32 [B] (-1 = bad sequence).  Returns dict(hist uint64-valued
     int64 [K+2], alpha float64 [K], mean_tokens float64 scalar tensor)."""
-    if n_accepted.dtype != torch.int32 or n_accepted.dim() != 1 or not n_accepted.is_contiguous():
-        raise TypeError("n_accepted must be a contiguous 1-D int32 tensor")
+    if (not isinstance(n_accepted, torch.Tensor) or n_accepted.dtype != torch.int32 or n_accepted.dim() != 1
+            or not n_accepted.is_contiguous() or not n_accepted.is_cuda):
+        raise TypeError("n_accepted must be a contiguous 1-D int32 CUDA tensor")
     dev = n_accepted.device
     B = n_accepted.shape[0]
     hist = torch.empty((K + 2,), dtype=torch.int64, device=dev)
@@ -289,8 +303,8 @@ def spec_ngram_draft(tokens, lengths, n_min: int, n_max: int, K: int, out_drafts
         raise ValueError("tokens must be [B, Lmax]")
     B, Lmax = tokens.shape
     _i32(tokens, (B, Lmax), "tokens")
-    _i32(lengths, (B,), "lengths")
     dev = tokens.device
+    _i32(lengths, (B,), "lengths", dev)
     drafts = _out(out_drafts, (B, max(int(K), 0)), torch.int32, dev, "out_drafts")  # K < 0: the C layer refuses
     n_drafts = _out(out_n_drafts, (B,), torch.int32, dev, "out_n_drafts")
     match_len = _out(out_match_len, (B,), torch.int32, dev, "out_match_len")

@@ -120,3 +120,20 @@ def test_python_binding_rejects_cpu_tensors():
     t = torch.zeros(1, 2, 8)
     with pytest.raises(ValueError):
         sv.spec_verify(t, t[:, :1], torch.zeros(1, 1, dtype=torch.int32), 1.0, 0)
+
+
+def test_python_binding_rejects_host_and_foreign_device_tensors():
+    import torch
+    import speculative_decoding_verification_36_gb300 as sv
+    from speculative_decoding_verification_36_gb300 import _same_device
+    with pytest.raises(TypeError):
+        sv.spec_acceptance_stats(torch.zeros(4, dtype=torch.int32), 3)
+    with pytest.raises(ValueError):
+        sv.spec_ngram_draft(torch.zeros(2, 8, dtype=torch.int32), torch.zeros(2, dtype=torch.int32), 1, 2, 3)
+    with pytest.raises(ValueError):
+        sv.spec_tree_verify_greedy(torch.zeros(1, 3, 8), torch.zeros(1, 2, dtype=torch.int32),
+                                   torch.zeros(1, 2, dtype=torch.int32))
+    # every tensor of a call must live on the target logits' device
+    _same_device(torch.zeros(1), torch.device("cpu"), "x")
+    with pytest.raises(ValueError):
+        _same_device(torch.zeros(1), torch.device("meta"), "x")

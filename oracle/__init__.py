@@ -61,7 +61,7 @@ def _load():
     lib.oracle_spec_verify.restype = i32
     lib.oracle_spec_verify_greedy.argtypes = [P, i32, i64, P, i64, i32, i32, i32, i32, P, P, P]
     lib.oracle_spec_verify_greedy.restype = i32
-    lib.oracle_tree_verify_greedy.argtypes = [P, i32, P, P, i32, i32, i32, P, P, P]
+    lib.oracle_tree_verify_greedy.argtypes = [P, i32, P, P, i32, i32, i32, i32, P, P, P]
     lib.oracle_tree_verify_greedy.restype = i32
     lib.oracle_acceptance_stats.argtypes = [P, i32, i32, P, P, P]
     lib.oracle_acceptance_stats.restype = None
@@ -213,8 +213,11 @@ def spec_verify_greedy(target, draft_tokens, used_rows_only: bool = False):
     return dict(tokens=tokens, n=n, row_argmax=argmax)
 
 
-def tree_verify_greedy(target, tree_tokens, parent_idx):
-    """Greedy tree verification.  target [B, N+1, V]; tokens, parents [B, N]."""
+def tree_verify_greedy(target, tree_tokens, parent_idx, used_rows_only: bool = False):
+    """Greedy tree verification.  target [B, N+1, V]; tokens, parents [B, N].
+    ``used_rows_only`` checks for bad data only what the result depends on
+    (every parent index, the root's row, the tokens of nodes whose parent is
+    accepted and the rows of accepted nodes), as the early-exit verify does."""
     lib = _load()
     t, dt = _as_logits(target)
     tok = _as_i32(tree_tokens)
@@ -229,7 +232,7 @@ def tree_verify_greedy(target, tree_tokens, parent_idx):
     par_buf = par if par.size else np.zeros(1, dtype=np.int32)
     mask_buf = mask if mask.size else np.zeros(1, dtype=np.uint32)
     rc = lib.oracle_tree_verify_greedy(_ptr(t), dt, _ptr(tok_buf), _ptr(par_buf), B, N, V,
-                                       _ptr(path), _ptr(length), _ptr(mask_buf))
+                                       int(bool(used_rows_only)), _ptr(path), _ptr(length), _ptr(mask_buf))
     if rc != 0:
         raise MemoryError("oracle_tree_verify_greedy failed to allocate")
     return dict(path=path, length=length, mask=mask)

@@ -487,9 +487,16 @@ int oracle_spec_verify_greedy(const void *target, int dtype, long long t_stride_
  * node's row, -1 padding), out_len B (path length + 1), out_mask
  * B x N x ceil(N/32) words with bit j of row i set iff j == i or j is an
  * ancestor of i.  Everything is computed by explicit ancestor walks.
+ *
+ * used_rows_only: the early-exit reading -- only what the result depends on
+ * is checked.  Every parent index (the mask depends on all of them), the
+ * root's row, the token of every node whose parent is accepted (it is
+ * compared with the parent's argmax) and the row of every accepted node (its
+ * argmax judges its children, or is the bonus token) are checked; the rows
+ * and tokens under a rejected node are never examined.
  */
 int oracle_tree_verify_greedy(const void *target, int dtype, const int32_t *tree_tokens,
-                              const int32_t *parent_idx, int B, int N, int V,
+                              const int32_t *parent_idx, int B, int N, int V, int used_rows_only,
                               int32_t *out_path, int32_t *out_len, uint32_t *out_mask)
 {
     const size_t esz = dtype == ORC_DTYPE_F32 ? 4 : 2;
@@ -513,22 +520,56 @@ int oracle_tree_verify_greedy(const void *target, int dtype, const int32_t *tree
         for (size_t w = 0; w < (size_t)N * W; ++w)
             mask[w] = 0;
         int bad = 0;
-        for (int rr = 0; rr <= N && !bad; ++rr)
-            bad = row_is_bad(tb + (size_t)rr * V * esz, dtype, V);
-        for (int i = 0; i < N && !bad; ++i)
-            bad = par[i] < -1 || par[i] >= i || tok[i] < 0 || tok[i] >= V;
-        if (bad) {
-            out_len[b] = -1;
-            continue;
+        if (used_rows_only) {
+            /* top-down: a node's row is examined only once the node is accepted */
+            for (int i = 0; i < N && !bad; ++i)
+                bad = par[i] < -1 || par[i] >= i;
+            if (!bad)
+                bad = row_is_bad(tb, dtype, V);
+            if (!bad)
+                g[0] = row_argmax(tb, dtype, V);
+            for (int i = 0; i < N && !bad; ++i) {
+                const int p = par[i];
+                if (p >= 0 && !acc[p]) {
+                    acc[i] = 0;
+                    continue;
+                }
+                if (tok[i] < 0 || tok[i] >= V) {
+                    bad = 1;
+                    break;
+                }
+                acc[i] = tok[i] == g[p + 1];
+                if (acc[i]) {
+                    const char *row = tb + (size_t)(i + 1) * V * esz;
+                    bad = row_is_bad(row, dtype, V);
+                    if (!bad)
+                        g[i + 1] = row_argmax(row, dtype, V);
+                }
+            }
+            if (bad) {
+                out_len[b] = -1;
+                continue;
+            }
+        } else {
+            for (int rr = 0; rr <= N && !bad; ++rr)
+                bad = row_is_bad(tb + (size_t)rr * V * esz, dtype, V);
+            for (int i = 0; i < N && !bad; ++i)
+                bad = par[i] < -1 || par[i] >= i || tok[i] < 0 || tok[i] >= V;
+            if (bad) {
+                out_len[b] = -1;
+                continue;
+            }
+            for (int rr = 0; rr <= N; ++rr)
+                g[rr] = row_argmax(tb + (size_t)rr * V * esz, dtype, V);
         }
-        for (int rr = 0; rr <= N; ++rr)
-            g[rr] = row_argmax(tb + (size_t)rr * V * esz, dtype, V);
-        /* acceptance and depth of every node by walking its ancestors */
+        /* acceptance and depth of every node by walking its ancestors (with
+         * used_rows_only a node is accepted only after its parent is, so
+         * every g the walk reads was computed) */
         for (int i = 0; i < N; ++i) {
             int ok = 1, d = 0;
             for (int node = i; node != -1; node = par[node]) {
                 int prow = par[node] + 1; /* parent -1 (root) uses row 0 */
-                if (tok[node] != g[prow])
+                if (used_rows_only ? !acc[node] : tok[node] != g[prow])
                     ok = 0;
                 d += 1;
             }

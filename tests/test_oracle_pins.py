@@ -814,3 +814,64 @@ def test_greedy_used_rows_only():
     r = oracle.spec_verify_greedy(t4, x, used_rows_only=True)
     assert all(r["n"][b] == -1 for b in allm)
     assert all(r["n"][b] == full["n"][b] for b in some)
+
+
+def test_tree_used_rows_only():
+    """The early-exit reading of the greedy tree verify: on clean data it
+    equals the full verify (pinned above by brute force); rows and tokens
+    under a rejected node never matter; a bad row of an accepted node (or of
+    the root), a bad token under an accepted parent, or a bad parent index
+    anywhere marks the sequence bad."""
+    rng = np.random.default_rng(41)
+    B, V = 48, 24
+    par = [-1, -1, 0, 0, 1, 1, 2, 2, 3, 3, 4, 4, 5, 5]  # depth-3 binary tree
+    N = len(par)
+    t = torch.tensor(2.0 * rng.standard_normal((B, N + 1, V)), dtype=torch.float32)
+    g = torch.argmax(t, dim=-1).numpy()
+    tok = np.zeros((B, N), dtype=np.int32)
+    for i, p in enumerate(par):  # a node carries its parent's argmax with probability 0.6
+        tok[:, i] = np.where(rng.random(B) < 0.6, g[:, p + 1], rng.integers(0, V, B))
+    parents = np.tile(np.array(par, dtype=np.int32), (B, 1))
+    full = oracle.tree_verify_greedy(t, tok, parents)
+    used = oracle.tree_verify_greedy(t, tok, parents, used_rows_only=True)
+    for k in ("path", "length", "mask"):
+        assert np.array_equal(full[k], used[k])
+    assert len(set(full["length"].tolist())) > 1
+
+    def accepted(b):
+        acc = []
+        for i, p in enumerate(par):
+            acc.append((p < 0 or acc[p]) and tok[b, i] == g[b, p + 1])
+        return acc
+
+    # spoil the rows and tokens of every node under a rejected node
+    t2, tok2 = t.clone(), tok.copy()
+    for b in range(B):
+        acc = accepted(b)
+        for i, p in enumerate(par):
+            if p >= 0 and not acc[p]:
+                t2[b, i + 1, 0] = float("nan")
+                tok2[b, i] = V + 3
+            if not acc[i]:
+                t2[b, i + 1, 1] = float("inf")  # a rejected node's own row is unused too
+    used2 = oracle.tree_verify_greedy(t2, tok2, parents, used_rows_only=True)
+    for k in ("path", "length", "mask"):
+        assert np.array_equal(used2[k], used[k])
+    assert (oracle.tree_verify_greedy(t2, tok2, parents)["length"] == -1).any()
+    # used rows and tokens are checked
+    for b in range(0, B, 5):
+        acc = accepted(b)
+        t3 = t.clone()
+        t3[b, 0, 2] = float("nan")
+        assert oracle.tree_verify_greedy(t3, tok, parents, used_rows_only=True)["length"][b] == -1
+        ai = [i for i in range(N) if acc[i]]
+        if ai:
+            t3 = t.clone()
+            t3[b, ai[-1] + 1, :] = float("-inf")
+            assert oracle.tree_verify_greedy(t3, tok, parents, used_rows_only=True)["length"][b] == -1
+        tok3 = tok.copy()
+        tok3[b, 0] = -1  # node 0's parent is the root, always accepted
+        assert oracle.tree_verify_greedy(t, tok3, parents, used_rows_only=True)["length"][b] == -1
+        par3 = parents.copy()
+        par3[b, N - 1] = N  # a bad parent index anywhere
+        assert oracle.tree_verify_greedy(t, tok, par3, used_rows_only=True)["length"][b] == -1

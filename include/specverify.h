@@ -243,6 +243,29 @@ int spec_tree_verify_greedy_bf16(const uint16_t *target_logits, const int32_t *t
                                  cudaStream_t stream);
 
 /*
+ * spec_tree_verify_greedy with early exit: the same arguments, layouts and
+ * outputs, but a node's row is read only while the node may still be
+ * accepted.  A node's row serves only to judge its children and as the bonus
+ * row ([P1] sec. 4: the longest accepted path is kept), so the rows under a
+ * rejected node cannot change the result.  Rows are streamed by node index;
+ * a row of a node already known to be rejected is skipped.  Path, length and
+ * mask equal spec_tree_verify_greedy's on valid inputs.  Bad data is checked
+ * on what is used: every parent index (the mask needs all of them), the
+ * root's row, the rows of accepted nodes and the tokens of nodes whose parent
+ * is accepted; bad data under a rejected node is not reported.  For
+ * 1 <= N <= 32 (one warp holds a sequence's nodes); larger trees read every
+ * row, as spec_tree_verify_greedy does.
+ */
+int spec_tree_verify_greedy_early_exit_f32(const float *target_logits, const int32_t *tree_tokens,
+                                           const int32_t *parent_idx, int B, int N, int V,
+                                           int32_t *out_path, int32_t *out_len, uint32_t *out_mask,
+                                           cudaStream_t stream);
+int spec_tree_verify_greedy_early_exit_bf16(const uint16_t *target_logits, const int32_t *tree_tokens,
+                                            const int32_t *parent_idx, int B, int N, int V,
+                                            int32_t *out_path, int32_t *out_len, uint32_t *out_mask,
+                                            cudaStream_t stream);
+
+/*
  * Stochastic verification of a candidate tree per sequence (temperature > 0).
  * The tree of "Speculative Decoding in Production: How Small Draft Models &
  * Medusa Heads Deliver 2x-3x LLM Speedups Without Accuracy Loss", sec. 4,

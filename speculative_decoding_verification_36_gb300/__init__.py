@@ -208,11 +208,13 @@ def spec_verify_greedy_argmax(target_logits, draft_tokens, stream=None):
 
 
 def spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx, out_path=None, out_len=None,
-                            out_mask=None, stream=None):
+                            out_mask=None, stream=None, early_exit: bool = False):
     """Greedy verification of a candidate tree per sequence.
 
     target_logits [B, N+1, V]; tree_tokens, parent_idx [B, N] int32.
-    Returns (out_path [B, N+1], out_len [B], out_mask [B, N, ceil(N/32)] as int32 bits)."""
+    Returns (out_path [B, N+1], out_len [B], out_mask [B, N, ceil(N/32)] as int32 bits).
+    early_exit=True calls spec_tree_verify_greedy_early_exit_*: the rows under
+    a rejected node are not read (and bad data there is not reported)."""
     bf16 = _is_bf16(target_logits, "target_logits")
     if target_logits.dim() != 3:
         raise ValueError("target_logits must be [B, N+1, V]")
@@ -228,7 +230,10 @@ def spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx, out_path=Non
     # torch has no uint32 arithmetic on every version: the mask words travel as int32 bits
     out_mask = _out(out_mask, (B, N, W), torch.int32, dev, "out_mask")
     lib = _lib.load()
-    fn = lib.spec_tree_verify_greedy_bf16 if bf16 else lib.spec_tree_verify_greedy_f32
+    if early_exit:
+        fn = lib.spec_tree_verify_greedy_early_exit_bf16 if bf16 else lib.spec_tree_verify_greedy_early_exit_f32
+    else:
+        fn = lib.spec_tree_verify_greedy_bf16 if bf16 else lib.spec_tree_verify_greedy_f32
     with torch.cuda.device(dev):
         _lib.check(fn(_ptr(target_logits), _ptr(tree_tokens) if N > 0 else None,
                       _ptr(parent_idx) if N > 0 else None, B, N, V, _ptr(out_path), _ptr(out_len),

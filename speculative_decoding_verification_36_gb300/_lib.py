@@ -46,6 +46,8 @@ SIGNATURES = {
     "spec_verify_greedy_argmax_bf16": [_P, _P, _I, _I, _I, _P, _P, _P, _P],
     "spec_tree_verify_greedy_f32": [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P],
     "spec_tree_verify_greedy_bf16": [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P],
+    "spec_tree_verify_greedy_early_exit_f32": [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P],
+    "spec_tree_verify_greedy_early_exit_bf16": [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P],
     "spec_tree_verify_sampling_f32": [_P, _P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_tree_verify_sampling_bf16": [_P, _P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_acceptance_stats": [_P, _I, _I, _P, _P, _P, _P],

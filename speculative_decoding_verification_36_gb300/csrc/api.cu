@@ -296,8 +296,11 @@ int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
   a.out_n = out_n;
   a.out_mask = out_mask;
   a.out_row_argmax = out_row_argmax;
-  // early exit for the chain (the resolution word holds positions 0..31)
-  a.early_exit = (early_exit && !tree && K >= 1 && K <= sv::kMaskMaxK && !out_row_argmax) ? 1 : 0;
+  // early exit: the chain's resolution word holds positions 0..31; a tree's
+  // nodes are resolved by one warp (N <= 32)
+  a.early_exit = (early_exit && !out_row_argmax &&
+                  (tree ? (K >= 1 && K <= sv::kTreeEarlyExitMaxN) : (K >= 1 && K <= sv::kMaskMaxK)))
+                     ? 1 : 0;
   a.status = d->status;
   void* ws = nullptr;
   rc = get_scratch(d, use_static, sv::greedy_workspace(B, a.R, a.CU), stream, &ws);
@@ -447,14 +450,14 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
 
 int tree_impl(bool bf16, const void* target, const int32_t* tree_tokens, const int32_t* parents,
               int B, int N, int V, int32_t* out_path, int32_t* out_len, uint32_t* out_mask,
-              cudaStream_t stream) {
+              cudaStream_t stream, bool early_exit = false) {
   if (!target || !out_path || !out_len || (N > 0 && (!tree_tokens || !parents || !out_mask)))
     return SPEC_ERR_NULL;
   if (B < 0 || N < 0 || N > sv::kMaxTreeNodes || V < 1 || !sizes_ok(B, N + 1, V))
     return SPEC_ERR_SHAPE;
   if (B == 0) return SPEC_OK;
   return argmax_impl(true, bf16, target, tree_tokens, parents, B, N, V, out_path, out_len, out_mask,
-                     nullptr, stream);
+                     nullptr, stream, false, early_exit);
 }
 
 // Stochastic tree verification: row statistics of all 2 (N + 1) rows of every
@@ -615,6 +618,22 @@ int spec_tree_verify_greedy_bf16(const uint16_t* target_logits, const int32_t* t
                                  cudaStream_t stream) {
   return tree_impl(true, target_logits, tree_tokens, parent_idx, B, N, V, out_path, out_len,
                    out_mask, stream);
+}
+
+int spec_tree_verify_greedy_early_exit_f32(const float* target_logits, const int32_t* tree_tokens,
+                                           const int32_t* parent_idx, int B, int N, int V,
+                                           int32_t* out_path, int32_t* out_len, uint32_t* out_mask,
+                                           cudaStream_t stream) {
+  return tree_impl(false, target_logits, tree_tokens, parent_idx, B, N, V, out_path, out_len,
+                   out_mask, stream, true);
+}
+
+int spec_tree_verify_greedy_early_exit_bf16(const uint16_t* target_logits, const int32_t* tree_tokens,
+                                            const int32_t* parent_idx, int B, int N, int V,
+                                            int32_t* out_path, int32_t* out_len, uint32_t* out_mask,
+                                            cudaStream_t stream) {
+  return tree_impl(true, target_logits, tree_tokens, parent_idx, B, N, V, out_path, out_len,
+                   out_mask, stream, true);
 }
 
 int spec_tree_verify_sampling_f32(const float* target_logits, const float* draft_logits,

@@ -373,6 +373,156 @@ __device__ __noinline__ void tree_finisher(const GreedyArgs& a, int b) {
   __syncwarp();
 }
 
+// Row argmax of row r (one warp): -2 for an unusable row (NaN, +inf, no
+// finite maximum).
+__device__ __forceinline__ int merged_row_argmax(const GreedyArgs& a, int b, int r) {
+  const int lane = threadIdx.x & 31;
+  const int C = a.CU * kSlices;
+  const uint2* pp = a.part + ((size_t)b * a.R + r) * C;
+  float v = neg_inf();
+  int i = INT_MAX;
+  bool nan = false;
+  for (int c = lane; c < C; c += 32) {
+    const uint2 w = wait_u2(pp + c, a.status);
+    am_merge(v, i, __uint_as_float(w.x), (int)(w.y & 0x7fffffffu));
+    nan |= (w.y >> 31) != 0;
+  }
+  warp_am(v, i);
+  nan = __any_sync(0xffffffffu, nan);
+  return (nan || !(v > neg_inf()) || !(v < INFINITY) || i == INT_MAX) ? -2 : i;
+}
+
+__device__ __noinline__ void ee_tree_update(const GreedyArgs& a, int b, unsigned long long rd);
+
+// Tree early exit, row finisher (one warp): the row's argmax, then the
+// sequence's update with this row done.
+__device__ __noinline__ void ee_tree_row_finisher(const GreedyArgs& a, int b, int r) {
+  const int lane = threadIdx.x & 31;
+  const int gv = merged_row_argmax(a, b, r);
+  unsigned long long rd = 0;
+  if (lane == 0) {
+    st_relaxed_s32(a.g + (size_t)b * a.R + r, gv);
+    rd = ~atomicAnd(a.resword + b, ~(1ull << r)) | (1ull << r);
+  }
+  rd = __shfl_sync(0xffffffffu, rd, 0);
+  ee_tree_update(a, b, rd);
+}
+
+// Tree early exit (one warp, N <= 32: lane j is node j).  Called by the
+// finisher of a row of sequence b with `rd`, the sequence's rows known to be
+// done (bit r: row r, row 0 the root's).  From the argmax of every done row it
+// derives, for every node, whether it is known accepted (every link of its
+// root path matches: node == argmax of the parent's row) or known rejected
+// (some link is known not to match); unknown links are those whose parent
+// row is not done.  The rejected nodes are published for the skip check.  Once
+// every node is resolved and the rows of the root and of every accepted node
+// are done, one warp (the first to get there) writes the outputs; the rows
+// under rejected nodes are never needed.  Bad data is checked on what is used:
+// every parent index, the root's row, the rows of accepted nodes and the
+// tokens of nodes whose parent is accepted.
+__device__ __noinline__ void ee_tree_update(const GreedyArgs& a, int b, unsigned long long rd) {
+  const int N = a.K;
+  const int lane = threadIdx.x & 31;
+  const bool valid = lane < N;
+  const int32_t* tok = a.tokens + (size_t)b * N;
+  const int32_t* par = a.parents + (size_t)b * N;
+  const int* g = a.g + (size_t)b * a.R;
+  const int p = valid ? __ldg(par + lane) : -1;
+  const int t = valid ? __ldg(tok + lane) : -1;
+  const bool bad_par = valid && (p < -1 || p >= lane);
+  const int prow = bad_par ? 0 : p + 1;
+  const bool pdone = valid && !bad_par && ((rd >> prow) & 1ull);
+  const int gp = pdone ? wait_s32(g + prow, a.status) : -3;
+  // the link into this node: known match, known mismatch, or unknown
+  bool acc = pdone && gp >= 0 && t == gp;
+  bool rej = pdone && !acc;
+  int link = (valid && !bad_par) ? p : -1;  // parent lane (-1: the root)
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int src = link >= 0 ? link : lane;
+    const bool acc_s = __shfl_sync(0xffffffffu, acc, src);
+    const bool rej_s = __shfl_sync(0xffffffffu, rej, src);
+    const int link_s = __shfl_sync(0xffffffffu, link, src);
+    if (link >= 0) {
+      acc = acc && acc_s;
+      rej = rej || rej_s;
+      link = link_s;
+    }
+  }
+  const unsigned full = N == 32 ? 0xffffffffu : ((1u << N) - 1u);
+  const unsigned A = __ballot_sync(0xffffffffu, valid && acc) & full;
+  const unsigned Rm = __ballot_sync(0xffffffffu, valid && rej) & full;
+  if (lane == 0 && Rm) atomicAnd(a.rejc + b, ~Rm);
+  if (__any_sync(0xffffffffu, bad_par)) {
+    // the mask needs every parent: the sequence is bad whatever its rows say
+  } else {
+    if ((A | Rm) != full) return;                                  // not resolved yet
+    if (!(rd & 1ull) || (((unsigned)(rd >> 1) & A) != A)) return;  // used rows still being read
+  }
+  int claim = 0;
+  if (lane == 0) claim = atomicCAS(a.decided + b, (int)kMarker, 1) == (int)kMarker ? 1 : 0;
+  if (!__shfl_sync(0xffffffffu, claim, 0)) return;
+  // the sequence's outputs (this warp alone)
+  const int W = (N + 31) >> 5;  // 1
+  int32_t* path = a.out_tokens + (size_t)b * (N + 1);
+  uint32_t* mask = a.out_mask + (size_t)b * N * W;
+  bool bad = __any_sync(0xffffffffu, bad_par);
+  if (!bad) {
+    const int g0 = wait_s32(g, a.status);
+    const bool pacc = valid && (p < 0 || ((A >> p) & 1u));
+    const bool tok_bad = pacc && (t < 0 || t >= a.V);
+    const bool row_bad = valid && ((A >> lane) & 1u) && wait_s32(g + lane + 1, a.status) < 0;
+    bad = g0 < 0 || __any_sync(0xffffffffu, tok_bad || row_bad);
+  }
+  if (bad) {
+    for (int j = lane; j <= N; j += 32) path[j] = -1;
+    for (int j = lane; j < N * W; j += 32) mask[j] = 0u;
+    if (lane == 0) {
+      a.out_n[b] = -1;
+      atomicOr(a.status, kStatusBadData);
+    }
+    __syncwarp();
+    return;
+  }
+  // depth and ancestor-or-self bits by pointer jumping over the parent links
+  int d = valid ? 1 : 0;
+  uint32_t bits = valid ? 1u << lane : 0u;
+  link = valid ? p : -1;
+#pragma unroll
+  for (int step = 0; step < 5; ++step) {
+    const int src = link >= 0 ? link : lane;
+    const int d_s = __shfl_sync(0xffffffffu, d, src);
+    const uint32_t bits_s = __shfl_sync(0xffffffffu, bits, src);
+    const int link_s = __shfl_sync(0xffffffffu, link, src);
+    if (link >= 0) {
+      d += d_s;
+      bits |= bits_s;
+      link = link_s;
+    }
+  }
+  if (valid) mask[lane] = bits;
+  // the deepest accepted node, lowest index on ties (the root: depth 0)
+  int kd = valid && ((A >> lane) & 1u) ? d : 0, ki = kd ? lane : INT_MAX;
+#pragma unroll
+  for (int off = 16; off > 0; off >>= 1) {
+    const int od = __shfl_xor_sync(0xffffffffu, kd, off);
+    const int oi = __shfl_xor_sync(0xffffffffu, ki, off);
+    if (od > kd || (od == kd && oi < ki)) {
+      kd = od;
+      ki = oi;
+    }
+  }
+  const int best = kd ? ki : -1;
+  const uint32_t bbits = best >= 0 ? __shfl_sync(0xffffffffu, bits, best) : 0u;
+  if (valid && ((bbits >> lane) & 1u)) path[d - 1] = t;
+  for (int j = kd + 1 + lane; j <= N; j += 32) path[j] = -1;
+  if (lane == 0) {
+    path[kd] = wait_s32(g + best + 1, a.status);
+    a.out_n[b] = kd + 1;
+  }
+  __syncwarp();
+}
+
 // Independent warps claim units in increasing order from their counters.
 // The warp taking a row's last ticket merges the row; the one merging a
 // sequence's last row runs its finisher.  The only waits are for stores that
@@ -397,8 +547,14 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) argmax_kernel(const __gr
       b = rem / a.CU;
       idx = r * a.CU + (rem - b * a.CU);
       if (r > 0) {
-        const int dn = bcast((int)ld_relaxed_if(lane == 0, a.decided + b, kMarker));
-        skip = dn >= 0 && dn < r;
+        if constexpr (TREE) {
+          // the row of node r - 1: skipped once the node is known rejected
+          const unsigned rej = ~(unsigned)bcast((int)ld_relaxed_if(lane == 0, a.rejc + b, 0xffffffffu));
+          skip = (rej >> (r - 1)) & 1u;
+        } else {
+          const int dn = bcast((int)ld_relaxed_if(lane == 0, a.decided + b, kMarker));
+          skip = dn >= 0 && dn < r;
+        }
       }
     } else {
       b = unit / a.map.A;
@@ -407,7 +563,9 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) argmax_kernel(const __gr
     if (!skip) {
       const int old = __shfl_sync(0xffffffffu, argmax_slice<E, VEC>(a, b, idx, w), 0);
       if (old == last) {
-        if constexpr (EE) {
+        if constexpr (EE && TREE) {
+          ee_tree_row_finisher(a, b, idx / a.CU);
+        } else if constexpr (EE) {
           ee_row_finisher(a, b, idx / a.CU);
         } else if (row_argmax_finisher(a, b, idx / a.CU)) {
           if (TREE)
@@ -427,8 +585,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) argmax_kernel(const __gr
 static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: [counters, tickets (start at -1), resolution words (all-ones:
-// empty)][marker-filled: part, g, decided, verdict][depth, acc]; one 0xff
-// fill initialises the first two parts.
+// empty)][marker-filled: part, g, decided, verdict, rejc][depth, acc]; one
+// 0xff fill initialises the first two parts.
 static void greedy_layout(int B, int R, int CU, size_t* off) {
   const size_t C = (size_t)CU * kSlices;
   size_t o = 0;
@@ -442,6 +600,7 @@ static void greedy_layout(int B, int R, int CU, size_t* off) {
   off[5] = o; o += align_up((size_t)B * R * 4, 256);                  // g
   off[11] = o; o += align_up((size_t)B * 4, 256);                     // decided
   off[12] = o; o += align_up((size_t)B * R * 4, 256);                 // verdict
+  off[13] = o; o += align_up((size_t)B * 4, 256);                     // rejc
   off[6] = o;                                                         // end of marker region
   off[7] = o; o += align_up((size_t)B * R * 4, 256);                  // depth
   off[8] = o; o += align_up((size_t)B * R * 4, 256);                  // acc
@@ -449,7 +608,7 @@ static void greedy_layout(int B, int R, int CU, size_t* off) {
 }
 
 WsLayout greedy_workspace(int B, int R, int CU) {
-  size_t off[13];
+  size_t off[14];
   greedy_layout(B, R, CU, off);
   WsLayout l;
   l.total = off[9];
@@ -460,7 +619,7 @@ WsLayout greedy_workspace(int B, int R, int CU) {
 }
 
 void greedy_bind_workspace(GreedyArgs& a, void* ws) {
-  size_t off[13];
+  size_t off[14];
   greedy_layout(a.B, a.R, a.CU, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
@@ -473,12 +632,13 @@ void greedy_bind_workspace(GreedyArgs& a, void* ws) {
   a.resword = (unsigned long long*)(p + off[10]);
   a.decided = (int*)(p + off[11]);
   a.verdict = (int*)(p + off[12]);
+  a.rejc = (unsigned*)(p + off[13]);
 }
 
 template <class E, int VEC, bool TREE>
 static cudaError_t launch_t(const GreedyArgs& a, int grid, cudaStream_t s) {
-  if (!TREE && a.early_exit)
-    argmax_kernel<E, VEC, false, true><<<grid, kThreads, 0, s>>>(a);
+  if (a.early_exit)
+    argmax_kernel<E, VEC, TREE, true><<<grid, kThreads, 0, s>>>(a);
   else
     argmax_kernel<E, VEC, TREE, false><<<grid, kThreads, 0, s>>>(a);
   return cudaGetLastError();

@@ -158,11 +158,14 @@ struct GreedyArgs {
   // finisher resolves its position and the resolution that decides the
   // sequence writes its outputs; rows after a decided sequence's n are skipped
   int early_exit;
-  unsigned long long* resword;  // [B] resolution words, stored complemented (all-ones: empty)
-  int* decided;                 // [B] n once decided (marker before)
+  unsigned long long* resword;  // [B] resolution words, stored complemented (all-ones: empty);
+                                // tree: bit r set when row r is done
+  int* decided;                 // [B] n once decided (marker before); tree: the output writer's claim
   int* verdict;                 // [B, R] position verdicts (marker before)
+  unsigned* rejc;               // [B] tree: complement of the rejected-node mask (all-ones: none)
   unsigned* status;
 };
+constexpr int kTreeEarlyExitMaxN = 32;  // tree early exit: one warp holds a sequence's nodes
 
 // Workspace layout of each kernel: `total` bytes; [0, zero_bytes) must be
 // zero-filled (neither kernel uses one) and [marker_off, marker_off +

@@ -147,3 +147,99 @@ def test_greedy_early_exit_full_size_c4():
     ref = oracle.spec_verify_greedy(x["target"][sel].cpu(), x["tokens"][sel].cpu(), used_rows_only=True)
     assert np.array_equal(tok_e[sel].cpu().numpy(), ref["tokens"])
     assert np.array_equal(n_e[sel].cpu().numpy(), ref["n"])
+
+
+# --------------------------------------------------------------------------
+# greedy tree: the rows under a rejected node are not read
+# --------------------------------------------------------------------------
+def _tree_inputs(B, V, par, p_match, seed, dtype=torch.bfloat16):
+    g = torch.Generator().manual_seed(seed)
+    N = len(par)
+    t = (3.0 * torch.randn(B, N + 1, V, generator=g)).to(dtype)
+    am = torch.argmax(t.float(), dim=-1)
+    tok = torch.empty(B, N, dtype=torch.int32)
+    for i, p in enumerate(par):
+        keep = torch.rand(B, generator=g) < p_match
+        tok[:, i] = torch.where(keep, am[:, p + 1], torch.randint(0, V, (B,), generator=g)).to(torch.int32)
+    parents = torch.tensor(par, dtype=torch.int32).unsqueeze(0).expand(B, N).contiguous()
+    return t.contiguous(), tok, parents
+
+
+def _binary(depth):
+    return [int(x) for x in wl.complete_binary_parents(depth).tolist()]
+
+
+@pytest.mark.parametrize("label,B,V,par,dtype", [
+    ("binary depth 4 (c5 shape)", 32, 4096, _binary(4), torch.bfloat16),
+    ("binary depth 3, fp32 scalar", 16, 1001, _binary(3), torch.float32),
+    ("32-node chain", 8, 512, [-1] + list(range(31)), torch.bfloat16),
+    ("32 root children", 8, 512, [-1] * 32, torch.bfloat16),
+    ("single node", 8, 64, [-1], torch.float32),
+    ("random 20 nodes", 12, 300, [-1, 0, 0, 1, -1, 2, 3, 3, 4, 0, 5, 9, 6, 12, 1, 8, 8, 11, 2, 17], torch.bfloat16),
+    ("33 nodes: every row is read", 4, 256, _binary(4) + [29, 29, 30], torch.bfloat16),
+])
+def test_tree_early_exit_parity(label, B, V, par, dtype):
+    t, tok, parents = _tree_inputs(B, V, par, 0.7, seed=len(par) + B)
+    full = sv.spec_tree_verify_greedy(_dev(t), _dev(tok), _dev(parents))
+    early = sv.spec_tree_verify_greedy(_dev(t), _dev(tok), _dev(parents), early_exit=True)
+    torch.cuda.synchronize()
+    assert sv.spec_get_status() == 0
+    for f, e in zip(full, early):
+        assert torch.equal(f, e), label
+    ref = oracle.tree_verify_greedy(t, tok, parents, used_rows_only=True)
+    assert np.array_equal(early[0].cpu().numpy(), ref["path"])
+    assert np.array_equal(early[1].cpu().numpy(), ref["length"])
+    assert np.array_equal(early[2].cpu().numpy().view(np.uint32), ref["mask"])
+
+
+def test_tree_early_exit_ignores_rows_under_rejected_nodes():
+    par = _binary(3)
+    N, B, V = len(par), 24, 700
+    t, tok, parents = _tree_inputs(B, V, par, 0.6, seed=3, dtype=torch.float32)
+    am = torch.argmax(t, dim=-1)
+    t2, tok2 = t.clone(), tok.clone()
+    for b in range(B):
+        acc = []
+        for i, p in enumerate(par):
+            acc.append(bool((p < 0 or acc[p]) and int(tok[b, i]) == int(am[b, p + 1])))
+        for i, p in enumerate(par):
+            if not acc[i]:
+                t2[b, i + 1, 5] = float("nan")  # a rejected node's row
+            if p >= 0 and not acc[p]:
+                tok2[b, i] = V + 9                # a token under a rejected node
+    sv.spec_get_status()
+    clean = sv.spec_tree_verify_greedy(_dev(t), _dev(tok), _dev(parents), early_exit=True)
+    spoiled = sv.spec_tree_verify_greedy(_dev(t2), _dev(tok2), _dev(parents), early_exit=True)
+    torch.cuda.synchronize()
+    assert sv.spec_get_status() == 0
+    for c, s in zip(clean, spoiled):
+        assert torch.equal(c, s)
+    # used bad data is flagged: the root row, and a parent index anywhere
+    t3 = t.clone()
+    t3[0, 0, 1] = float("inf")
+    par3 = parents.clone()
+    par3[1, N - 1] = N + 4
+    for tt, pp, b in ((t3, parents, 0), (t, par3, 1)):
+        ref = oracle.tree_verify_greedy(tt, tok, pp, used_rows_only=True)
+        path, length, mask = sv.spec_tree_verify_greedy(_dev(tt), _dev(tok), _dev(pp), early_exit=True)
+        torch.cuda.synchronize()
+        assert sv.spec_get_status() & sv.SPEC_FLAG_BAD_DATA
+        assert int(length[b]) == -1 and ref["length"][b] == -1
+        assert np.array_equal(length.cpu().numpy(), ref["length"])
+        assert np.array_equal(path.cpu().numpy(), ref["path"])
+    assert sv.spec_get_status() == 0
+
+
+def test_tree_early_exit_full_size_c5():
+    p = wl.preset("c5")
+    x = wl.make_tree(p, device=DEV, seed=6)
+    full = sv.spec_tree_verify_greedy(x["target"], x["tokens"], x["parents"])
+    early = sv.spec_tree_verify_greedy(x["target"], x["tokens"], x["parents"], early_exit=True)
+    torch.cuda.synchronize()
+    assert sv.spec_get_status() == 0
+    for f, e in zip(full, early):
+        assert torch.equal(f, e)
+    ref = oracle.tree_verify_greedy(x["target"][:8].cpu(), x["tokens"][:8].cpu(), x["parents"][:8].cpu(),
+                                    used_rows_only=True)
+    assert np.array_equal(early[0][:8].cpu().numpy(), ref["path"])
+    assert np.array_equal(early[1][:8].cpu().numpy(), ref["length"])

@@ -5,7 +5,8 @@
 Builds the library if needed, generates the preset's synthetic inputs on
 cuda:0 and makes N calls of the entry point the preset exercises
 (spec_verify for c1-c4, or spec_verify_early_exit with --early-exit;
-spec_tree_verify_greedy for c5; spec_tree_verify_sampling at tau = 1 on the
+spec_tree_verify_greedy for c5, its early exit with --early-exit;
+spec_tree_verify_sampling at tau = 1 on the
 c5 tree for c5s; spec_ngram_draft (n 1..4, K = 8) on 256 repetitive
 histories of up to 131072 tokens for ngram), then synchronises.
 """
@@ -18,7 +19,7 @@ import sys
 def main(argv=None) -> int:
     ap = argparse.ArgumentParser()
     ap.add_argument("preset", choices=["c1", "c2", "c3", "c4", "c5", "c5s", "ngram"])
-    ap.add_argument("--early-exit", action="store_true", help="chain presets: the early-exit verify")
+    ap.add_argument("--early-exit", action="store_true", help="c1-c5: the early-exit verify")
     ap.add_argument("--batch", type=int, default=0, help="sequences (default: the preset's B)")
     ap.add_argument("--calls", type=int, default=3)
     args = ap.parse_args(argv)
@@ -52,7 +53,7 @@ def main(argv=None) -> int:
     elif args.preset == "c5":
         x = wl.make_tree(p, device=dev, seed=0)
         for _ in range(args.calls):
-            spec_tree_verify_greedy(x["target"], x["tokens"], x["parents"])
+            spec_tree_verify_greedy(x["target"], x["tokens"], x["parents"], early_exit=args.early_exit)
     else:
         x = wl.make_chain(p, device=dev, seed=0)
         verify = spec_verify_early_exit if args.early_exit else spec_verify

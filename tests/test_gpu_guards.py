@@ -47,14 +47,13 @@ def test_chain_outputs_are_guarded():
         p, x = _chain(name, **over)
         tok, n = Guarded((p.B, p.K + 1), torch.int32), Guarded((p.B,), torch.int32)
         sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 1, out_tokens=tok.t, out_n_accepted=n.t)
-        if p.temperature > 0:
-            tok2, n2 = Guarded((p.B, p.K + 1), torch.int32), Guarded((p.B,), torch.int32)
-            sv.spec_verify_early_exit(x["target"], x["draft"], x["tokens"], p.temperature, 1,
-                                      out_tokens=tok2.t, out_n_accepted=n2.t)
-            torch.cuda.synchronize()
-            assert tok2.intact() and n2.intact()
-            assert torch.equal(tok.t, tok2.t)
+        # the early exit (sampled, or greedy at temperature 0)
+        tok2, n2 = Guarded((p.B, p.K + 1), torch.int32), Guarded((p.B,), torch.int32)
+        sv.spec_verify_early_exit(x["target"], x["draft"], x["tokens"], p.temperature, 1,
+                                  out_tokens=tok2.t, out_n_accepted=n2.t)
         torch.cuda.synchronize()
+        assert tok2.intact() and n2.intact()
+        assert torch.equal(tok.t, tok2.t)
         assert tok.intact() and n.intact(), name
         assert (n.t >= 0).all()
     assert sv.spec_get_status() == 0
@@ -82,10 +81,11 @@ def test_tree_and_ngram_outputs_are_guarded():
     tr = wl.make_tree(wl.preset("c5", B=3, V=777), device=DEV, seed=5)
     B, N = 3, tr["tokens"].shape[1]
     path, ln, mask = Guarded((B, N + 1), torch.int32), Guarded((B,), torch.int32), Guarded((B, N, 1), torch.int32)
-    sv.spec_tree_verify_greedy(tr["target"], tr["tokens"], tr["parents"], out_path=path.t, out_len=ln.t,
-                               out_mask=mask.t)
-    torch.cuda.synchronize()
-    assert path.intact() and ln.intact() and mask.intact()
+    for ee in (False, True):
+        sv.spec_tree_verify_greedy(tr["target"], tr["tokens"], tr["parents"], out_path=path.t, out_len=ln.t,
+                                   out_mask=mask.t, early_exit=ee)
+        torch.cuda.synchronize()
+        assert path.intact() and ln.intact() and mask.intact()
     h = wl.make_ngram_histories(6, 5000, V=50, seed=3)
     d, nd, ml = Guarded((6, 7), torch.int32), Guarded((6,), torch.int32), Guarded((6,), torch.int32)
     sv.spec_ngram_draft(h["tokens"].to(DEV), h["lengths"].to(DEV), 1, 5, 7, out_drafts=d.t, out_n_drafts=nd.t,

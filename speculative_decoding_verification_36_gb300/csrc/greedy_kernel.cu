@@ -19,6 +19,14 @@
 // slice of one row is reduced to (max, lowest argmax, NaN seen); the warp
 // taking a sequence's last ticket merges the slices in order and writes that
 // sequence's outputs.
+//
+// Early exit ("Speculative Decoding for LLM Inference ..." section "The
+// draft-and-verify loop": what follows the first rejection is discarded):
+// rows are streamed by position (chain) or node index (tree), and a row that
+// cannot change the result -- a position after a decided sequence's first
+// mismatch, a node already known to be rejected -- is skipped.  Row finishers
+// resolve positions / nodes as their rows complete, and the warp whose
+// resolution settles the sequence writes its outputs.
 #include "sv_common.cuh"
 #include "sv_kernels.h"
 

@@ -115,3 +115,48 @@ def test_a_failed_scratch_allocation_is_reported_and_harmless():
     assert torch.equal(tok.t, ref_tok) and torch.equal(n.t, ref_n) and tok.intact()
     assert lib.spec_test_fail_allocations(0) == 0
     assert sv.spec_get_status() == 0
+
+
+def test_concurrent_calls_from_two_host_threads():
+    """Two host threads, each on its own stream, call the sampled verify, the
+    early exit and the tree verify back to back at the same time (the binding
+    releases the GIL inside the library).  Every result equals the same call
+    made alone: the scratch pool, the shared side stream and the device state
+    are safe under concurrent callers, and concurrent persistent launches
+    make progress."""
+    import threading
+    chains = [_chain("c2", B=8, K=4, V=5000 + 100 * k) for k in range(2)]
+    tr = wl.make_tree(wl.preset("c5", B=4, depth=3, V=3000), device=DEV, seed=9)
+    want = []
+    for (p, x) in chains:
+        a = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 5)
+        e = sv.spec_verify_early_exit(x["target"], x["draft"], x["tokens"], p.temperature, 5)
+        want.append((a, e))
+    wt = sv.spec_tree_verify_greedy(tr["target"], tr["tokens"], tr["parents"])
+    torch.cuda.synchronize()
+    errors = []
+
+    def worker(k):
+        try:
+            p, x = chains[k]
+            s = torch.cuda.Stream(device=DEV)
+            with torch.cuda.stream(s):
+                for _ in range(40):
+                    a = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 5)
+                    e = sv.spec_verify_early_exit(x["target"], x["draft"], x["tokens"], p.temperature, 5)
+                    t = sv.spec_tree_verify_greedy(tr["target"], tr["tokens"], tr["parents"])
+                    s.synchronize()
+                    for got, ref in ((a, want[k][0]), (e, want[k][1]), (t, wt)):
+                        if not all(torch.equal(g, r) for g, r in zip(got, ref)):
+                            errors.append(k)
+                            return
+        except Exception as exc:  # reported below
+            errors.append(repr(exc))
+
+    threads = [threading.Thread(target=worker, args=(k,)) for k in range(2)]
+    for th in threads:
+        th.start()
+    for th in threads:
+        th.join(timeout=300)
+    assert not errors, errors
+    assert sv.spec_get_status() == 0

@@ -40,6 +40,12 @@
  *     (nothing is launched) or from the CUDA runtime.
  *   - Results are deterministic: the same inputs and seed give bit-identical
  *     outputs on every run.
+ *   - Calls may be captured into a CUDA graph on `stream` (the scratch then
+ *     comes from graph memory nodes of the library's pool and is initialised
+ *     on the captured stream).  Make one call on the device before the first
+ *     capture: it creates the library's device state and pool, which a
+ *     capture in global mode would not allow.  Calls may also come from
+ *     several host threads at once, each on its own stream.
  */
 #ifndef SPECVERIFY_H
 #define SPECVERIFY_H

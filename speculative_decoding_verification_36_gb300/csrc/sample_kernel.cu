@@ -478,58 +478,6 @@ __device__ float tail_slice_mass(const SampleArgs& a, int b, int s, const SeqInf
 // select finisher (one warp): inverse CDF over the tail slices' masses
 // ---------------------------------------------------------------------------
 
-// First position i < count with positive mass whose running sum (from `run`
-// on, in index order) exceeds theta; when rounding leaves theta past every
-// running sum, the last position with mass.  Values are read 128 at a time
-// (four per lane, one round of loads), the running sum is a warp prefix in
-// fp64 over each group of 32.  Returns -1 when no value is positive; *before
-// gets the running sum just before the chosen position.
-template <class LOAD>
-__device__ __forceinline__ int warp_cdf_search(int count, double theta, double run, LOAD load,
-                                               double* before) {
-  const int lane = threadIdx.x & 31;
-  int last = -1;
-  double last_before = 0.0;
-  for (int b0 = 0; b0 < count; b0 += 128) {
-    double vals[4];
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int i = b0 + 32 * q + lane;
-      vals[q] = i < count ? load(i) : 0.0;
-    }
-#pragma unroll
-    for (int q = 0; q < 4; ++q) {
-      const int c0 = b0 + 32 * q;
-      if (c0 >= count) break;
-      const double v = vals[q];
-      const bool pos = v > 0.0;
-      double incl = v;
-#pragma unroll
-      for (int off = 1; off < 32; off <<= 1) {
-        const double o = __shfl_up_sync(0xffffffffu, incl, off);
-        if (lane >= off) incl += o;
-      }
-      double excl = __shfl_up_sync(0xffffffffu, incl, 1);
-      if (lane == 0) excl = 0.0;
-      const unsigned hit = __ballot_sync(0xffffffffu, pos && run + incl > theta);
-      const unsigned has = __ballot_sync(0xffffffffu, pos);
-      if (hit) {
-        const int L = __ffs(hit) - 1;
-        *before = __shfl_sync(0xffffffffu, run + excl, L);
-        return c0 + L;
-      }
-      if (has) {
-        const int L = 31 - __clz(has);
-        last = c0 + L;
-        last_before = __shfl_sync(0xffffffffu, run + excl, L);
-      }
-      run += __shfl_sync(0xffffffffu, incl, 31);
-    }
-  }
-  *before = last_before;
-  return last;
-}
-
 template <class E, int VEC, bool RING>
 __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   using S = typename E::storage;

@@ -586,20 +586,19 @@ __device__ __forceinline__ float resid_factor(float d) {
 }
 
 // resid_factor on both elements of a pair, with every operation rounding as
-// in the scalar version (bit-identical results).
-__device__ __forceinline__ f2_t resid_factor2(f2_t d) {
-  const f2_t hd = f2mul(d, f2(-0.5f, -0.5f));
-  const f2_t eh = f2(ex2(f2lo(hd)), ex2(f2hi(hd)));
-  const f2_t A = f2sub(f2(1.f, 1.f), f2mul(eh, eh));
-  const f2_t x = f2mul(d, f2(0.346573590279972655f, 0.346573590279972655f));
-  const f2_t xx = f2mul(x, x);
-  f2_t p = f2fma(xx, f2(1.f / 2520.f, 1.f / 2520.f), f2(1.f / 60.f, 1.f / 60.f));
-  p = f2fma(xx, p, f2(1.f / 3.f, 1.f / 3.f));
-  p = f2fma(xx, p, f2(2.f, 2.f));
-  const f2_t Bv = f2mul(f2mul(x, p), eh);
-  const float r0 = fmaxf(f2lo(d) >= 1.4f ? f2lo(A) : f2lo(Bv), 0.f);
-  const float r1 = fmaxf(f2hi(d) >= 1.4f ? f2hi(A) : f2hi(Bv), 0.f);
-  return f2(r0, r1);
+// in the scalar version (bit-identical results); float2 arithmetic on register
+// pairs.
+__device__ __forceinline__ float2 resid_factor2(float2 d) {
+  const float2 hd = __fmul2_rn(d, make_float2(-0.5f, -0.5f));
+  const float2 eh = make_float2(ex2(hd.x), ex2(hd.y));
+  const float2 A = __fadd2_rn(make_float2(1.f, 1.f), __fmul2_rn(make_float2(-1.f, -1.f), __fmul2_rn(eh, eh)));
+  const float2 x = __fmul2_rn(d, make_float2(0.346573590279972655f, 0.346573590279972655f));
+  const float2 xx = __fmul2_rn(x, x);
+  float2 p = __ffma2_rn(xx, make_float2(1.f / 2520.f, 1.f / 2520.f), make_float2(1.f / 60.f, 1.f / 60.f));
+  p = __ffma2_rn(xx, p, make_float2(1.f / 3.f, 1.f / 3.f));
+  p = __ffma2_rn(xx, p, make_float2(2.f, 2.f));
+  const float2 Bv = __fmul2_rn(__fmul2_rn(x, p), eh);
+  return make_float2(fmaxf(d.x >= 1.4f ? A.x : Bv.x, 0.f), fmaxf(d.y >= 1.4f ? A.y : Bv.y, 0.f));
 }
 
 __device__ __forceinline__ float tail_weight(float zT, float zD, const TailConsts& k) {
@@ -612,18 +611,34 @@ __device__ __forceinline__ float tail_weight(float zT, float zD, const TailConst
   return __fmul_rn(eT, resid_factor(delta));
 }
 
-// The same weights for an element pair with packed f32x2 arithmetic: every
-// operation rounds exactly as the scalar version above.
-__device__ __forceinline__ f2_t tail_weight2(f2_t zT, f2_t zD, const TailConsts& k) {
-  const f2_t dT = f2sub(zT, f2(k.mT, k.mT));
-  const f2_t aT = f2mul(dT, f2(k.c_hi, k.c_hi));
-  const f2_t eT = f2(ex2(f2lo(aT)), ex2(f2hi(aT)));
+// The same weights for an element pair with float2 arithmetic on register
+// pairs: every operation rounds exactly as the scalar version above.  eTo
+// receives the bonus weights 2^{(zT - mT) c} of the pair (the first factor of
+// the residual).
+__device__ __forceinline__ float2 tail_weight2_both(float2 zT, float2 zD, const TailConsts& k, float2& eTo) {
+  const float2 dT = __fadd2_rn(zT, make_float2(-k.mT, -k.mT));
+  const float2 aT = __fmul2_rn(dT, make_float2(k.c_hi, k.c_hi));
+  const float2 eT = make_float2(ex2(aT.x), ex2(aT.y));
+  eTo = eT;
   if (!k.residual) return eT;
-  const f2_t dD = f2sub(zD, f2(k.mD, k.mD));
-  const f2_t D = f2sub(dT, dD);
-  const f2_t delta = f2add(f2fma(D, f2(k.c_hi, k.c_hi), f2(-k.lam_hi, -k.lam_hi)),
-                           f2fma(D, f2(k.c_lo, k.c_lo), f2(-k.lam_lo, -k.lam_lo)));
-  return f2mul(eT, resid_factor2(delta));
+  const float2 dD = __fadd2_rn(zD, make_float2(-k.mD, -k.mD));
+  const float2 D = __fadd2_rn(dT, __fmul2_rn(dD, make_float2(-1.f, -1.f)));
+  const float2 delta = __fadd2_rn(__ffma2_rn(D, make_float2(k.c_hi, k.c_hi), make_float2(-k.lam_hi, -k.lam_hi)),
+                                  __ffma2_rn(D, make_float2(k.c_lo, k.c_lo), make_float2(-k.lam_lo, -k.lam_lo)));
+  return __fmul2_rn(eT, resid_factor2(delta));
+}
+__device__ __forceinline__ float2 tail_weight2(float2 zT, float2 zD, const TailConsts& k) {
+  float2 e;
+  return tail_weight2_both(zT, zD, k, e);
+}
+template <class E, int VEC>
+__device__ __forceinline__ float2 elem_pair2(const Raw<E, VEC>& r, int p) {
+  if constexpr (VEC == 8) {
+    const uint32_t w = word_of(r.w, p);
+    return make_float2(bf16_lo(w), bf16_hi(w));
+  } else {
+    return make_float2(__uint_as_float(word_of(r.w, 2 * p)), __uint_as_float(word_of(r.w, 2 * p + 1)));
+  }
 }
 
 // The VEC weights of one lane's vector, in element order.
@@ -635,9 +650,9 @@ __device__ __forceinline__ void lane_weights(const Raw<E, VEC>& zt, const Raw<E,
   } else {
 #pragma unroll
     for (int p = 0; p < VEC / 2; ++p) {
-      const f2_t wp = tail_weight2(elem_pair<E, VEC>(zt, p), elem_pair<E, VEC>(zd, p), k);
-      w[2 * p] = f2lo(wp);
-      w[2 * p + 1] = f2hi(wp);
+      const float2 wp = tail_weight2(elem_pair2<E, VEC>(zt, p), elem_pair2<E, VEC>(zd, p), k);
+      w[2 * p] = wp.x;
+      w[2 * p + 1] = wp.y;
     }
   }
 }
@@ -651,6 +666,25 @@ __device__ __forceinline__ float lane_mass(const Raw<E, VEC>& zt, const Raw<E, V
   float ls = 0.f;
 #pragma unroll
   for (int q = 0; q < VEC; ++q) ls = __fadd_rn(ls, w[q]);
+  return ls;
+}
+
+// The same sum, and in `bonus` the sum of the bonus weights 2^{(zT - mT) c} of
+// the same elements (vector path), each in element order.
+template <class E, int VEC>
+__device__ __forceinline__ float lane_mass_both(const Raw<E, VEC>& zt, const Raw<E, VEC>& zd,
+                                                const TailConsts& k, float& bonus) {
+  float ls = 0.f, lb = 0.f;
+#pragma unroll
+  for (int p = 0; p < VEC / 2; ++p) {
+    float2 e;
+    const float2 wp = tail_weight2_both(elem_pair2<E, VEC>(zt, p), elem_pair2<E, VEC>(zd, p), k, e);
+    ls = __fadd_rn(ls, wp.x);
+    ls = __fadd_rn(ls, wp.y);
+    lb = __fadd_rn(lb, e.x);
+    lb = __fadd_rn(lb, e.y);
+  }
+  bonus = lb;
   return ls;
 }
 
@@ -682,6 +716,61 @@ __device__ __forceinline__ float warp_sum(float x) {
 #pragma unroll
   for (int off = 16; off > 0; off >>= 1) x += __shfl_xor_sync(0xffffffffu, x, off);
   return x;
+}
+
+// ---------------------------------------------------------------------------
+// Inverse-CDF search over a run of masses (one warp)
+// ---------------------------------------------------------------------------
+// First position i < count with positive mass whose running sum (from `run`
+// on, in index order) exceeds theta; when rounding leaves theta past every
+// running sum, the last position with mass.  Values are read 128 at a time
+// (four per lane, one round of loads), the running sum is a warp prefix in
+// fp64 over each group of 32.  Returns -1 when no value is positive; *before
+// gets the running sum just before the chosen position.
+template <class LOAD>
+__device__ __forceinline__ int warp_cdf_search(int count, double theta, double run, LOAD load,
+                                               double* before) {
+  const int lane = threadIdx.x & 31;
+  int last = -1;
+  double last_before = 0.0;
+  for (int b0 = 0; b0 < count; b0 += 128) {
+    double vals[4];
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int i = b0 + 32 * q + lane;
+      vals[q] = i < count ? load(i) : 0.0;
+    }
+#pragma unroll
+    for (int q = 0; q < 4; ++q) {
+      const int c0 = b0 + 32 * q;
+      if (c0 >= count) break;
+      const double v = vals[q];
+      const bool pos = v > 0.0;
+      double incl = v;
+#pragma unroll
+      for (int off = 1; off < 32; off <<= 1) {
+        const double o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+      }
+      double excl = __shfl_up_sync(0xffffffffu, incl, 1);
+      if (lane == 0) excl = 0.0;
+      const unsigned hit = __ballot_sync(0xffffffffu, pos && run + incl > theta);
+      const unsigned has = __ballot_sync(0xffffffffu, pos);
+      if (hit) {
+        const int L = __ffs(hit) - 1;
+        *before = __shfl_sync(0xffffffffu, run + excl, L);
+        return c0 + L;
+      }
+      if (has) {
+        const int L = 31 - __clz(has);
+        last = c0 + L;
+        last_before = __shfl_sync(0xffffffffu, run + excl, L);
+      }
+      run += __shfl_sync(0xffffffffu, incl, 31);
+    }
+  }
+  *before = last_before;
+  return last;
 }
 
 // ---------------------------------------------------------------------------

@@ -13,7 +13,6 @@
 
 #include <stdlib.h>
 
-#include <algorithm>
 #include <atomic>
 #include <mutex>
 
@@ -52,15 +51,6 @@ struct DeviceState {
   int occ_tree[2][2] = {{0, 0}, {0, 0}};
   int occ_tree_stats[2][2] = {{0, 0}, {0, 0}};
   int walk_clusters[2][2][5] = {};  // [bf16][vec][log2 C]: walk clusters resident at once
-  int smem_optin = 0;               // largest dynamic shared memory per CTA
-  // resident clusters of the cluster-streamed sampling kernel, by launch shape
-  struct ClusterFit {
-    int bf16, ent, C;
-    size_t smem;
-    int clusters;
-  };
-  ClusterFit cluster_fit[32];
-  int n_cluster_fit = 0;
 };
 
 constexpr int kMaxDevices = 64;
@@ -84,10 +74,6 @@ int get_device_state(DeviceState** out) {
   if (!d.init) {
     e = cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    e = cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
-    e = sv::cluster_prepare(d.smem_optin);
-    if (e != cudaSuccess) return cuda_fail(e, "cudaFuncSetAttribute");
     e = cudaGetSymbolAddress((void**)&d.status, g_spec_status);
     if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress");
     for (int bf = 0; bf < 2; ++bf)
@@ -339,120 +325,6 @@ int greedy_impl(bool bf16, const void* target, const int32_t* tokens, int B, int
                      out_row_argmax, stream, use_static, early_exit);
 }
 
-// Resident clusters of C CTAs of the cluster-streamed sampling kernel with
-// `smem` bytes of shared memory each (occupancy calculator, cached per device).
-int cluster_fit(DeviceState* d, bool bf16, bool ent, int C, size_t smem) {
-  std::lock_guard<std::mutex> lock(g_mu);
-  for (int j = 0; j < d->n_cluster_fit && j < 32; ++j) {
-    const DeviceState::ClusterFit& f = d->cluster_fit[j];
-    if (f.bf16 == (int)bf16 && f.ent == (int)ent && f.C == C && f.smem == smem) return f.clusters;
-  }
-  const int n = sv::cluster_max_active(bf16, ent, C, smem);
-  DeviceState::ClusterFit& f = d->cluster_fit[d->n_cluster_fit % 32];
-  f.bf16 = bf16;
-  f.ent = ent;
-  f.C = C;
-  f.smem = smem;
-  f.clusters = n;
-  ++d->n_cluster_fit;
-  return n;
-}
-
-// Launch shape of the cluster-streamed sampling kernel.  It applies when the
-// rows are 16-byte aligned (bulk copies).  Cluster width: the narrowest power
-// of two that leaves at most 160 KB of a unit to each CTA (a unit's
-// statistics then complete within a few microseconds of its first byte, so a
-// draw's second read of it is served by L2), widened while the units are too
-// few to occupy the SMs.  Sub-chunks: at most kClMaxStepsW warp steps per
-// compute warp, as few as the chunk allows; ring depth: as many buffers as
-// shared memory holds, while the ring spans fewer units than the CTA's unit
-// slots.
-struct ClusterPlan {
-  int C, S, LC, SB, NSC, clusters;
-  size_t smem;
-};
-bool plan_cluster(DeviceState* d, bool bf16, bool ent, int B, int K, int V, ClusterPlan* p) {
-  const int vec = bf16 ? 8 : 4;
-  const size_t esz = bf16 ? 2 : 4;
-  const long long stepw = 32LL * vec;
-  const int rows = K > 0 ? 2 : 1;
-  const long long units = (long long)B * (K + 1);
-  const long long unit_bytes = (long long)rows * V * (long long)esz;
-  int C = 1;
-  while (C < sv::kClMaxC && (unit_bytes + C - 1) / C > 160 * 1024) C *= 2;
-  while (C < sv::kClMaxC && units * C < d->sms) C *= 2;
-  const long long sb_max = (long long)sv::kClCompute * sv::kClMaxStepsW * stepw;
-  for (; C <= sv::kClMaxC; C *= 2) {
-    long long LC = ((long long)V + C - 1) / C;
-    LC = (LC + vec - 1) / vec * vec;
-    const long long nsc = (LC + sb_max - 1) / sb_max;
-    if (nsc > sv::kClMaxSub) continue;
-    const long long SB = ((LC + nsc - 1) / nsc + stepw - 1) / stepw * stepw;
-    const size_t buf = (size_t)rows * (size_t)SB * esz;
-    const int s_cap = (int)std::min<long long>(sv::kClMaxStages, (long long)(sv::kClSlots - 1) * nsc);
-    int S = 0;
-    while (S < s_cap && sv::cluster_smem_bytes(S + 1, buf) <= (size_t)d->smem_optin) ++S;
-    if (S < 2) continue;
-    const size_t smem = sv::cluster_smem_bytes(S, buf);
-    const int n = cluster_fit(d, bf16, ent, C, smem);
-    if (n < 1) continue;
-    p->C = C;
-    p->S = S;
-    p->LC = (int)LC;
-    p->SB = (int)SB;
-    p->NSC = (int)nsc;
-    p->smem = smem;
-    p->clusters = n;
-    return true;
-  }
-  return false;
-}
-
-// Sampled verify through the cluster-streamed kernel (plan from plan_cluster).
-int cluster_verify(DeviceState* d, const ClusterPlan& cp, bool bf16, const void* target, const void* draft,
-                   const int32_t* tokens, int B, int K, int V, float temperature, uint64_t seed,
-                   int32_t* out_tokens, int32_t* out_n, float* out_row_stats, float* out_pq,
-                   float* out_resid, float* out_entropy, cudaStream_t stream, bool use_static) {
-  sv::ClusterArgs a;
-  memset(&a, 0, sizeof a);
-  a.target = target;
-  a.draft = draft;
-  a.tokens = tokens;
-  a.B = B;
-  a.K = K;
-  a.V = V;
-  a.C = cp.C;
-  a.S = cp.S;
-  a.LC = cp.LC;
-  a.SB = cp.SB;
-  a.NSC = cp.NSC;
-  a.U = B * (K + 1);
-  a.div_b = sv::make_fastdiv((uint32_t)B);
-  const double c = 1.4426950408889634074 / (double)temperature;  // log2(e) / tau
-  a.c64 = c;
-  a.c_hi = (float)c;
-  a.c_lo = (float)(c - (double)a.c_hi);
-  a.inv_tau = 1.0 / (double)temperature;
-  a.seed = seed;
-  a.out_tokens = out_tokens;
-  a.out_n = out_n;
-  a.out_row_stats = out_row_stats;
-  a.out_pq = out_pq;
-  a.out_resid = out_resid;
-  a.out_entropy = out_entropy;
-  a.status = d->status;
-  void* ws = nullptr;
-  int rc = get_scratch(d, use_static, sv::cluster_workspace(B, K), stream, &ws);
-  if (rc) return rc;
-  sv::cluster_bind_workspace(a, ws);
-  const int clusters = a.U < cp.clusters ? a.U : cp.clusters;
-  cudaError_t e = sv::launch_cluster(a, bf16, out_entropy != nullptr, clusters, cp.smem, stream);
-  cudaError_t e2 = put_scratch(use_static, ws, stream);
-  if (e != cudaSuccess) return cuda_fail(e, "sampling verify launch");
-  if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
-  return SPEC_OK;
-}
-
 int verify_impl(bool bf16, const void* target, const void* draft, const int32_t* tokens, int B,
                 int K, int V, float temperature, uint64_t seed, int32_t* out_tokens, int32_t* out_n,
                 float* out_row_stats, float* out_pq, float* out_resid, float* out_entropy,
@@ -471,15 +343,6 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   if (rc) return rc;
   const size_t esz = bf16 ? 2 : 4;
   const bool vec = aligned16(target) && (K == 0 || aligned16(draft)) && ((size_t)V * esz) % 16 == 0;
-  // The cluster-streamed kernel is parity-complete but not yet faster than the
-  // persistent kernel on any measured workload, so it is not selected yet.
-  constexpr bool kClusterPath = false;
-  if (kClusterPath && vec && !early_exit && (long long)B * (K + 1) < (1LL << 30)) {
-    ClusterPlan cp;
-    if (plan_cluster(d, bf16, out_entropy != nullptr, B, K, V, &cp))
-      return cluster_verify(d, cp, bf16, target, draft, tokens, B, K, V, temperature, seed, out_tokens, out_n,
-                            out_row_stats, out_pq, out_resid, out_entropy, stream, use_static);
-  }
   const int capacity = d->sms * d->occ_sample[bf16][vec];
   sv::SampleArgs a;
   memset(&a, 0, sizeof a);

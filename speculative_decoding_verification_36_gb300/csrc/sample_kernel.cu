@@ -662,7 +662,7 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int i, int r
   const uint32_t xt = ld_relaxed_if(lane == 0 && ti >= 0, a.tokens + (size_t)b * a.K + ti, kMarker);
   const float cc = a.c_hi;
   float m = neg_inf();
-  f2_t acc = f2(0.f, 0.f), tacc = f2(0.f, 0.f);
+  float2 acc = make_float2(0.f, 0.f), tacc = make_float2(0.f, 0.f);
   // two register buffers: the next batch is in flight while one is reduced
   const int nb = v1 > v0 ? (v1 - v0 + BATCH - 1) / BATCH : 0;
   int e = v0 + lane * VEC;
@@ -689,10 +689,11 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int i, int r
       stats_batch<E, VEC, ENT>(z1, m, acc, tacc, cc);
     }
   }
-  float sum = f2lo(acc) + f2hi(acc);
+  float sum = acc.x + acc.y;
   float tsum = 0.f;
+  if constexpr (!ENT) sum *= exp_fma_fix(m, cc);  // the fused exponents' common factor out
   if constexpr (ENT) {
-    tsum = f2lo(tacc) + f2hi(tacc);
+    tsum = tacc.x + tacc.y;
     warp_mst(m, sum, tsum, cc);
   } else {
     warp_ms(m, sum, cc);

@@ -168,6 +168,17 @@ __device__ __forceinline__ f2_t elem_pair(const Raw<E, VEC>& r, int p) {
   }
 }
 
+// The same pair as a float2 (register pair).
+template <class E, int VEC>
+__device__ __forceinline__ float2 elem_pair2(const Raw<E, VEC>& r, int p) {
+  if constexpr (VEC == 8) {
+    const uint32_t w = word_of(r.w, p);
+    return make_float2(bf16_lo(w), bf16_hi(w));
+  } else {
+    return make_float2(__uint_as_float(word_of(r.w, 2 * p)), __uint_as_float(word_of(r.w, 2 * p + 1)));
+  }
+}
+
 // Maximum over a batch of kUnroll loaded vectors (NaN never wins: max ignores
 // a NaN operand).
 template <class E, int VEC>
@@ -509,45 +520,75 @@ __device__ __forceinline__ void load_batch(Raw<E, VEC> (&z)[kUnroll], const type
 }
 
 // One batch into the lane's running (m, s): the batch max first, one rescale
-// if it rose, then 2^{(z - m) c} summed with packed pair arithmetic.
+// if it rose, then the exponentials, with float2 arithmetic on register pairs.
+// Without the entropy accumulator each exponent is one fused multiply-add,
+// z c - fl(m c): every term then carries the same factor 2^e with
+// e = m c - fl(m c) (the rounding of the product, below 2^-24 |m c|), which
+// exp_fma_fix takes out of the lane's sum once, at the end; rescales use the
+// same rounded products, so terms added before and after a rescale carry the
+// same factor.  With the entropy accumulator the exponent is (z - m) c, whose
+// terms the accumulator t = sum 2^d d needs exactly.
 template <class E, int VEC, bool ENT>
-__device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], float& m, f2_t& acc,
-                                            f2_t& tacc, float cc) {
+__device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], float& m, float2& acc,
+                                            float2& tacc, float cc) {
   const float bm = batch_max<E, VEC>(z);
   if (bm > m) {
-    const float delta = (m - bm) * cc;
-    const float f = ex2(delta);
     if constexpr (ENT) {
+      const float delta = (m - bm) * cc;
+      const float f = ex2(delta);
       // t' = 2^delta (t + delta s); an empty accumulator stays empty
-      tacc = m == neg_inf() ? f2(0.f, 0.f) : f2mul(f2(f, f), f2fma(f2(delta, delta), acc, tacc));
+      tacc = m == neg_inf() ? make_float2(0.f, 0.f)
+                            : __fmul2_rn(make_float2(f, f), __ffma2_rn(make_float2(delta, delta), acc, tacc));
+      acc = __fmul2_rn(acc, make_float2(f, f));
+    } else {
+      const float f = ex2(__fsub_rn(__fmul_rn(m, cc), __fmul_rn(bm, cc)));  // 0 when m was -inf
+      acc = __fmul2_rn(acc, make_float2(f, f));
     }
-    acc = f2mul(acc, f2(f, f));
     m = bm;
   }
   const float base = (m == neg_inf()) ? 0.f : m;
   if constexpr (VEC == 1) {
-    float lo = f2lo(acc), tlo = f2lo(tacc);
+    const float nmc = -__fmul_rn(base, cc);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      const float d = (z[u].f - base) * cc;
-      const float e = ex2(d);
-      lo += e;
-      if constexpr (ENT) tlo = fmaf(e, fmaxf(d, -126.f), tlo);
+      if constexpr (ENT) {
+        const float d = (z[u].f - base) * cc;
+        const float e = ex2(d);
+        acc.x += e;
+        tacc.x = fmaf(e, fmaxf(d, -126.f), tacc.x);
+      } else {
+        acc.x += ex2(__fmaf_rn(z[u].f, cc, nmc));
+      }
     }
-    acc = f2(lo, f2hi(acc));
-    if constexpr (ENT) tacc = f2(tlo, f2hi(tacc));
   } else {
-    const f2_t b2 = f2(base, base), c2 = f2(cc, cc);
+    const float2 c2 = make_float2(cc, cc);
+    const float2 nb = make_float2(-base, -base);
+    const float2 nmc = make_float2(-__fmul_rn(base, cc), -__fmul_rn(base, cc));
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
       for (int p = 0; p < VEC / 2; ++p) {
-        if constexpr (ENT)
-          f2_exp_acc_ent(acc, tacc, elem_pair<E, VEC>(z[u], p), b2, c2);
-        else
-          f2_exp_acc(acc, elem_pair<E, VEC>(z[u], p), b2, c2);
+        const float2 zz = elem_pair2<E, VEC>(z[u], p);
+        if constexpr (ENT) {
+          const float2 d = __fmul2_rn(__fadd2_rn(zz, nb), c2);
+          const float2 e = make_float2(ex2(d.x), ex2(d.y));
+          acc = __fadd2_rn(acc, e);
+          tacc = __ffma2_rn(e, make_float2(fmaxf(d.x, -126.f), fmaxf(d.y, -126.f)), tacc);
+        } else {
+          const float2 d = __ffma2_rn(zz, c2, nmc);
+          acc = __fadd2_rn(acc, make_float2(ex2(d.x), ex2(d.y)));
+        }
       }
   }
+}
+
+// The factor 2^{-e}, e = m c - fl(m c), that makes a lane sum formed with the
+// fused exponents of stats_batch (without entropy) the sum of 2^{(z - m) c}.
+// |e| < 2^-24 |m c|, so the first-order form is exact to far below fp32.
+__device__ __forceinline__ float exp_fma_fix(float m, float cc) {
+  const float base = (m == neg_inf()) ? 0.f : m;
+  const float e = __fmaf_rn(base, cc, -__fmul_rn(base, cc));
+  return __fmaf_rn(-e, 0.69314718055994530942f, 1.f);
 }
 
 // ---------------------------------------------------------------------------
@@ -612,14 +653,11 @@ __device__ __forceinline__ float tail_weight(float zT, float zD, const TailConst
 }
 
 // The same weights for an element pair with float2 arithmetic on register
-// pairs: every operation rounds exactly as the scalar version above.  eTo
-// receives the bonus weights 2^{(zT - mT) c} of the pair (the first factor of
-// the residual).
-__device__ __forceinline__ float2 tail_weight2_both(float2 zT, float2 zD, const TailConsts& k, float2& eTo) {
+// pairs: every operation rounds exactly as the scalar version above.
+__device__ __forceinline__ float2 tail_weight2(float2 zT, float2 zD, const TailConsts& k) {
   const float2 dT = __fadd2_rn(zT, make_float2(-k.mT, -k.mT));
   const float2 aT = __fmul2_rn(dT, make_float2(k.c_hi, k.c_hi));
   const float2 eT = make_float2(ex2(aT.x), ex2(aT.y));
-  eTo = eT;
   if (!k.residual) return eT;
   const float2 dD = __fadd2_rn(zD, make_float2(-k.mD, -k.mD));
   const float2 D = __fadd2_rn(dT, __fmul2_rn(dD, make_float2(-1.f, -1.f)));
@@ -627,20 +665,6 @@ __device__ __forceinline__ float2 tail_weight2_both(float2 zT, float2 zD, const 
                                   __ffma2_rn(D, make_float2(k.c_lo, k.c_lo), make_float2(-k.lam_lo, -k.lam_lo)));
   return __fmul2_rn(eT, resid_factor2(delta));
 }
-__device__ __forceinline__ float2 tail_weight2(float2 zT, float2 zD, const TailConsts& k) {
-  float2 e;
-  return tail_weight2_both(zT, zD, k, e);
-}
-template <class E, int VEC>
-__device__ __forceinline__ float2 elem_pair2(const Raw<E, VEC>& r, int p) {
-  if constexpr (VEC == 8) {
-    const uint32_t w = word_of(r.w, p);
-    return make_float2(bf16_lo(w), bf16_hi(w));
-  } else {
-    return make_float2(__uint_as_float(word_of(r.w, 2 * p)), __uint_as_float(word_of(r.w, 2 * p + 1)));
-  }
-}
-
 // The VEC weights of one lane's vector, in element order.
 template <class E, int VEC>
 __device__ __forceinline__ void lane_weights(const Raw<E, VEC>& zt, const Raw<E, VEC>& zd,
@@ -666,25 +690,6 @@ __device__ __forceinline__ float lane_mass(const Raw<E, VEC>& zt, const Raw<E, V
   float ls = 0.f;
 #pragma unroll
   for (int q = 0; q < VEC; ++q) ls = __fadd_rn(ls, w[q]);
-  return ls;
-}
-
-// The same sum, and in `bonus` the sum of the bonus weights 2^{(zT - mT) c} of
-// the same elements (vector path), each in element order.
-template <class E, int VEC>
-__device__ __forceinline__ float lane_mass_both(const Raw<E, VEC>& zt, const Raw<E, VEC>& zd,
-                                                const TailConsts& k, float& bonus) {
-  float ls = 0.f, lb = 0.f;
-#pragma unroll
-  for (int p = 0; p < VEC / 2; ++p) {
-    float2 e;
-    const float2 wp = tail_weight2_both(elem_pair2<E, VEC>(zt, p), elem_pair2<E, VEC>(zd, p), k, e);
-    ls = __fadd_rn(ls, wp.x);
-    ls = __fadd_rn(ls, wp.y);
-    lb = __fadd_rn(lb, e.x);
-    lb = __fadd_rn(lb, e.y);
-  }
-  bonus = lb;
   return ls;
 }
 

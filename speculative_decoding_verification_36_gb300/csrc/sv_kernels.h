@@ -211,66 +211,6 @@ int tree_stats_blocks_per_sm(bool bf16, bool vec);
 int tree_walk_clusters(bool bf16, bool vec, int C);
 
 
-// Cluster-streamed sampling verify (cluster_kernel.cu).  Position unit (b, i)
-// -- target row i and draft row i of sequence b, or target row K alone for
-// i = K -- is read by one thread-block cluster of C CTAs: CTA r owns elements
-// [r LC, (r+1) LC) of both rows and streams them through a ring of S
-// shared-memory buffers in NSC sub-chunks of SB elements per row.  Units are
-// taken in position-major order (u = i B + b), unit u by cluster u mod G.
-constexpr int kClCompute = 16;                        // compute warps per CTA
-constexpr int kClProducer = kClCompute;               // warp that issues the copies
-constexpr int kClDecider = kClCompute + 1;            // warp that takes the verdicts
-constexpr int kClService = kClCompute + 2;            // warp that stores results and commits
-constexpr int kClThreads = (kClCompute + 3) * 32;
-constexpr int kClMaxStages = 8;     // ring buffers per CTA
-constexpr int kClMaxStepsW = 4;     // warp steps per compute warp and sub-chunk
-constexpr int kClMaxSub = 4;        // sub-chunks per unit and CTA
-constexpr int kClMaxC = 16;         // CTAs per cluster
-constexpr int kClSlots = 8;         // units in flight per CTA (more than the ring spans)
-constexpr int kClRing = 16;         // finished units queued for the service warp
-constexpr int kClDrawSlots = 16;    // draws in flight per cluster (the producer's priority keeps fewer)
-struct ClusterArgs {
-  const void* target;
-  const void* draft;
-  const int32_t* tokens;
-  int B, K, V;
-  int C;        // CTAs per cluster
-  int S;        // ring buffers per CTA
-  int LC;       // elements of each row per CTA (a multiple of the vector width)
-  int SB;       // elements of each row per sub-chunk (a whole number of warp steps)
-  int NSC;      // sub-chunks per unit: ceil(LC / SB)
-  int U;        // units: B * (K + 1)
-  FastDiv div_b;  // u / B
-  float c_hi, c_lo;  // log2(e)/temperature as a float pair
-  double c64;        // the same in double
-  double inv_tau;    // 1 / temperature
-  uint64_t seed;
-  int32_t* out_tokens;
-  int32_t* out_n;
-  float* out_row_stats;  // optional [B, 2K+1, 2]
-  float* out_pq;         // optional [B, K, 2]
-  float* out_resid;      // optional [B]
-  float* out_entropy;    // optional [B, 2K+1]
-  // workspace, filled with all-ones bytes: arrive starts at -1, firstrej at
-  // "no rejection" (0xffffffff), verdict and slot hold the marker
-  int* arrive;        // [B] units of the sequence finished (the last one commits)
-  unsigned* firstrej; // [B] lowest position known to be rejected or bad
-  int* verdict;       // [B, K+1]
-  uint2* slot;        // [B, K+1] (token, Z / sT) drawn at a position
-  unsigned* status;
-};
-WsLayout cluster_workspace(int B, int K);
-void cluster_bind_workspace(ClusterArgs& a, void* ws);
-// Dynamic shared memory of a launch with S ring buffers of `buf_bytes`.
-size_t cluster_smem_bytes(int S, size_t buf_bytes);
-// Once per device: allow up to smem_max bytes of dynamic shared memory and
-// clusters of up to 16 CTAs.
-cudaError_t cluster_prepare(int smem_max);
-cudaError_t launch_cluster(const ClusterArgs& a, bool bf16, bool ent, int clusters, size_t smem,
-                           cudaStream_t s);
-// Clusters of C CTAs with `smem` bytes each that fit on the device at once (0: none).
-int cluster_max_active(bool bf16, bool ent, int C, size_t smem);
-
 // Bind workspace pointers into the argument blocks.
 void sample_bind_workspace(SampleArgs& a, void* ws);
 void greedy_bind_workspace(GreedyArgs& a, void* ws);

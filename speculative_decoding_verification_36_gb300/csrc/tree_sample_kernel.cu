@@ -67,7 +67,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) tree_stats_kernel(const 
     const int v0 = s * a.SL, v1 = min(a.V, v0 + a.SL);
     const float cc = a.c_hi;
     float m = neg_inf();
-    f2_t acc = f2(0.f, 0.f), tacc = f2(0.f, 0.f);
+    float2 acc = make_float2(0.f, 0.f), tacc = make_float2(0.f, 0.f);
     const int nb = v1 > v0 ? (v1 - v0 + BATCH - 1) / BATCH : 0;
     int e = v0 + lane * VEC;
     Raw<E, VEC> z0[kUnroll], z1[kUnroll];
@@ -83,7 +83,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) tree_stats_kernel(const 
         stats_batch<E, VEC, false>(z1, m, acc, tacc, cc);
       }
     }
-    float sum = f2lo(acc) + f2hi(acc);
+    float sum = (acc.x + acc.y) * exp_fma_fix(m, cc);  // the fused exponents' common factor out
     warp_ms(m, sum, cc);
     float2* pp = a.part + (size_t)row_id * a.CS;
     int old = 0;

@@ -379,6 +379,30 @@ int spec_ngram_draft(const int32_t *tokens, const int32_t *lengths, int B, int s
 int spec_test_fail_allocations(int n);
 
 /*
+ * Test hook, for failure-detection tests: every bounded wait inside the
+ * kernels of later calls on the current device gives up after `iterations`
+ * polls (0 restores the default, about half a second).  A wait that gives up
+ * sets SPEC_FLAG_TIMEOUT, the kernel returns without faulting, and that call's
+ * outputs are invalid; the device stays usable.  Synchronises the device
+ * first.  Returns SPEC_OK or SPEC_ERR_CUDA.  The pages have no counterpart; it
+ * exists so that the timeout path can be exercised without a real stall.
+ */
+int spec_test_spin_limit(uint32_t iterations);
+
+/*
+ * Test hook, for failure-detection tests: runs each of the library's seven
+ * bounded-wait helpers once on a slot that nothing writes and once on a slot
+ * already written, under the limit spec_test_spin_limit set (synchronous; its
+ * own status words, not the device status word).  out_flags (host, 2 words):
+ * [0] bit k set when helper k gave up on the unwritten slot and flagged
+ * SPEC_FLAG_TIMEOUT (the decision read also returns "no decision");
+ * [1] bit k set when helper k flagged the written slot.  A correct library
+ * returns {0x7f, 0}.  Returns SPEC_OK, SPEC_ERR_NULL or SPEC_ERR_CUDA.  With
+ * the default limit each unwritten wait lasts about half a second or more.
+ */
+int spec_test_wait_probe(uint32_t* out_flags);
+
+/*
  * Synchronises `stream`, then returns in *flags_out (may be NULL) the device
  * status word of the current device (an OR of SPEC_FLAG_* set by every call
  * since the last read) and clears it.  Returns SPEC_OK or SPEC_ERR_CUDA.

@@ -27,7 +27,7 @@ from ._lib import SPEC_FLAG_BAD_DATA, SPEC_FLAG_TIMEOUT, SpecError
 __all__ = [
     "spec_verify", "spec_verify_early_exit", "spec_verify_static_scratch", "spec_verify_stats", "spec_verify_greedy_argmax",
     "spec_tree_verify_greedy", "spec_tree_verify_sampling", "spec_acceptance_stats", "spec_ngram_draft",
-    "spec_get_status", "SpecError",
+    "spec_get_status", "spec_test_spin_limit", "spec_test_wait_probe", "SpecError",
     "SPEC_FLAG_BAD_DATA", "SPEC_FLAG_TIMEOUT",
 ]
 
@@ -329,3 +329,26 @@ def spec_get_status(stream=None, device=None) -> int:
     with torch.cuda.device(dev):
         _lib.check(_lib.load().spec_get_status(_stream(stream), ctypes.addressof(flags)))
     return int(flags.value)
+
+
+def spec_test_spin_limit(iterations: int, device=None) -> None:
+    """Test hook for failure-detection tests: every bounded wait inside the
+    kernels of later calls on the device gives up after `iterations` polls and
+    flags SPEC_FLAG_TIMEOUT; 0 restores the default limit.  Synchronises the
+    device first."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _lib.check(_lib.load().spec_test_spin_limit(int(iterations)))
+
+
+def spec_test_wait_probe(device=None) -> tuple:
+    """Test hook: runs every bounded-wait helper of the library on a slot that
+    nothing writes and on one already written, under the current limit.
+    Returns (helpers that gave up on the unwritten slot, helpers that flagged
+    the written one) as bit masks; a correct library gives (0x7f, 0)."""
+    import ctypes
+    flags = (ctypes.c_uint32 * 2)()
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    with torch.cuda.device(dev):
+        _lib.check(_lib.load().spec_test_wait_probe(ctypes.addressof(flags)))
+    return int(flags[0]), int(flags[1])

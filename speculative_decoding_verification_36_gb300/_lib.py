@@ -53,6 +53,8 @@ SIGNATURES = {
     "spec_acceptance_stats": [_P, _I, _I, _P, _P, _P, _P],
     "spec_ngram_draft": [_P, _P, _I, _I, _I, _I, _I, _P, _P, _P, _P],
     "spec_test_fail_allocations": [_I],
+    "spec_test_spin_limit": [ctypes.c_uint32],
+    "spec_test_wait_probe": [ctypes.c_void_p],
     "spec_get_status": [_P, _P],
     "spec_status_string": [_I],
 }

@@ -123,41 +123,17 @@ int ensure_pool(DeviceState* d) {
 
 bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
-// Tuning knobs (environment, read once per process), defaults measured on
-// GB300 with the c3 workload:
-//   SPECVERIFY_SLICE_BYTES        bytes of logits per statistics slice of the
-//                                 sampling kernel (12288; 8192 for a batch
-//                                 with fewer than ~6 slices per warp)
-//   SPECVERIFY_ARGMAX_SLICE_BYTES the same for the greedy and tree kernels (8192)
-//   SPECVERIFY_TAIL_BYTES         bytes of one row per tail slice (half a
-//                                 statistics slice)
-//   SPECVERIFY_CLAIM_TAIL         final statistics slices not claimed ahead (1)
-//   SPECVERIFY_FRONT_POS          draft positions whose row pairs are spread
-//                                 through the stream (1)
-//   SPECVERIFY_FRONT_SPAN         percent of the stream they are spread over
-//                                 (60; 0 gives plain position-major order)
-//   SPECVERIFY_L2_KEEP            positions whose rows are prefetched into L2
-//                                 with evict_last, as likely tail rows (2)
-//   SPECVERIFY_L2_OTHER           prefetch policy of the other rows: 0 the
-//                                 default, 1 evict_first, 2 evict_normal (0)
-//   SPECVERIFY_LATE_TAILS         percent of the decision queue (the latest
-//                                 decisions) whose tail items free warps claim
-//                                 instead of fixed owners (6; 25 with early
-//                                 exit; 100 for a small batch)
-int env_int(const char* name, int dflt) {
-  const char* v = getenv(name);
-  if (!v || !*v) return dflt;
-  const long x = strtol(v, nullptr, 10);
-  return (x > 0 && x < (1L << 30)) ? (int)x : dflt;
-}
-
-// The same for a knob that may be zero or negative.
-int env_int_signed(const char* name, int dflt) {
-  const char* v = getenv(name);
-  if (!v || !*v) return dflt;
-  const long x = strtol(v, nullptr, 10);
-  return (x > -(1L << 30) && x < (1L << 30)) ? (int)x : dflt;
-}
+// Launch parameters of the persistent kernels, measured on GB300 with the c3
+// workload (the measurements are in the design notes):
+constexpr int kSliceBytes = 12288;        // statistics slice of the sampling kernel
+constexpr int kSmallSliceBytes = 8192;    // ... for a batch with fewer than ~6 slices per warp
+constexpr int kArgmaxSliceBytes = 8192;   // slice of the greedy and tree kernels
+constexpr int kClaimTail = 1;             // final statistics slices not claimed ahead
+constexpr int kFrontPositions = 1;        // draft positions whose row pairs are spread through the stream
+constexpr int kFrontSpanPercent = 60;     // ... over this percent of it (position 0 decides most sequences)
+constexpr int kL2KeepPositions = 2;       // positions whose rows are prefetched into L2 with evict_last
+constexpr int kLateTailPercent = 6;       // latest decisions whose tail items free warps claim
+constexpr int kLateTailPercentEarlyExit = 25;
 
 // Slice length: a whole number of warp load batches (32 lanes x kUnroll
 // vectors) covering about `bytes`; a row shorter than one slice is one slice.
@@ -288,8 +264,7 @@ int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
   a.K = K;
   a.V = V;
   a.R = K + 1;
-  static const int slice_bytes = env_int("SPECVERIFY_ARGMAX_SLICE_BYTES", 8192);
-  choose_slices(V, vec ? (bf16 ? 8 : 4) : 1, esz, slice_bytes, &a.SL, &a.CS, &a.CU);
+  choose_slices(V, vec ? (bf16 ? 8 : 4) : 1, esz, kArgmaxSliceBytes, &a.SL, &a.CS, &a.CU);
   a.map.A = a.R * a.CU;
   a.map.total = B * a.map.A;
   a.out_tokens = out_tokens;
@@ -358,19 +333,17 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   // 12 KB statistics slices; a batch too small to give every warp of the grid
   // about six of them streams 8 KB slices and lets free warps take all of its
   // tail items (c2: 68 us instead of 75 us per call)
-  static const int slice_bytes_env = env_int("SPECVERIFY_SLICE_BYTES", 0);
-  choose_slices(V, vec_elems, esz, slice_bytes_env > 0 ? slice_bytes_env : 12288, &a.SL, &a.CS, &CU);
+  choose_slices(V, vec_elems, esz, kSliceBytes, &a.SL, &a.CS, &CU);
   bool small = false;
-  if (slice_bytes_env <= 0 && (long long)B * a.R * a.CS < 6LL * capacity * sv::kWarps) {
+  if ((long long)B * a.R * a.CS < 6LL * capacity * sv::kWarps) {
     small = true;
-    choose_slices(V, vec_elems, esz, 8192, &a.SL, &a.CS, &CU);
+    choose_slices(V, vec_elems, esz, kSmallSliceBytes, &a.SL, &a.CS, &CU);
   }
   // tail slices: whole warp steps, half a statistics slice per row, so that a
   // tail item (target and draft slice) carries as many bytes as a statistics
   // slice
   const int step = 32 * vec_elems;
-  static const int tail_bytes = env_int("SPECVERIFY_TAIL_BYTES", 0);
-  const long long tl_elems = tail_bytes > 0 ? tail_bytes / (long long)esz : (a.SL + 1) / 2;
+  const long long tl_elems = (a.SL + 1) / 2;
   a.P = (int)((tl_elems + step - 1) / step);
   if (a.P < 1) a.P = 1;
   a.TL = a.P * step;
@@ -385,14 +358,12 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   // `front_span` percent of the stream (100 or more, or a span shorter than
   // their own share: position-major order).
   {
-    static const int front_pos = env_int_signed("SPECVERIFY_FRONT_POS", 1);
-    static const int front_span = env_int_signed("SPECVERIFY_FRONT_SPAN", 60);
     // early exit keeps plain position-major order: a sequence's later rows
     // then come after its decision, so they can be skipped
-    const int fp = early_exit ? 0 : (front_pos < 0 ? 0 : (front_pos > K ? K : front_pos));
+    const int fp = early_exit ? 0 : (kFrontPositions > K ? K : kFrontPositions);
     a.NA = fp * B * 2 * a.CS;
     a.FQ = 64;
-    const double span = (double)front_span / 100.0 * (double)a.F;
+    const double span = (double)kFrontSpanPercent / 100.0 * (double)a.F;
     int fa = a.FQ;
     if (a.NA > 0 && span > (double)a.NA) fa = (int)ceil((double)a.FQ * (double)a.NA / span);
     a.FA = fa < 1 ? 1 : (fa > a.FQ ? a.FQ : fa);
@@ -404,20 +375,15 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
     a.div_fq = sv::make_fastdiv((uint32_t)a.FQ);
   }
   const int grid = grid_for((a.F + sv::kSlices - 1) / sv::kSlices, capacity);
-  static const int claim_tail = env_int("SPECVERIFY_CLAIM_TAIL", 1);
-  a.claim_tail = claim_tail;
-  static const int l2_keep = env_int_signed("SPECVERIFY_L2_KEEP", 2);
-  static const int l2_other = env_int_signed("SPECVERIFY_L2_OTHER", 0);
-  a.l2_keep = l2_keep;
-  a.l2_other = l2_other;
+  a.claim_tail = kClaimTail;
+  a.l2_keep = kL2KeepPositions;
   a.early_exit = early_exit ? 1 : 0;
   // the tail items of the last late_tails percent of queue positions (the
   // latest decisions) go to whichever warps are free
   // (measured on c3: 6 % with the full read, 25 % with early exit, where
   // most of the grid is free once the first position has been streamed)
-  static const int late_tails = env_int_signed("SPECVERIFY_LATE_TAILS", -1);
   {
-    const int want = late_tails >= 0 ? late_tails : (small ? 100 : (early_exit ? 25 : 6));
+    const int want = small ? 100 : (early_exit ? kLateTailPercentEarlyExit : kLateTailPercent);
     const int pct = want > 100 ? 100 : want;
     int late = (int)(((long long)B * pct + 99) / 100);
     if (late > B) late = B;
@@ -488,8 +454,7 @@ int tree_sample_impl(bool bf16, const void* target, const void* draft, const int
   a.V = V;
   a.RR = 2 * (N + 1);
   int CU = 0;
-  static const int slice_bytes = env_int("SPECVERIFY_SLICE_BYTES", 12288);
-  choose_slices(V, vec_elems, esz, slice_bytes, &a.SL, &a.CS, &CU);
+  choose_slices(V, vec_elems, esz, kSliceBytes, &a.SL, &a.CS, &CU);
   a.F = (long long)B * a.RR * a.CS;
   // walk: the widest cluster (16, 8, 4, 2 CTAs) for which every sequence's
   // cluster is resident at once, else one CTA per sequence; each pass gives
@@ -713,6 +678,29 @@ int spec_ngram_draft(const int32_t* tokens, const int32_t* lengths, int B, int s
 }
 
 int spec_test_fail_allocations(int n) { return g_fail_allocs.exchange(n < 0 ? 0 : n); }
+
+int spec_test_spin_limit(uint32_t iterations) {
+  DeviceState* d = nullptr;
+  const int rc = get_device_state(&d);
+  if (rc) return rc;
+  const unsigned n = iterations ? iterations : sv::kSpinLimit;
+  cudaError_t e = cudaDeviceSynchronize();  // no launch in flight sees a changed limit
+  if (e == cudaSuccess) e = sv::sample_set_spin_limit(n);
+  if (e == cudaSuccess) e = sv::greedy_set_spin_limit(n);
+  if (e == cudaSuccess) e = sv::tree_sample_set_spin_limit(n);
+  if (e != cudaSuccess) return cuda_fail(e, "spin limit");
+  return SPEC_OK;
+}
+
+int spec_test_wait_probe(uint32_t* out_flags) {
+  if (!out_flags) return SPEC_ERR_NULL;
+  DeviceState* d = nullptr;
+  const int rc = get_device_state(&d);
+  if (rc) return rc;
+  const cudaError_t e = sv::sample_wait_probe(out_flags);
+  if (e != cudaSuccess) return cuda_fail(e, "wait probe");
+  return SPEC_OK;
+}
 
 int spec_get_status(cudaStream_t stream, uint32_t* flags_out) {
   DeviceState* d = nullptr;

@@ -677,4 +677,6 @@ int tree_blocks_per_sm(bool bf16, bool vec) {
   return vec ? occ(argmax_kernel<F32, 4, true, false>) : occ(argmax_kernel<F32, 1, true, false>);
 }
 
+cudaError_t greedy_set_spin_limit(unsigned n) { return set_spin_limit_here(n); }
+
 }  // namespace sv

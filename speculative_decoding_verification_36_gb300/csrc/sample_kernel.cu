@@ -94,21 +94,36 @@ __device__ __forceinline__ uint32_t poll_decision(const SampleArgs& a, bool pred
   return ld_relaxed_if(pred, a.queue + pos, kMarker);
 }
 
+// Lane 0's bounded wait for the first word of queue entry pos (kMarker if the
+// wait ran out, which is flagged).
+__device__ __forceinline__ uint32_t wait_decision(const SampleArgs& a, int pos) {
+  unsigned it = 0, nap = 64;
+  uint32_t seen = poll_decision(a, true, pos);
+  while (!word_set(seen) && ++it < spin_limit()) {
+    __nanosleep(nap);
+    if (nap < 1024) nap <<= 1;
+    seen = poll_decision(a, true, pos);
+  }
+  if (!word_set(seen)) atomicOr(a.status, kStatusTimeout);
+  return seen;
+}
+
 // The whole entry, once its first word has been seen; the other fields were
 // stored at the same moment, so the bounded wait is at most a few round trips.
 __device__ __noinline__ SeqInfo read_decision(const SampleArgs& a, int pos) {
   const uint32_t* e = (const uint32_t*)(a.queue + pos);
   uint4 x = ld_relaxed_v4(e), y = ld_relaxed_v4(e + 4);
   unsigned it = 0;
-  while (!(word_set(x.x) && word_set(x.y) && word_set(x.z) && word_set(x.w) && word_set(y.x) &&
-           word_set(y.y) && word_set(y.z) && word_set(y.w)) &&
-         ++it < kSpinLimit) {
+  bool ok;
+  while (!(ok = word_set(x.x) && word_set(x.y) && word_set(x.z) && word_set(x.w) && word_set(y.x) &&
+                word_set(y.y) && word_set(y.z) && word_set(y.w)) &&
+         ++it < spin_limit()) {
     __nanosleep(64);
     x = ld_relaxed_v4(e);
     y = ld_relaxed_v4(e + 4);
   }
   SeqInfo si;
-  if (it >= kSpinLimit) {
+  if (!ok) {
     atomicOr(a.status, kStatusTimeout);
     si.mode = kModeBad;  // treated as undecided: the tail slices do nothing
   } else {
@@ -672,10 +687,6 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int i, int r
       const unsigned bytes = (unsigned)((v1 - v0) * sizeof(S));
       if (i < a.l2_keep)
         prefetch_l2_pol(row + v0, bytes, l2_policy_evict_last());
-      else if (a.l2_other == 1)
-        prefetch_l2_pol(row + v0, bytes, l2_policy_evict_first());
-      else if (a.l2_other == 2)
-        prefetch_l2_pol(row + v0, bytes, l2_policy_evict_normal());
       else
         prefetch_l2(row + v0, bytes);
     }
@@ -757,8 +768,12 @@ __device__ __forceinline__ int next_live_counter(int ctr, unsigned dead) {
 // warp holding a claimed statistics slice never waits, and a warp waits for a
 // queue entry only when it has no statistics work left; every sequence is
 // decided once the statistics slices of its positions up to the first
-// rejection are done.  So every queue entry is eventually written and every
-// wait ends, whatever part of the grid is resident.
+// rejection are done.  Every statistics slice is claimed by a CTA that is
+// already running: the first claims are numbered by the order in which CTAs
+// start (a per-launch ticket), not by their index, and the rest come from the
+// counters.  So every queue entry is eventually written and every wait ends,
+// whatever part of the grid is resident at a time (another kernel may hold
+// some SMs until after this launch's first CTAs finish).
 template <class E, int VEC, bool ENT>
 __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __grid_constant__ SampleArgs a) {
   const int lane = threadIdx.x & 31;
@@ -766,7 +781,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
   const int TT = a.B * a.TC;                       // tail items in all
   const int TO = a.TTo;                            // owned tail items: the first TTo
   const int W = kSlices * (int)gridDim.x;          // warps in the grid
-  int t = w * (int)gridDim.x + (int)blockIdx.x;    // this warp's next owned tail item
+  // this CTA's start order in the launch (its first claims and owned tail
+  // items follow it), one ticket for the whole CTA
+  __shared__ int cta_order;
+  if (threadIdx.x == 0) cta_order = ticket_take(a.ctaticket);
+  __syncthreads();
+  const int tk = cta_order;
+  int t = w * (int)gridDim.x + tk;                 // this warp's next owned tail item
   if (t >= TO) t = TT;
   // Statistics claims rotate over the eight counters (warp slot w starts at
   // counter w), so every warp draws equally from every counter and the
@@ -776,13 +797,13 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
   // slice is processed before a tail item that became ready (other warps'
   // decisions may wait on it); the claim after it is then deferred until the
   // tail item is done.
-  // The first claim of every warp is static (claim index blockIdx.x on
-  // counter w), so the first slices start streaming without a round trip;
-  // claims made through the counters are offset by the grid size.
+  // The first claim of every warp comes with its CTA's ticket (claim index tk
+  // on counter w), so the first slices start streaming after one round trip
+  // per CTA; claims made through the counters are offset by the grid size.
   const int k0 = (int)gridDim.x;
   unsigned dead = 0;
   int ctr = w;
-  int f = (int)blockIdx.x * kSlices + ctr;
+  int f = tk * kSlices + ctr;
   bool held = true;  // f is the result of a claim on counter ctr
   uint32_t seen = poll_decision(a, lane == 0 && t < TO, fdiv(t, a.div_tc));
   for (;;) {
@@ -844,16 +865,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
       const int j = TO + bcast(ticket_take_if(lane == 0, a.dclaim));
       if (j >= TT) break;
       uint32_t dseen = kMarker;
-      if (lane == 0) {
-        unsigned it = 0, nap = 64;
-        dseen = poll_decision(a, true, fdiv(j, a.div_tc));
-        while (!word_set(dseen) && ++it < kSpinLimit) {
-          __nanosleep(nap);
-          if (nap < 1024) nap <<= 1;
-          dseen = poll_decision(a, true, fdiv(j, a.div_tc));
-        }
-        if (!word_set(dseen)) atomicOr(a.status, kStatusTimeout);
-      }
+      if (lane == 0) dseen = wait_decision(a, fdiv(j, a.div_tc));
       if (!word_set(bcast((int)dseen))) break;
       const int pos = fdiv(j, a.div_tc);
       const SeqInfo si = read_decision(a, pos);
@@ -861,16 +873,7 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) sample_kernel(const __gr
       continue;
     }
     // no statistics work left: wait for this warp's next owned decision
-    if (lane == 0) {
-      unsigned it = 0, nap = 64;
-      seen = poll_decision(a, true, fdiv(t, a.div_tc));
-      while (!word_set(seen) && ++it < kSpinLimit) {
-        __nanosleep(nap);
-        if (nap < 1024) nap <<= 1;
-        seen = poll_decision(a, true, fdiv(t, a.div_tc));
-      }
-      if (!word_set(seen)) atomicOr(a.status, kStatusTimeout);
-    }
+    if (lane == 0) seen = wait_decision(a, fdiv(t, a.div_tc));
     if (!word_set(bcast((int)seen))) break;
   }
 }
@@ -893,6 +896,7 @@ static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t*
   off[3] = o; o += align_up((size_t)B * 4, 16);                             // tailticket
   off[4] = o; o += 128;                                                      // qcount
   off[22] = o; o += 128;                                                     // dclaim
+  off[23] = o; o += 128;                                                     // ctaticket
   off[15] = o; o += align_up((size_t)B * 4, 16);                            // posticket
   off[17] = o; o += align_up((size_t)B * 8, 16);                            // resword
   o = align_up(o, 256);
@@ -912,7 +916,7 @@ static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t*
 }
 
 WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
-  size_t off[23];
+  size_t off[24];
   sample_layout(B, K, CS, TC, P, ent, off);
   WsLayout l;
   l.total = off[12];
@@ -923,7 +927,7 @@ WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
 }
 
 void sample_bind_workspace(SampleArgs& a, void* ws) {
-  size_t off[23];
+  size_t off[24];
   sample_layout(a.B, a.K, a.CS, a.TC, a.P, a.out_entropy != nullptr, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
@@ -932,6 +936,7 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.tailticket = (int*)(p + off[3]);
   a.qcount = (int*)(p + off[4]);
   a.dclaim = (int*)(p + off[22]);
+  a.ctaticket = (int*)(p + off[23]);
   a.posticket = (int*)(p + off[15]);
   a.resword = (unsigned long long*)(p + off[17]);
   a.part = (float2*)(p + off[6]);
@@ -972,6 +977,56 @@ static int blocks_sample_t() {
 int sample_blocks_per_sm(bool bf16, bool vec) {
   if (bf16) return vec ? blocks_sample_t<BF16, 8>() : blocks_sample_t<BF16, 1>();
   return vec ? blocks_sample_t<F32, 4>() : blocks_sample_t<F32, 1>();
+}
+
+cudaError_t sample_set_spin_limit(unsigned n) { return set_spin_limit_here(n); }
+
+// Test probe of the bounded waits (one thread).  Helper k waits once on a
+// slot that nothing writes (marker-filled, status word st[k]) and once on a
+// slot already written (st[kProbeWaits + k]).  flags[0] bit k: the first wait
+// ran out and flagged it; flags[1] bit k: the second one did (never expected).
+constexpr int kProbeWaits = 7;
+__global__ void wait_probe_kernel(uint32_t* slots, unsigned* st, uint32_t* flags) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  for (int half = 0; half < 2; ++half) {
+    uint32_t* sl = slots + half * 16;  // 16 words: one queue entry and its neighbours
+    unsigned* s = st + half * kProbeWaits;
+    (void)wait_u2(sl, s + 0);
+    (void)wait_s32((const int*)sl, s + 1);
+    (void)wait_f32((const float*)sl, s + 2);
+    (void)wait_f32_acquire((const float*)sl, s + 3);
+    (void)wait_result(sl, s + 4);
+    SampleArgs a = {};
+    a.queue = (SeqInfo*)sl;
+    a.status = s + 5;
+    const SeqInfo si = read_decision(a, 0);
+    if (si.mode != kModeBad && half == 0) atomicOr(s + 5, 4u);  // expired, yet taken as a decision
+    a.status = s + 6;
+    (void)wait_decision(a, 0);
+  }
+  uint32_t f0 = 0, f1 = 0;
+  for (int k = 0; k < kProbeWaits; ++k) {
+    if (st[k] == kStatusTimeout) f0 |= 1u << k;
+    if (st[kProbeWaits + k] != 0) f1 |= 1u << k;
+  }
+  flags[0] = f0;
+  flags[1] = f1;
+}
+
+cudaError_t sample_wait_probe(uint32_t* flags_host) {
+  uint32_t* buf = nullptr;  // [32 slot words][2 x kProbeWaits status words][2 flags]
+  cudaError_t e = cudaMalloc(&buf, (32 + 2 * kProbeWaits + 2) * sizeof(uint32_t));
+  if (e != cudaSuccess) return e;
+  e = cudaMemset(buf, 0xff, 16 * sizeof(uint32_t));  // unwritten: every word the marker
+  if (e == cudaSuccess) e = cudaMemset(buf + 16, 0, (16 + 2 * kProbeWaits + 2) * sizeof(uint32_t));
+  if (e == cudaSuccess) {
+    wait_probe_kernel<<<1, 32>>>(buf, buf + 32, buf + 32 + 2 * kProbeWaits);
+    e = cudaGetLastError();
+  }
+  if (e == cudaSuccess)
+    e = cudaMemcpy(flags_host, buf + 32 + 2 * kProbeWaits, 2 * sizeof(uint32_t), cudaMemcpyDeviceToHost);
+  const cudaError_t e2 = cudaFree(buf);
+  return e != cudaSuccess ? e : e2;
 }
 
 }  // namespace sv

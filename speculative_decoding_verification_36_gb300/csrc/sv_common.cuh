@@ -14,7 +14,18 @@
 
 namespace sv {
 
-constexpr unsigned kSpinLimit = 1u << 22;  // bounded waits: about 0.5 s with 128 ns naps
+
+// The limit in force for every bounded wait of this translation unit's
+// kernels (one copy per translation unit and device).  spec_test_spin_limit
+// lowers it so that a test can make waits run out on purpose.  It is read
+// with a volatile load, and only once a wait has found its slot unset: no
+// device code writes it, and the host changes it between launches.
+static __device__ unsigned g_spin_limit = kSpinLimit;
+__device__ __forceinline__ unsigned spin_limit() { return *(const volatile unsigned*)&g_spin_limit; }
+// Host side: set this translation unit's copy on the current device.
+static inline cudaError_t set_spin_limit_here(unsigned n) {
+  return cudaMemcpyToSymbol(g_spin_limit, &n, sizeof n);
+}
 
 // status bits OR-ed into the library's device status word
 constexpr unsigned kStatusBadData = 1u;  // NaN / +inf logit, empty row, bad token or parent
@@ -219,16 +230,6 @@ __device__ __forceinline__ uint64_t l2_policy_evict_last() {
   asm("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(pol));
   return pol;
 }
-__device__ __forceinline__ uint64_t l2_policy_evict_first() {
-  uint64_t pol;
-  asm("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_normal() {
-  uint64_t pol;
-  asm("createpolicy.fractional.L2::evict_normal.b64 %0, 1.0;" : "=l"(pol));
-  return pol;
-}
 
 // Asynchronous 16-byte copies global -> shared (no register staging), grouped
 // per thread: a thread waits only for its own groups, and every lane reads
@@ -324,7 +325,7 @@ __device__ __forceinline__ int ticket_take(int* p) { return atom_add_relaxed(p, 
 __device__ __forceinline__ uint2 wait_u2(const void* p, unsigned* status) {
   uint2 v = ld_relaxed_u2(p);
   unsigned it = 0;
-  while (v.x == kMarker && ++it < kSpinLimit) {
+  while (v.x == kMarker && ++it < spin_limit()) {
     __nanosleep(64);
     v = ld_relaxed_u2(p);
   }
@@ -334,7 +335,7 @@ __device__ __forceinline__ uint2 wait_u2(const void* p, unsigned* status) {
 __device__ __forceinline__ int wait_s32(const int* p, unsigned* status) {
   int v = ld_relaxed_s32(p);
   unsigned it = 0;
-  while (v == (int)kMarker && ++it < kSpinLimit) {
+  while (v == (int)kMarker && ++it < spin_limit()) {
     __nanosleep(64);
     v = ld_relaxed_s32(p);
   }
@@ -344,7 +345,7 @@ __device__ __forceinline__ int wait_s32(const int* p, unsigned* status) {
 __device__ __forceinline__ float wait_f32(const float* p, unsigned* status) {
   float v = ld_relaxed_f32(p);
   unsigned it = 0;
-  while (__float_as_uint(v) == kMarker && ++it < kSpinLimit) {
+  while (__float_as_uint(v) == kMarker && ++it < spin_limit()) {
     __nanosleep(64);
     v = ld_relaxed_f32(p);
   }
@@ -354,7 +355,7 @@ __device__ __forceinline__ float wait_f32(const float* p, unsigned* status) {
 __device__ __forceinline__ float wait_f32_acquire(const float* p, unsigned* status) {
   float v = ld_acquire_f32(p);
   unsigned it = 0;
-  while (__float_as_uint(v) == kMarker && ++it < kSpinLimit) {
+  while (__float_as_uint(v) == kMarker && ++it < spin_limit()) {
     __nanosleep(64);
     v = ld_acquire_f32(p);
   }
@@ -366,7 +367,7 @@ __device__ __forceinline__ float wait_f32_acquire(const float* p, unsigned* stat
 __device__ __forceinline__ uint4 wait_result(const void* p, unsigned* status) {
   uint4 v = ld_relaxed_v4(p);
   unsigned it = 0;
-  while ((v.x == kMarker || v.y == kMarker || v.z == kMarker) && ++it < kSpinLimit) {
+  while ((v.x == kMarker || v.y == kMarker || v.z == kMarker) && ++it < spin_limit()) {
     __nanosleep(64);
     v = ld_relaxed_v4(p);
   }

@@ -29,6 +29,7 @@ constexpr int kUnroll = 2;     // 16-byte vectors per lane per load batch; two b
 constexpr int kMaxK = 255;
 constexpr int kMaskMaxK = 31;  // resolution words hold positions 0..31 (K <= 31)
 constexpr int kMaxTreeNodes = 1024;
+constexpr unsigned kSpinLimit = 1u << 22;  // bounded waits: about 0.5 s with 128 ns naps
 
 // Division by a per-launch constant d >= 1 for dividends below 2^31, as one
 // widening multiply and a shift (Granlund and Montgomery, "Division by
@@ -91,7 +92,6 @@ struct SampleArgs {
   FastDiv div_fq;
   int claim_tail;  // within this many slices of the end, claims are not made ahead
   int l2_keep;     // rows of positions < l2_keep are prefetched into L2 with evict_last
-  int l2_other;    // the other rows: 0 default prefetch, 1 evict_first, 2 evict_normal
   int early_exit;  // read only the rows the result depends on (positions 0..n, row K if n = K)
   int TTo;         // owned tail items (the first TTo); the rest are claimed by free warps
   FastDiv div_pos, div_pair, div_cs, div_tc;  // division by B * 2 * CS, 2 * CS, CS and TC
@@ -107,7 +107,7 @@ struct SampleArgs {
   float* out_entropy;    // optional [B, R]: entropy (nats) of each row's softmax
   // workspace, filled with all-ones bytes before the launch: the counters and
   // tickets (counter, unitticket, seqticket, posticket, tailticket, qcount,
-  // dclaim) then start at -1, the resolution words at the empty
+  // dclaim, ctaticket) then start at -1, the resolution words at the empty
   // set (stored complemented), and the result slots (part, rowstat, zx,
   // verdict, result, tailsum, queue, pieces) hold the kMarker "not yet
   // written" pattern.
@@ -122,6 +122,7 @@ struct SampleArgs {
   int* tailticket;  // [B] finished tail slices
   int* qcount;      // decision-queue positions taken so far
   int* dclaim;      // tail items of the last queue positions claimed so far
+  int* ctaticket;   // CTAs started so far (each CTA's first claims follow its ticket)
   float2* part;     // [B, R, CS] per-slice (m, s)
   float2* rowstat;  // [B, R] merged (m, s) of each row
   float* zx;        // [B, R] logit at the drafted token, written by the slice holding it
@@ -261,5 +262,15 @@ constexpr size_t kCounterBytes = (size_t)kSlices * kCounterStride * 8;
 
 // The bit pattern of a slot that has not been written yet.
 constexpr unsigned kMarker = 0xffffffffu;
+
+// The bounded-wait limit of each kernel translation unit on the current device
+// (spec_test_spin_limit).
+cudaError_t sample_set_spin_limit(unsigned n);
+// Runs every bounded-wait helper on an unwritten and a written slot (test
+// hook; synchronous).  flags_host[0]: bits of the helpers that ran out on the
+// unwritten slot; flags_host[1]: bits of those that flagged a written one.
+cudaError_t sample_wait_probe(uint32_t* flags_host);
+cudaError_t greedy_set_spin_limit(unsigned n);
+cudaError_t tree_sample_set_spin_limit(unsigned n);
 
 }  // namespace sv

@@ -640,4 +640,6 @@ int tree_stats_blocks_per_sm(bool bf16, bool vec) {
   return vec ? blocks_tree_stats_t<F32, 4>() : blocks_tree_stats_t<F32, 1>();
 }
 
+cudaError_t tree_sample_set_spin_limit(unsigned n) { return set_spin_limit_here(n); }
+
 }  // namespace sv

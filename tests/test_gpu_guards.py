@@ -160,3 +160,69 @@ def test_concurrent_calls_from_two_host_threads():
         th.join(timeout=300)
     assert not errors, errors
     assert sv.spec_get_status() == 0
+
+
+def test_every_bounded_wait_gives_up_on_a_slot_nothing_writes():
+    """Each bounded-wait helper of the kernels, run on a slot that nothing
+    writes under a lowered limit, gives up and flags SPEC_FLAG_TIMEOUT (the
+    decision read also reports no decision); on a slot already written none
+    flags anything.  The device status word is untouched and the next call
+    works."""
+    try:
+        sv.spec_test_spin_limit(2000)
+        expired, written = sv.spec_test_wait_probe()
+    finally:
+        sv.spec_test_spin_limit(0)
+    assert expired == 0x7F, hex(expired)
+    assert written == 0, hex(written)
+    assert sv.spec_get_status() == 0
+    p, x = _chain("c2", B=4, K=3, V=3000)
+    a = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 2)
+    torch.cuda.synchronize()
+    assert (a[1] >= 0).all() and sv.spec_get_status() == 0
+
+
+def test_a_lowered_wait_limit_never_hangs_or_writes_out_of_place():
+    """A full-width sampled verify with every wait limited to one poll (most of
+    its waits find their slot already written, so whether one runs out depends
+    on timing) returns; if a wait ran out the status word says so (and a row
+    left without statistics is reported as bad data), and in any
+    case nothing is written outside the outputs or out of range, and a call
+    that flagged nothing gives the normal result.  With the default limit back
+    the next call matches the oracle."""
+    import oracle
+    from parity import chain_report
+    p, x = _chain("c3", B=64)
+    want_t, want_n = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 4)
+    torch.cuda.synchronize()
+    tok, n = Guarded((p.B, p.K + 1), torch.int32), Guarded((p.B,), torch.int32)
+    assert sv.spec_get_status() == 0
+    try:
+        sv.spec_test_spin_limit(1)
+        for _ in range(3):
+            sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 4, out_tokens=tok.t,
+                           out_n_accepted=n.t)
+            torch.cuda.synchronize()
+            status = sv.spec_get_status()
+            # an expired wait on a row's partials leaves the row without
+            # statistics, which is also reported as bad data
+            assert status in (0, sv.SPEC_FLAG_TIMEOUT, sv.SPEC_FLAG_TIMEOUT | sv.SPEC_FLAG_BAD_DATA), status
+            assert tok.intact() and n.intact()
+            # a sequence whose commit was given up keeps its previous value
+            nn, tt = n.t.cpu().numpy(), tok.t.cpu().numpy()
+            assert (((nn >= -1) & (nn <= p.K)) | (nn == CANARY_I)).all()
+            assert (((tt >= -1) & (tt < p.V)) | (tt == CANARY_I)).all()
+            if status == 0:
+                assert torch.equal(tok.t, want_t) and torch.equal(n.t, want_n)
+    finally:
+        sv.spec_test_spin_limit(0)
+    tokens, n2 = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 4)
+    torch.cuda.synchronize()
+    assert sv.spec_get_status() == 0
+    assert torch.equal(tokens, want_t) and torch.equal(n2, want_n)
+    sel = [0, 17, 40, 63]
+    idx = torch.tensor(sel)
+    ref = oracle.spec_verify(x["target"][idx].cpu(), x["draft"][idx].cpu(), x["tokens"][idx].cpu(),
+                             p.temperature, 4, seq_ids=sel)
+    rep = chain_report(tokens.cpu().numpy()[sel], n2.cpu().numpy()[sel], ref)
+    assert not rep["mismatch"], rep

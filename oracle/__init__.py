@@ -67,6 +67,8 @@ def _load():
     lib.oracle_acceptance_stats.restype = None
     lib.oracle_row_entropy.argtypes = [P, i32, i64, i32, f64, P]
     lib.oracle_row_entropy.restype = None
+    lib.oracle_adaptive_k.argtypes = [P, P, i32, i32, f64, f64, i32, i32, P, P]
+    lib.oracle_adaptive_k.restype = None
     lib.oracle_tree_verify_sampling.argtypes = [P, P, i32, P, P, i32, i32, i32, f64, u64, P, P, P]
     lib.oracle_tree_verify_sampling.restype = i32
     lib.oracle_ngram_draft.argtypes = [P, i64, P, i32, i32, i32, i32, P, P, P]
@@ -263,6 +265,28 @@ def row_entropy(logits, temperature: float):
     t_buf = t if t.size else np.zeros(1, dtype=t.dtype)
     lib.oracle_row_entropy(_ptr(t_buf), dt, rows, V, float(temperature), _ptr(out))
     return out[:rows].reshape(shape)
+
+
+def adaptive_k(target_entropy, n_accepted, K: int, h_lo: float, h_hi: float, k_min: int, k_max: int):
+    """Suggested next draft length per sequence from the mean entropy of the
+    target rows 0..n the iteration consulted.  target_entropy [B, K+1] (nats),
+    n_accepted [B] (-1: bad).  Returns dict(k_next [B] int32 (-1 for a bad
+    sequence), mean_entropy [B] float64)."""
+    if not (0 <= k_min <= k_max) or not (h_lo <= h_hi):
+        raise ValueError("need 0 <= k_min <= k_max and h_lo <= h_hi")
+    lib = _load()
+    h = np.ascontiguousarray(np.asarray(target_entropy, dtype=np.float64))
+    n = np.ascontiguousarray(np.asarray(n_accepted, dtype=np.int32).reshape(-1))
+    B = n.size
+    if h.shape != (B, K + 1):
+        raise ValueError(f"target_entropy must be [B, K+1] = [{B}, {K + 1}]")
+    k_next = np.zeros(max(B, 1), dtype=np.int32)
+    hmean = np.zeros(max(B, 1), dtype=np.float64)
+    h_buf = h if h.size else np.zeros(1, dtype=np.float64)
+    n_buf = n if n.size else np.zeros(1, dtype=np.int32)
+    lib.oracle_adaptive_k(_ptr(h_buf), _ptr(n_buf), int(B), int(K), float(h_lo), float(h_hi), int(k_min),
+                          int(k_max), _ptr(k_next), _ptr(hmean))
+    return dict(k_next=k_next[:B], mean_entropy=hmean[:B])
 
 
 def tree_verify_sampling(target, draft, tree_tokens, parent_idx, temperature: float, seed: int):

@@ -670,6 +670,54 @@ void oracle_row_entropy(const void *logits, int dtype, long long rows, int V, do
 }
 
 /*
+ * Suggested draft length for each sequence's next iteration, from the entropy
+ * of the target distributions this iteration consulted
+ *   [P3] "Speculative Decoding at Scale: Latency Reduction in Distributed LLM
+ *   Serving", sec. 3 "Engineering Recommendations" (speculation depth tuning:
+ *   a shorter draft where the text is uncertain, a longer one where it is
+ *   predictable); [P2] "How much speedup to expect" (the draft length trades
+ *   tokens per iteration against wasted work on rejections).
+ * The page gives no formula; the rule here is the plain reading of it:
+ *   Hbar_b = (1 / (n_b + 1)) * sum_{i=0..n_b} H(p_{b,i}),
+ * the mean entropy (nats) of target rows 0..n_b -- the rows whose verdicts
+ * (acceptances, then the rejection or the bonus) made this iteration's
+ * tokens -- and
+ *   K_next = clamp(K + 1, k_min, k_max)  when Hbar_b < h_lo,
+ *            clamp(K - 1, k_min, k_max)  when Hbar_b > h_hi,
+ *            clamp(K,     k_min, k_max)  otherwise (also for a NaN mean).
+ * target_entropy: B x (K+1), row i of sequence b = H(p_{b,i}); n: B (-1 marks a
+ * bad sequence, which gets K_next = -1 and a NaN mean).  The caller
+ * guarantees 0 <= k_min <= k_max and h_lo <= h_hi.
+ */
+void oracle_adaptive_k(const double *target_entropy, const int32_t *n, int B, int K, double h_lo,
+                       double h_hi, int k_min, int k_max, int32_t *out_k, double *out_hmean)
+{
+    for (int b = 0; b < B; ++b) {
+        const int nb = n[b];
+        if (nb < 0 || nb > K) {
+            out_k[b] = -1;
+            out_hmean[b] = NAN;
+            continue;
+        }
+        double sum = 0.0;
+        for (int i = 0; i <= nb; ++i)
+            sum += target_entropy[(size_t)b * (size_t)(K + 1) + (size_t)i];
+        const double hbar = sum / (double)(nb + 1);
+        int k = K;
+        if (hbar < h_lo)
+            k = K + 1;
+        else if (hbar > h_hi)
+            k = K - 1;
+        if (k < k_min)
+            k = k_min;
+        if (k > k_max)
+            k = k_max;
+        out_k[b] = k;
+        out_hmean[b] = hbar;
+    }
+}
+
+/*
  * Stochastic (temperature > 0) verification of a token tree per sequence.
  *   [P4] sec. 4 "Tree-Based Speculative Verification & Custom 2D Attention
  *   Masks" (a tree of candidates verified in one target pass, the longest

@@ -544,6 +544,69 @@ def test_row_entropy_closed_forms():
 
 
 # --------------------------------------------------------------------------
+# adaptive draft length (page 3, sec. 3 "Engineering Recommendations")
+# --------------------------------------------------------------------------
+def _khint_batch(tau=0.7):
+    """Four sequences, K = 3, V = 64, whose target row i is uniform over its
+    first M_i tokens (entropy ln M_i exactly), M = (8, 1, 64, 2):
+      0: drafts equal to the target rows, tokens inside the support: n = 3;
+      1: draft row 0 uniform over 32 tokens, token 10 has p = 0: n = 0;
+      2: position 0 drafted from the target row itself (accepted), token 5 at
+         position 1 has p = 0: n = 1;
+      3: a NaN logit in target row 2: bad."""
+    K, V = 3, 64
+    M = (8, 1, 64, 2)
+    target = torch.full((4, K + 1, V), -float("inf"))
+    for i, m in enumerate(M):
+        target[:, i, :m] = 0.0
+    draft = target[:, :K].clone()
+    tokens = torch.zeros(4, K, dtype=torch.int32)
+    draft[1, 0] = -float("inf")
+    draft[1, 0, :32] = 0.0
+    tokens[1, 0] = 10
+    tokens[2, 0] = 3
+    tokens[2, 1] = 5
+    draft[2, 1] = 0.0  # uniform over all 64: q(5) > 0 = p(5)
+    target[3, 2, 7] = float("nan")
+    return target, draft, tokens, K, M, tau
+
+
+def test_adaptive_k_closed_forms():
+    target, draft, tokens, K, M, tau = _khint_batch()
+    out = oracle.spec_verify(target, draft, tokens, tau, 5)
+    assert out["n"].tolist() == [3, 0, 1, -1]
+    h = oracle.row_entropy(target, tau)
+    ln = [math.log(m) for m in M]
+    assert np.abs(h[:3] - np.array(ln)).max() < 1e-12
+    r = oracle.adaptive_k(h, out["n"], K, 1.2, 1.9, 1, 8)
+    # mean over target rows 0..n: 2.5 ln 2, ln 8, 1.5 ln 2
+    want = [2.5 * math.log(2), 3 * math.log(2), 1.5 * math.log(2)]
+    assert np.abs(r["mean_entropy"][:3] - np.array(want)).max() < 1e-12
+    assert np.isnan(r["mean_entropy"][3])
+    # 1.73 in [1.2, 1.9]: keep; 2.08 > 1.9: lower; 1.04 < 1.2: raise; bad: -1
+    assert r["k_next"].tolist() == [3, 2, 4, -1]
+
+
+def test_adaptive_k_clamps_and_bounds():
+    target, draft, tokens, K, M, tau = _khint_batch()
+    out = oracle.spec_verify(target, draft, tokens, tau, 5)
+    h = oracle.row_entropy(target, tau)
+    assert oracle.adaptive_k(h, out["n"], K, 1.2, 1.9, 3, 3)["k_next"].tolist() == [3, 3, 3, -1]
+    assert oracle.adaptive_k(h, out["n"], K, 1.2, 1.9, 0, 2)["k_next"].tolist() == [2, 2, 2, -1]
+    assert oracle.adaptive_k(h, out["n"], K, 1.2, 1.9, 5, 9)["k_next"].tolist() == [5, 5, 5, -1]
+    # every mean below h_lo: all raised; every mean above h_hi: all lowered
+    assert oracle.adaptive_k(h, out["n"], K, 10.0, 10.0, 0, 255)["k_next"].tolist() == [4, 4, 4, -1]
+    assert oracle.adaptive_k(h, out["n"], K, -1.0, -1.0, 0, 255)["k_next"].tolist() == [2, 2, 2, -1]
+    # K = 0: only the bonus row counts
+    h0 = np.array([[0.5], [3.0]])
+    assert oracle.adaptive_k(h0, [0, 0], 0, 1.0, 2.0, 0, 4)["k_next"].tolist() == [1, 0]
+    with pytest.raises(ValueError):
+        oracle.adaptive_k(h, out["n"], K, 2.0, 1.0, 0, 8)
+    with pytest.raises(ValueError):
+        oracle.adaptive_k(h, out["n"], K, 1.0, 2.0, 5, 4)
+
+
+# --------------------------------------------------------------------------
 # stochastic tree verification (page 4, sec. 4, with the page 1 sec. 2 rule)
 # --------------------------------------------------------------------------
 def test_tree_sampling_on_a_chain_is_the_chain_verify():

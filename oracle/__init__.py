@@ -292,7 +292,8 @@ def adaptive_k(target_entropy, n_accepted, K: int, h_lo: float, h_hi: float, k_m
 def tree_verify_sampling(target, draft, tree_tokens, parent_idx, temperature: float, seed: int):
     """Stochastic verification of a token tree.  target, draft [B, N+1, V];
     tokens, parents [B, N].  Returns dict(path [B, N+1], length [B],
-    boundary [B] (1 when some draw lay within 1e-6 of its decision boundary))."""
+    boundary_at [B, N+1] (1 where a draw that decided that path entry lay
+    within 1e-6 of its decision boundary), boundary [B] (any of them))."""
     lib = _load()
     t, dt = _as_logits(target)
     d, dd = _as_logits(draft)
@@ -304,7 +305,7 @@ def tree_verify_sampling(target, draft, tree_tokens, parent_idx, temperature: fl
     N = N1 - 1
     path = np.full((B, N1), -1, dtype=np.int32)
     length = np.zeros(B, dtype=np.int32)
-    boundary = np.zeros(B, dtype=np.int32)
+    boundary = np.zeros((B, N1), dtype=np.int32)
     tok_buf = tok if tok.size else np.zeros(1, dtype=np.int32)
     par_buf = par if par.size else np.zeros(1, dtype=np.int32)
     rc = lib.oracle_tree_verify_sampling(_ptr(t), _ptr(d), dt, _ptr(tok_buf), _ptr(par_buf), B, N, V,
@@ -312,7 +313,7 @@ def tree_verify_sampling(target, draft, tree_tokens, parent_idx, temperature: fl
                                          _ptr(length), _ptr(boundary))
     if rc != 0:
         raise MemoryError("oracle_tree_verify_sampling failed to allocate")
-    return dict(path=path, length=length, boundary=boundary)
+    return dict(path=path, length=length, boundary_at=boundary, boundary=boundary.any(axis=1).astype(np.int32))
 
 
 def ngram_draft(tokens, lengths, n_min: int, n_max: int, K: int):

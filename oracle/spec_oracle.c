@@ -736,9 +736,11 @@ void oracle_adaptive_k(const double *target_entropy, const int32_t *n, int B, in
  *   at the stopping node uses (b, row of the node, 1, 0).
  * out_path: B x (N+1): accepted tokens root to leaf, then the drawn token, -1
  *   after; out_len: B, the number of entries written (depth + 1).
- * boundary (may be NULL): B, 1 when some draw of the sequence lies within 1e-6
- *   of its decision boundary (|u - min(1, P(x)/Q(x))|, or the distance of w * Z
- *   to the nearest cumulative sum relative to Z).
+ * boundary (may be NULL): B x (N+1), entry [b][j] 1 when a draw that decided
+ *   path entry j (the acceptance tests of the children of the node at depth
+ *   j, or the final draw when the walk stops there) lies within 1e-6 of its
+ *   decision boundary (|u - min(1, P(x)/Q(x))|, or the distance of w * Z to
+ *   the nearest cumulative sum relative to Z); a diagnostic only.
  * Bad data (any bad row of the sequence, a token outside [0, V), a parent not in
  * [-1, i)) gives out_len = -1 and -1 everywhere.  Returns 0, or -1 if memory
  * could not be allocated.
@@ -765,8 +767,10 @@ int oracle_tree_verify_sampling(const void *target, const void *draft, int dtype
         int32_t *path = out_path + (size_t)b * (N + 1);
         for (int j = 0; j <= N; ++j)
             path[j] = -1;
-        if (boundary)
-            boundary[b] = 0;
+        int32_t *bnd = boundary ? boundary + (size_t)b * (N + 1) : NULL;
+        if (bnd)
+            for (int j = 0; j <= N; ++j)
+                bnd[j] = 0;
         int bad = 0;
         for (int r = 0; r <= N; ++r)
             if (row_is_bad(T + r * rowb, dtype, V) || row_is_bad(D + r * rowb, dtype, V))
@@ -790,12 +794,12 @@ int oracle_tree_verify_sampling(const void *target, const void *draft, int dtype
                 const int x = tok[c];
                 const double r = oracle_uniform(seed, (uint64_t)b, (uint64_t)c, 0);
                 const int ok = P[x] >= Q[x] || r * Q[x] < P[x];
-                if (boundary && Q[x] > 0.0) {
+                if (bnd && Q[x] > 0.0) {
                     double a = P[x] / Q[x];
                     if (a > 1.0)
                         a = 1.0;
                     if (fabs(r - a) < 1e-6)
-                        boundary[b] = 1;
+                        bnd[len] = 1;
                 }
                 if (ok) {
                     accepted = c;
@@ -823,9 +827,10 @@ int oracle_tree_verify_sampling(const void *target, const void *draft, int dtype
             z += P[v];
         const double w = oracle_uniform(seed, (uint64_t)b, (uint64_t)(u + 1), 1);
         double dist;
-        path[len++] = inverse_cdf(P, V, w * z, &dist);
-        if (boundary && dist < 1e-6 * z)
-            boundary[b] = 1;
+        const int32_t drawn = inverse_cdf(P, V, w * z, &dist);
+        if (bnd && dist < 1e-6 * z)
+            bnd[len] = 1;
+        path[len++] = drawn;
         out_len[b] = len;
     }
     free(P); free(Q); free(R);

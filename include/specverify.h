@@ -64,6 +64,8 @@ extern "C" {
 #define SPEC_ERR_CUDA (-4)        /* CUDA runtime error; spec_status_string(-4) gives the message */
 #define SPEC_ERR_SCRATCH (-5)     /* spec_verify_bf16_static_scratch: the problem needs more than
                                      SPEC_STATIC_SCRATCH_BYTES of scratch */
+#define SPEC_ERR_HINT (-6)        /* spec_verify_khint_*: k_min < 0, k_max > 255, k_min > k_max,
+                                     a NaN threshold or h_lo > h_hi */
 
 /* Size of the fixed per-device scratch buffer of spec_verify_bf16_static_scratch. */
 #define SPEC_STATIC_SCRATCH_BYTES ((size_t)8 << 20)
@@ -205,6 +207,38 @@ int spec_verify_stats_bf16(const uint16_t *target_logits, const uint16_t *draft_
                            uint64_t seed, int32_t *out_tokens, int32_t *out_n_accepted,
                            float *out_row_stats, float *out_pq, float *out_resid_mass,
                            float *out_row_entropy, cudaStream_t stream);
+
+/*
+ * spec_verify_* plus a suggested draft length for each sequence's next
+ * iteration, from the same streaming pass ([P3] sec. 3 "Engineering
+ * Recommendations": a shorter draft where the target is uncertain, a longer
+ * one where it is predictable; [P2] "How much speedup to expect": the draft
+ * length trades tokens per iteration against work wasted on rejections).
+ * The pages give no formula.  Here
+ *   Hbar_b = mean over target rows i = 0..n_b of H(softmax(z_i / tau)) (nats),
+ * the rows whose verdicts made this call's tokens, and
+ *   out_k_next[b] = clamp(K + 1, k_min, k_max) if Hbar_b < h_lo,
+ *                   clamp(K - 1, k_min, k_max) if Hbar_b > h_hi,
+ *                   clamp(K,     k_min, k_max) otherwise,
+ * or -1 for a sequence flagged bad.  The mean is the fp64 sum of the rows'
+ * fp32 entropies over n_b + 1, compared in fp64.
+ *   temperature   must be > 0 (else SPEC_ERR_TEMPERATURE).
+ *   h_lo, h_hi    thresholds in nats, h_lo <= h_hi; k_min, k_max in [0, 255],
+ *                 k_min <= k_max (else SPEC_ERR_HINT).
+ *   out_k_next    [B] int32, required.
+ *   out_mean_entropy [B] float, may be NULL: Hbar_b (NaN for a bad sequence).
+ * Tokens and n_accepted are those of spec_verify_* with the same seed.
+ */
+int spec_verify_khint_f32(const float *target_logits, const float *draft_logits,
+                          const int32_t *draft_tokens, int B, int K, int V, float temperature,
+                          uint64_t seed, double h_lo, double h_hi, int k_min, int k_max,
+                          int32_t *out_tokens, int32_t *out_n_accepted, int32_t *out_k_next,
+                          float *out_mean_entropy, cudaStream_t stream);
+int spec_verify_khint_bf16(const uint16_t *target_logits, const uint16_t *draft_logits,
+                           const int32_t *draft_tokens, int B, int K, int V, float temperature,
+                           uint64_t seed, double h_lo, double h_hi, int k_min, int k_max,
+                           int32_t *out_tokens, int32_t *out_n_accepted, int32_t *out_k_next,
+                           float *out_mean_entropy, cudaStream_t stream);
 
 /*
  * Greedy verification (temperature 0) that also writes the lowest-id argmax of

@@ -10,6 +10,7 @@ library's CUDA kernels.  There is no CPU fallback.
     spec_verify_early_exit(...)       # reads only the rows the result depends on
     spec_verify_static_scratch(...)   # no allocation: a fixed per-device scratch buffer
     spec_verify_stats(...)            # plus row statistics, p(x), q(x), mass
+    spec_verify_khint(..., h_lo, h_hi, k_min, k_max)  # plus a suggested next draft length
     spec_verify_greedy_argmax(...)    # greedy chain plus every row's argmax
     spec_tree_verify_greedy(target_logits, tree_tokens, parent_idx)
     spec_tree_verify_sampling(target_logits, draft_logits, tree_tokens, parent_idx, T, seed)
@@ -25,7 +26,8 @@ from . import _lib
 from ._lib import SPEC_FLAG_BAD_DATA, SPEC_FLAG_TIMEOUT, SpecError
 
 __all__ = [
-    "spec_verify", "spec_verify_early_exit", "spec_verify_static_scratch", "spec_verify_stats", "spec_verify_greedy_argmax",
+    "spec_verify", "spec_verify_early_exit", "spec_verify_static_scratch", "spec_verify_stats", "spec_verify_khint",
+    "spec_verify_greedy_argmax",
     "spec_tree_verify_greedy", "spec_tree_verify_sampling", "spec_acceptance_stats", "spec_ngram_draft",
     "spec_get_status", "spec_test_spin_limit", "spec_test_wait_probe", "SpecError",
     "SPEC_FLAG_BAD_DATA", "SPEC_FLAG_TIMEOUT",
@@ -188,6 +190,31 @@ def spec_verify_stats(target_logits, draft_logits, draft_tokens, temperature: fl
     if entropy:
         out["row_entropy"] = ent
     return out
+
+
+def spec_verify_khint(target_logits, draft_logits, draft_tokens, temperature: float, seed: int,
+                      h_lo: float, h_hi: float, k_min: int, k_max: int, stream=None, out_tokens=None,
+                      out_n_accepted=None, out_k_next=None, out_mean_entropy=None):
+    """spec_verify plus a suggested next draft length per sequence (temperature > 0).
+
+    The mean entropy (nats) of target rows 0..n moves K one step up when below
+    h_lo, one step down when above h_hi; the result is clamped to [k_min,
+    k_max], -1 for a bad sequence.  Returns (tokens [B,K+1], n [B], k_next [B]
+    int32, mean_entropy [B] float32)."""
+    bf16, B, K, V = _chain_args(target_logits, draft_logits, draft_tokens, temperature)
+    dev = target_logits.device
+    tokens = _out(out_tokens, (B, K + 1), torch.int32, dev, "out_tokens")
+    n = _out(out_n_accepted, (B,), torch.int32, dev, "out_n_accepted")
+    k_next = _out(out_k_next, (B,), torch.int32, dev, "out_k_next")
+    hmean = _out(out_mean_entropy, (B,), torch.float32, dev, "out_mean_entropy")
+    lib = _lib.load()
+    fn = lib.spec_verify_khint_bf16 if bf16 else lib.spec_verify_khint_f32
+    with torch.cuda.device(dev):
+        _lib.check(fn(_ptr(target_logits), _ptr(draft_logits), _ptr(draft_tokens) if K > 0 else None,
+                      B, K, V, float(temperature), int(seed) & (2**64 - 1), float(h_lo), float(h_hi),
+                      int(k_min), int(k_max), _ptr(tokens), _ptr(n), _ptr(k_next), _ptr(hmean),
+                      _stream(stream)))
+    return tokens, n, k_next, hmean
 
 
 def spec_verify_greedy_argmax(target_logits, draft_tokens, stream=None):

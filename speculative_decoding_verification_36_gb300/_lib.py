@@ -21,6 +21,7 @@ SPEC_ERR_SHAPE = -2
 SPEC_ERR_TEMPERATURE = -3
 SPEC_ERR_CUDA = -4
 SPEC_ERR_SCRATCH = -5
+SPEC_ERR_HINT = -6
 SPEC_STATIC_SCRATCH_BYTES = 8 << 20
 SPEC_FLAG_BAD_DATA = 1
 SPEC_FLAG_TIMEOUT = 2
@@ -32,6 +33,7 @@ _P = ctypes.c_void_p
 _I = ctypes.c_int
 _F = ctypes.c_float
 _U64 = ctypes.c_uint64
+_D = ctypes.c_double
 
 # name -> argtypes (restype is int for all but spec_status_string)
 SIGNATURES = {
@@ -42,6 +44,8 @@ SIGNATURES = {
     "spec_verify_early_exit_bf16": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P],
     "spec_verify_stats_f32": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P, _P, _P, _P, _P],
     "spec_verify_stats_bf16": [_P, _P, _P, _I, _I, _I, _F, _U64, _P, _P, _P, _P, _P, _P, _P],
+    "spec_verify_khint_f32": [_P, _P, _P, _I, _I, _I, _F, _U64, _D, _D, _I, _I, _P, _P, _P, _P, _P],
+    "spec_verify_khint_bf16": [_P, _P, _P, _I, _I, _I, _F, _U64, _D, _D, _I, _I, _P, _P, _P, _P, _P],
     "spec_verify_greedy_argmax_f32": [_P, _P, _I, _I, _I, _P, _P, _P, _P],
     "spec_verify_greedy_argmax_bf16": [_P, _P, _I, _I, _I, _P, _P, _P, _P],
     "spec_tree_verify_greedy_f32": [_P, _P, _P, _I, _I, _I, _P, _P, _P, _P],

@@ -300,11 +300,19 @@ int greedy_impl(bool bf16, const void* target, const int32_t* tokens, int B, int
                      out_row_argmax, stream, use_static, early_exit);
 }
 
+// The draft-length suggestion's parameters and outputs (spec_verify_khint_*).
+struct KHint {
+  double h_lo, h_hi;
+  int k_min, k_max;
+  int32_t* out_k;
+  float* out_hmean;
+};
+
 int verify_impl(bool bf16, const void* target, const void* draft, const int32_t* tokens, int B,
                 int K, int V, float temperature, uint64_t seed, int32_t* out_tokens, int32_t* out_n,
                 float* out_row_stats, float* out_pq, float* out_resid, float* out_entropy,
                 cudaStream_t stream,
-                bool use_static = false, bool early_exit = false) {
+                bool use_static = false, bool early_exit = false, const KHint* kh = nullptr) {
   if (!(temperature >= 0.f) || (temperature > 0.f && temperature < 1e-30f))
     return SPEC_ERR_TEMPERATURE;
   if (temperature == 0.f)
@@ -401,9 +409,17 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.out_pq = out_pq;
   a.out_resid = out_resid;
   a.out_entropy = out_entropy;
+  if (kh) {
+    a.out_khint = kh->out_k;
+    a.out_hmean = kh->out_hmean;
+    a.h_lo = kh->h_lo;
+    a.h_hi = kh->h_hi;
+    a.k_min = kh->k_min;
+    a.k_max = kh->k_max;
+  }
   a.status = d->status;
   void* ws = nullptr;
-  rc = get_scratch(d, use_static, sv::sample_workspace(B, K, a.CS, a.TC, a.P, out_entropy != nullptr),
+  rc = get_scratch(d, use_static, sv::sample_workspace(B, K, a.CS, a.TC, a.P, out_entropy != nullptr || kh != nullptr),
                    stream, &ws);
   if (rc) return rc;
   sv::sample_bind_workspace(a, ws);
@@ -543,6 +559,36 @@ int spec_verify_stats_f32(const float* target_logits, const float* draft_logits,
   return verify_impl(false, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed,
                      out_tokens, out_n_accepted, out_row_stats, out_pq, out_resid_mass,
                      out_row_entropy, stream);
+}
+
+static int khint_impl(bool bf16, const void* target, const void* draft, const int32_t* tokens, int B,
+                      int K, int V, float temperature, uint64_t seed, double h_lo, double h_hi,
+                      int k_min, int k_max, int32_t* out_tokens, int32_t* out_n, int32_t* out_k,
+                      float* out_hmean, cudaStream_t stream) {
+  if (!(temperature > 0.f)) return SPEC_ERR_TEMPERATURE;  // the entropies need tau > 0
+  if (!out_k) return SPEC_ERR_NULL;
+  if (k_min < 0 || k_max > sv::kMaxK || k_min > k_max || !(h_lo <= h_hi)) return SPEC_ERR_HINT;
+  const KHint kh = {h_lo, h_hi, k_min, k_max, out_k, out_hmean};
+  return verify_impl(bf16, target, draft, tokens, B, K, V, temperature, seed, out_tokens, out_n,
+                     nullptr, nullptr, nullptr, nullptr, stream, false, false, &kh);
+}
+
+int spec_verify_khint_f32(const float* target_logits, const float* draft_logits,
+                          const int32_t* draft_tokens, int B, int K, int V, float temperature,
+                          uint64_t seed, double h_lo, double h_hi, int k_min, int k_max,
+                          int32_t* out_tokens, int32_t* out_n_accepted, int32_t* out_k_next,
+                          float* out_mean_entropy, cudaStream_t stream) {
+  return khint_impl(false, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed, h_lo,
+                    h_hi, k_min, k_max, out_tokens, out_n_accepted, out_k_next, out_mean_entropy, stream);
+}
+
+int spec_verify_khint_bf16(const uint16_t* target_logits, const uint16_t* draft_logits,
+                           const int32_t* draft_tokens, int B, int K, int V, float temperature,
+                           uint64_t seed, double h_lo, double h_hi, int k_min, int k_max,
+                           int32_t* out_tokens, int32_t* out_n_accepted, int32_t* out_k_next,
+                           float* out_mean_entropy, cudaStream_t stream) {
+  return khint_impl(true, target_logits, draft_logits, draft_tokens, B, K, V, temperature, seed, h_lo,
+                    h_hi, k_min, k_max, out_tokens, out_n_accepted, out_k_next, out_mean_entropy, stream);
 }
 
 int spec_verify_stats_bf16(const uint16_t* target_logits, const uint16_t* draft_logits,
@@ -729,6 +775,8 @@ const char* spec_status_string(int code) {
       return "bad temperature: NaN, negative, or in (0, 1e-30)";
     case SPEC_ERR_CUDA:
       return g_cuda_msg;
+    case SPEC_ERR_HINT:
+      return "bad draft-length parameters: need 0 <= k_min <= k_max <= 255 and h_lo <= h_hi (no NaN)";
     case SPEC_ERR_SCRATCH:
       return "the problem needs more scratch than the static buffer holds "
              "(SPEC_STATIC_SCRATCH_BYTES)";

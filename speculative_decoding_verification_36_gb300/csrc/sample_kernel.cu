@@ -172,7 +172,29 @@ __device__ __forceinline__ int resolve_position(const SampleArgs& a, int b, int 
   return ticket_take(a.posticket + b) == a.K ? a.K + 1 : -1;  // K + 1: scan the verdicts
 }
 
-// Commit (one warp): writes out_tokens, out_n and out_resid.  A sequence's
+// The suggested next draft length of sequence b, decided at n (one warp): the
+// mean entropy of target rows 0..n (fp64 sum of the stored fp32 values)
+// against the two thresholds, one step from K, clamped to [k_min, k_max].
+__device__ __noinline__ void commit_khint(const SampleArgs& a, int b, int n) {
+  const int lane = threadIdx.x & 31;
+  const float* h = a.hrow + (size_t)b * (a.K + 1);
+  double sum = 0.0;
+  for (int i = lane; i <= n; i += 32) sum += (double)wait_f32(h + i, a.status);
+  sum = warp_sum_f64(sum);
+  if (lane == 0) {
+    const double hbar = sum / (double)(n + 1);
+    int k = a.K;
+    if (hbar < a.h_lo)
+      k = a.K + 1;
+    else if (hbar > a.h_hi)
+      k = a.K - 1;
+    a.out_khint[b] = max(a.k_min, min(a.k_max, k));
+    if (a.out_hmean) a.out_hmean[b] = (float)hbar;
+  }
+}
+
+// Commit (one warp): writes out_tokens, out_n and out_resid (and the draft
+// length suggestion when asked for).  A sequence's
 // commit count gathers K + 2 arrivals: one per position unit (with kUnitBad
 // added when the unit saw bad data) and one for the result (the drawn token,
 // or a bad decision).  Whichever arrives last commits, with the bad-data
@@ -193,6 +215,8 @@ __device__ __noinline__ void commit_sequence(const SampleArgs& a, int b, bool ro
       a.out_n[b] = -1;
       atomicOr(a.status, kStatusBadData);
       if (a.out_resid) a.out_resid[b] = NAN;
+      if (a.out_khint) a.out_khint[b] = -1;
+      if (a.out_hmean) a.out_hmean[b] = NAN;
     }
   } else {
     const int n = (int)res.x;
@@ -202,6 +226,7 @@ __device__ __noinline__ void commit_sequence(const SampleArgs& a, int b, bool ro
       a.out_n[b] = n;
       if (a.out_resid) a.out_resid[b] = __uint_as_float(res.z);
     }
+    if (a.out_khint) commit_khint(a, b, n);
   }
   __syncwarp();
 }
@@ -320,7 +345,14 @@ __device__ __forceinline__ void store_row(const SampleArgs& a, int b, int r, flo
     a.out_row_stats[k * 2 + 1] = s;
   }
   // nats: ln s - ln 2 * t / s (NaN for a row without mass or with NaN)
-  if constexpr (ENT) a.out_entropy[k] = (float)(log((double)s) - 0.69314718055994530942 * (double)t / (double)s);
+  if constexpr (ENT) {
+    const float h = (float)(log((double)s) - 0.69314718055994530942 * (double)t / (double)s);
+    if (a.out_entropy) a.out_entropy[k] = h;
+    // the target rows' entropies for the committing warp (a NaN never takes
+    // the marker's bit pattern)
+    if (a.out_khint && r <= a.K)
+      st_relaxed_f32(a.hrow + (size_t)b * (a.K + 1) + r, __float_as_uint(h) == kMarker ? NAN : h);
+  }
 }
 
 // Unit finisher (one warp): position i of sequence b.
@@ -885,8 +917,8 @@ static size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 // Workspace: [counters, tickets, resolution words, queue count (all start at
 // all-ones)][marker-filled result slots: part, rowstat, tailsum, queue,
-// pieces, zx, verdict, result, and part_t when the entropy is asked
-// for]; one 0xff fill initialises both parts.
+// pieces, zx, verdict, result, and part_t and hrow when the entropy is
+// asked for]; one 0xff fill initialises both parts.
 static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t* off) {
   const int R = 2 * K + 1;
   size_t o = 0;
@@ -911,6 +943,7 @@ static void sample_layout(int B, int K, int CS, int TC, int P, bool ent, size_t*
   off[20] = o; o += align_up((size_t)B * sizeof(uint4), 256);               // result
   off[21] = o; o += align_up((size_t)B * 4, 256);                           // decided
   off[14] = o; if (ent) o += align_up((size_t)B * R * CS * sizeof(float), 256);  // part_t
+  off[16] = o; if (ent) o += align_up((size_t)B * (K + 1) * sizeof(float), 256);  // hrow
   off[9] = o;                                                                // end of marker region
   off[12] = o;
 }
@@ -928,7 +961,8 @@ WsLayout sample_workspace(int B, int K, int CS, int TC, int P, bool ent) {
 
 void sample_bind_workspace(SampleArgs& a, void* ws) {
   size_t off[24];
-  sample_layout(a.B, a.K, a.CS, a.TC, a.P, a.out_entropy != nullptr, off);
+  const bool ent = a.out_entropy != nullptr || a.out_khint != nullptr;
+  sample_layout(a.B, a.K, a.CS, a.TC, a.P, ent, off);
   char* p = (char*)ws;
   a.counter = (unsigned long long*)(p + off[0]);
   a.unitticket = (int*)(p + off[1]);
@@ -948,12 +982,13 @@ void sample_bind_workspace(SampleArgs& a, void* ws) {
   a.verdict = (int*)(p + off[18]);
   a.result = (uint4*)(p + off[20]);
   a.decided = (int*)(p + off[21]);
-  a.part_t = a.out_entropy ? (float*)(p + off[14]) : nullptr;
+  a.part_t = ent ? (float*)(p + off[14]) : nullptr;
+  a.hrow = a.out_khint ? (float*)(p + off[16]) : nullptr;
 }
 
 template <class E, int VEC>
 static cudaError_t launch_sample_t(const SampleArgs& a, int grid, cudaStream_t s) {
-  if (a.out_entropy)
+  if (a.out_entropy || a.out_khint)
     sample_kernel<E, VEC, true><<<grid, kThreads, 0, s>>>(a);
   else
     sample_kernel<E, VEC, false><<<grid, kThreads, 0, s>>>(a);

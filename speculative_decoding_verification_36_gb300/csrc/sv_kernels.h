@@ -105,6 +105,13 @@ struct SampleArgs {
   float* out_pq;         // optional [B, K, 2]: p_i(x_i), q_i(x_i)
   float* out_resid;      // optional [B]: mass of the replacement distribution
   float* out_entropy;    // optional [B, R]: entropy (nats) of each row's softmax
+  // optional suggested next draft length: K moved one step up when the mean
+  // entropy of target rows 0..n is below h_lo, down when above h_hi, then
+  // clamped to [k_min, k_max]; -1 for a bad sequence
+  int32_t* out_khint;    // [B]
+  float* out_hmean;      // optional [B]: that mean entropy (nats)
+  double h_lo, h_hi;
+  int k_min, k_max;
   // workspace, filled with all-ones bytes before the launch: the counters and
   // tickets (counter, unitticket, seqticket, posticket, tailticket, qcount,
   // dclaim, ctaticket) then start at -1, the resolution words at the empty
@@ -126,7 +133,8 @@ struct SampleArgs {
   float2* part;     // [B, R, CS] per-slice (m, s)
   float2* rowstat;  // [B, R] merged (m, s) of each row
   float* zx;        // [B, R] logit at the drafted token, written by the slice holding it
-  float* part_t;    // [B, R, CS] per-slice entropy accumulator (only with out_entropy)
+  float* part_t;    // [B, R, CS] per-slice entropy accumulator (with out_entropy or out_khint)
+  float* hrow;      // [B, K+1] entropy of each target row (only with out_khint)
   float* tailsum;   // [B, TC] per tail-slice mass
   SeqInfo* queue;   // [B] decisions in the order they were made
   float* pieces;    // [B, TC, P] per-piece mass

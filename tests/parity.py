@@ -43,3 +43,51 @@ def rel_err(a, b):
     a = np.asarray(a, dtype=np.float64)
     b = np.asarray(b, dtype=np.float64)
     return np.abs(a - b) / np.maximum(np.abs(b), 1e-300)
+
+
+def oracle_chain_threads(target, draft, tokens, temperature, seed, threads=None, **kw):
+    """oracle.spec_verify over a whole batch, split into chunks that run on
+    host threads (the oracle's C code runs without the GIL).  Each chunk
+    passes its batch indices as sequence numbers, so the result is that of
+    one call over the whole batch.  Inputs may live on any device."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    target, draft, tokens = target.cpu(), draft.cpu(), tokens.cpu()
+    B = target.shape[0]
+    threads = threads or min(16, os.cpu_count() or 1)
+    bounds = np.linspace(0, B, min(B, 4 * threads) + 1).astype(int)
+    chunks = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+
+    def one(c):
+        a, b = c
+        return oracle.spec_verify(target[a:b], draft[a:b], tokens[a:b], temperature, seed,
+                                  seq_ids=np.arange(a, b), **kw)
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(one, chunks))
+    return {k: np.concatenate([p[k] for p in parts]) for k in parts[0]}
+
+
+def oracle_greedy_threads(target, tokens, threads=None, **kw):
+    """oracle.spec_verify_greedy over a whole batch on host threads."""
+    import os
+    from concurrent.futures import ThreadPoolExecutor
+
+    import oracle
+
+    target, tokens = target.cpu(), tokens.cpu()
+    B = target.shape[0]
+    threads = threads or min(16, os.cpu_count() or 1)
+    bounds = np.linspace(0, B, min(B, 4 * threads) + 1).astype(int)
+    chunks = [(int(a), int(b)) for a, b in zip(bounds[:-1], bounds[1:]) if b > a]
+
+    def one(c):
+        a, b = c
+        return oracle.spec_verify_greedy(target[a:b], tokens[a:b], **kw)
+
+    with ThreadPoolExecutor(threads) as ex:
+        parts = list(ex.map(one, chunks))
+    return {k: np.concatenate([p[k] for p in parts]) for k in parts[0]}

@@ -222,14 +222,19 @@ def host_threads() -> int:
 def oracle_parallel_seq_per_s(x_cpu, p, budget_s: float, threads: int):
     """The same oracle, one sequence per call, on `threads` host threads at
     once (the C oracle holds no global state, and ctypes releases the GIL
-    during the call)."""
+    during the call), cycling over the batch until the time budget is used
+    and at least once over the whole batch.  Also returns the oracle's result
+    for every sequence of the batch (seed 0, its batch index as sequence
+    number), for the parity check of the bench line."""
     from concurrent.futures import ThreadPoolExecutor
     import oracle
     oracle.build()
+    results = {}
 
     def one(b):
-        oracle.spec_verify(x_cpu["target"][b:b + 1], x_cpu["draft"][b:b + 1], x_cpu["tokens"][b:b + 1],
-                           p.temperature, 0, seq_ids=[b])
+        r = oracle.spec_verify(x_cpu["target"][b:b + 1], x_cpu["draft"][b:b + 1], x_cpu["tokens"][b:b + 1],
+                               p.temperature, 0, seq_ids=[b])
+        results.setdefault(b, r)
 
     done = 0
     with ThreadPoolExecutor(max_workers=threads) as ex:
@@ -237,10 +242,29 @@ def oracle_parallel_seq_per_s(x_cpu, p, budget_s: float, threads: int):
         while True:
             list(ex.map(one, [(done + t) % p.B for t in range(threads)]))
             done += threads
-            if time.perf_counter() - t0 > budget_s:
+            if time.perf_counter() - t0 > budget_s and done >= p.B:
                 break
         dt = time.perf_counter() - t0
-    return done / dt, done, dt
+    return done / dt, done, dt, results
+
+
+def cpu_model() -> str:
+    """The host CPU's model name (lscpu, else /proc/cpuinfo, else platform)."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        for line in open("/proc/cpuinfo"):
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
 
 
 def parity_sample(gpu_tokens, gpu_n, first):
@@ -338,8 +362,17 @@ def run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps):
     serving process would place them."""
     import torch
     local = gpu_local_cpus(dev)
+    saved = os.sched_getaffinity(0)
     if local:
         os.sched_setaffinity(0, local)
+    try:
+        return _run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps, local)
+    finally:
+        os.sched_setaffinity(0, saved)
+
+
+def _run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps, local):
+    import torch
     host = [{k: sets[i][k].cpu().pin_memory() for k in ("target", "draft", "tokens")}
             for i in range(len(sets))]
     host_out = (torch.empty((p.B, p.K + 1), dtype=torch.int32).pin_memory(),
@@ -371,6 +404,182 @@ def run_e2e(sv, sets, p, rank, world, dev, stream, e2e_steps):
     e2e_ms = max_over_ranks(e0.elapsed_time(e1), world)
     e2e_value = world * p.B * e2e_steps / (e2e_ms / 1e3)
     return e2e_value, h2d, d2h, (len(local) if local else None)
+
+
+# --------------------------------------------------------------------------
+# the other workloads and entry points, reported beside the headline
+# --------------------------------------------------------------------------
+def time_calls(call, steps, warm, stream, dev, flush=None):
+    """Average device milliseconds per call: CUDA events on `stream` around
+    each call, after `warm` untimed calls; `flush()` runs (untimed) before
+    every timed call when given."""
+    import torch
+    for i in range(warm):
+        call(i)
+    torch.cuda.synchronize(dev)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    for i in range(steps):
+        if flush is not None:
+            flush()
+        ev[i][0].record(stream)
+        call(i)
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    return sum(a.elapsed_time(b) for a, b in ev) / steps
+
+
+def chain_rows_used(n, K):
+    """Rows an early-exit verify depends on: target and draft rows 0..n, or
+    all 2K + 1 rows when every draft is accepted (n = K)."""
+    return sum(2 * K + 1 if int(v) >= K else 2 * (int(v) + 1) for v in n)
+
+
+def extra_entry(ms, seqs, nbytes, peak, steps, l2, **more):
+    gbs = nbytes / (ms / 1e3) / 1e9
+    d = {"value": seqs / (ms / 1e3), "unit": "seq/s", "us_per_call": ms * 1e3, "bytes_per_step": int(nbytes),
+         "achieved_gbs": gbs, "frac": gbs / peak, "steps": steps, "l2": l2}
+    d.update(more)
+    return d
+
+
+def run_extras(sv, wl, dev, stream, steps, peak):
+    """CUDA-event timings, bytes per call and the fraction of the measured HBM
+    bandwidth for every workload and entry point besides the headline: c1,
+    c2 and c4 (full read and early exit), the c3 early exit, the c3 verify
+    with row entropies or with the draft-length suggestion, the c5 tree
+    (greedy, its early exit, and stochastic), and n-gram drafting."""
+    import torch
+    out = {}
+    flushbuf = torch.empty(128 * 2**20, dtype=torch.float32, device=dev)  # 512 MB, read to evict L2
+    flushbuf.fill_(1.0)
+
+    def flush():
+        flushbuf.sum()
+
+    def big(nbytes):
+        return nbytes >= 2 * L2_BYTES
+
+    def l2_note(nbytes, sets):
+        if big(nbytes):
+            return f"inputs larger than L2 ({nbytes / 1e6:.0f} MB per call), {sets} input sets alternate"
+        return f"L2 flushed before every call ({nbytes / 1e6:.1f} MB per call)"
+
+    def chain(name, early=False):
+        p = wl.preset(name)
+        sets = [wl.make_chain(p, device=dev, seed=10 + i) for i in range(2)]
+        esz = 4 if p.dtype == torch.float32 else 2
+        rows = 2 * p.K + 1 if p.temperature > 0 else p.K + 1
+        full = p.B * rows * p.V * esz
+        fn = sv.spec_verify_early_exit if early else sv.spec_verify
+
+        def call(i):
+            x = sets[i % 2]
+            fn(x["target"], x["draft"], x["tokens"], p.temperature, i, stream=stream)
+
+        ms = time_calls(call, steps, 3, stream, dev, None if big(full) else flush)
+        if early:
+            x = sets[0]
+            _, n = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 0, stream=stream)
+            K = p.K
+            used = chain_rows_used(n.cpu().tolist(), K) if p.temperature > 0 else \
+                sum(int(v) + 1 for v in n.cpu().tolist())
+            nbytes = used * p.V * esz
+            e = extra_entry(ms, p.B, nbytes, peak, steps, l2_note(full, 2),
+                            bytes_note="rows the result depends on (input set 0, seed 0)")
+        else:
+            e = extra_entry(ms, p.B, full, peak, steps, l2_note(full, 2))
+        e["config"] = f"B={p.B} K={p.K} V={p.V} {str(p.dtype).split('.')[-1]} tau={p.temperature}"
+        del sets
+        return e
+
+    out["c1"] = chain("c1")
+    out["c2"] = chain("c2")
+    out["c2_early_exit"] = chain("c2", early=True)
+    out["c3_early_exit"] = chain("c3", early=True)
+    out["c4"] = chain("c4")
+    out["c4_early_exit"] = chain("c4", early=True)
+
+    # c3 with the entropy pass: row entropies, and the draft-length suggestion
+    p = wl.preset("c3")
+    sets = [wl.make_chain(p, device=dev, seed=20 + i) for i in range(2)]
+    full = p.B * (2 * p.K + 1) * p.V * 2
+
+    def plain(i):
+        x = sets[i % 2]
+        sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, i, stream=stream)
+
+    def khint(i):
+        x = sets[i % 2]
+        sv.spec_verify_khint(x["target"], x["draft"], x["tokens"], p.temperature, i, 1.0, 2.0, 1, 16,
+                             stream=stream)
+
+    def stats(i):
+        x = sets[i % 2]
+        sv.spec_verify_stats(x["target"], x["draft"], x["tokens"], p.temperature, i, stream=stream,
+                             entropy=True)
+
+    ms_plain = time_calls(plain, steps, 3, stream, dev)
+    ms_k = time_calls(khint, steps, 3, stream, dev)
+    ms_s = time_calls(stats, steps, 3, stream, dev)
+    out["c3_khint"] = extra_entry(ms_k, p.B, full, peak, steps, l2_note(full, 2),
+                                  entry_point="spec_verify_khint_bf16",
+                                  cost_vs_spec_verify_pct=100.0 * (ms_k / ms_plain - 1.0),
+                                  spec_verify_us_same_run=ms_plain * 1e3)
+    out["c3_stats_entropy"] = extra_entry(ms_s, p.B, full, peak, steps, l2_note(full, 2),
+                                          entry_point="spec_verify_stats_bf16 (row stats, p/q, residual "
+                                                      "mass and row entropies)",
+                                          cost_vs_spec_verify_pct=100.0 * (ms_s / ms_plain - 1.0))
+    del sets
+
+    # c5: tree greedy (full read and early exit) and stochastic tree
+    p = wl.preset("c5")
+    trees = [wl.make_tree(p, device=dev, seed=30 + i) for i in range(2)]
+    full = p.B * (p.N + 1) * p.V * 2
+    for early in (False, True):
+        def tcall(i, early=early):
+            x = trees[i % 2]
+            sv.spec_tree_verify_greedy(x["target"], x["tokens"], x["parents"], stream=stream, early_exit=early)
+
+        ms = time_calls(tcall, steps, 3, stream, dev, None if big(full) else flush)
+        if early:
+            x = trees[0]
+            _, ln, _ = sv.spec_tree_verify_greedy(x["target"], x["tokens"], x["parents"], stream=stream)
+            nbytes = sum(int(v) for v in ln.cpu().tolist()) * p.V * 2
+            out["c5_early_exit"] = extra_entry(ms, p.B, nbytes, peak, steps, l2_note(full, 2),
+                                               bytes_note="rows on the accepted path (input set 0)")
+        else:
+            out["c5"] = extra_entry(ms, p.B, full, peak, steps, l2_note(full, 2),
+                                    config=f"B={p.B} N={p.N} V={p.V} bf16, complete binary tree depth {p.depth}")
+    del trees
+    trees = [wl.make_tree_sampling(p, 1.0, device=dev, seed=40 + i) for i in range(2)]
+    full_s = 2 * p.B * (p.N + 1) * p.V * 2
+
+    def scall(i):
+        x = trees[i % 2]
+        sv.spec_tree_verify_sampling(x["target"], x["draft"], x["tokens"], x["parents"], 1.0, i, stream=stream)
+
+    ms = time_calls(scall, steps, 3, stream, dev, None if big(full_s) else flush)
+    out["c5_stochastic_tree"] = extra_entry(ms, p.B, full_s, peak, steps, l2_note(full_s, 2),
+                                            config=f"B={p.B} N={p.N} V={p.V} bf16 target and draft, tau 1")
+    del trees
+
+    # n-gram drafting: 256 histories of up to 131072 tokens (16 seeded
+    # histories repeated), n 1..4, K = 8
+    h = wl.make_ngram_histories(16, 131072, seed=1)
+    tok = h["tokens"].repeat(16, 1).contiguous().to(dev)
+    ln = h["lengths"].repeat(16).contiguous().to(dev)
+    nbytes = int(ln.sum().item()) * 4
+
+    def ncall(i):
+        sv.spec_ngram_draft(tok, ln, 1, 4, 8, stream=stream)
+
+    ms = time_calls(ncall, steps, 3, stream, dev, flush)
+    out["ngram"] = extra_entry(ms, 256, nbytes, peak, steps, l2_note(nbytes, 1),
+                               config="B=256 histories up to 131072 tokens, n 1..4, K=8")
+    out["ngram"]["unit"] = "histories/s"
+    del tok, ln, flushbuf
+    torch.cuda.synchronize(dev)
+    return out
 
 
 def run_gpu(args):
@@ -456,6 +665,27 @@ def run_gpu(args):
         barrier(world)
         ee_ms = max_over_ranks(a0.elapsed_time(a1), world) / args.early_exit_steps
 
+    # the oracle on the host cores, before the end-to-end leg binds the
+    # process to the GPU's socket (rank 0 at N = 1 only), and the parity of
+    # the whole batch of input set 0 (seed 0) against it
+    cpu_line = parity = None
+    if world == 1 and not args.no_cpu_baseline:
+        threads = host_threads()
+        x_cpu = {k: sets[0][k].cpu() for k in ("target", "draft", "tokens")}
+        v, done, dt, _ = oracle_seq_per_s(x_cpu, p, args.cpu_budget, 1 << 30)
+        vp, donep, dtp, results = oracle_parallel_seq_per_s(x_cpu, p, args.cpu_budget, threads)
+        cpu_line = {"value": vp, "unit": UNIT, "cores": threads, "kind": "oracle",
+                    "sample": f"{donep} c3 sequences (cycling over the batch of {p.B}) in {dtp:.1f} s, "
+                              f"fp64 C oracle, one sequence per call on {threads} host threads",
+                    "single_thread": {"value": v, "sample": f"{done} sequences in {dt:.1f} s"},
+                    "cpu_model": cpu_model(), "os_cpu_count": os.cpu_count(),
+                    "affinity_cpus": threads}
+        x = sets[0]
+        tok0, n0 = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 0, stream=stream)
+        torch.cuda.synchronize(dev)
+        parity = parity_sample(tok0.cpu().numpy(), n0.cpu().numpy(), results)
+        del x_cpu
+
     # end to end through the public API from pinned host buffers
     e2e_steps = min(args.steps, args.e2e_steps)
     e2e_value, h2d, d2h, e2e_cpus = None, 0, 0, None
@@ -497,23 +727,12 @@ def run_gpu(args):
         "clocks": clk.summary(),
         "status_flags": flags,
     }
-    if world == 1 and not args.no_cpu_baseline:
-        x_cpu = {k: sets[0][k][:64].cpu() for k in ("target", "draft", "tokens")}
-        pp = wl.preset(WORKLOAD, B=64)
-        v, done, dt, first = oracle_seq_per_s(x_cpu, pp, args.cpu_budget, 1 << 30)
-        threads = host_threads()
-        vp, donep, dtp = oracle_parallel_seq_per_s(x_cpu, pp, args.cpu_budget, threads)
-        line["cpu_baseline"] = {"value": vp, "unit": UNIT, "cores": threads, "kind": "oracle",
-                                "sample": f"{donep} c3 sequences (cycling over the first 64 of the batch) "
-                                          f"in {dtp:.1f} s, fp64 C oracle, one sequence per call on "
-                                          f"{threads} host threads",
-                                "single_thread": {"value": v, "sample": f"{done} sequences in {dt:.1f} s"}}
-        # the verify of input set 0 with seed 0, checked against the oracle
-        # on the sequences above
-        x = sets[0]
-        tok0, n0 = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 0, stream=stream)
-        torch.cuda.synchronize(dev)
-        line["parity_sample"] = parity_sample(tok0.cpu().numpy(), n0.cpu().numpy(), first)
+    if cpu_line is not None:
+        line["cpu_baseline"] = cpu_line
+        line["parity_sample"] = parity
+    if world == 1 and args.extras_steps > 0:
+        line["extra"] = run_extras(sv, wl, dev, stream, args.extras_steps, peak)
+        line["extra_status_flags"] = sv.spec_get_status()
     if world == 1:
         # acceptance statistics of one batch (spec_acceptance_stats on the GPU)
         x = sets[0]
@@ -547,6 +766,8 @@ def main(argv=None):
     ap.add_argument("--sets", type=int, default=2, choices=[1, 2],
                     help="input sets alternated between steps")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--extras-steps", type=int, default=100,
+                    help="timed calls per extra workload (c1, c2, c4, c5, early exits, ...); 0 skips them")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args(argv)
     if args.impl == "reference":

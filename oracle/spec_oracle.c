@@ -35,12 +35,15 @@
  *   - p = softmax(z_target / tau), q = softmax(z_draft / tau), the same tau for
  *     both; tau == 0 selects greedy verification.
  *   - accept iff p(x) >= q(x) or u * q(x) < p(x)   (strict "<"; [P1] writes
- *     "u <= alpha", which differs only on a set of measure zero).
+ *     "u <= alpha"; with u on a grid of 2^-52 the two differ with
+ *     probability at most 2^-52 per draw).
  *   - uniforms come from Philox-4x64-10 with key (seed, 0x5350454356455249)
  *     and counter (sequence b, position, stream, 0); stream 0 is the
  *     acceptance draw, stream 1 the resampling draw.  The first output word r
- *     maps to u = (2 * (r >> 41) + 1) * 2^-24, an odd multiple of 2^-24 in
- *     (0, 1).
+ *     maps to u = (2 * (r >> 12) + 1) * 2^-53, an odd multiple of 2^-53 in
+ *     (0, 1), exact in fp64: the 52 top bits of r, so that a token of
+ *     probability p is drawn with probability p to within 2^-52 (the method
+ *     draws u from U(0, 1): [P1] sec. 2, [P2] "The correctness guarantee").
  *   - the replacement / bonus token is drawn by inverse CDF in vocabulary
  *     order: the smallest j with C_j > w * Z, C_j = sum_{v <= j} r(v).
  *   - greedy ties go to the lowest token id.
@@ -105,8 +108,8 @@ double oracle_uniform(uint64_t seed, uint64_t b, uint64_t position, uint64_t str
     const uint64_t ctr[4] = {b, position, stream, 0};
     uint64_t out[4];
     oracle_philox4x64_10(ctr, key, out);
-    uint64_t top23 = out[0] >> 41;
-    return (double)(2 * top23 + 1) * ldexp(1.0, -24);
+    const uint64_t top52 = out[0] >> 12;
+    return (double)(2 * top52 + 1) * ldexp(1.0, -53);
 }
 
 /* ------------------------------------------------------------------------ */

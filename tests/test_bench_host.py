@@ -80,3 +80,15 @@ def test_stored_traffic_is_tied_to_the_sources(tmp_path, monkeypatch):
     assert bench.stored_traffic() == 12345.0
     f.write_text("source_sha256: 0000\ndram_bytes_per_launch: 12345\n")
     assert bench.stored_traffic() is None
+
+
+def test_rows_an_early_exit_depends_on():
+    # n < K: target and draft rows 0..n; n = K: all 2K + 1 rows
+    assert bench.chain_rows_used([0, 8, 3], 8) == 2 + 17 + 8
+
+
+def test_oracle_rates_reports_both_legs():
+    calls = []
+    r = bench.oracle_rates(lambda b: calls.append(b), 5, 0.01, 2)
+    assert r["single_thread"] > 0 and r["all_cores"] > 0 and r["cores"] == 2
+    assert set(calls) <= set(range(5))

@@ -59,10 +59,19 @@ def test_uniform_uses_counter_layout_and_is_odd_multiple():
     for seed, b, pos, stream in [(0, 0, 0, 0), (7, 3, 2, 1), (2**40 + 5, 255, 7, 0)]:
         u = oracle.uniform(seed, b, pos, stream)
         r0 = int(_numpy_block([b, pos, stream, 0], [seed, key_hi])[0])
-        k = u * 2**24
+        k = u * 2**53
         assert k == int(k) and int(k) % 2 == 1
-        assert int(k) // 2 == r0 >> 41
+        assert int(k) // 2 == r0 >> 12
         assert 0.0 < u < 1.0
+
+
+def test_uniform_has_52_random_bits():
+    """u resolves probabilities far below the 2^-23 grid of a float draw: over
+    many draws its low bits (below 2^-24) are spread evenly."""
+    us = np.array([oracle.uniform(3, b, 1, 1) for b in range(4096)])
+    low = np.array([(int(u * 2**53) >> 1) & 0xFFFFFFF for u in us])  # bits 2^-52 .. 2^-25
+    assert len(np.unique(low)) > 4000
+    assert abs(low.mean() / 2**28 - 0.5) < 0.05
 
 
 def test_uniform_distribution_ks():

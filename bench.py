@@ -442,7 +442,33 @@ def extra_entry(ms, seqs, nbytes, peak, steps, l2, **more):
     return d
 
 
-def run_extras(sv, wl, dev, stream, steps, peak):
+def oracle_rates(one, B, budget_s, threads):
+    """The oracle on this host's cores for one extra workload: `one(b)` runs
+    it on item b of the batch; single-threaded, then on `threads` host
+    threads at once (ctypes releases the GIL), each for about budget_s.
+    Returns items per second for both."""
+    from concurrent.futures import ThreadPoolExecutor
+    done, t0 = 0, time.perf_counter()
+    while True:
+        one(done % B)
+        done += 1
+        if time.perf_counter() - t0 > budget_s:
+            break
+    single = done / (time.perf_counter() - t0)
+    done = 0
+    with ThreadPoolExecutor(max_workers=threads) as ex:
+        t0 = time.perf_counter()
+        while True:
+            list(ex.map(one, [(done + t) % B for t in range(threads)]))
+            done += threads
+            if time.perf_counter() - t0 > budget_s:
+                break
+        multi = done / (time.perf_counter() - t0)
+    return {"single_thread": single, "all_cores": multi, "cores": threads, "kind": "oracle",
+            "budget_s_each": budget_s}
+
+
+def run_extras(sv, wl, dev, stream, steps, peak, cpu_budget=0.0):
     """CUDA-event timings, bytes per call and the fraction of the measured HBM
     bandwidth for every workload and entry point besides the headline: c1,
     c2 and c4 (full read and early exit), the c3 early exit, the c3 verify
@@ -489,6 +515,20 @@ def run_extras(sv, wl, dev, stream, steps, peak):
         else:
             e = extra_entry(ms, p.B, full, peak, steps, l2_note(full, 2))
         e["config"] = f"B={p.B} K={p.K} V={p.V} {str(p.dtype).split('.')[-1]} tau={p.temperature}"
+        if cpu_budget > 0 and not early:
+            import oracle
+            oracle.build()
+            xc = {k: (v.cpu() if v is not None else None) for k, v in sets[0].items() if k in ("target", "draft", "tokens")}
+            if p.temperature > 0:
+                def one(b):
+                    oracle.spec_verify(xc["target"][b:b + 1], xc["draft"][b:b + 1], xc["tokens"][b:b + 1],
+                                       p.temperature, 0, seq_ids=[b])
+            else:
+                def one(b):
+                    oracle.spec_verify_greedy(xc["target"][b:b + 1], xc["tokens"][b:b + 1])
+            e["cpu_oracle"] = oracle_rates(one, p.B, cpu_budget, host_threads())
+            e["cpu_oracle"]["unit"] = "seq/s"
+            del xc
         del sets
         return e
 
@@ -550,6 +590,15 @@ def run_extras(sv, wl, dev, stream, steps, peak):
         else:
             out["c5"] = extra_entry(ms, p.B, full, peak, steps, l2_note(full, 2),
                                     config=f"B={p.B} N={p.N} V={p.V} bf16, complete binary tree depth {p.depth}")
+    if cpu_budget > 0:
+        import oracle
+        tc = {k: trees[0][k].cpu() for k in ("target", "tokens", "parents")}
+
+        def tone(b):
+            oracle.tree_verify_greedy(tc["target"][b:b + 1], tc["tokens"][b:b + 1], tc["parents"][b:b + 1])
+
+        out["c5"]["cpu_oracle"] = dict(oracle_rates(tone, p.B, cpu_budget, host_threads()), unit="seq/s")
+        del tc
     del trees
     trees = [wl.make_tree_sampling(p, 1.0, device=dev, seed=40 + i) for i in range(2)]
     full_s = 2 * p.B * (p.N + 1) * p.V * 2
@@ -561,6 +610,18 @@ def run_extras(sv, wl, dev, stream, steps, peak):
     ms = time_calls(scall, steps, 3, stream, dev, None if big(full_s) else flush)
     out["c5_stochastic_tree"] = extra_entry(ms, p.B, full_s, peak, steps, l2_note(full_s, 2),
                                             config=f"B={p.B} N={p.N} V={p.V} bf16 target and draft, tau 1")
+    if cpu_budget > 0:
+        import oracle
+        tc = {k: trees[0][k].cpu() for k in ("target", "draft", "tokens", "parents")}
+
+        def sone(b):
+            # sequence b alone draws with sequence number 0: a timing, not a parity check
+            oracle.tree_verify_sampling(tc["target"][b:b + 1], tc["draft"][b:b + 1], tc["tokens"][b:b + 1],
+                                        tc["parents"][b:b + 1], 1.0, b)
+
+        out["c5_stochastic_tree"]["cpu_oracle"] = dict(oracle_rates(sone, p.B, cpu_budget, host_threads()),
+                                                       unit="seq/s")
+        del tc
     del trees
 
     # n-gram drafting: 256 histories of up to 131072 tokens (16 seeded
@@ -577,6 +638,14 @@ def run_extras(sv, wl, dev, stream, steps, peak):
     out["ngram"] = extra_entry(ms, 256, nbytes, peak, steps, l2_note(nbytes, 1),
                                config="B=256 histories up to 131072 tokens, n 1..4, K=8")
     out["ngram"]["unit"] = "histories/s"
+    if cpu_budget > 0:
+        import oracle
+        htok, hlen = tok[:16].cpu(), ln[:16].cpu()
+
+        def gone(b):
+            oracle.ngram_draft(htok[b:b + 1], hlen[b:b + 1], 1, 4, 8)
+
+        out["ngram"]["cpu_oracle"] = dict(oracle_rates(gone, 16, cpu_budget, host_threads()), unit="histories/s")
     del tok, ln, flushbuf
     torch.cuda.synchronize(dev)
     return out
@@ -731,7 +800,8 @@ def run_gpu(args):
         line["cpu_baseline"] = cpu_line
         line["parity_sample"] = parity
     if world == 1 and args.extras_steps > 0:
-        line["extra"] = run_extras(sv, wl, dev, stream, args.extras_steps, peak)
+        line["extra"] = run_extras(sv, wl, dev, stream, args.extras_steps, peak,
+                                   0.0 if args.no_cpu_baseline else args.extras_cpu_budget)
         line["extra_status_flags"] = sv.spec_get_status()
     if world == 1:
         # acceptance statistics of one batch (spec_acceptance_stats on the GPU)
@@ -766,6 +836,8 @@ def main(argv=None):
     ap.add_argument("--sets", type=int, default=2, choices=[1, 2],
                     help="input sets alternated between steps")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--extras-cpu-budget", type=float, default=1.5,
+                    help="seconds of oracle timing per extra workload, single-threaded and all cores")
     ap.add_argument("--extras-steps", type=int, default=100,
                     help="timed calls per extra workload (c1, c2, c4, c5, early exits, ...); 0 skips them")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -89,7 +89,8 @@ extern "C" {
  *   seed           64-bit Philox-4x64-10 key word.  Position i's acceptance
  *                  uniform uses counter (b, i, 0, 0), the resampling uniform
  *                  counter (b, n, 1, 0); key (seed, 0x5350454356455249).  The
- *                  first output word r gives u = (2 (r >> 41) + 1) 2^-24.
+ *                  first output word r gives u = (2 (r >> 12) + 1) 2^-53, an
+ *                  odd multiple of 2^-53 in (0, 1).
  *   out_tokens     [B, K+1] int32: x_0 .. x_{n-1}, then the resampled (n < K)
  *                  or bonus (n == K) token, then -1 padding.
  *   out_n_accepted [B] int32: n in [0, K], or -1 for bad data.

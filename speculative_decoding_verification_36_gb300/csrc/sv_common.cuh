@@ -807,12 +807,13 @@ __device__ __forceinline__ uint64_t philox_first_word(uint64_t seed, uint64_t se
   return c0;
 }
 
-// u = (2 * (r >> 41) + 1) * 2^-24: an odd multiple of 2^-24 strictly inside (0, 1),
-// exact in fp32 and fp64.
+// u = (2 * (r >> 12) + 1) * 2^-53: an odd multiple of 2^-53 strictly inside
+// (0, 1), exact in fp64 (the top 52 bits of r: a token of probability p is
+// drawn with probability p to within 2^-52).
 __device__ __forceinline__ double uniform_draw(uint64_t seed, uint64_t seq, uint64_t pos,
                                                uint64_t stream) {
   uint64_t r = philox_first_word(seed, seq, pos, stream);
-  return (double)(2 * (r >> 41) + 1) * 0x1.0p-24;
+  return (double)(2 * (r >> 12) + 1) * 0x1.0p-53;
 }
 
 }  // namespace sv

@@ -295,7 +295,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
   __shared__ int s_tok[kMaxTreeNodes];
   __shared__ float s_zt[kMaxTreeNodes];  // node i's token: its logit in the parent's target row
   __shared__ float s_zd[kMaxTreeNodes];  // ... and in the parent's draft row
-  __shared__ float s_u[kMaxTreeNodes];   // node i's acceptance uniform (exact in fp32)
+  __shared__ double s_u[kMaxTreeNodes];  // node i's acceptance uniform
   __shared__ double s_wm[NW];                 // this CTA's warp masses of the last pass
   __shared__ double s_cta[2][kMaxWalkCluster];  // every CTA's mass, pushed by its owner
   __shared__ float s_steps[NW][kWalkSteps];
@@ -335,7 +335,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
     const int x = s_tok[i], pr = s_par[i];
     s_zt[i] = E::load1(tree_row<E>(a, b, pr + 1) + x);
     s_zd[i] = E::load1(tree_row<E>(a, b, N1 + pr + 1) + x);
-    s_u[i] = (float)uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0);
+    s_u[i] = uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0);
   }
   if (tid == 0) {
     sh.u = -1;
@@ -410,7 +410,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
           const double delta = (((double)zT - sh.mT) - ((double)zD - sh.mD)) * a.c64 - sh.lam;
           const double rho = exp2(delta);
           const double g = sh.k == 0 ? rho : fmax(0.0, rho - sh.A) / sh.B;  // P_k(x) / Q(x)
-          accept = g >= 1.0 || (double)s_u[c] < g;
+          accept = g >= 1.0 || s_u[c] < g;
         }
         sh.decision = accept;
         if (accept) {

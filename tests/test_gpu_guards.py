@@ -226,3 +226,27 @@ def test_a_lowered_wait_limit_never_hangs_or_writes_out_of_place():
                              p.temperature, 4, seq_ids=sel)
     rep = chain_report(tokens.cpu().numpy()[sel], n2.cpu().numpy()[sel], ref)
     assert not rep["mismatch"], rep
+
+
+def test_two_full_capacity_launches_side_by_side():
+    """Two full-size c3 verifies (B=256, grids sized to the whole device) on
+    two streams at once: each launch starts with only part of its grid
+    resident, beside the other.  Work goes only to CTAs that have started
+    (each CTA's first claims follow a per-launch ticket), so both finish
+    with no expired wait and with the results of the same calls made alone."""
+    p = wl.preset("c3")
+    xs = [wl.make_chain(p, device=DEV, seed=40 + k) for k in range(2)]
+    want = []
+    for k, x in enumerate(xs):
+        want.append(sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 100 + k))
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(device=DEV) for _ in range(2)]
+    for rnd in range(5):
+        got = []
+        for k, (x, s) in enumerate(zip(xs, streams)):
+            with torch.cuda.stream(s):
+                got.append(sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 100 + k))
+        torch.cuda.synchronize()
+        assert sv.spec_get_status() == 0, rnd
+        for k in range(2):
+            assert torch.equal(got[k][0], want[k][0]) and torch.equal(got[k][1], want[k][1]), (rnd, k)

@@ -266,6 +266,7 @@ int argmax_impl(bool tree, bool bf16, const void* target, const int32_t* tokens,
   a.R = K + 1;
   choose_slices(V, vec ? (bf16 ? 8 : 4) : 1, esz, kArgmaxSliceBytes, &a.SL, &a.CS, &a.CU);
   a.map.A = a.R * a.CU;
+  if ((long long)B * a.map.A >= INT_MAX) return SPEC_ERR_SHAPE;  // slices are indexed with int
   a.map.total = B * a.map.A;
   a.out_tokens = out_tokens;
   a.out_n = out_n;
@@ -356,6 +357,10 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   if (a.P < 1) a.P = 1;
   a.TL = a.P * step;
   a.TC = (int)(((long long)V + a.TL - 1) / a.TL);
+  // the kernel indexes slices, tail items and pieces with int: sizes_ok
+  // assumes at least 1024 elements per slice, checked here for the slices
+  // actually chosen
+  if ((long long)B * a.R * a.CS >= INT_MAX || (long long)B * a.TC * a.P >= INT_MAX) return SPEC_ERR_SHAPE;
   a.F = B * a.R * a.CS;
   a.FP = K * B * 2 * a.CS;
   a.div_pos = sv::make_fastdiv((uint32_t)(B * 2 * a.CS));

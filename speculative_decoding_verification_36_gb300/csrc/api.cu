@@ -125,13 +125,15 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 
 // Launch parameters of the persistent kernels, measured on GB300 with the c3
 // workload (the measurements are in the design notes):
-constexpr int kSliceBytes = 12288;        // statistics slice of the sampling kernel
+constexpr int kSliceBytes = 16384;        // statistics slice of the sampling kernel (full read)
+constexpr int kSliceBytesEarlyExit = 12288;  // ... with early exit, and of the stochastic tree's statistics
 constexpr int kSmallSliceBytes = 8192;    // ... for a batch with fewer than ~6 slices per warp
+constexpr int kTailBytes = 6144;          // bytes of each of the two rows in a tail item (not small batches)
 constexpr int kArgmaxSliceBytes = 8192;   // slice of the greedy and tree kernels
 constexpr int kClaimTail = 1;             // final statistics slices not claimed ahead
 constexpr int kFrontPositions = 1;        // draft positions whose row pairs are spread through the stream
 constexpr int kFrontSpanPercent = 60;     // ... over this percent of it (position 0 decides most sequences)
-constexpr int kL2KeepPositions = 2;       // positions whose rows are prefetched into L2 with evict_last
+constexpr int kL2KeepPositions = 1;       // positions whose rows are prefetched into L2 with evict_last
 constexpr int kLateTailPercent = 6;       // latest decisions whose tail items free warps claim
 constexpr int kLateTailPercentEarlyExit = 25;
 
@@ -339,20 +341,21 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   a.R = 2 * K + 1;
   const int vec_elems = vec ? (bf16 ? 8 : 4) : 1;
   int CU = 0;
-  // 12 KB statistics slices; a batch too small to give every warp of the grid
-  // about six of them streams 8 KB slices and lets free warps take all of its
-  // tail items (c2: 68 us instead of 75 us per call)
-  choose_slices(V, vec_elems, esz, kSliceBytes, &a.SL, &a.CS, &CU);
-  bool small = false;
-  if ((long long)B * a.R * a.CS < 6LL * capacity * sv::kWarps) {
-    small = true;
+  // A batch too small to give every warp of the grid about six 12 KB
+  // statistics slices streams 8 KB slices and lets free warps take all of its
+  // tail items (c2: 68 us instead of 75 us per call).  Larger batches stream
+  // 16 KB slices, or 12 KB with early exit (c3: 252 instead of 256 us with
+  // the full read; the early exit is 4 us slower with 16 KB).
+  choose_slices(V, vec_elems, esz, kSliceBytesEarlyExit, &a.SL, &a.CS, &CU);
+  const bool small = (long long)B * a.R * a.CS < 6LL * capacity * sv::kWarps;
+  if (small)
     choose_slices(V, vec_elems, esz, kSmallSliceBytes, &a.SL, &a.CS, &CU);
-  }
-  // tail slices: whole warp steps, half a statistics slice per row, so that a
-  // tail item (target and draft slice) carries as many bytes as a statistics
-  // slice
+  else if (!early_exit)
+    choose_slices(V, vec_elems, esz, kSliceBytes, &a.SL, &a.CS, &CU);
+  // tail slices: whole warp steps; half a statistics slice per row for a
+  // small batch, else kTailBytes per row (c3: 6 KB, against 8 KB or 12 KB)
   const int step = 32 * vec_elems;
-  const long long tl_elems = (a.SL + 1) / 2;
+  const long long tl_elems = small ? (a.SL + 1) / 2 : (long long)kTailBytes / (long long)esz;
   a.P = (int)((tl_elems + step - 1) / step);
   if (a.P < 1) a.P = 1;
   a.TL = a.P * step;
@@ -475,7 +478,7 @@ int tree_sample_impl(bool bf16, const void* target, const void* draft, const int
   a.V = V;
   a.RR = 2 * (N + 1);
   int CU = 0;
-  choose_slices(V, vec_elems, esz, kSliceBytes, &a.SL, &a.CS, &CU);
+  choose_slices(V, vec_elems, esz, kSliceBytesEarlyExit, &a.SL, &a.CS, &CU);
   a.F = (long long)B * a.RR * a.CS;
   // walk: the widest cluster (16, 8, 4, 2 CTAs) for which every sequence's
   // cluster is resident at once, else one CTA per sequence; each pass gives

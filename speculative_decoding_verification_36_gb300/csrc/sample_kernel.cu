@@ -734,9 +734,10 @@ __device__ __noinline__ int stats_slice(const SampleArgs& a, int b, int i, int r
   }
   float sum = acc.x + acc.y;
   float tsum = 0.f;
-  if constexpr (!ENT) sum *= exp_fma_fix(m, cc);  // the fused exponents' common factor out
+  // the fused exponents' common offset out (see exp_fma_err)
+  if constexpr (ENT) tsum = exp_fma_fix(m, cc) * __fmaf_rn(-exp_fma_err(m, cc), sum, tacc.x + tacc.y);
+  sum *= exp_fma_fix(m, cc);
   if constexpr (ENT) {
-    tsum = tacc.x + tacc.y;
     warp_mst(m, sum, tsum, cc);
   } else {
     warp_ms(m, sum, cc);

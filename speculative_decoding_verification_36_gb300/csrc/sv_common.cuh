@@ -534,17 +534,15 @@ __device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], flo
                                             float2& tacc, float cc) {
   const float bm = batch_max<E, VEC>(z);
   if (bm > m) {
+    // the sums are relative to fl(m c), the base of the fused exponents
+    const float delta = __fsub_rn(__fmul_rn(m, cc), __fmul_rn(bm, cc));  // -inf when m was -inf
+    const float f = ex2(delta);
     if constexpr (ENT) {
-      const float delta = (m - bm) * cc;
-      const float f = ex2(delta);
       // t' = 2^delta (t + delta s); an empty accumulator stays empty
       tacc = m == neg_inf() ? make_float2(0.f, 0.f)
                             : __fmul2_rn(make_float2(f, f), __ffma2_rn(make_float2(delta, delta), acc, tacc));
-      acc = __fmul2_rn(acc, make_float2(f, f));
-    } else {
-      const float f = ex2(__fsub_rn(__fmul_rn(m, cc), __fmul_rn(bm, cc)));  // 0 when m was -inf
-      acc = __fmul2_rn(acc, make_float2(f, f));
     }
+    acc = __fmul2_rn(acc, make_float2(f, f));
     m = bm;
   }
   const float base = (m == neg_inf()) ? 0.f : m;
@@ -552,44 +550,37 @@ __device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], flo
     const float nmc = -__fmul_rn(base, cc);
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
-      if constexpr (ENT) {
-        const float d = (z[u].f - base) * cc;
-        const float e = ex2(d);
-        acc.x += e;
-        tacc.x = fmaf(e, fmaxf(d, -126.f), tacc.x);
-      } else {
-        acc.x += ex2(__fmaf_rn(z[u].f, cc, nmc));
-      }
+      const float d = __fmaf_rn(z[u].f, cc, nmc);
+      const float e = ex2(d);
+      acc.x += e;
+      if constexpr (ENT) tacc.x = fmaf(e, fmaxf(d, -126.f), tacc.x);  // 0 * -inf would be NaN
     }
   } else {
     const float2 c2 = make_float2(cc, cc);
-    const float2 nb = make_float2(-base, -base);
     const float2 nmc = make_float2(-__fmul_rn(base, cc), -__fmul_rn(base, cc));
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u)
 #pragma unroll
       for (int p = 0; p < VEC / 2; ++p) {
-        const float2 zz = elem_pair2<E, VEC>(z[u], p);
-        if constexpr (ENT) {
-          const float2 d = __fmul2_rn(__fadd2_rn(zz, nb), c2);
-          const float2 e = make_float2(ex2(d.x), ex2(d.y));
-          acc = __fadd2_rn(acc, e);
-          tacc = __ffma2_rn(e, make_float2(fmaxf(d.x, -126.f), fmaxf(d.y, -126.f)), tacc);
-        } else {
-          const float2 d = __ffma2_rn(zz, c2, nmc);
-          acc = __fadd2_rn(acc, make_float2(ex2(d.x), ex2(d.y)));
-        }
+        const float2 d = __ffma2_rn(elem_pair2<E, VEC>(z[u], p), c2, nmc);
+        const float2 e = make_float2(ex2(d.x), ex2(d.y));
+        acc = __fadd2_rn(acc, e);
+        if constexpr (ENT) tacc = __ffma2_rn(e, make_float2(fmaxf(d.x, -126.f), fmaxf(d.y, -126.f)), tacc);
       }
   }
 }
 
-// The factor 2^{-e}, e = m c - fl(m c), that makes a lane sum formed with the
-// fused exponents of stats_batch (without entropy) the sum of 2^{(z - m) c}.
-// |e| < 2^-24 |m c|, so the first-order form is exact to far below fp32.
-__device__ __forceinline__ float exp_fma_fix(float m, float cc) {
+// e = m c - fl(m c): stats_batch's fused exponents d_f = z c - fl(m c) exceed
+// the exact (z - m) c by e, so a lane's sums relative to fl(m c) relate to
+// the exact ones as s = 2^{-e} s_f and t = sum d 2^d = 2^{-e} (t_f - e s_f).
+// |e| < 2^-24 |m c|: the first-order factor 1 - e ln 2 is exact to far below
+// fp32.
+__device__ __forceinline__ float exp_fma_err(float m, float cc) {
   const float base = (m == neg_inf()) ? 0.f : m;
-  const float e = __fmaf_rn(base, cc, -__fmul_rn(base, cc));
-  return __fmaf_rn(-e, 0.69314718055994530942f, 1.f);
+  return __fmaf_rn(base, cc, -__fmul_rn(base, cc));
+}
+__device__ __forceinline__ float exp_fma_fix(float m, float cc) {
+  return __fmaf_rn(-exp_fma_err(m, cc), 0.69314718055994530942f, 1.f);
 }
 
 // ---------------------------------------------------------------------------

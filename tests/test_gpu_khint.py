@@ -124,6 +124,12 @@ def test_khint_full_size_c3():
     x = wl.make_chain(p, device=DEV, seed=3)
     ref, h, hbar = _oracle_khint(x, p, 3)
     k_next, n, want = _check(x, p, 3, 1, 16, ref, h, hbar)
+    # the entropy pass sums the rows exactly as the plain verify does: the
+    # same tokens and counts bit for bit
+    t0, n0 = sv.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 3)
+    t1, n1, _, _ = sv.spec_verify_khint(x["target"], x["draft"], x["tokens"], p.temperature, 3, 1.0, 2.0, 1, 16)
+    torch.cuda.synchronize()
+    assert torch.equal(t0, t1) and torch.equal(n0, n1)
     # the thresholds split the batch: some sequences move each way
     assert (k_next == p.K + 1).any() and (k_next == p.K - 1).any() and (k_next == p.K).any()
     assert sv.spec_get_status() == 0

@@ -719,15 +719,17 @@ int spec_ngram_draft(const int32_t* tokens, const int32_t* lengths, int B, int s
   // match_len is optional: without it the kernel writes into scratch
   sv::WsLayout l;
   const size_t keys = ((size_t)B * 8 + 255) / 256 * 256;
-  l.total = keys + (out_match_len ? 0 : ((size_t)B * 4 + 255) / 256 * 256);
+  const size_t tickets = ((size_t)B * 4 + 255) / 256 * 256;
+  l.total = keys + tickets + (out_match_len ? 0 : ((size_t)B * 4 + 255) / 256 * 256);
   l.zero_bytes = 0;
   l.marker_off = 0;
-  l.marker_bytes = keys;  // all-ones: empty keys (stored complemented)
+  l.marker_bytes = keys + tickets;  // all-ones: empty keys (stored complemented), tickets at -1
   void* ws = nullptr;
   rc = get_scratch(d, false, l, stream, &ws);
   if (rc) return rc;
   a.key = (unsigned long long*)ws;
-  a.match_len = out_match_len ? out_match_len : (int32_t*)((char*)ws + keys);
+  a.ticket = (int*)((char*)ws + keys);
+  a.match_len = out_match_len ? out_match_len : (int32_t*)((char*)ws + keys + tickets);
   cudaError_t e = sv::launch_ngram(a, stream);
   cudaError_t e2 = put_scratch(false, ws, stream);
   if (e != cudaSuccess) return cuda_fail(e, "n-gram drafting launch");

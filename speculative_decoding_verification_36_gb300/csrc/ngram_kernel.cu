@@ -18,9 +18,10 @@
 // (m << 32) | e, so that the largest key is the longest match and, for that
 // length, the latest end; one atomic per CTA folds it into the sequence's key
 // (stored complemented: atomicMin, so that the all-ones workspace fill is the
-// empty key); nothing waits for it, so a CTA retires right after.  A second
-// small launch (one warp per sequence) writes the drafts.  Every history
-// token is read from HBM once.
+// empty key), then takes the sequence's ticket; nothing waits for either, so
+// a CTA retires right after, except the one that takes the sequence's last
+// ticket, whose first warp then writes the drafts.  Every history token is
+// read from HBM once.
 #include "sv_common.cuh"
 #include "sv_kernels.h"
 
@@ -29,6 +30,39 @@ namespace sv {
 constexpr int kNgramThreads = 256;
 constexpr int kNgramPerThread = 16;
 constexpr int kNgramChunk = kNgramThreads * kNgramPerThread;  // candidate ends per CTA
+
+__device__ __forceinline__ unsigned long long ld_relaxed_u64(const unsigned long long* p) {
+  unsigned long long v;
+  asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+  return v;
+}
+
+// The drafts of sequence b (one warp), once every CTA of the sequence has
+// folded its best end into the key.
+__device__ __noinline__ void ngram_finish(const NgramArgs& a, int b, int lane) {
+  const int32_t* h = a.tokens + (long long)b * a.stride;
+  const long long L = a.lengths[b];
+  int32_t* out = a.drafts + (long long)b * a.K;
+  if (L < 0 || L > a.stride) {
+    for (int i = lane; i < a.K; i += 32) out[i] = -1;
+    if (lane == 0) {
+      a.n_drafts[b] = -1;
+      a.match_len[b] = -1;
+      atomicOr(a.status, kStatusBadData);
+    }
+    return;
+  }
+  const unsigned long long key = ~ld_relaxed_u64(a.key + b);
+  const int m = (int)(key >> 32);
+  const long long e = (long long)(key & 0xffffffffull);
+  const long long room = m ? L - e : 0;
+  const int d = (int)(room < a.K ? room : a.K);
+  for (int i = lane; i < a.K; i += 32) out[i] = i < d ? __ldg(h + e + i) : -1;
+  if (lane == 0) {
+    a.n_drafts[b] = d;
+    a.match_len[b] = m;
+  }
+}
 
 __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(const __grid_constant__ NgramArgs a) {
   // s_tok[kNgramMaxN + i] holds h[c0 + i] (16-byte aligned, for vector
@@ -111,39 +145,19 @@ __global__ void __launch_bounds__(kNgramThreads) ngram_kernel(const __grid_const
   }
   if ((tid & 31) == 0) s_best[tid >> 5] = best;
   __syncthreads();
+  __shared__ int s_last;
   if (tid == 0) {
     for (int w = 1; w < kNgramThreads / 32; ++w) best = s_best[w] > best ? s_best[w] : best;
     if (best) atomicMin(a.key + b, ~best);
+    // the key update is visible before this CTA's ticket: the CTA taking
+    // the last ticket sees every CTA's key
+    __threadfence();
+    s_last = ticket_take(a.ticket + b) == a.chunks - 1;
   }
-}
-
-// The drafts (one warp per sequence), launched after the scan on the same
-// stream, so every CTA's key update is visible.
-__global__ void __launch_bounds__(kNgramThreads) ngram_finish_kernel(const __grid_constant__ NgramArgs a) {
-  const int b = (int)(blockIdx.x * (kNgramThreads / 32) + (threadIdx.x >> 5));
-  const int lane = threadIdx.x & 31;
-  if (b >= a.B) return;
-  const int32_t* h = a.tokens + (long long)b * a.stride;
-  const long long L = a.lengths[b];
-  int32_t* out = a.drafts + (long long)b * a.K;
-  if (L < 0 || L > a.stride) {
-    for (int i = lane; i < a.K; i += 32) out[i] = -1;
-    if (lane == 0) {
-      a.n_drafts[b] = -1;
-      a.match_len[b] = -1;
-      atomicOr(a.status, kStatusBadData);
-    }
-    return;
-  }
-  const unsigned long long key = ~a.key[b];
-  const int m = (int)(key >> 32);
-  const long long e = (long long)(key & 0xffffffffull);
-  const long long room = m ? L - e : 0;
-  const int d = (int)(room < a.K ? room : a.K);
-  for (int i = lane; i < a.K; i += 32) out[i] = i < d ? __ldg(h + e + i) : -1;
-  if (lane == 0) {
-    a.n_drafts[b] = d;
-    a.match_len[b] = m;
+  __syncthreads();
+  if (s_last && tid < 32) {
+    __threadfence();
+    ngram_finish(a, b, tid);
   }
 }
 
@@ -153,10 +167,6 @@ cudaError_t launch_ngram(const NgramArgs& a, cudaStream_t s) {
   const long long grid = (long long)a.B * a.chunks;
   if (grid <= 0) return cudaSuccess;
   ngram_kernel<<<(unsigned)grid, kNgramThreads, 0, s>>>(a);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  const int per = kNgramThreads / 32;
-  ngram_finish_kernel<<<(unsigned)((a.B + per - 1) / per), kNgramThreads, 0, s>>>(a);
   return cudaGetLastError();
 }
 

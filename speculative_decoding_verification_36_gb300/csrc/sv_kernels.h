@@ -245,7 +245,8 @@ struct NgramArgs {
   int32_t* drafts;         // [B, K]
   int32_t* n_drafts;       // [B]
   int32_t* match_len;      // [B]
-  unsigned long long* key;
+  unsigned long long* key;  // [B] best (match length, end), complemented; all-ones = none
+  int* ticket;              // [B] CTAs of the sequence done so far, from -1
   unsigned* status;
 };
 int ngram_chunk();

@@ -382,16 +382,14 @@ __device__ __noinline__ void unit_finisher(const SampleArgs& a, int b, int i) {
     // a valid token always has a slice that records the logits at it
     if (__float_as_uint(zT) == kMarker) zT = wait_f32(a.zx + (size_t)b * R + rT, a.status);
     if (__float_as_uint(zD) == kMarker) zD = wait_f32(a.zx + (size_t)b * R + rD, a.status);
-    // log2 of the unnormalised probabilities, from exact differences
-    const double lp = ((double)zT - (double)mT) * a.c64;
-    const double lq = ((double)zD - (double)mD) * a.c64;
     bool accept = true;  // q(x) = 0 <= p(x)
-    if (zD != neg_inf()) {
-      const double u = uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0);
-      accept = u < exp2(lp - lq) * ((double)sD / (double)sT);  // u < p(x) / q(x)
-    }
+    if (zD != neg_inf())
+      accept = accept_draw(zT, mT, zD, mD, sT, sD, a.c_hi, a.c_lo,
+                           uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0));
     verdict = accept ? kVerdictAccept : kVerdictReject;
-    if (a.out_pq && lane == 0) {
+    if (a.out_pq && lane == 0) {  // the stats export (not the verify path): fp64 from exact differences
+      const double lp = ((double)zT - (double)mT) * a.c64;
+      const double lq = ((double)zD - (double)mD) * a.c64;
       a.out_pq[((size_t)b * K + i) * 2 + 0] = (float)(exp2(lp) / (double)sT);
       a.out_pq[((size_t)b * K + i) * 2 + 1] = (float)(exp2(lq) / (double)sD);
     }
@@ -576,7 +574,7 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   const int tsel =
       warp_cdf_search(C, theta, 0.0, [&](int t) { return (double)ld_relaxed_f32(ts + t); }, &acc);
   if (tsel < 0) {  // no slice with mass: only an expired wait can cause this
-    const uint4 res = make_uint4((uint32_t)n, kResultBad, __float_as_uint((float)(Z / (double)si.sT)), 0u);
+    const uint4 res = make_uint4((uint32_t)n, kResultBad, __float_as_uint(__fdiv_rn((float)Z, si.sT)), 0u);
     if (lane == 0) {
       atomicOr(a.status, kStatusTimeout);
       st_relaxed_v4(a.result + b, res.x, res.y, res.z, res.w);
@@ -591,7 +589,7 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   const int psel = warp_cdf_search(
       np, theta, acc, [&](int q) { return (double)wait_f32(gp + q, a.status); }, &acc2);
   if (psel < 0) {  // pieces inconsistent with their slice mass (expired wait)
-    const uint4 res = make_uint4((uint32_t)n, kResultBad, __float_as_uint((float)(Z / (double)si.sT)), 0u);
+    const uint4 res = make_uint4((uint32_t)n, kResultBad, __float_as_uint(__fdiv_rn((float)Z, si.sT)), 0u);
     if (lane == 0) {
       atomicOr(a.status, kStatusTimeout);
       st_relaxed_v4(a.result + b, res.x, res.y, res.z, res.w);
@@ -640,7 +638,7 @@ __device__ __noinline__ void select_finisher(const SampleArgs& a, SeqInfo si) {
   }
   token = __shfl_sync(0xffffffffu, token, L);
   const uint4 res = make_uint4((uint32_t)n, token >= 0 ? (uint32_t)token : kResultBad,
-                               __float_as_uint((float)(Z / (double)si.sT)), 0u);
+                               __float_as_uint(__fdiv_rn((float)Z, si.sT)), 0u);
   if (lane == 0) st_relaxed_v4(a.result + b, res.x, res.y, res.z, res.w);
   commit_result(a, b, res);
 }

@@ -570,6 +570,39 @@ __device__ __forceinline__ void stats_batch(const Raw<E, VEC> (&z)[kUnroll], flo
   }
 }
 
+// Error-free sum a + b = hi + lo (Knuth's TwoSum), round-to-nearest steps.
+__device__ __forceinline__ float2 two_sum(float a, float b) {
+  const float s = __fadd_rn(a, b);
+  const float bb = __fsub_rn(s, a);
+  return make_float2(s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb)));
+}
+
+// The acceptance test u < p(x) / q(x) for a drafted token with q(x) > 0:
+// p(x) / q(x) = 2^{((zT - mT) - (zD - mD)) c} sD / sT.  The exponent comes
+// from error-free differences and c = c_hi + c_lo (about 45 bits), 2^f from
+// the ex2 instruction (relative error below 2^-21) and sD / sT from one
+// correctly rounded division, so alpha is within about 4e-7 (relative) of
+// the exact ratio.  A decision can then differ from the exact one only when
+// |u - min(1, alpha)| is below 4e-7, inside the 1e-6 band the boundary
+// accounting allows; q == p gives alpha == 1 exactly.  fp32 instead of fp64:
+// on this GPU a double exp2 and division on the decision path cost over a
+// microsecond per call.
+__device__ __forceinline__ bool accept_draw(float zT, float mT, float zD, float mD, float sT, float sD,
+                                            float c_hi, float c_lo, double u) {
+  if (zT == neg_inf()) return false;  // p(x) = 0 < u
+  const float2 dT = two_sum(zT, -mT), dD = two_sum(zD, -mD);
+  const float2 E = two_sum(dT.x, -dD.x);
+  const float El = __fadd_rn(E.y, __fsub_rn(dT.y, dD.y));
+  const float xh = __fmul_rn(E.x, c_hi);
+  const float xl = __fadd_rn(__fmaf_rn(E.x, c_hi, -xh), __fmaf_rn(E.x, c_lo, __fmul_rn(El, c_hi)));
+  // row sums lie in [1, V]: sD / sT is within [2^-31, 2^31]
+  if (xh > 160.f) return true;
+  if (xh < -160.f) return false;
+  const float n = floorf(xh);
+  const float g = __fmul_rn(ex2(__fsub_rn(xh, n)), __fmaf_rn(xl, 0.69314718055994530942f, 1.f));
+  return u < (double)ldexpf(__fmul_rn(g, __fdiv_rn(sD, sT)), (int)n);
+}
+
 // e = m c - fl(m c): stats_batch's fused exponents d_f = z c - fl(m c) exceed
 // the exact (z - m) c by e, so a lane's sums relative to fl(m c) relate to
 // the exact ones as s = 2^{-e} s_f and t = sum d 2^d = 2^{-e} (t_f - e s_f).

@@ -285,9 +285,12 @@ __device__ __noinline__ void decide_sequence(const SampleArgs& a, int b, int n, 
     if (n < K) {
       si.mode = kModeResidual;
       si.mD = __uint_as_float(stD.x);
-      const double lam = log2((double)si.sT) - log2((double)__uint_as_float(stD.y));
-      si.lam_hi = (float)lam;
-      si.lam_lo = (float)(lam - (double)si.lam_hi);
+      // log2(sT / sD) as a float pair (fp32 pairs: a double log2 costs about
+      // a microsecond of latency here)
+      const float2 lt = log2_pair(si.sT), ld = log2_pair(__uint_as_float(stD.y));
+      const float2 lam = pair_add(lt, make_float2(-ld.x, -ld.y));
+      si.lam_hi = lam.x;
+      si.lam_lo = lam.y;
     } else {
       si.mode = kModeBonus;
       si.mD = 0.f;

@@ -577,6 +577,55 @@ __device__ __forceinline__ float2 two_sum(float a, float b) {
   return make_float2(s, __fadd_rn(__fsub_rn(a, __fsub_rn(s, bb)), __fsub_rn(b, bb)));
 }
 
+// Float pairs (hi + lo, |lo| <= ulp(hi) / 2): renormalising sum, product
+// (the product's error from one FMA) and sum.
+__device__ __forceinline__ float2 fast_two_sum(float a, float b) {  // |a| >= |b|
+  const float s = __fadd_rn(a, b);
+  return make_float2(s, __fsub_rn(b, __fsub_rn(s, a)));
+}
+__device__ __forceinline__ float2 pair_mul(float2 a, float2 b) {
+  const float p = __fmul_rn(a.x, b.x);
+  const float e = __fadd_rn(__fmaf_rn(a.x, b.x, -p), __fadd_rn(__fmul_rn(a.x, b.y), __fmul_rn(a.y, b.x)));
+  return fast_two_sum(p, e);
+}
+__device__ __forceinline__ float2 pair_add(float2 a, float2 b) {
+  const float2 s = two_sum(a.x, b.x);
+  return fast_two_sum(s.x, __fadd_rn(s.y, __fadd_rn(a.y, b.y)));
+}
+
+// log2(x) of a positive normal float as a float pair, within about 2e-11:
+// x = 2^e m with m in [sqrt(1/2), sqrt(2)), ln m = 2 atanh(s) with
+// s = (m - 1) / (m + 1), |s| < 0.172, atanh(s) = s + s^3/3 + s^5/5 + ...;
+// s and s^3/3 are float pairs, s^5/5 + ... (below 3e-5 of s) is fp32.
+__device__ __forceinline__ float2 log2_pair(float x) {
+  const int bits = __float_as_int(x);
+  int e = ((bits >> 23) & 0xff) - 127;
+  float m = __int_as_float((bits & 0x007fffff) | 0x3f800000);  // [1, 2)
+  if (m > 1.41421356f) {
+    m = __fmul_rn(m, 0.5f);
+    e += 1;
+  }
+  const float num = __fsub_rn(m, 1.f);  // exact
+  const float2 den = two_sum(m, 1.f);
+  const float sh = __fdiv_rn(num, den.x);
+  const float rem = __fmaf_rn(-sh, den.x, num);  // exact remainder
+  const float2 sv = fast_two_sum(sh, __fdiv_rn(__fmaf_rn(-sh, den.y, rem), den.x));
+  const float t = __fmul_rn(sv.x, sv.x);
+  float q = 1.f / 15.f;  // Q(t) = 1/5 + t/7 + t^2/9 + t^3/11 + t^4/13 + t^5/15
+  q = __fmaf_rn(q, t, 1.f / 13.f);
+  q = __fmaf_rn(q, t, 1.f / 11.f);
+  q = __fmaf_rn(q, t, 1.f / 9.f);
+  q = __fmaf_rn(q, t, 1.f / 7.f);
+  q = __fmaf_rn(q, t, 1.f / 5.f);
+  const float2 s3 = pair_mul(pair_mul(sv, sv), sv);
+  const float2 s33 = pair_mul(s3, make_float2(0.333333343f, -9.93410776e-9f));  // 1/3 as a pair
+  const float tail = __fmul_rn(__fmul_rn(s3.x, t), q);                          // s^5 Q(s^2)
+  const float2 at = pair_add(pair_add(sv, s33), make_float2(tail, 0.f));
+  const float2 l2m = pair_mul(make_float2(__fmul_rn(at.x, 2.f), __fmul_rn(at.y, 2.f)),
+                              make_float2(1.44269502f, 1.92596303e-8f));  // 1/ln 2 as a pair
+  return pair_add(make_float2((float)e, 0.f), l2m);
+}
+
 // The acceptance test u < p(x) / q(x) for a drafted token with q(x) > 0:
 // p(x) / q(x) = 2^{((zT - mT) - (zD - mD)) c} sD / sT.  The exponent comes
 // from error-free differences and c = c_hi + c_lo (about 45 bits), 2^f from

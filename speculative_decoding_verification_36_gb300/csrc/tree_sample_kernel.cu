@@ -262,6 +262,26 @@ __device__ int chunk_select(const typename E::storage* rowT, const typename E::s
   return -1;
 }
 
+// log2 of a double x >= 1 from its float split x = hi + lo: log2(hi) as a
+// float pair, plus lo / (hi ln 2) (error about 1e-11).  A double log2 costs
+// about a microsecond of latency on this GPU, on the walk's serial path.
+__device__ __forceinline__ double log2_split(double x) {
+  const float hi = (float)x;
+  const float lo = (float)(x - (double)hi);
+  const float2 l = log2_pair(hi);
+  return (double)l.x + ((double)l.y + (double)__fdiv_rn(lo, hi) * 1.4426950408889634074);
+}
+
+// 2^d for d < 0 from the ex2 instruction on the fractional part: relative
+// error below 3e-7.  An acceptance decision u < 2^d taken with it can differ
+// from the exact one only for |u - 2^d| below 3e-7, inside the 1e-6
+// boundary band of the parity accounting.
+__device__ __forceinline__ double exp2_neg(double d) {
+  if (d < -160.0) return 0.0;
+  const double n = floor(d);
+  return ldexp((double)ex2((float)(d - n)), (int)n);
+}
+
 struct WalkShared {
   // residual state of the current node (thread 0 keeps it; fp64 stays in thread 0)
   double A, B, L, lam, sT;
@@ -389,7 +409,9 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
       sh.mT = st.x;
       sh.mD = sd.x;
       sh.sT = (double)st.y;
-      sh.lam = log2((double)st.y) - log2((double)sd.y);  // log2(sT / sD)
+      const float2 lt = log2_pair(st.y), ld = log2_pair(sd.y);  // log2(sT / sD) as a float pair
+      const float2 lp = pair_add(lt, make_float2(-ld.x, -ld.y));
+      sh.lam = (double)lp.x + (double)lp.y;
       sh.k = 0;
       sh.A = 0.0;
       sh.B = 1.0;
@@ -408,9 +430,13 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
           accept = true;  // Q(x) = 0
         } else {
           const double delta = (((double)zT - sh.mT) - ((double)zD - sh.mD)) * a.c64 - sh.lam;
-          const double rho = exp2(delta);
-          const double g = sh.k == 0 ? rho : fmax(0.0, rho - sh.A) / sh.B;  // P_k(x) / Q(x)
-          accept = g >= 1.0 || s_u[c] < g;
+          if (sh.k == 0) {  // P_0(x) / Q(x) = 2^delta
+            accept = delta >= 0.0 || s_u[c] < exp2_neg(delta);
+          } else {  // after a rejection, (rho - A) may cancel: fp64 throughout
+            const double rho = exp2(delta);
+            const double g = fmax(0.0, rho - sh.A) / sh.B;  // P_k(x) / Q(x)
+            accept = g >= 1.0 || s_u[c] < g;
+          }
         }
         sh.decision = accept;
         if (accept) {
@@ -419,7 +445,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
           sh.u = c;
         } else {
           // constants of the pass for B_{k+1}: threshold moved by L_{k+1} = log2(A_k + B_k)
-          const double shifted = sh.lam + log2(sh.A + sh.B);
+          const double shifted = sh.lam + log2_split(sh.A + sh.B);
           sh.lam_hi = (float)shifted;
           sh.lam_lo = (float)(shifted - (double)sh.lam_hi);
           sh.residual = 1;
@@ -437,7 +463,7 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
         sh.current = Bk > 0.0;
         if (Bk > 0.0) {  // else only rounding emptied the residual: keep P
           const double A1 = sh.A + sh.B;
-          sh.L = log2(A1);
+          sh.L = log2_split(A1);
           sh.A = A1;
           sh.B = Bk;
           sh.k += 1;

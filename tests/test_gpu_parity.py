@@ -73,6 +73,30 @@ def test_sampling_parity(name, over):
     assert not rep["mismatch"], rep
 
 
+@pytest.mark.parametrize("name,over", [("c1", dict(B=6, temperature=0.05)),     # c = 28.9: sharp rows
+                                       ("c2", dict(B=6, V=4096, temperature=0.05)),
+                                       ("c1", dict(B=6, temperature=20.0)),       # c = 0.07: flat rows
+                                       ("c3", dict(B=4, V=8192, temperature=20.0)),
+                                       ("c2", dict(B=3, K=6, V=1001, temperature=3.0))])
+def test_sampling_parity_extreme_temperatures(name, over):
+    """The acceptance test (exponent from error-free differences, ex2) and
+    log2(sT / sD) (float pairs) across temperatures whose exponent
+    differences are very large or very small."""
+    p = wl.preset(name, **over)
+    x = wl.make_chain(p, seed=17)
+    tokens, n = run_chain(x, seed=17)
+    check_chain_outputs(tokens, n, x, p.K, p.V)
+    ref = oracle.spec_verify(x["target"], x["draft"], x["tokens"], p.temperature, 17)
+    rep = chain_report(tokens, n, ref)
+    print(f"{name} {over}: n={n.tolist()} boundary={rep['boundary']}")
+    assert not rep["mismatch"], rep
+    out = sv.spec_verify_stats(_dev(x["target"]), _dev(x["draft"]), _dev(x["tokens"]), p.temperature, 17)
+    torch.cuda.synchronize()
+    same = out["n"].cpu().numpy() == ref["n"]
+    e_z = rel_err(out["resid_mass"].cpu().numpy()[same], ref["resid_mass"][same]).max()
+    assert e_z <= 1e-5, e_z
+
+
 @pytest.mark.parametrize("name,over", [("c1", {}), ("c3", dict(B=8)), ("c2", dict(B=4, V=1001)),
                                        ("c2", dict(B=6))])
 def test_sampling_probabilities(name, over):

@@ -19,7 +19,8 @@
 //     draft position (position-major, with position 0 spread through the
 //     first part of the stream).  The warp that takes the last ticket of a
 //     position's row pair merges both rows, runs steps 2-3 for that position
-//     in fp64 and records the verdict; the verdict that completes the prefix
+//     (the ratio from error-free fp32 differences, see accept_draw) and
+//     records the verdict; the verdict that completes the prefix
 //     0..n fixes n (step 4) and appends the sequence's decision to the
 //     decision queue, without waiting for the rows after the first rejection.
 //   * tail slice = a segment of the tail row (pair) of a decided sequence:

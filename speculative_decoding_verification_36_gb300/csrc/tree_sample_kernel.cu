@@ -23,7 +23,8 @@
 // weight with the threshold moved by L_k.  So each rejection costs one pass
 // over the row pair for B_k, no distribution is ever stored, and the
 // acceptance ratio of a child x is P_k(x) / Q(x) = max(0, rho(x) - A_k) / B_k,
-// evaluated in fp64.
+// evaluated in fp64 (for the first child, k = 0, the ratio 2^delta comes
+// from ex2: see exp2_neg).
 //
 // Two kernels: row statistics (m, s) of every target and draft row (a flat
 // list of slices over all sequences, each warp taking every W-th slice, the

@@ -646,9 +646,51 @@ def run_extras(sv, wl, dev, stream, steps, peak, cpu_budget=0.0):
             oracle.ngram_draft(htok[b:b + 1], hlen[b:b + 1], 1, 4, 8)
 
         out["ngram"]["cpu_oracle"] = dict(oracle_rates(gone, 16, cpu_budget, host_threads()), unit="histories/s")
+
+    # A bare read of each entry's bytes: torch's max over a float32 buffer of
+    # the same size, timed like the entry (L2 flushed first when the bytes
+    # fit in twice L2).  One read pass of that size, nothing else, is the
+    # practical ceiling the entry's call can be held against.
+    reads = {}
+
+    def plain_read_ms(nbytes):
+        if nbytes not in reads:
+            x = torch.ones(max(1, nbytes // 4), dtype=torch.float32, device=dev)
+            reads[nbytes] = time_calls(lambda i: x.max(), steps, 3, stream, dev, None if big(nbytes) else flush)
+            del x
+        return reads[nbytes]
+
+    for e in out.values():
+        nb = e.get("bytes_per_step")
+        if nb:
+            ms = plain_read_ms(nb)
+            e["plain_read"] = {"us_per_call": ms * 1e3, "call_vs_read": e["us_per_call"] / (ms * 1e3),
+                               "kind": "torch max over a float32 buffer of the same bytes"}
+    p3 = wl.preset("c3")
+    c3_bytes = algorithmic_bytes(p3)
+    ms = plain_read_ms(c3_bytes)
+    out["c3_plain_read"] = {"us_per_call": ms * 1e3, "bytes": c3_bytes,
+                            "kind": "torch max over a float32 buffer of the headline's bytes per step",
+                            "l2": l2_note(c3_bytes, 1)}
     del tok, ln, flushbuf
     torch.cuda.synchronize(dev)
     return out
+
+
+def read_sweep(dev, steps=50):
+    """One read pass (torch max over a float32 buffer) at growing sizes, L2
+    flushed before each call, CUDA events: what a bare read reaches at each
+    size on this GPU."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    flushbuf = torch.ones(128 * 2**20, dtype=torch.float32, device=dev)
+    rows = []
+    for mib in (64, 105, 134, 180, 256, 512, 1024, 2048):
+        x = torch.ones(mib * 2**20 // 4, dtype=torch.float32, device=dev)
+        ms = time_calls(lambda i: x.max(), steps, 3, stream, dev, lambda: flushbuf.sum())
+        rows.append({"MiB": mib, "us_per_call": round(ms * 1e3, 2), "GBs": round(x.numel() * 4 / ms / 1e6, 1)})
+        del x
+    return rows
 
 
 def run_gpu(args):
@@ -841,9 +883,17 @@ def main(argv=None):
     ap.add_argument("--extras-steps", type=int, default=100,
                     help="timed calls per extra workload (c1, c2, c4, c5, early exits, ...); 0 skips them")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--read-sweep", action="store_true",
+                    help="print one JSON line of bare-read times over growing sizes and exit")
     args = ap.parse_args(argv)
     if args.impl == "reference":
         return run_reference(args)
+    if args.read_sweep:
+        import torch
+        dev = torch.device("cuda", 0)
+        print(json.dumps({"read_sweep": read_sweep(dev), "kind": "torch max over a float32 buffer, "
+                          "L2 flushed by a 512 MB read before each call, CUDA events"}))
+        return 0
     return run_gpu(args)
 
 

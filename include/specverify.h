@@ -393,10 +393,15 @@ int spec_acceptance_stats(const int32_t *n_accepted, int B, int K, uint64_t *out
  * Bad data: a length outside [0, stride] gives n_drafts = match_len = -1 and
  * -1 drafts for that sequence and sets SPEC_FLAG_BAD_DATA.
  * Each history token is read from device memory once; scratch (8 bytes per
- * sequence) comes from the library's stream-ordered pool.  Returns SPEC_OK,
- * SPEC_ERR_NULL (an output, or tokens / lengths with B > 0, is NULL),
- * SPEC_ERR_SHAPE (B < 0, stride < 1 or above 2^30, bad n_min / n_max / K) or
- * SPEC_ERR_CUDA.  Asynchronous on `stream`.
+ * 4096 positions of every row, plus 256 bytes) comes from the library's
+ * stream-ordered pool.  Two kernels run on `stream`, the second with
+ * programmatic stream serialisation (capturable into a CUDA graph).  A
+ * bounded wait that ran out sets SPEC_FLAG_TIMEOUT; the outputs are then in
+ * range (drafts copied from the history or -1) but may miss the best match.
+ * Returns SPEC_OK, SPEC_ERR_NULL (an output, or tokens / lengths with B > 0,
+ * is NULL), SPEC_ERR_SHAPE (B < 0, stride < 1 or above 2^30, bad n_min /
+ * n_max / K, or B * ceil(stride / 4096) >= 2^31 - 2^20) or SPEC_ERR_CUDA.
+ * Asynchronous on `stream`.
  */
 int spec_ngram_draft(const int32_t *tokens, const int32_t *lengths, int B, int stride, int n_min,
                      int n_max, int K, int32_t *out_drafts, int32_t *out_n_drafts,

@@ -51,6 +51,7 @@ struct DeviceState {
   int occ_tree[2][2] = {{0, 0}, {0, 0}};
   int occ_tree_stats[2][2] = {{0, 0}, {0, 0}};
   int walk_clusters[2][2][5] = {};  // [bf16][vec][log2 C]: walk clusters resident at once
+  int occ_ngram = 0;                // n-gram scan CTAs per SM
 };
 
 constexpr int kMaxDevices = 64;
@@ -84,6 +85,7 @@ int get_device_state(DeviceState** out) {
         d.occ_tree_stats[bf][v] = sv::tree_stats_blocks_per_sm(bf, v);
         for (int c = 0; c < 5; ++c) d.walk_clusters[bf][v][c] = sv::tree_walk_clusters(bf, v, 1 << c);
       }
+    d.occ_ngram = sv::ngram_blocks_per_sm();
     d.init = true;
   }
   *out = &d;
@@ -194,7 +196,8 @@ int run_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, void
     e = cudaMallocFromPoolAsync(ws, l.total, d->pool, d->side);
     if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
     if (l.zero_bytes) e = cudaMemsetAsync(*ws, 0, l.zero_bytes, d->side);
-    if (e == cudaSuccess) e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, d->side);
+    if (e == cudaSuccess && l.marker_bytes)
+      e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, d->side);
     if (e == cudaSuccess) e = cudaEventRecord(d->side_done, d->side);
     if (e == cudaSuccess) e = cudaStreamWaitEvent(stream, d->side_done, 0);
     if (e != cudaSuccess) {
@@ -206,7 +209,8 @@ int run_scratch(DeviceState* d, const sv::WsLayout& l, cudaStream_t stream, void
   e = cudaMallocFromPoolAsync(ws, l.total, d->pool, stream);
   if (e != cudaSuccess) return cuda_fail(e, "cudaMallocFromPoolAsync");
   if (l.zero_bytes) e = cudaMemsetAsync(*ws, 0, l.zero_bytes, stream);
-  if (e == cudaSuccess) e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, stream);
+  if (e == cudaSuccess && l.marker_bytes)
+    e = cudaMemsetAsync((char*)*ws + l.marker_off, 0xff, l.marker_bytes, stream);
   if (e != cudaSuccess) {
     cudaFreeAsync(*ws, stream);
     return cuda_fail(e, "cudaMemsetAsync");
@@ -698,10 +702,12 @@ int spec_ngram_draft(const int32_t* tokens, const int32_t* lengths, int B, int s
   if (B == 0) return SPEC_OK;
   if (!tokens || !lengths || !out_n_drafts || (K > 0 && !out_drafts)) return SPEC_ERR_NULL;
   const long long chunks = ((long long)stride + sv::ngram_chunk() - 1) / sv::ngram_chunk();
-  if ((long long)B * chunks >= (1LL << 31)) return SPEC_ERR_SHAPE;
+  // entries are 32-bit; the claim counter overshoots the total by two claims per CTA
+  if ((long long)B * chunks >= (1LL << 31) - (1LL << 20)) return SPEC_ERR_SHAPE;
   DeviceState* d = nullptr;
   int rc = get_device_state(&d);
   if (rc) return rc;
+  if (d->occ_ngram < 1) return cuda_fail(cudaErrorInvalidConfiguration, "n-gram scan shared memory");
   sv::NgramArgs a;
   memset(&a, 0, sizeof a);
   a.tokens = tokens;
@@ -717,20 +723,23 @@ int spec_ngram_draft(const int32_t* tokens, const int32_t* lengths, int B, int s
   a.n_drafts = out_n_drafts;
   a.status = d->status;
   // match_len is optional: without it the kernel writes into scratch
+  const long long entries = (long long)B * chunks;
   sv::WsLayout l;
-  const size_t keys = ((size_t)B * 8 + 255) / 256 * 256;
-  const size_t tickets = ((size_t)B * 4 + 255) / 256 * 256;
-  l.total = keys + tickets + (out_match_len ? 0 : ((size_t)B * 4 + 255) / 256 * 256);
-  l.zero_bytes = 0;
+  const size_t slots = ((size_t)entries * 8 + 255) / 256 * 256;
+  const size_t counter = 256;
+  l.total = slots + counter + (out_match_len ? 0 : ((size_t)B * 4 + 255) / 256 * 256);
+  l.zero_bytes = slots + counter;  // no chunk's best end yet; the counter at 0
   l.marker_off = 0;
-  l.marker_bytes = keys + tickets;  // all-ones: empty keys (stored complemented), tickets at -1
+  l.marker_bytes = 0;
   void* ws = nullptr;
   rc = get_scratch(d, false, l, stream, &ws);
   if (rc) return rc;
-  a.key = (unsigned long long*)ws;
-  a.ticket = (int*)((char*)ws + keys);
-  a.match_len = out_match_len ? out_match_len : (int32_t*)((char*)ws + keys + tickets);
-  cudaError_t e = sv::launch_ngram(a, stream);
+  a.slot = (unsigned long long*)ws;
+  a.counter = (int*)((char*)ws + slots);
+  a.match_len = out_match_len ? out_match_len : (int32_t*)((char*)ws + slots + counter);
+  const long long capacity = (long long)d->sms * d->occ_ngram;
+  const int grid = (int)(entries < capacity ? entries : capacity);
+  cudaError_t e = sv::launch_ngram(a, grid, stream);
   cudaError_t e2 = put_scratch(false, ws, stream);
   if (e != cudaSuccess) return cuda_fail(e, "n-gram drafting launch");
   if (e2 != cudaSuccess) return cuda_fail(e2, "cudaFreeAsync");
@@ -748,6 +757,7 @@ int spec_test_spin_limit(uint32_t iterations) {
   if (e == cudaSuccess) e = sv::sample_set_spin_limit(n);
   if (e == cudaSuccess) e = sv::greedy_set_spin_limit(n);
   if (e == cudaSuccess) e = sv::tree_sample_set_spin_limit(n);
+  if (e == cudaSuccess) e = sv::ngram_set_spin_limit(n);
   if (e != cudaSuccess) return cuda_fail(e, "spin limit");
   return SPEC_OK;
 }

@@ -230,27 +230,30 @@ cudaError_t launch_sample(const SampleArgs& a, bool bf16, bool vec, int grid, cu
 cudaError_t launch_greedy(const GreedyArgs& a, bool bf16, bool vec, int grid, cudaStream_t s);
 cudaError_t launch_tree(const GreedyArgs& a, bool bf16, bool vec, int grid, cudaStream_t s);
 
-// N-gram (prompt-lookup) drafting (ngram_kernel.cu).  CTA (b, c) scans chunk
-// c of sequence b's candidate match ends; a second launch writes the drafts.
-// Workspace (filled with all-ones bytes): key [B] (the best (m << 32) | e,
-// stored complemented).
+// N-gram (prompt-lookup) drafting (ngram_kernel.cu).  A persistent scan grid
+// claims (sequence, chunk) entries from a counter and stores each chunk's best
+// end in the entry's slot; a second launch (programmatic stream serialisation)
+// reduces each sequence's slots and writes the drafts.
+// Workspace (zeroed): slot [B * chunks], counter.
 constexpr int kNgramMaxN = 32;  // longest n-gram matched
 struct NgramArgs {
   const int32_t* tokens;   // [B, stride] histories
   long long stride;        // row stride and the largest valid length
   const int32_t* lengths;  // [B]
   int B, n_min, n_max, K;
-  int chunks;              // CTAs per sequence: ceil((stride) / chunk)
-  int vec;                 // every row starts on a 16-byte boundary (16-byte loads)
+  int chunks;              // entries per sequence: ceil(stride / chunk)
+  int vec;                 // every row starts on a 16-byte boundary (bulk copies)
   int32_t* drafts;         // [B, K]
   int32_t* n_drafts;       // [B]
   int32_t* match_len;      // [B]
-  unsigned long long* key;  // [B] best (match length, end), complemented; all-ones = none
-  int* ticket;              // [B] CTAs of the sequence done so far, from -1
+  unsigned long long* slot;  // [B, chunks] best (m << 32) | e of each chunk, 0 = none
+  int* counter;              // entries claimed so far
   unsigned* status;
 };
 int ngram_chunk();
-cudaError_t launch_ngram(const NgramArgs& a, cudaStream_t s);
+int ngram_blocks_per_sm();  // scan CTAs resident per SM (0: the launch cannot be configured)
+cudaError_t ngram_set_spin_limit(unsigned n);
+cudaError_t launch_ngram(const NgramArgs& a, int grid, cudaStream_t s);
 
 // Acceptance statistics: zeroes hist[0..K+1], counts n_accepted into it and,
 // when alpha / mean_tokens are given, derives them (acceptance_kernel.cu).

@@ -62,3 +62,25 @@ def test_captured_tree_verify_replays_like_eager_calls():
         for a, b, c in zip(out, out_e, ref):
             assert torch.equal(a, c) and torch.equal(b, c)
     assert sv.spec_get_status() == 0
+
+
+def test_captured_ngram_drafting_replays_like_eager_calls():
+    """The scan and the finishing launch (programmatic stream serialisation)
+    captured together, replayed over new histories."""
+    sets = [wl.make_ngram_histories(24, 9000, V=60, seed=s, copy_prob=0.6) for s in range(3)]
+    tok = sets[0]["tokens"].to(DEV)
+    ln = sets[0]["lengths"].to(DEV)
+    sv.spec_ngram_draft(tok, ln, 1, 6, 7)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = sv.spec_ngram_draft(tok, ln, 1, 6, 7)
+    for h in sets:
+        tok.copy_(h["tokens"].to(DEV))
+        ln.copy_(h["lengths"].to(DEV))
+        g.replay()
+        ref = sv.spec_ngram_draft(h["tokens"].to(DEV), h["lengths"].to(DEV), 1, 6, 7)
+        torch.cuda.synchronize()
+        for a, b in zip(out, ref):
+            assert torch.equal(a, b)
+    assert sv.spec_get_status() == 0

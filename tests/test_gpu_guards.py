@@ -228,6 +228,41 @@ def test_a_lowered_wait_limit_never_hangs_or_writes_out_of_place():
     assert not rep["mismatch"], rep
 
 
+def test_ngram_lowered_wait_limit_returns_and_flags_only_timeouts():
+    """N-gram drafting with every stage wait limited to one poll: the scan's
+    consumers may give up on a stage whose bulk copy is still landing; the
+    call still returns (the producer drains its copies with its own limit),
+    flags at most a timeout, writes nothing out of place and only values a
+    history holds (a chunk left unscanned reads as no match).  With the
+    default limit back the next call matches the oracle."""
+    import oracle
+    h = wl.make_ngram_histories(64, 40000, V=50, seed=12, copy_prob=0.6)
+    tok, ln = h["tokens"].to(DEV), h["lengths"].to(DEV)
+    B, K = tok.shape[0], 9
+    d, nd, ml = Guarded((B, K), torch.int32), Guarded((B,), torch.int32), Guarded((B,), torch.int32)
+    assert sv.spec_get_status() == 0
+    try:
+        sv.spec_test_spin_limit(1)
+        for _ in range(3):
+            sv.spec_ngram_draft(tok, ln, 1, 6, K, out_drafts=d.t, out_n_drafts=nd.t, out_match_len=ml.t)
+            torch.cuda.synchronize()
+            status = sv.spec_get_status()
+            assert status in (0, sv.SPEC_FLAG_TIMEOUT), status
+            assert d.intact() and nd.intact() and ml.intact()
+            n_, m_, d_ = nd.t.cpu().numpy(), ml.t.cpu().numpy(), d.t.cpu().numpy()
+            assert ((n_ >= 0) & (n_ <= K)).all() and ((m_ == 0) | ((m_ >= 1) & (m_ <= 6))).all()
+            assert ((d_ >= -1) & (d_ < 50)).all()
+    finally:
+        sv.spec_test_spin_limit(0)
+    drafts, nd2, ml2 = sv.spec_ngram_draft(tok, ln, 1, 6, K)
+    torch.cuda.synchronize()
+    assert sv.spec_get_status() == 0
+    ref = oracle.ngram_draft(h["tokens"].numpy(), h["lengths"].numpy(), 1, 6, K)
+    np.testing.assert_array_equal(nd2.cpu().numpy(), ref["n_drafts"])
+    np.testing.assert_array_equal(ml2.cpu().numpy(), ref["match_len"])
+    np.testing.assert_array_equal(drafts.cpu().numpy(), ref["drafts"])
+
+
 def test_two_full_capacity_launches_side_by_side():
     """Two full-size c3 verifies (B=256, grids sized to the whole device) on
     two streams at once: each launch starts with only part of its grid

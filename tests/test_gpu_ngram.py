@@ -87,3 +87,58 @@ def test_ngram_rejects_bad_arguments():
     for n_min, n_max, K in ((0, 2, 4), (3, 2, 4), (1, 33, 4), (1, 2, -1), (1, 2, 4097)):
         with pytest.raises(sv.SpecError):
             sv.spec_ngram_draft(t, ln, n_min, n_max, K)
+
+
+def test_ngram_timed_workload_whole_batch():
+    """The timed workload (256 histories of up to 131072 tokens, 32 chunks per
+    sequence, about 13 chunks claimed per scan CTA), every sequence against
+    the oracle, twice in a row (fresh scratch and claim counter each call)."""
+    h = wl.make_ngram_histories(16, 131072, seed=1)
+    tok = h["tokens"].repeat(16, 1)
+    ln = h["lengths"].repeat(16)
+    ref = oracle.ngram_draft(tok.numpy(), ln.numpy(), 1, 4, 8)
+    for _ in range(2):
+        drafts, nd, ml = _run(tok, ln, 1, 4, 8)
+        np.testing.assert_array_equal(nd, ref["n_drafts"])
+        np.testing.assert_array_equal(ml, ref["match_len"])
+        np.testing.assert_array_equal(drafts, ref["drafts"])
+    assert sv.spec_get_status() == 0
+
+
+def test_ngram_rows_off_16_byte_boundaries():
+    """Rows that cannot take bulk copies are staged with plain loads: a stride
+    that is not a multiple of 4 tokens, and a base pointer 4 bytes past a
+    16-byte boundary, both over histories of several chunks."""
+    h = wl.make_ngram_histories(12, 23001, V=40, seed=8, copy_prob=0.6)
+    _check(h["tokens"].numpy(), h["lengths"].numpy(), 2, 6, 9)
+    h = wl.make_ngram_histories(12, 23000, V=40, seed=9, copy_prob=0.6)
+    B, S = h["tokens"].shape
+    flat = torch.zeros(B * S + 1, dtype=torch.int32, device=DEV)
+    t = flat[1:].view(B, S)
+    t.copy_(h["tokens"].to(DEV))
+    assert t.data_ptr() % 16 == 4
+    ln = h["lengths"].to(DEV)
+    drafts, nd, ml = sv.spec_ngram_draft(t, ln, 1, 5, 7)
+    torch.cuda.synchronize()
+    ref = oracle.ngram_draft(h["tokens"].numpy(), h["lengths"].numpy(), 1, 5, 7)
+    np.testing.assert_array_equal(nd.cpu().numpy(), ref["n_drafts"])
+    np.testing.assert_array_equal(ml.cpu().numpy(), ref["match_len"])
+    np.testing.assert_array_equal(drafts.cpu().numpy(), ref["drafts"])
+    assert sv.spec_get_status() == 0
+
+
+def test_ngram_match_at_every_chunk_boundary():
+    """Histories whose only earlier occurrence of the suffix straddles a
+    4096-token chunk boundary (the match's tokens sit in the halo staged
+    before the chunk), at each boundary of a 5-chunk row."""
+    S, n = 5 * 4096, 6
+    for boundary in range(4096, S, 4096):
+        for shift in (-3, 0, 1, 4):
+            row = np.arange(S, dtype=np.int32) + 1000  # all distinct
+            suffix = np.array([7, 8, 9, 10, 11, 12], dtype=np.int32)
+            e = boundary + shift  # the occurrence ends at e (exclusive)
+            row[e - n:e] = suffix
+            L = S - 5
+            row[L - n:L] = suffix
+            ref = _check(row[None, :], np.array([L], dtype=np.int32), 1, 8, 5)
+            assert ref["match_len"][0] == n and ref["drafts"][0, 0] == row[e]

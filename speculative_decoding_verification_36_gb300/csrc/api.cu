@@ -130,6 +130,7 @@ bool aligned16(const void* p) { return ((uintptr_t)p & 15u) == 0; }
 constexpr int kSliceBytes = 16384;        // statistics slice of the sampling kernel (full read)
 constexpr int kSliceBytesEarlyExit = 12288;  // ... with early exit, and of the stochastic tree's statistics
 constexpr int kSmallSliceBytes = 8192;    // ... for a batch with fewer than ~6 slices per warp
+constexpr int kTinySliceBytes = 4096;     // ... for one whose 8 KB slices would leave warps without one
 constexpr int kTailBytes = 6144;          // bytes of each of the two rows in a tail item
 constexpr int kSmallTailBytes = 2048;     // ... for a small batch
 constexpr int kArgmaxSliceBytes = 8192;   // slice of the greedy and tree kernels
@@ -353,9 +354,13 @@ int verify_impl(bool bf16, const void* target, const void* draft, const int32_t*
   // the full read; the early exit is 4 us slower with 16 KB).
   choose_slices(V, vec_elems, esz, kSliceBytesEarlyExit, &a.SL, &a.CS, &CU);
   const bool small = (long long)B * a.R * a.CS < 6LL * capacity * sv::kWarps;
-  if (small)
+  if (small) {
     choose_slices(V, vec_elems, esz, kSmallSliceBytes, &a.SL, &a.CS, &CU);
-  else if (!early_exit)
+    // fewer 8 KB slices than warps (c1: 144 of 4864): 4 KB slices, each in
+    // fewer dependent load rounds (c1 -0.7 us; 1 KB slices were slower)
+    if ((long long)B * a.R * a.CS < (long long)capacity * sv::kWarps)
+      choose_slices(V, vec_elems, esz, kTinySliceBytes, &a.SL, &a.CS, &CU);
+  } else if (!early_exit)
     choose_slices(V, vec_elems, esz, kSliceBytes, &a.SL, &a.CS, &CU);
   // tail slices: whole warp steps, kSmallTailBytes per row for a small batch
   // (c2: 2 KB, -0.7 us against 4 KB), else kTailBytes (c3: 6 KB, against 8

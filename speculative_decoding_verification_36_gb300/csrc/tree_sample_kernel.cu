@@ -60,6 +60,8 @@ __global__ void __launch_bounds__(kThreads, kMinBlocks) tree_stats_kernel(const 
   constexpr int BATCH = 32 * VEC * kUnroll;
   const int lane = threadIdx.x & 31;
   const long long W = (long long)gridDim.x * kWarps;
+  // the walk launch may become resident as this grid's CTAs retire
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   for (long long f = (long long)blockIdx.x * kWarps + (threadIdx.x >> 5); f < a.F; f += W) {
     const long long row_id = f / a.CS;
     const int s = (int)(f - row_id * a.CS);
@@ -329,7 +331,10 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
   const float2* rs = a.rowstat + (size_t)b * a.RR;
   int32_t* path = a.out_path + (size_t)b * N1;
 
-  // inputs of the sequence and the bad-data check (identical in every CTA)
+  // The launch is programmatically dependent on the statistics launch: until
+  // griddepcontrol.wait below only the sequence's inputs are read, so this
+  // part overlaps the end of the statistics.
+  // Inputs of the sequence and their check (identical in every CTA).
   bool bad = false;
   for (int i = tid; i < N; i += kWalkThreads) {
     const int p = __ldg(a.parents + (size_t)b * N + i), t = __ldg(a.tokens + (size_t)b * N + i);
@@ -337,11 +342,23 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
     s_tok[i] = t;
     bad |= p < -1 || p >= i || t < 0 || t >= a.V;
   }
-  for (int r = tid; r < a.RR; r += kWalkThreads) {
-    const float2 v = __ldcg(rs + r);
-    bad |= !(v.y > 0.f) || !(v.y < INFINITY) || !(v.x < INFINITY) || !(v.x > neg_inf());
-  }
   bad = __syncthreads_or(bad);
+  if (!bad) {
+    // every node's decision inputs at once, off the walk's serial path
+    for (int i = tid; i < N; i += kWalkThreads) {
+      const int x = s_tok[i], pr = s_par[i];
+      s_zt[i] = E::load1(tree_row<E>(a, b, pr + 1) + x);
+      s_zd[i] = E::load1(tree_row<E>(a, b, N1 + pr + 1) + x);
+      s_u[i] = uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0);
+    }
+    // the row statistics, written by the statistics launch
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    for (int r = tid; r < a.RR; r += kWalkThreads) {
+      const float2 v = __ldcg(rs + r);
+      bad |= !(v.y > 0.f) || !(v.y < INFINITY) || !(v.x < INFINITY) || !(v.x > neg_inf());
+    }
+    bad = __syncthreads_or(bad);
+  }
   if (rank == 0)
     for (int j = tid; j <= N; j += kWalkThreads) path[j] = -1;
   if (bad) {  // every CTA of the cluster returns here; no shared memory was shared yet
@@ -350,13 +367,6 @@ __global__ void __launch_bounds__(kWalkThreads, 1) tree_walk_kernel(const __grid
       atomicOr(a.status, kStatusBadData);
     }
     return;
-  }
-  // every node's decision inputs at once, off the walk's serial path
-  for (int i = tid; i < N; i += kWalkThreads) {
-    const int x = s_tok[i], pr = s_par[i];
-    s_zt[i] = E::load1(tree_row<E>(a, b, pr + 1) + x);
-    s_zd[i] = E::load1(tree_row<E>(a, b, N1 + pr + 1) + x);
-    s_u[i] = uniform_draw(a.seed, (uint64_t)b, (uint64_t)i, 0);
   }
   if (tid == 0) {
     sh.u = -1;
@@ -606,13 +616,17 @@ static cudaError_t launch_tree_sample_t(const TreeSampleArgs& a, int stats_grid,
   cfg.gridDim = dim3((unsigned)a.B * (unsigned)a.C);
   cfg.blockDim = dim3(kWalkThreads);
   cfg.stream = s;
-  cudaLaunchAttribute at[1];
+  cudaLaunchAttribute at[2];
   at[0].id = cudaLaunchAttributeClusterDimension;
   at[0].val.clusterDim.x = (unsigned)a.C;
   at[0].val.clusterDim.y = 1;
   at[0].val.clusterDim.z = 1;
+  // programmatic dependent launch: the walk reads its inputs while the
+  // statistics finish and waits for them in griddepcontrol.wait
+  at[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  at[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = at;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, tree_walk_kernel<E, VEC>, a);
 }
 

@@ -104,14 +104,6 @@ __device__ __forceinline__ bool mbar_try(unsigned long long* bar, unsigned parit
       : "memory");
   return ok != 0;
 }
-// Bounded wait: false once `limit` further suspensions have passed without
-// the phase.
-__device__ __forceinline__ bool mbar_wait(unsigned long long* bar, unsigned parity, unsigned limit) {
-  if (mbar_try(bar, parity)) return true;
-  for (unsigned it = 0; it < limit; ++it)
-    if (mbar_try(bar, parity)) return true;
-  return false;
-}
 // One bulk copy global -> shared, completing `bytes` on the mbarrier.  Both
 // addresses and the size are multiples of 16 bytes.
 __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned bytes, unsigned long long* bar) {
@@ -122,7 +114,8 @@ __device__ __forceinline__ void bulk_load(void* dst, const void* src, unsigned b
       : "memory");
 }
 // Warp-uniform bounded wait: every lane tries, and the warp leaves together
-// once all lanes have seen the phase (or after `limit` further tries).
+// once all lanes have seen the phase; false after `limit` further tries
+// (each suspends for at most about kNgramSuspendNs).
 __device__ __forceinline__ bool warp_wait(unsigned long long* bar, unsigned parity, unsigned limit) {
   if (__all_sync(0xffffffffu, mbar_try(bar, parity))) return true;
   for (unsigned it = 0; it < limit; ++it)

@@ -137,3 +137,25 @@ def test_python_binding_rejects_host_and_foreign_device_tensors():
     _same_device(torch.zeros(1), torch.device("cpu"), "x")
     with pytest.raises(ValueError):
         _same_device(torch.zeros(1), torch.device("meta"), "x")
+
+
+def test_ngram_checks(lib):
+    f = lib.spec_ngram_draft
+
+    def call(tok=FAKE, ln=FAKE, B=2, stride=8, n_min=1, n_max=4, K=3, d=FAKE, nd=FAKE, ml=FAKE):
+        return f(tok, ln, B, stride, n_min, n_max, K, d, nd, ml, None)
+
+    assert call(tok=None) == _lib.SPEC_ERR_NULL
+    assert call(ln=None) == _lib.SPEC_ERR_NULL
+    assert call(nd=None) == _lib.SPEC_ERR_NULL
+    assert call(d=None) == _lib.SPEC_ERR_NULL
+    assert call(d=None, K=0, B=0) == _lib.SPEC_OK
+    for bad in (dict(B=-1), dict(stride=0), dict(stride=2**30 + 1), dict(n_min=0), dict(n_min=5, n_max=4),
+                dict(n_max=33), dict(K=-1), dict(K=4097)):
+        assert call(**bad) == _lib.SPEC_ERR_SHAPE, bad
+    # 32-bit (sequence, chunk) entries: B * ceil(stride / 4096) stays below
+    # 2^31 - 2^20, refused on the host before any device work
+    chunks = -(-2**30 // 4096)
+    limit_b = ((2**31 - 2**20) + chunks - 1) // chunks
+    assert call(B=limit_b, stride=2**30) == _lib.SPEC_ERR_SHAPE
+    assert call(B=0, stride=2**30) == _lib.SPEC_OK

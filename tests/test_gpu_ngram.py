@@ -142,3 +142,26 @@ def test_ngram_match_at_every_chunk_boundary():
             row[L - n:L] = suffix
             ref = _check(row[None, :], np.array([L], dtype=np.int32), 1, 8, 5)
             assert ref["match_len"][0] == n and ref["drafts"][0, 0] == row[e]
+
+
+def test_ngram_two_full_grids_side_by_side():
+    """Two timed-workload calls on two streams at once: each persistent scan
+    grid is sized to the whole device, so each starts with only part of it
+    resident beside the other.  No scan CTA waits for another (entries are
+    claimed from a counter), so both finish with no expired wait and with
+    the results of the same calls made alone."""
+    hs = [wl.make_ngram_histories(16, 131072, seed=s) for s in (1, 2)]
+    xs = [(h["tokens"].repeat(16, 1).to(DEV), h["lengths"].repeat(16).to(DEV)) for h in hs]
+    alone = [sv.spec_ngram_draft(t, ln, 1, 4, 8) for t, ln in xs]
+    torch.cuda.synchronize()
+    streams = [torch.cuda.Stream(device=DEV) for _ in range(2)]
+    for _ in range(3):
+        got = []
+        for (t, ln), s in zip(xs, streams):
+            with torch.cuda.stream(s):
+                got.append(sv.spec_ngram_draft(t, ln, 1, 4, 8, stream=s))
+        torch.cuda.synchronize()
+        assert sv.spec_get_status() == 0
+        for g, a in zip(got, alone):
+            for x, y in zip(g, a):
+                assert torch.equal(x, y)

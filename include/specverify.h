@@ -334,7 +334,10 @@ int spec_tree_verify_greedy_early_exit_bf16(const uint16_t *target_logits, const
  * emitted token is then distributed exactly as p at its position.  Every row
  * of both inputs is checked for bad data, leaves' draft rows included.
  * N <= 1024.  temperature 0 is SPEC_ERR_TEMPERATURE here (the greedy tree is
- * spec_tree_verify_greedy_*).
+ * spec_tree_verify_greedy_*).  Two kernels run on `stream`: the row
+ * statistics, then the walk, launched with programmatic stream serialisation
+ * (capturable into a CUDA graph); scratch comes from the library's
+ * stream-ordered pool.  Asynchronous on `stream`.
  */
 int spec_tree_verify_sampling_f32(const float *target_logits, const float *draft_logits,
                                   const int32_t *tree_tokens, const int32_t *parent_idx, int B,

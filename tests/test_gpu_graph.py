@@ -84,3 +84,25 @@ def test_captured_ngram_drafting_replays_like_eager_calls():
         for a, b in zip(out, ref):
             assert torch.equal(a, b)
     assert sv.spec_get_status() == 0
+
+
+def test_captured_stochastic_tree_replays_like_eager_calls():
+    """The statistics launch and the walk's cluster launch (programmatically
+    dependent on it) captured together, replayed over new trees."""
+    tp = wl.preset("c5", B=6, depth=3, V=6000)
+    sets = [wl.make_tree_sampling(tp, 1.0, device=DEV, seed=s) for s in range(3)]
+    tgt, drf, tok, par = (sets[0][k].clone() for k in ("target", "draft", "tokens", "parents"))
+    sv.spec_tree_verify_sampling(tgt, drf, tok, par, 1.0, 7)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        out = sv.spec_tree_verify_sampling(tgt, drf, tok, par, 1.0, 7)
+    for x in sets:
+        for buf, k in ((tgt, "target"), (drf, "draft"), (tok, "tokens"), (par, "parents")):
+            buf.copy_(x[k])
+        g.replay()
+        ref = sv.spec_tree_verify_sampling(x["target"], x["draft"], x["tokens"], x["parents"], 1.0, 7)
+        torch.cuda.synchronize()
+        for a, b in zip(out, ref):
+            assert torch.equal(a, b)
+    assert sv.spec_get_status() == 0
